@@ -1,0 +1,395 @@
+#!/usr/bin/env python3
+"""Benchmark of the DSA decode step on GB300: queries/s at batch 64 x 8K context.
+
+Workload (the BF16 decode configuration): 64 requests with contexts drawn
+uniformly from [2048, 8192], one query token each, index_topk 2048, 64 e4m3
+indexer heads x 128 with fp32 per-token key scales, 16 MLA heads over a bf16
+576-wide latent cache in 64-token pages under random block tables. Inputs are
+seeded synthetic tensors (inputs.make_config("decode")).
+
+One step = one pass of the whole hot path through the C ABI (dsa_decode_step:
+lightning indexer -> radix top-k -> sparse MLA + split combine), captured once
+in a CUDA graph and replayed. Between timed steps a 256 MiB buffer is written
+to flush L2 (outside the timed events). Under torchrun every rank runs its own
+replica of the workload (data-parallel over requests, no collective in the
+path); `value` counts the queries of all ranks over the slowest rank's time.
+
+`--impl reference` times the float64 CPU oracle on this host's cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from dsa_sparse_attention_02_gb300 import _lib, inputs, runner  # noqa: E402
+
+METRIC = "DSA decode queries/s at batch 64×ctx 8K; achieved HBM GB/s vs GB300 peak"
+WORKLOAD = ("decode: batch 64, context ~U[2048,8192], 1 query token, index_topk 2048, "
+            "64 e4m3 indexer heads x 128 (+fp32 per-token key scale), 16 MLA heads, "
+            "bf16 576-wide latent KV, 64-token pages, random block tables")
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def algorithmic_bytes(wl):
+    """Bytes the step must move at least: every index key (128 e4m3 + 4 B scale) of every
+    request, and every selected 576-wide bf16 latent row (1152 B)."""
+    idx_bytes = int(wl.seq_lens.astype(np.int64).sum()) * (128 + 4)
+    _, pos = _positions(wl)
+    selected = int(np.minimum(pos + 1, wl.topk).sum())
+    return idx_bytes, selected * 576 * 2, selected
+
+
+def _positions(wl):
+    req = np.repeat(np.arange(wl.B), wl.n_q)
+    pos = np.concatenate([np.arange(L - n, L) for L, n in zip(wl.seq_lens, wl.n_q)])
+    return req, pos
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_PATH) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dsa_sparse_attention_02_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current source."""
+    try:
+        with open(TRAFFIC_PATH) as f:
+            t = json.load(f)
+        if t.get("source_hash") != kernel_source_hash():
+            return None
+        return t["kernels"][kernel]["dram_bytes_per_launch"]
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) != 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def oracle_step_time(wl, nq, reps_min_s):
+    """Runs the oracle over `nq` queries of the workload repeatedly for >= reps_min_s;
+    returns seconds per query."""
+    import oracle
+    ts = list(range(min(nq, wl.T)))
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle.dsa_step(wl, ts=ts)
+        n += len(ts)
+        el = time.perf_counter() - t0
+        if el >= reps_min_s:
+            return el / n
+
+
+def cpu_baseline(wl, budget_s=12.0):
+    import oracle  # noqa: F401  (the oracle is the baseline)
+    sec_per_q = oracle_step_time(wl, wl.T, budget_s)
+    return {"value": 1.0 / sec_per_q, "unit": "queries/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"float64 numpy oracle (indexer, top-k, attention) over all {wl.T} queries of the "
+                      f"decode workload, repeated for >= {budget_s:.0f} s; BLAS threads = host cores"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    wl = inputs.make_config("decode")
+    per_q = oracle_step_time(wl, 2, 1.0)                       # calibration
+    budget = 90.0                                              # whole run
+    nq = int(max(1, min(wl.T, budget / max(1, args.steps + args.warmup) / per_q)))
+    for _ in range(args.warmup):
+        oracle_step_time(wl, nq, 0.0)
+    import oracle
+    ts = list(range(nq))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.dsa_step(wl, ts=ts)
+    el = time.perf_counter() - t0
+    value = nq * args.steps / el
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "queries/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * el / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded PCG64)",
+            "config": {"workload": WORKLOAD, "queries_per_step": nq},
+            "cpu_baseline": {"value": value, "unit": "queries/s", "cores": os.cpu_count(),
+                             "kind": "oracle",
+                             "sample": f"{nq} of the 64 queries per step (float64 numpy oracle)"},
+            "e2e": {"value": value, "unit": "queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    wl = inputs.make_config("decode", seed=inputs.CONFIG_SEEDS["decode"] + 1000 * rank)
+    dw = runner.DeviceWorkload(wl, dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    # warm-up (eager), then capture one step in a CUDA graph
+    for _ in range(args.warmup):
+        dw.step()
+    torch.cuda.synchronize()
+    if dw.check_error() != 0:
+        raise SystemExit("device error during warm-up")
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        dw.step()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph):
+        dw.step()
+    for _ in range(3):
+        flush.fill_(1)
+        graph.replay()
+    torch.cuda.synchronize()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            starts[i].record(stream)
+            graph.replay()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    if dist:
+        dist.barrier()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = float(sum(step_ms))
+    if dw.check_error() != 0:
+        raise SystemExit("device error during the timed steps")
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = wl.T * world * args.steps / (total_ms / 1000.0)
+
+    # ---- end to end through the public API with host buffers
+    e2e = measure_e2e(dw, graph, flush, stream, max(20, min(args.steps, 200)))
+    # ---- per-kernel breakdown for the roofline of the dominant kernel
+    comp = measure_components(dw, flush, stream, max(20, min(args.steps, 200)))
+
+    idx_b, lat_b, selected = algorithmic_bytes(wl)
+    peak, peak_kind = load_peaks()
+    attn_gbs = lat_b / (comp["attend_ms"] / 1000.0) / 1e9
+    step_gbs = (idx_b + lat_b) / (ms_per_step / 1000.0) / 1e9
+    launches_per_step = 4           # indexer, top-k, sparse MLA split, combine
+    line = {
+        "metric": METRIC, "value": value, "unit": "queries/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3+bf16", "data": "synthetic (seeded PCG64, decode configuration)",
+        "config": {"workload": WORKLOAD, "queries_per_step_per_gpu": wl.T,
+                   "l2": "flushed between timed steps (256 MiB write outside the events)",
+                   "timed": "CUDA-graph replay of dsa_decode_step, CUDA events per step",
+                   "step_ms_p10_p50_p90": [float(np.percentile(step_ms, q)) for q in (10, 50, 90)],
+                   "wall_s_timed_region": wall},
+        "hbm": {"algorithmic_bytes_per_step": idx_b + lat_b, "index_key_bytes": idx_b,
+                "selected_latent_bytes": lat_b, "achieved_gbs": step_gbs,
+                "frac_of_peak": step_gbs / peak, "peak_gbs": peak, "peak_kind": peak_kind,
+                "frac_of_8tbs_nominal": step_gbs / 8000.0},
+        "roofline": {"kernel": "sparse MLA attend (split kernel + combine)", "bound": "hbm",
+                     "achieved": attn_gbs, "peak": peak, "unit": "GB/s", "frac": attn_gbs / peak,
+                     "peak_kind": peak_kind, "algorithmic_bytes_per_launch": lat_b,
+                     "avg_launch_ms": comp["attend_ms"],
+                     "traffic": load_traffic("sparse_mla_kernel")},
+        "components_ms": comp,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def measure_e2e(dw, graph, flush, stream, n):
+    """Same metric with per-step host inputs: H2D of the step's inputs from pinned memory,
+    the step, and D2H of its outputs, all inside the timed events."""
+    lay = dw.layers[0]
+    dev_in = [lay.q, dw.q_idx, dw.q_scale, dw.w, dw.seq_lens, dw.cu_q, dw.block_table]
+    host_in = [t.detach().cpu().pin_memory() for t in dev_in]
+    dev_out = [lay.out, lay.lse]
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dev_out]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    ms = []
+    for i in range(n):
+        flush.fill_(i & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for d, h in zip(dev_in, host_in):
+            d.copy_(h, non_blocking=True)
+        graph.replay()
+        for h, d in zip(host_out, dev_out):
+            h.copy_(d, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    avg = sum(ms) / len(ms)
+    return {"value": dw.wl.T / (avg / 1000.0), "unit": "queries/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": avg}
+
+
+def measure_components(dw, flush, stream, n):
+    """Average device time of each entry point of the step, launched alone with the
+    GPU kept busy (a sleep kernel) while the host enqueues, L2 flushed before each."""
+    wl = dw.wl
+    g = dw.geom
+    stride = int(-(-wl.max_seq_len // 64) * 64)
+    scores = torch.empty(wl.T, stride, dtype=torch.float32, device=dw.device)
+    idx = torch.empty(wl.T, wl.topk, dtype=torch.int32, device=dw.device)
+    lay = dw.layers[0]
+    ws = _lib.workspace(max(_lib.dsa_topk_workspace_size(g, wl.topk),
+                            _lib.dsa_sparse_mla_attend_workspace_size(g, lay.q.shape[1], wl.topk)),
+                        dw.device)
+    acc = {"indexer_ms": 0.0, "topk_ms": 0.0, "attend_ms": 0.0}
+    for i in range(n):
+        flush.fill_(i & 0xFF)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        torch.cuda._sleep(400_000)
+        ev[0].record(stream)
+        _lib.dsa_indexer_scores(g, dw.qk_dtype, dw.q_idx, dw.q_scale, dw.w, dw.idx_k, dw.idx_k_scale,
+                                scores, ws)
+        ev[1].record(stream)
+        _lib.dsa_topk(g, scores, wl.topk, idx, ws)
+        ev[2].record(stream)
+        flush.fill_((i + 1) & 0xFF)
+        torch.cuda._sleep(400_000)
+        ev3 = torch.cuda.Event(enable_timing=True)
+        ev3.record(stream)
+        _lib.dsa_sparse_mla_attend(g, lay.kv_dtype, lay.q, lay.kv, idx, wl.topk, wl.sm_scale, lay.out,
+                                   lay.lse, ws)
+        ev[3].record(stream)
+        ev[3].synchronize()
+        acc["indexer_ms"] += ev[0].elapsed_time(ev[1])
+        acc["topk_ms"] += ev[1].elapsed_time(ev[2])
+        acc["attend_ms"] += ev3.elapsed_time(ev[3])
+    return {k: v / n for k, v in acc.items()}
+
+
+if __name__ == "__main__":
+    main()

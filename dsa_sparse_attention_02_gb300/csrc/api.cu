@@ -1,0 +1,341 @@
+// Host side of the C ABI declared in include/dsa.h: argument validation,
+// workspace layout, TMA descriptor encoding and kernel launches.
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include "dsa.h"
+#include "kernels.cuh"
+
+
+using namespace dsa;
+
+namespace {
+
+constexpr size_t kHeaderBytes = 256;
+constexpr int kMaxTopk = 16384;
+constexpr int kTopkCap = 16384;
+
+thread_local char g_last_error[256] = "";
+
+void set_error(const char* what, const char* detail) {
+  snprintf(g_last_error, sizeof(g_last_error), "%s: %s", what, detail);
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D row-major tensor [rows, cols] with a 128-byte-swizzled box of box_cols x box_rows.
+bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t cols, uint64_t rows,
+               uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) { set_error("cudaGetDriverEntryPointByVersion", "cuTensorMapEncodeTiled unavailable"); return false; }
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  const CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[96];
+    snprintf(buf, sizeof(buf), "CUresult %d (dims %llu x %llu, box %u x %u)", (int)r, (unsigned long long)cols,
+             (unsigned long long)rows, box_cols, box_rows);
+    set_error("cuTensorMapEncodeTiled", buf);
+    return false;
+  }
+  return true;
+}
+
+dsa_status_t check_geom(const dsa_geom_t* g) {
+  if (!g) return DSA_ERR_INVALID_ARG;
+  if (g->B < 0 || g->T < 0 || g->max_seq_len < 1 || g->num_pages < 1) return DSA_ERR_INVALID_ARG;
+  if (g->page_size != 64) return DSA_ERR_UNSUPPORTED;
+  if (g->T > 0 && g->B < 1) return DSA_ERR_INVALID_ARG;
+  if (g->bt_stride < (g->max_seq_len + 63) / 64) return DSA_ERR_INVALID_ARG;
+  if ((int64_t)g->num_pages * 64 > INT32_MAX) return DSA_ERR_UNSUPPORTED;
+  if (g->B > 0 && (!g->seq_lens || !g->cu_q || !g->block_table)) return DSA_ERR_INVALID_ARG;
+  return DSA_OK;
+}
+
+GeomDev to_dev(const dsa_geom_t* g) {
+  GeomDev d;
+  d.B = g->B; d.T = g->T; d.max_seq_len = g->max_seq_len; d.num_pages = g->num_pages; d.bt_stride = g->bt_stride;
+  d.seq_lens = g->seq_lens; d.cu_q = g->cu_q; d.block_table = g->block_table;
+  return d;
+}
+
+dsa_status_t from_cuda(cudaError_t e, const char* what = "kernel launch") {
+  if (e == cudaSuccess) return DSA_OK;
+  set_error(what, cudaGetErrorString(e));
+  return DSA_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- indexer
+dsa_status_t check_indexer(const dsa_geom_t* g, dsa_dtype_t dt, int Hi, const void* q_idx, const float* q_scale,
+                           const float* w, const void* kc, const float* ks, const float* scores, int64_t stride) {
+  dsa_status_t s = check_geom(g);
+  if (s != DSA_OK) return s;
+  if (dt != DSA_BF16 && dt != DSA_E4M3) return DSA_ERR_INVALID_ARG;
+  if (Hi < 1 || Hi > 64) return DSA_ERR_INVALID_ARG;
+  if (g->B > indexer_max_requests()) return DSA_ERR_UNSUPPORTED;
+  if (stride < g->max_seq_len) return DSA_ERR_INVALID_ARG;
+  if (g->T == 0) return DSA_OK;
+  if (!q_idx || !w || !kc || !scores) return DSA_ERR_INVALID_ARG;
+  if (dt == DSA_E4M3 && (!q_scale || !ks)) return DSA_ERR_INVALID_ARG;
+  if (dt == DSA_BF16 && (q_scale || ks)) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q_idx) || !aligned16(kc)) return DSA_ERR_INVALID_ARG;
+  return DSA_OK;
+}
+
+dsa_status_t run_indexer(const dsa_geom_t* g, dsa_dtype_t dt, int Hi, const void* q_idx, const float* q_scale,
+                         const float* w, const void* kc, const float* ks, float* scores, int64_t stride, int* err,
+                         cudaStream_t st) {
+  const bool fp8 = dt == DSA_E4M3;
+  CUtensorMap mk, mq;
+  const CUtensorMapDataType tdt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const uint32_t box_cols = fp8 ? 128 : 64;
+  const uint64_t row_bytes = fp8 ? 128 : 256;
+  if (!encode_2d(&mk, tdt, kc, 128, (uint64_t)g->num_pages * 64, row_bytes, box_cols, 64)) return DSA_ERR_CUDA;
+  if (!encode_2d(&mq, tdt, q_idx, 128, (uint64_t)g->T * Hi, row_bytes, box_cols, (uint32_t)Hi)) return DSA_ERR_CUDA;
+  IndexerArgs A;
+  A.g = to_dev(g); A.Hi = Hi; A.q_scale = q_scale; A.w = w; A.k_scale = ks; A.scores = scores; A.stride = stride;
+  A.err = err;
+  const bool multi = g->T > g->B;   // some request has more than one query token
+  return from_cuda(indexer_launch(fp8, Hi, multi, mk, mq, A, num_sms(), st));
+}
+
+// ---------------------------------------------------------------- top-k
+dsa_status_t check_topk(const dsa_geom_t* g, const float* scores, int64_t stride, int k, const int* idx) {
+  dsa_status_t s = check_geom(g);
+  if (s != DSA_OK) return s;
+  if (k < 1 || k > kMaxTopk) return DSA_ERR_INVALID_ARG;
+  if (stride < g->max_seq_len) return DSA_ERR_INVALID_ARG;
+  if (g->max_seq_len > kTopkCap) {
+    const int64_t nch = (g->max_seq_len + kTopkCap - 1) / kTopkCap;
+    if (nch * k > kTopkCap) return DSA_ERR_UNSUPPORTED;
+  }
+  if (g->T == 0) return DSA_OK;
+  if (!scores || !idx) return DSA_ERR_INVALID_ARG;
+  return DSA_OK;
+}
+
+// ---------------------------------------------------------------- attention
+dsa_status_t check_attend(const dsa_geom_t* g, dsa_dtype_t dt, int H, const void* q, const void* kv, const int* idx,
+                          int k, float sm_scale, const void* out) {
+  dsa_status_t s = check_geom(g);
+  if (s != DSA_OK) return s;
+  if (dt != DSA_BF16 && dt != DSA_E4M3) return DSA_ERR_INVALID_ARG;
+  if (H < 1 || H > 128 || (H > 16 && H % 16 != 0)) return DSA_ERR_INVALID_ARG;
+  if (k < 1 || k > kMaxTopk) return DSA_ERR_INVALID_ARG;
+  if (!std::isfinite(sm_scale)) return DSA_ERR_INVALID_ARG;
+  if (g->T == 0) return DSA_OK;
+  if (!q || !kv || !idx || !out) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv)) return DSA_ERR_INVALID_ARG;
+  return DSA_OK;
+}
+
+size_t attend_scratch_bytes(const dsa_geom_t* g, int H, int k) {
+  const int64_t C = (k + 127) / 128;
+  const int grid = mla_grid((int64_t)g->T * C, num_sms());
+  return mla_partial_bytes(g->T, H, grid);
+}
+
+dsa_status_t run_attend(const dsa_geom_t* g, dsa_dtype_t dt, int H, const void* q, const void* kv, const int* idx,
+                        int k, float sm_scale, void* out, float* lse, void* scratch, int* err, cudaStream_t st) {
+  CUtensorMap mq;
+  const uint32_t box_rows = H < 16 ? (uint32_t)H : 16u;
+  if (!encode_2d(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, 576, (uint64_t)g->T * H, 1152, 64, box_rows))
+    return DSA_ERR_CUDA;
+  MlaArgs A;
+  A.g = to_dev(g); A.H = H; A.k = k; A.C = (k + 127) / 128; A.n_chunks = (int64_t)g->T * A.C;
+  A.kv = reinterpret_cast<const uint8_t*>(kv); A.idx = idx; A.scale_log2 = sm_scale * 1.4426950408889634f;
+  A.out = reinterpret_cast<__nv_bfloat16*>(out); A.lse = lse;
+  const int grid = mla_grid(A.n_chunks, num_sms());
+  const size_t rows = (size_t)(g->T + grid) * H;
+  A.o_part = reinterpret_cast<float*>(scratch);
+  A.ml_part = A.o_part + rows * 512;
+  A.err = err;
+  return from_cuda(mla_launch(dt == DSA_E4M3, mq, A, grid, st));
+}
+
+int64_t step_score_stride(const dsa_geom_t* g) { return (int64_t)align_up((size_t)g->max_seq_len, 64); }
+
+}  // namespace
+
+extern "C" {
+
+const char* dsa_status_string(dsa_status_t s) {
+  switch (s) {
+    case DSA_OK: return "ok";
+    case DSA_ERR_INVALID_ARG: return "invalid argument";
+    case DSA_ERR_UNSUPPORTED: return "unsupported argument combination";
+    case DSA_ERR_CUDA: return "CUDA error";
+    case DSA_ERR_TIMEOUT: return "device wait timed out";
+    case DSA_ERR_WORKSPACE: return "workspace too small or misaligned";
+    case DSA_ERR_BAD_INDEX: return "device data out of range (page id, index or sequence geometry)";
+  }
+  return "unknown status";
+}
+
+int32_t dsa_abi_version(void) { return DSA_ABI_VERSION; }
+
+const char* dsa_last_error(void) { return g_last_error; }
+
+size_t dsa_indexer_scores_workspace_size(const dsa_geom_t*) { return kHeaderBytes; }
+
+dsa_status_t dsa_indexer_scores(const dsa_geom_t* geom, dsa_dtype_t qk_dtype, int32_t Hi, const void* q_idx,
+                                const float* q_scale, const float* w, const void* idx_k_cache,
+                                const float* idx_k_scale, float* scores, int64_t score_stride, void* ws,
+                                size_t ws_bytes, void* stream) {
+  dsa_status_t s = check_indexer(geom, qk_dtype, Hi, q_idx, q_scale, w, idx_k_cache, idx_k_scale, scores, score_stride);
+  if (s != DSA_OK) return s;
+  if (!ws || ws_bytes < kHeaderBytes || (reinterpret_cast<uintptr_t>(ws) & 255u)) return DSA_ERR_WORKSPACE;
+  if (geom->T == 0 || geom->B == 0) return DSA_OK;
+  return run_indexer(geom, qk_dtype, Hi, q_idx, q_scale, w, idx_k_cache, idx_k_scale, scores, score_stride,
+                     reinterpret_cast<int*>(ws), reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t dsa_topk_workspace_size(const dsa_geom_t* geom, int32_t k) {
+  if (!geom || k < 1) return kHeaderBytes;
+  return kHeaderBytes + align_up(topk_workspace_bytes(geom->T, geom->max_seq_len, k), 256);
+}
+
+dsa_status_t dsa_topk(const dsa_geom_t* geom, const float* scores, int64_t score_stride, int32_t k, int32_t* idx,
+                      void* ws, size_t ws_bytes, void* stream) {
+  dsa_status_t s = check_topk(geom, scores, score_stride, k, idx);
+  if (s != DSA_OK) return s;
+  if (!ws || ws_bytes < dsa_topk_workspace_size(geom, k) || (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return DSA_ERR_WORKSPACE;
+  if (geom->T == 0) return DSA_OK;
+  return from_cuda(topk_launch(to_dev(geom), scores, score_stride, k, idx,
+                               reinterpret_cast<uint8_t*>(ws) + kHeaderBytes, reinterpret_cast<int*>(ws),
+                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t dsa_sparse_mla_attend_workspace_size(const dsa_geom_t* geom, int32_t H, int32_t k) {
+  if (!geom || H < 1 || k < 1) return kHeaderBytes;
+  return kHeaderBytes + align_up(attend_scratch_bytes(geom, H, k), 256);
+}
+
+dsa_status_t dsa_sparse_mla_attend(const dsa_geom_t* geom, dsa_dtype_t kv_dtype, int32_t H, const void* q,
+                                   const void* kv_cache, const int32_t* idx, int32_t k, float sm_scale, void* out,
+                                   float* lse, void* ws, size_t ws_bytes, void* stream) {
+  dsa_status_t s = check_attend(geom, kv_dtype, H, q, kv_cache, idx, k, sm_scale, out);
+  if (s != DSA_OK) return s;
+  if (!ws || ws_bytes < dsa_sparse_mla_attend_workspace_size(geom, H, k) || (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return DSA_ERR_WORKSPACE;
+  if (geom->T == 0) return DSA_OK;
+  return run_attend(geom, kv_dtype, H, q, kv_cache, idx, k, sm_scale, out, lse,
+                    reinterpret_cast<uint8_t*>(ws) + kHeaderBytes, reinterpret_cast<int*>(ws),
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t dsa_decode_step_workspace_size(const dsa_step_args_t* a) {
+  if (!a) return kHeaderBytes;
+  const dsa_geom_t* g = &a->geom;
+  size_t bytes = kHeaderBytes;
+  if (!a->reuse_idx) {
+    bytes += align_up((size_t)g->T * step_score_stride(g) * sizeof(float), 256);
+    if (!a->idx_out) bytes += align_up((size_t)g->T * (a->topk > 0 ? a->topk : 1) * sizeof(int32_t), 256);
+  }
+  size_t scratch = attend_scratch_bytes(g, a->H > 0 ? a->H : 1, a->topk > 0 ? a->topk : 1);
+  if (!a->reuse_idx && a->topk > 0) {
+    const size_t tk = topk_workspace_bytes(g->T, g->max_seq_len, a->topk);
+    if (tk > scratch) scratch = tk;
+  }
+  return bytes + align_up(scratch, 256);
+}
+
+dsa_status_t dsa_decode_step(const dsa_step_args_t* a, void* ws, size_t ws_bytes, void* stream) {
+  if (!a) return DSA_ERR_INVALID_ARG;
+  const dsa_geom_t* g = &a->geom;
+  const int64_t stride = step_score_stride(g);
+  dsa_status_t s;
+  if (!a->reuse_idx) {
+    s = check_indexer(g, a->qk_dtype, a->Hi, a->q_idx, a->q_scale, a->w, a->idx_k_cache, a->idx_k_scale,
+                      reinterpret_cast<const float*>(ws), stride);
+    if (s != DSA_OK) return s;
+    s = check_topk(g, reinterpret_cast<const float*>(ws), stride, a->topk, reinterpret_cast<const int*>(ws));
+    if (s != DSA_OK) return s;
+  }
+  s = check_attend(g, a->kv_dtype, a->H, a->q, a->kv_cache, a->reuse_idx ? a->reuse_idx : reinterpret_cast<const int*>(ws),
+                   a->topk, a->sm_scale, a->out);
+  if (s != DSA_OK) return s;
+  if (!ws || ws_bytes < dsa_decode_step_workspace_size(a) || (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return DSA_ERR_WORKSPACE;
+  if (g->T == 0) return DSA_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* p = reinterpret_cast<uint8_t*>(ws);
+  int* err = reinterpret_cast<int*>(ws);
+  p += kHeaderBytes;
+  const int32_t* idx = a->reuse_idx;
+  if (!idx) {
+    float* scores = reinterpret_cast<float*>(p);
+    p += align_up((size_t)g->T * stride * sizeof(float), 256);
+    int32_t* idx_buf = a->idx_out;
+    if (!idx_buf) {
+      idx_buf = reinterpret_cast<int32_t*>(p);
+      p += align_up((size_t)g->T * a->topk * sizeof(int32_t), 256);
+    }
+    s = run_indexer(g, a->qk_dtype, a->Hi, a->q_idx, a->q_scale, a->w, a->idx_k_cache, a->idx_k_scale, scores, stride,
+                    err, st);
+    if (s != DSA_OK) return s;
+    s = from_cuda(topk_launch(to_dev(g), scores, stride, a->topk, idx_buf, p, err, st));
+    if (s != DSA_OK) return s;
+    idx = idx_buf;
+  }
+  return run_attend(g, a->kv_dtype, a->H, a->q, a->kv_cache, idx, a->topk, a->sm_scale, a->out, a->lse, p, err, st);
+}
+
+dsa_status_t dsa_get_error(void* ws, void* stream) {
+  if (!ws) return DSA_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return from_cuda(e, "cudaStreamSynchronize");
+  int code = 0;
+  e = cudaMemcpy(&code, ws, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return from_cuda(e, "cudaMemcpy");
+  if (code != 0) {
+    e = cudaMemset(ws, 0, sizeof(int));
+    if (e != cudaSuccess) return from_cuda(e, "cudaMemset");
+  }
+  return static_cast<dsa_status_t>(code);
+}
+
+dsa_status_t dsa_clear_error(void* ws, void* stream) {
+  if (!ws) return DSA_ERR_INVALID_ARG;
+  return from_cuda(cudaMemsetAsync(ws, 0, kHeaderBytes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

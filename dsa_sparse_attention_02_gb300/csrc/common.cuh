@@ -1,0 +1,84 @@
+// Geometry shared by the kernels: flattened varlen queries over paged caches.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+#include "ptx.cuh"
+
+namespace dsa {
+
+constexpr int kPage = 64;
+constexpr int kDimIdx = 128;      // indexer head dim
+constexpr int kDimLatent = 512;   // latent (value) width
+constexpr int kDimRope = 64;
+constexpr int kDimQK = 576;       // 512 latent + 64 RoPE
+constexpr int kFp8Record = 656;   // e4m3 latent record bytes per token
+
+struct GeomDev {
+  int B, T, max_seq_len, num_pages, bt_stride;
+  const int* seq_lens;
+  const int* cu_q;
+  const int* block_table;
+};
+
+// Request of flattened query t: the largest b with cu_q[b] <= t (binary search).
+__device__ __forceinline__ int query_request(const GeomDev& g, int t) {
+  int lo = 0, hi = g.B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(g.cu_q + mid) <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+struct QueryInfo {
+  int b;      // request
+  int pos;    // causal position; keys 0..pos are visible
+  int len;    // seq_lens[b]
+  bool ok;    // geometry consistent
+};
+
+__device__ __forceinline__ QueryInfo query_info(const GeomDev& g, int t) {
+  QueryInfo qi;
+  qi.b = query_request(g, t);
+  const int q0 = __ldg(g.cu_q + qi.b), q1 = __ldg(g.cu_q + qi.b + 1);
+  qi.len = __ldg(g.seq_lens + qi.b);
+  qi.pos = qi.len - (q1 - q0) + (t - q0);
+  qi.ok = (t >= q0) && (t < q1) && (qi.len <= g.max_seq_len) && (qi.pos >= 0) &&
+          (qi.pos < qi.len);
+  return qi;
+}
+
+// Physical row (page*64 + s%64) of request b's logical token s, or -1 if the page id
+// is out of range.
+__device__ __forceinline__ int64_t physical_row(const GeomDev& g, int b, int s) {
+  const int page = __ldg(g.block_table + (int64_t)b * g.bt_stride + (s >> 6));
+  if (page < 0 || page >= g.num_pages) return -1;
+  return (int64_t)page * kPage + (s & 63);
+}
+
+// Static balanced split of `n` work items over `g` CTAs: CTA c owns
+// [floor(c*n/g), floor((c+1)*n/g)). owner(x) is the CTA holding item x.
+__host__ __device__ __forceinline__ int64_t split_begin(int64_t c, int64_t n, int64_t g) {
+  return (c * n) / g;
+}
+__host__ __device__ __forceinline__ int64_t split_owner(int64_t x, int64_t n, int64_t g) {
+  return ((x + 1) * g - 1) / n;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Named barrier among `count` threads (a multiple of 32) of the CTA.
+__device__ __forceinline__ void named_bar(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+}  // namespace dsa

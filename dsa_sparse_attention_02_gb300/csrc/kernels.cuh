@@ -1,0 +1,51 @@
+// Internal interface between the host API layer and the kernel files.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include "common.cuh"
+
+namespace dsa {
+
+// ---- lightning indexer (indexer.cu)
+struct IndexerArgs {
+  GeomDev g;
+  int Hi;
+  const float* q_scale;   // [T, Hi] or null (bf16)
+  const float* w;         // [T, Hi]
+  const float* k_scale;   // [P*64] or null (bf16)
+  float* scores;
+  int64_t stride;
+  int* err;
+};
+cudaError_t indexer_launch(bool fp8, int Hi, bool multi_query, const CUtensorMap& mk, const CUtensorMap& mq,
+                           const IndexerArgs& A, int grid, cudaStream_t st);
+int indexer_max_requests();
+
+// ---- radix top-k (topk.cu)
+size_t topk_workspace_bytes(int T, int max_seq_len, int k);
+cudaError_t topk_launch(const GeomDev& g, const float* scores, int64_t stride, int k, int* idx,
+                        void* scratch, int* err, cudaStream_t st);
+
+// ---- sparse MLA + combine (sparse_mla.cu)
+struct MlaArgs {
+  GeomDev g;
+  int H;               // total heads
+  int k;               // idx row length
+  int C;               // chunks per query
+  int64_t n_chunks;    // T * C
+  const uint8_t* kv;   // paged latent cache
+  const int* idx;      // [T, k]
+  float scale_log2;    // sm_scale * log2(e)
+  __nv_bfloat16* out;  // [T, H, 512]
+  float* lse;          // [T, H] or null
+  float* o_part;       // [T + G, H, 512]
+  float* ml_part;      // [T + G, H, 2]  (running max in log2 units, sum)
+  int* err;
+};
+int mla_grid(int64_t n_chunks, int num_sms);
+size_t mla_partial_bytes(int T, int H, int grid);
+cudaError_t mla_launch(bool fp8_kv, const CUtensorMap& map_q, MlaArgs A, int grid, cudaStream_t st);
+
+}  // namespace dsa

@@ -1,0 +1,276 @@
+// Radix top-k over fp32 score rows (the "radix top-k" of lmdeploy
+// "feat: support GLM-5.2", Changes; negative-index padding per lmdeploy
+// "glm5.3-flash support", Operator-level gains).
+//
+// One CTA of 1024 threads per row segment of at most 16384 entries, held in
+// registers (entry e is item e/1024 of thread e%1024). Scores map to 32-bit keys
+// whose unsigned order is the float order (-0 folded onto +0). Four 8-bit MSB-first
+// passes build a shared-memory histogram of the keys still matching the prefix
+// (warp-aggregated with match.any) and narrow the prefix to the bin holding the
+// k-th largest key; the passes stop early once that bin is taken whole. An
+// element is then taken if its masked key is above the prefix, or equal to it and
+// among the first `rem` equal ones by position (ties to the lower position). The
+// output positions come from one ordered ballot/prefix scan, so indices leave in
+// ascending order.
+//
+// Rows longer than one CTA's capacity are split into chunks whose exact top-k
+// (with their keys) become candidates; a second pass over the concatenated
+// candidates, which are in ascending original position, gives the row's top-k.
+// Any element of the row's top-k is in its chunk's top-k, so this is exact.
+#include <cstdint>
+#include "kernels.cuh"
+
+namespace dsa {
+
+constexpr int kTopkThreads = 1024;
+constexpr int kTopkItems = 16;
+constexpr int kTopkCapacity = kTopkThreads * kTopkItems;  // 16384
+
+__device__ __forceinline__ uint32_t orderable_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;  // -0 == +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+struct TopkLaunch {
+  GeomDev g;
+  int k;
+  int mode;                // 0: scores -> final idx; 1: scores chunk -> candidates; 2: candidates -> final idx
+  const float* scores;     // modes 0, 1
+  int64_t score_stride;
+  int chunk;               // mode 1: chunk length; mode 2: unused
+  int nchunks;             // mode 1: chunks per row; mode 2: candidate chunks per row (row len = nchunks*k)
+  const uint32_t* cand_key_in;   // mode 2
+  const int* cand_idx_in;        // mode 2
+  uint32_t* cand_key_out;        // mode 1
+  int* cand_idx_out;             // mode 1
+  int* idx_out;                  // modes 0, 2: [T, k]
+  int* err;
+};
+
+__global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkLaunch L) {
+  __shared__ int hist[256];
+  __shared__ int sel_bin, sel_above, sel_cnt;
+  __shared__ int wt_gt[kTopkItems][32], wt_eq[kTopkItems][32];
+  __shared__ int row_len_s;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int t, c = 0;
+  if (L.mode == 1) { t = blockIdx.x / L.nchunks; c = blockIdx.x % L.nchunks; }
+  else t = blockIdx.x;
+
+  if (tid == 0) {
+    int n;
+    if (L.mode == 2) {
+      // A row with no more valid keys than k keeps all of them: its candidates are
+      // exactly positions 0..pos, so it takes the short path below with n = pos+1.
+      const QueryInfo qi = query_info(L.g, t);
+      const int valid = qi.ok ? qi.pos + 1 : 0;
+      n = valid <= L.k ? valid : L.nchunks * L.k;
+    } else {
+      const QueryInfo qi = query_info(L.g, t);
+      if (!qi.ok) { record_error(L.err, kDevBadIndex); n = 0; }
+      else n = qi.pos + 1;
+      if (L.mode == 1) n = max(0, min(L.chunk, n - c * L.chunk));
+    }
+    row_len_s = n;
+  }
+  __syncthreads();
+  const int n = row_len_s;
+  const int k = L.k;
+
+  // Where the row's entries and outputs live.
+  const int64_t in_base = (L.mode == 0) ? (int64_t)t * L.score_stride
+                        : (L.mode == 1) ? (int64_t)t * L.score_stride + (int64_t)c * L.chunk
+                                        : (int64_t)t * L.nchunks * k;
+  const int64_t out_base = (L.mode == 1) ? ((int64_t)t * L.nchunks + c) * k : (int64_t)t * k;
+  const int idx_offset = (L.mode == 1) ? c * L.chunk : 0;
+
+  if (n <= k) {
+    // Everything valid is taken; positions are already ascending.
+    for (int i = tid; i < k; i += kTopkThreads) {
+      if (L.mode == 1) {
+        const bool v = i < n;
+        L.cand_key_out[out_base + i] = v ? orderable_key(L.scores[in_base + i]) : 0u;
+        L.cand_idx_out[out_base + i] = v ? idx_offset + i : -1;
+      } else if (L.mode == 0) {
+        L.idx_out[out_base + i] = i < n ? i : -1;
+      } else {  // mode 2: the first chunk's candidates are positions 0..n-1 in order
+        L.idx_out[out_base + i] = i < n ? L.cand_idx_in[in_base + i] : -1;
+      }
+    }
+    return;
+  }
+
+  // ---- load keys (n > k here, n <= capacity)
+  uint32_t key[kTopkItems];
+  uint32_t valid_bits = 0;
+#pragma unroll
+  for (int i = 0; i < kTopkItems; ++i) {
+    const int e = i * kTopkThreads + tid;
+    key[i] = 0u;
+    if (e < n) {
+      if (L.mode == 2) {
+        key[i] = L.cand_key_in[in_base + e];
+        if (L.cand_idx_in[in_base + e] >= 0) valid_bits |= 1u << i;
+      } else {
+        key[i] = orderable_key(L.scores[in_base + e]);
+        valid_bits |= 1u << i;
+      }
+    }
+  }
+
+  // ---- radix passes
+  uint32_t prefix = 0u, pmask = 0u;
+  int rem = k;
+#pragma unroll 1
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    if (tid < 256) hist[tid] = 0;
+    if (tid == 0) { sel_bin = 0; sel_above = 0; sel_cnt = -1; }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kTopkItems; ++i) {
+      const bool cand = ((valid_bits >> i) & 1u) && ((key[i] & pmask) == prefix);
+      const uint32_t bin = cand ? ((key[i] >> shift) & 0xFFu) : 0x100u;
+      const unsigned peers = __match_any_sync(0xffffffffu, bin);
+      if (cand && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+    }
+    __syncthreads();
+    if (warp == 0) {
+      int cnt[8], s = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) { cnt[j] = hist[255 - 8 * lane - j]; s += cnt[j]; }
+      int incl = s;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      const int excl = incl - s;
+      if (excl < rem && rem <= incl) {
+        int acc = excl;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (acc + cnt[j] >= rem) {
+            sel_bin = 255 - 8 * lane - j; sel_above = acc; sel_cnt = cnt[j];
+            break;
+          }
+          acc += cnt[j];
+        }
+      }
+    }
+    __syncthreads();
+    rem -= sel_above;
+    prefix |= (uint32_t)sel_bin << shift;
+    pmask |= 0xFFu << shift;
+    const bool whole = (sel_cnt == rem);
+    __syncthreads();   // sel_* are rewritten by the next pass
+    if (whole) break;
+  }
+
+  // ---- ordered compaction: ranks among "above" and "equal" elements
+#pragma unroll
+  for (int i = 0; i < kTopkItems; ++i) {
+    const bool v = (valid_bits >> i) & 1u;
+    const uint32_t m = key[i] & pmask;
+    const unsigned gb = __ballot_sync(0xffffffffu, v && m > prefix);
+    const unsigned eb = __ballot_sync(0xffffffffu, v && m == prefix);
+    if (lane == 0) { wt_gt[i][warp] = __popc(gb); wt_eq[i][warp] = __popc(eb); }
+  }
+  __syncthreads();
+  if (warp < 2) {
+    // Exclusive scan of the per-(item, warp) counts in (item, warp) order, which is
+    // position order; warp 0 scans the "above" counts, warp 1 the "equal" counts.
+    int (*tab)[32] = warp == 0 ? wt_gt : wt_eq;
+    int lv[16], sv = 0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int e = lane * 16 + j;
+      lv[j] = tab[e >> 5][e & 31];
+      sv += lv[j];
+    }
+    int iv = sv;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, iv, o);
+      if (lane >= o) iv += v;
+    }
+    int av = iv - sv;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int e = lane * 16 + j;
+      tab[e >> 5][e & 31] = av;
+      av += lv[j];
+    }
+  }
+  __syncthreads();
+  const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+  for (int i = 0; i < kTopkItems; ++i) {
+    const bool v = (valid_bits >> i) & 1u;
+    const uint32_t m = key[i] & pmask;
+    const bool is_gt = v && m > prefix, is_eq = v && m == prefix;
+    const unsigned gb = __ballot_sync(0xffffffffu, is_gt);
+    const unsigned eb = __ballot_sync(0xffffffffu, is_eq);
+    if (!is_gt && !is_eq) continue;
+    const int rg = wt_gt[i][warp] + __popc(gb & lt);
+    const int re = wt_eq[i][warp] + __popc(eb & lt);
+    if (is_eq && re >= rem) continue;
+    const int pos = rg + min(re, rem);
+    const int e = i * kTopkThreads + tid;
+    if (L.mode == 1) {
+      L.cand_key_out[out_base + pos] = key[i];
+      L.cand_idx_out[out_base + pos] = idx_offset + e;
+    } else if (L.mode == 0) {
+      L.idx_out[out_base + pos] = e;
+    } else {
+      L.idx_out[out_base + pos] = L.cand_idx_in[in_base + e];
+    }
+  }
+}
+
+// Host-side launch sequence (called from the API layer). Returns a cudaError_t.
+struct TopkPlan {
+  int levels;      // 1: direct; 2: chunks + merge
+  int chunk;
+  int nchunks;
+};
+
+TopkPlan topk_plan(int max_seq_len, int k) {
+  TopkPlan p;
+  if (max_seq_len <= kTopkCapacity) { p.levels = 1; p.chunk = 0; p.nchunks = 1; return p; }
+  p.levels = 2;
+  p.chunk = kTopkCapacity;
+  p.nchunks = (max_seq_len + kTopkCapacity - 1) / kTopkCapacity;
+  return p;
+}
+
+size_t topk_workspace_bytes(int T, int max_seq_len, int k) {
+  const TopkPlan p = topk_plan(max_seq_len, k);
+  if (p.levels == 1) return 0;
+  return (size_t)T * p.nchunks * k * (sizeof(uint32_t) + sizeof(int));
+}
+
+cudaError_t topk_launch(const GeomDev& g, const float* scores, int64_t stride, int k, int* idx,
+                        void* scratch, int* err, cudaStream_t st) {
+  const TopkPlan p = topk_plan(g.max_seq_len, k);
+  TopkLaunch L{};
+  L.g = g; L.k = k; L.scores = scores; L.score_stride = stride; L.idx_out = idx; L.err = err;
+  if (p.levels == 1) {
+    L.mode = 0;
+    topk_kernel<<<g.T, kTopkThreads, 0, st>>>(L);
+    return cudaGetLastError();
+  }
+  uint32_t* ck = reinterpret_cast<uint32_t*>(scratch);
+  int* ci = reinterpret_cast<int*>(ck + (size_t)g.T * p.nchunks * k);
+  L.mode = 1; L.chunk = p.chunk; L.nchunks = p.nchunks; L.cand_key_out = ck; L.cand_idx_out = ci;
+  topk_kernel<<<g.T * p.nchunks, kTopkThreads, 0, st>>>(L);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  L.mode = 2; L.cand_key_in = ck; L.cand_idx_in = ci;
+  topk_kernel<<<g.T, kTopkThreads, 0, st>>>(L);
+  return cudaGetLastError();
+}
+
+}  // namespace dsa

@@ -1,0 +1,192 @@
+/*
+ * dsa.h -- C ABI of the GB300 (sm_103a) DSA sparse-attention step.
+ *
+ * The step (DeepSeek-V3.2-style DSA as used by GLM-5.2 decode and MTP verify):
+ *   1. lightning indexer   I[t,s] = sum_h w[t,h] * ReLU(q[t,h,:] . k[s,:])
+ *      over every cached index key s <= pos(t) of the query's request
+ *      (mlx-lm "GLM-5.2 (glm_moe_dsa) inference", IndexShare commit, names the
+ *      lightning indexer; lmdeploy "feat: support GLM-5.2", Changes: "DSA indexing");
+ *   2. radix top-k         the index_topk largest I[t,s], ties to the lower s,
+ *      ascending, -1 padded when fewer keys are causally valid
+ *      (lmdeploy "feat: support GLM-5.2", Changes: radix top-k; lmdeploy
+ *      "glm5.3-flash support", Operator-level gains: negative-index padding;
+ *      mlx-lm small-L gather commit: re-masking when fewer than K keys are valid);
+ *   3. sparse absorbed MLA over the selected 576-wide latent rows (512 latent +
+ *      64 RoPE), value = the 512 latent columns, read straight from the paged
+ *      cache (lmdeploy "feat: support GLM-5.2", Five-layer ablations: zero-copy
+ *      BF16 sparse MLA; FP8 sparse FlashMLA cache path);
+ *   IndexShare: a shared layer reuses the previous full layer's selection and
+ *      skips steps 1-2 (mlx-lm IndexShare commit; lmdeploy shared top-k reuse).
+ *
+ * Conventions common to every entry point
+ *   - Pointers named "device" must be device memory of the current CUDA device;
+ *     the library never dereferences them on the host. All device buffers are
+ *     owned by the caller; the library allocates no device memory, keeps no
+ *     device state, and never synchronizes except in dsa_get_error().
+ *   - `stream` is a cudaStream_t passed as void*; all work is enqueued on it.
+ *   - Paged caches hold 64-token pages; page p holds tokens p*64 .. p*64+63 of
+ *     whatever request maps it. Request b's logical token s lives in page
+ *     block_table[b*bt_stride + s/64], row s%64.
+ *   - Query positions: query j (0-based) of request b sits at position
+ *     pos = seq_lens[b] - n_b + j with n_b = cu_q[b+1]-cu_q[b]; seq_lens counts
+ *     the cached tokens including the query tokens' own keys. Keys 0..pos are
+ *     visible to it.
+ *   - Workspace: every entry point takes `ws`/`ws_bytes`, device memory of at
+ *     least the size its *_workspace_size() function returns, 256-byte aligned.
+ *     Its first 256 bytes hold the device error word; zero them once before
+ *     first use (dsa_clear_error). Calls on the same workspace must be ordered
+ *     on one stream.
+ *   - Host-side argument errors return DSA_ERR_INVALID_ARG / DSA_ERR_UNSUPPORTED
+ *     / DSA_ERR_WORKSPACE before anything is enqueued. Zero work (T == 0) is a
+ *     no-op returning DSA_OK. Launch failures return DSA_ERR_CUDA.
+ *   - Device-side data errors (a page id outside [0, num_pages), seq_lens or
+ *     cu_q inconsistent with the host sizes, a selected index outside the
+ *     request) never fault: the offending element is skipped and the error word
+ *     is set to DSA_ERR_BAD_INDEX; a bounded wait that expires sets
+ *     DSA_ERR_TIMEOUT. dsa_get_error() reports either.
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DSA_ABI_VERSION 1
+
+typedef enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1,
+  DSA_ERR_UNSUPPORTED = 2,
+  DSA_ERR_CUDA = 3,
+  DSA_ERR_TIMEOUT = 4,
+  DSA_ERR_WORKSPACE = 5,
+  DSA_ERR_BAD_INDEX = 6
+} dsa_status_t;
+
+typedef enum { DSA_BF16 = 0, DSA_E4M3 = 1 } dsa_dtype_t;
+
+/* Request geometry shared by every entry point. */
+typedef struct {
+  int32_t B;                  /* requests, >= 0                                      */
+  int32_t T;                  /* flattened query tokens = cu_q[B], >= 0              */
+  int32_t max_seq_len;        /* host upper bound on every seq_lens[b], >= 1         */
+  int32_t num_pages;          /* physical pages in each paged cache, >= 1            */
+  int32_t page_size;          /* must be 64                                          */
+  int32_t bt_stride;          /* int32 elements between block-table rows,
+                                 >= ceil(max_seq_len/64)                             */
+  const int32_t* seq_lens;    /* device [B]    cached tokens incl. the query tokens  */
+  const int32_t* cu_q;        /* device [B+1]  query-token offsets, cu_q[0] = 0      */
+  const int32_t* block_table; /* device [B, bt_stride] physical page ids             */
+} dsa_geom_t;
+
+/*
+ * dsa_indexer_scores -- step 1 (lightning indexer).
+ *   qk_dtype DSA_E4M3: q_idx [T, Hi, 128] e4m3 bytes, q_scale [T, Hi] fp32,
+ *     idx_k_cache [num_pages, 64, 128] e4m3 bytes, idx_k_scale [num_pages, 64] fp32
+ *     (one scale per token); the scores use q = code*q_scale, k = code*k_scale.
+ *   qk_dtype DSA_BF16: q_idx [T, Hi, 128] bf16, idx_k_cache [num_pages, 64, 128]
+ *     bf16; q_scale and idx_k_scale must be NULL.
+ *   w [T, Hi] fp32 head weights. 1 <= Hi <= 64.
+ *   scores [T, score_stride] fp32 (device, written): for query t and s <= pos(t),
+ *     scores[t*score_stride + s] = I[t,s]; entries pos(t) < s < seq_len are set to
+ *     -inf; entries s >= seq_len are not written. score_stride >= max_seq_len.
+ *   All pointers device, 16-byte aligned; the caches are contiguous.
+ */
+dsa_status_t dsa_indexer_scores(const dsa_geom_t* geom, dsa_dtype_t qk_dtype, int32_t Hi,
+                                const void* q_idx, const float* q_scale, const float* w,
+                                const void* idx_k_cache, const float* idx_k_scale,
+                                float* scores, int64_t score_stride,
+                                void* ws, size_t ws_bytes, void* stream);
+size_t dsa_indexer_scores_workspace_size(const dsa_geom_t* geom);
+
+/*
+ * dsa_topk -- step 2 (radix top-k), exact.
+ *   scores [T, score_stride] fp32 (device, read): row t is read at s = 0..pos(t) only.
+ *   idx [T, k] int32 (device, written): the min(k, pos(t)+1) positions with the
+ *     largest scores, ties broken toward the lower position, in ascending order,
+ *     followed by -1 up to k. -0.0 and +0.0 compare equal. Scores must not be NaN.
+ *   1 <= k <= 16384.
+ */
+dsa_status_t dsa_topk(const dsa_geom_t* geom, const float* scores, int64_t score_stride,
+                      int32_t k, int32_t* idx, void* ws, size_t ws_bytes, void* stream);
+size_t dsa_topk_workspace_size(const dsa_geom_t* geom, int32_t k);
+
+/*
+ * dsa_sparse_mla_attend -- step 3 (absorbed MLA over the selected latent rows).
+ *   q [T, H, 576] bf16 (device): the absorbed query (W_UK already folded in).
+ *   kv_dtype DSA_BF16: kv_cache [num_pages, 64, 576] bf16.
+ *   kv_dtype DSA_E4M3: kv_cache [num_pages, 64, 656] bytes per token: 512 e4m3
+ *     latent codes, 4 little-endian fp32 scales (latent element 128c+e is
+ *     code*scale[c]), 64 bf16 RoPE values.
+ *   idx [T, k] int32 (device): logical positions of the request's tokens; -1 is
+ *     padding and is skipped.
+ *   For each (t, h): z_i = sm_scale * q[t,h,:] . kv[s_i,:] over the selected s_i,
+ *     out[t,h,:] = sum_i softmax(z)_i * kv[s_i, 0:512]  (bf16, [T, H, 512], device)
+ *     lse[t,h]   = ln(sum_i exp(z_i))                    (fp32, [T, H], device, or NULL)
+ *   An all-padding row gives out = 0 and lse = -inf.
+ *   H: 1..16 or a multiple of 16 up to 128. 1 <= k <= 16384.
+ */
+dsa_status_t dsa_sparse_mla_attend(const dsa_geom_t* geom, dsa_dtype_t kv_dtype, int32_t H,
+                                   const void* q, const void* kv_cache, const int32_t* idx,
+                                   int32_t k, float sm_scale, void* out, float* lse,
+                                   void* ws, size_t ws_bytes, void* stream);
+size_t dsa_sparse_mla_attend_workspace_size(const dsa_geom_t* geom, int32_t H, int32_t k);
+
+/* Arguments of the fused step. */
+typedef struct {
+  dsa_geom_t geom;
+  int32_t topk;                /* index_topk, 1..16384                                  */
+  /* indexer inputs (ignored when reuse_idx != NULL) */
+  dsa_dtype_t qk_dtype;
+  int32_t Hi;
+  const void* q_idx;
+  const float* q_scale;
+  const float* w;
+  const void* idx_k_cache;
+  const float* idx_k_scale;
+  /* IndexShare: a shared layer passes the full layer's selection here [T, topk] */
+  const int32_t* reuse_idx;
+  /* optional output of the selection [T, topk] (for the next shared layers) */
+  int32_t* idx_out;
+  /* attention inputs and outputs */
+  dsa_dtype_t kv_dtype;
+  int32_t H;
+  const void* q;
+  const void* kv_cache;
+  float sm_scale;
+  void* out;                   /* [T, H, 512] bf16   */
+  float* lse;                  /* [T, H] fp32 or NULL */
+} dsa_step_args_t;
+
+/*
+ * dsa_decode_step -- the fused DSA step on one stream: indexer -> top-k ->
+ *   sparse MLA (+ split combine), or, with reuse_idx != NULL (IndexShare), the
+ *   sparse MLA alone over reuse_idx. No host synchronization; the enqueued work
+ *   depends only on the host fields of `args`, so it can be captured in a CUDA
+ *   graph. Scores and (when idx_out is NULL) the selection live in `ws`.
+ */
+dsa_status_t dsa_decode_step(const dsa_step_args_t* args, void* ws, size_t ws_bytes,
+                             void* stream);
+size_t dsa_decode_step_workspace_size(const dsa_step_args_t* args);
+
+/* Synchronizes `stream`, reads the device error word of `ws` (DSA_OK if none)
+ * and clears it. Returns DSA_ERR_CUDA if the stream itself reports an error. */
+dsa_status_t dsa_get_error(void* ws, void* stream);
+/* Enqueues a clear of the error word of `ws` on `stream`. */
+dsa_status_t dsa_clear_error(void* ws, void* stream);
+
+const char* dsa_status_string(dsa_status_t status);
+/* Text describing the last failure seen by an entry point on the calling host
+ * thread (the failing call and its CUDA error), or "" if none. Owned by the
+ * library; valid until the next entry-point call on the same thread. */
+const char* dsa_last_error(void);
+int32_t dsa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSA_H_ */

@@ -1,0 +1,100 @@
+"""The C-ABI library loads and exports every function include/dsa.h declares; host-side
+argument validation answers before anything reaches a GPU (no compute calls here)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+import dsa_sparse_attention_02_gb300 as dsa
+from dsa_sparse_attention_02_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dsa.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsa_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(_lib.LIB_PATH):
+        from dsa_sparse_attention_02_gb300 import build
+        build.build()
+    return _lib.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(_lib.EXPORTED) == names
+
+
+def test_abi_version_and_status_strings(lib):
+    assert dsa.dsa_abi_version() == 1
+    assert _lib.status_string(0) == "ok"
+    assert "invalid" in _lib.status_string(1)
+
+
+def _geom(**kw):
+    g = dict(B=1, T=1, max_seq_len=128, num_pages=4, page_size=64, bt_stride=2,
+             seq_lens=1, cu_q=1, block_table=1)       # dummy non-null pointers: never dereferenced
+    g.update(kw)
+    return _lib.dsa_geom_t(g["B"], g["T"], g["max_seq_len"], g["num_pages"], g["page_size"],
+                           g["bt_stride"], g["seq_lens"], g["cu_q"], g["block_table"])
+
+
+def _topk(lib, g, k=8, scores=16, idx=16, ws=256, ws_bytes=1 << 20):
+    return lib.dsa_topk(C.byref(g), scores, g.max_seq_len, k, idx, ws, ws_bytes, None)
+
+
+def test_host_validation(lib):
+    assert lib.dsa_topk(None, 16, 128, 8, 16, 256, 1 << 20, None) == _lib.DSA_ERR_INVALID_ARG
+    assert _topk(lib, _geom(page_size=32)) == _lib.DSA_ERR_UNSUPPORTED
+    assert _topk(lib, _geom(), k=0) == _lib.DSA_ERR_INVALID_ARG
+    assert _topk(lib, _geom(), k=20000) == _lib.DSA_ERR_INVALID_ARG
+    assert _topk(lib, _geom(bt_stride=1)) == _lib.DSA_ERR_INVALID_ARG
+    assert _topk(lib, _geom(), scores=None) == _lib.DSA_ERR_INVALID_ARG
+    assert _topk(lib, _geom(), ws=None) == _lib.DSA_ERR_WORKSPACE
+    assert _topk(lib, _geom(), ws=260) == _lib.DSA_ERR_WORKSPACE          # misaligned
+    assert _topk(lib, _geom(max_seq_len=200000, bt_stride=4000), k=4096) == _lib.DSA_ERR_UNSUPPORTED
+    # zero work: OK without touching the device
+    assert _topk(lib, _geom(T=0)) == _lib.DSA_OK
+    g = _geom()
+    # indexer: Hi out of range, bf16 with a scale pointer, misaligned cache
+    assert lib.dsa_indexer_scores(C.byref(g), _lib.DSA_E4M3, 65, 16, 16, 16, 16, 16, 16, 128, 256,
+                                  4096, None) == _lib.DSA_ERR_INVALID_ARG
+    assert lib.dsa_indexer_scores(C.byref(g), _lib.DSA_BF16, 4, 16, 16, 16, 16, None, 16, 128, 256,
+                                  4096, None) == _lib.DSA_ERR_INVALID_ARG
+    assert lib.dsa_indexer_scores(C.byref(g), _lib.DSA_E4M3, 4, 16, 16, 16, 24, 16, 16, 128, 256,
+                                  4096, None) == _lib.DSA_ERR_INVALID_ARG
+    assert lib.dsa_indexer_scores(C.byref(g), _lib.DSA_E4M3, 4, 16, 16, 16, 16, 16, 16, 64, 256,
+                                  4096, None) == _lib.DSA_ERR_INVALID_ARG   # stride < max_seq_len
+    # attention: unsupported head count, bad dtype, non-finite scale
+    assert lib.dsa_sparse_mla_attend(C.byref(g), _lib.DSA_BF16, 24, 16, 16, 16, 64, 0.1, 16, None,
+                                     256, 1 << 24, None) == _lib.DSA_ERR_INVALID_ARG
+    assert lib.dsa_sparse_mla_attend(C.byref(g), 7, 16, 16, 16, 16, 64, 0.1, 16, None,
+                                     256, 1 << 24, None) == _lib.DSA_ERR_INVALID_ARG
+    assert lib.dsa_sparse_mla_attend(C.byref(g), _lib.DSA_BF16, 16, 16, 16, 16, 64, float("inf"),
+                                     16, None, 256, 1 << 24, None) == _lib.DSA_ERR_INVALID_ARG
+    assert lib.dsa_get_error(None, None) == _lib.DSA_ERR_INVALID_ARG
+
+
+def test_workspace_sizes_are_consistent(lib):
+    g = _geom(T=64, B=64, max_seq_len=131072, bt_stride=2048)
+    assert lib.dsa_topk_workspace_size(C.byref(g), 2048) >= 256 + 64 * 8 * 2048 * 8
+    g2 = _geom(T=64, B=64, max_seq_len=8192, bt_stride=128)
+    assert lib.dsa_topk_workspace_size(C.byref(g2), 2048) == 256
+    a = _lib.dsa_step_args_t()
+    a.geom = g2
+    a.topk = 2048
+    a.H = 16
+    base = lib.dsa_decode_step_workspace_size(C.byref(a))
+    assert base >= 256 + 64 * 8192 * 4 + 64 * 2048 * 4
+    a.reuse_idx = 16
+    assert lib.dsa_decode_step_workspace_size(C.byref(a)) < base

@@ -1,0 +1,110 @@
+"""dsa_sparse_mla_attend on the GPU against the float64 oracle over the same index rows."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dsa_sparse_attention_02_gb300 import _lib, inputs, runner
+from gpu_helpers import DEV, assert_close
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"bf16": 2e-2, "e4m3": 5e-2}
+
+
+def _random_idx(rng, wl, k, pad_frac=0.1, empty_rows=()):
+    _, pos = oracle.query_positions(wl.seq_lens, wl.n_q)
+    idx = np.full((wl.T, k), -1, dtype=np.int32)
+    for t in range(wl.T):
+        if t in empty_rows:
+            continue
+        n = min(k, int(pos[t]) + 1)
+        sel = rng.choice(int(pos[t]) + 1, size=n, replace=False)
+        if rng.random() < 0.5:
+            sel = np.sort(sel)
+        row = np.full(k, -1, dtype=np.int32)
+        row[:n] = sel
+        drop = rng.random(k) < pad_frac               # scattered -1 padding
+        row[drop] = -1
+        idx[t] = row
+    return idx
+
+
+def _attend(wl, dw, layer, idx_np, k):
+    L = dw.layers[layer]
+    idx = torch.from_numpy(idx_np).to(DEV)
+    out = torch.full_like(L.out, float("nan"))
+    lse = torch.full_like(L.lse, float("nan"))
+    ws = _lib.workspace(_lib.dsa_sparse_mla_attend_workspace_size(dw.geom, L.q.shape[1], k), DEV)
+    _lib.dsa_sparse_mla_attend(dw.geom, L.kv_dtype, L.q, L.kv, idx, k, wl.sm_scale, out, lse, ws)
+    assert _lib.dsa_get_error(ws) == 0
+    return out.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def _check(wl, layer, idx_np, out, lse, ts=None):
+    lay = wl.layers[layer]
+    ts = range(wl.T) if ts is None else ts
+    ref = oracle.sparse_mla(lay.q, lay.kv, lay.kv_dtype, {t: idx_np[t] for t in ts}, wl.seq_lens,
+                            wl.n_q, wl.block_table, wl.sm_scale, ts)
+    tol = TOL[lay.kv_dtype]
+    worst = 0.0
+    for t in ts:
+        o_ref, l_ref = ref[t]
+        worst = max(worst, assert_close(out[t], o_ref, tol, tol, f"out t={t}"))
+        assert_close(lse[t], l_ref, tol, tol, f"lse t={t}")
+    return worst
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
+@pytest.mark.parametrize("k", [64, 200, 2048])
+def test_attend_random_selections(kv_dtype, k):
+    rng = np.random.default_rng(k)
+    wl = inputs.make_workload("attn", [300, 1000, 2500, 4100], [1, 2, 1, 3], topk=k, hi=4,
+                              qk_dtype="bf16", kv_dtypes=(kv_dtype,), seed=31)
+    dw = runner.DeviceWorkload(wl, DEV)
+    idx = _random_idx(rng, wl, k, empty_rows=(1,))
+    out, lse = _attend(wl, dw, 0, idx, k)
+    worst = _check(wl, 0, idx, out, lse)
+    assert np.all(out[1] == 0) and np.all(np.isneginf(lse[1]))      # all-padding row
+    print(f"{kv_dtype} k={k}: max |O err| {worst:.3g}")
+
+
+@pytest.mark.parametrize("heads", [8, 32])
+def test_attend_head_counts(heads):
+    rng = np.random.default_rng(heads)
+    wl = inputs.make_workload("attn", [700, 3000], [2, 1], topk=512, hi=4, qk_dtype="bf16",
+                              kv_dtypes=("bf16",), heads=heads, seed=32)
+    dw = runner.DeviceWorkload(wl, DEV)
+    idx = _random_idx(rng, wl, 512)
+    out, lse = _attend(wl, dw, 0, idx, 512)
+    _check(wl, 0, idx, out, lse)
+
+
+def test_attend_many_queries_split_over_ctas():
+    # 300 queries x 16 chunks: most queries are split across CTAs and merged by the combine
+    rng = np.random.default_rng(7)
+    wl = inputs.make_workload("attn", [6000] * 3, [100] * 3, topk=2048, hi=4, qk_dtype="bf16",
+                              kv_dtypes=("bf16",), seed=33)
+    dw = runner.DeviceWorkload(wl, DEV)
+    idx = _random_idx(rng, wl, 2048, pad_frac=0.02)
+    out, lse = _attend(wl, dw, 0, idx, 2048)
+    _check(wl, 0, idx, out, lse, ts=list(range(0, wl.T, 13)))
+
+
+def test_attend_indices_outside_request_are_skipped_and_reported():
+    rng = np.random.default_rng(8)
+    wl = inputs.make_workload("attn", [500, 900], [1, 1], topk=128, hi=4, qk_dtype="bf16",
+                              kv_dtypes=("bf16",), seed=34)
+    dw = runner.DeviceWorkload(wl, DEV)
+    idx = _random_idx(rng, wl, 128, pad_frac=0.0)
+    bad = idx.copy()
+    bad[0, 5] = 10_000                                  # beyond seq_lens[0]
+    L = dw.layers[0]
+    ws = _lib.workspace(_lib.dsa_sparse_mla_attend_workspace_size(dw.geom, 16, 128), DEV)
+    _lib.dsa_sparse_mla_attend(dw.geom, L.kv_dtype, L.q, L.kv, torch.from_numpy(bad).to(DEV), 128,
+                               wl.sm_scale, L.out, L.lse, ws)
+    assert _lib.dsa_get_error(ws) == _lib.DSA_ERR_BAD_INDEX
+    assert _lib.dsa_get_error(ws) == 0                  # reading clears it
+    skipped = bad.copy()
+    skipped[0, 5] = -1
+    _check(wl, 0, skipped, L.out.float().cpu().numpy(), L.lse.cpu().numpy())

@@ -1,0 +1,144 @@
+"""dsa_decode_step end to end on the GPU: index sets and attention against the oracle
+on every configuration (reduced and full size, sampled queries at full size),
+IndexShare reuse, determinism and CUDA-graph capture."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dsa_sparse_attention_02_gb300 import _lib, inputs, runner
+from gpu_helpers import DEV, assert_close, index_set_parity
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"bf16": 2e-2, "e4m3": 5e-2}
+
+
+def _verify(wl, dw, ts):
+    idx = dw.idx.cpu().numpy()
+    ref_scores = oracle.indexer_scores(wl.q_idx, wl.q_scale, wl.w, wl.idx_k, wl.idx_k_scale,
+                                       wl.qk_dtype, wl.seq_lens, wl.n_q, wl.block_table, ts)
+    for t in ts:
+        ok, msg = index_set_parity(idx[t], ref_scores[t], wl.topk)
+        assert ok, (t, msg)
+    sel = {t: idx[t] for t in ts}
+    for li, (lay, dl) in enumerate(zip(wl.layers, dw.layers)):
+        ref = oracle.sparse_mla(lay.q, lay.kv, lay.kv_dtype, sel, wl.seq_lens, wl.n_q,
+                                wl.block_table, wl.sm_scale, ts)
+        out = dl.out.float().cpu().numpy()
+        lse = dl.lse.cpu().numpy()
+        tol = TOL[lay.kv_dtype]
+        for t in ts:
+            assert_close(out[t], ref[t][0], tol, tol, f"layer {li} out t={t}")
+            assert_close(lse[t], ref[t][1], tol, tol, f"layer {li} lse t={t}")
+
+
+SMALL = [
+    ("tiny", dict()),
+    ("decode", dict(batch=6)),
+    ("mtp", dict(batch=3, ctx_scale=0.25)),
+    ("prefill", dict(ctx_scale=1 / 8)),
+    ("longctx", dict(batch=2, ctx_scale=1 / 16)),
+]
+
+
+@pytest.mark.parametrize("name,kw", SMALL, ids=[c[0] for c in SMALL])
+def test_step_small_configs(name, kw):
+    wl = inputs.make_config(name, **kw)
+    dw = runner.DeviceWorkload(wl, DEV)
+    dw.step()
+    torch.cuda.synchronize()
+    assert dw.check_error() == 0
+    ts = list(range(wl.T)) if wl.T <= 64 else list(np.linspace(0, wl.T - 1, 16).astype(int))
+    _verify(wl, dw, ts)
+
+
+FULL = [
+    ("decode", 64),   # the bench configuration: every query checked
+    ("mtp", 10),
+    ("prefill", 8),
+    ("longctx", 4),
+]
+
+
+@pytest.mark.parametrize("name,nsample", FULL, ids=[c[0] for c in FULL])
+def test_step_full_size_sampled(name, nsample):
+    wl = inputs.make_config(name)
+    dw = runner.DeviceWorkload(wl, DEV)
+    dw.step()
+    torch.cuda.synchronize()
+    assert dw.check_error() == 0
+    ts = list(np.unique(np.linspace(0, wl.T - 1, nsample).astype(int)))
+    _verify(wl, dw, ts)
+
+
+def test_indexshare_layer_reuses_full_layer_selection():
+    wl = inputs.make_config("mtp", batch=2, ctx_scale=0.3)
+    dw = runner.DeviceWorkload(wl, DEV)
+    dw.step()
+    torch.cuda.synchronize()
+    idx = dw.idx.clone()
+    out1 = dw.layers[1].out.clone()
+    # layer 1 alone through the standalone entry point over layer 0's selection
+    L = dw.layers[1]
+    out = torch.empty_like(L.out)
+    ws = _lib.workspace(_lib.dsa_sparse_mla_attend_workspace_size(dw.geom, 16, wl.topk), DEV)
+    _lib.dsa_sparse_mla_attend(dw.geom, L.kv_dtype, L.q, L.kv, idx, wl.topk, wl.sm_scale, out, None, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out1)
+    # a shared-layer step leaves the selection untouched and reproduces layer 1
+    a = _lib.make_step_args(dw.geom, wl.topk, reuse_idx=idx, kv_dtype=L.kv_dtype, q=L.q, kv_cache=L.kv,
+                            sm_scale=wl.sm_scale, out=out, lse=None)
+    ws2 = _lib.workspace(_lib.dsa_decode_step_workspace_size(a), DEV)
+    _lib.dsa_decode_step(a, ws2)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out1) and torch.equal(idx, dw.idx)
+
+
+def test_step_is_deterministic_and_graph_capturable():
+    wl = inputs.make_config("decode", batch=8)
+    dw = runner.DeviceWorkload(wl, DEV)
+    dw.step()
+    torch.cuda.synchronize()
+    idx0, out0, lse0 = dw.idx.clone(), dw.layers[0].out.clone(), dw.layers[0].lse.clone()
+    dw.step()
+    torch.cuda.synchronize()
+    assert torch.equal(idx0, dw.idx) and torch.equal(out0, dw.layers[0].out)
+    assert torch.equal(lse0, dw.layers[0].lse)
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        dw.step()
+    torch.cuda.current_stream().wait_stream(s)
+    dw.layers[0].out.zero_()
+    dw.idx.zero_()
+    with torch.cuda.graph(graph):
+        dw.step()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(idx0, dw.idx) and torch.equal(out0, dw.layers[0].out)
+    assert dw.check_error() == 0
+
+
+def test_causality_on_gpu():
+    # rewriting every key and latent row after the first query's position changes nothing for it
+    wl = inputs.make_config("mtp", batch=1, ctx_scale=0.3)
+    dw = runner.DeviceWorkload(wl, DEV)
+    dw.step()
+    torch.cuda.synchronize()
+    idx0 = dw.idx[0].clone()
+    out0 = dw.layers[0].out[0].clone()
+    _, pos = oracle.query_positions(wl.seq_lens, wl.n_q)
+    p0 = int(pos[0])
+    rows = oracle.physical_rows(wl.block_table[0], np.arange(p0 + 1, int(wl.seq_lens[0])))
+    wl2 = inputs.Workload(**{**wl.__dict__})
+    wl2.idx_k = wl.idx_k.copy()
+    wl2.idx_k.reshape(-1, 128)[rows] = np.uint8(0x48)
+    kv = wl.layers[0].kv.copy()
+    kv.reshape(-1, kv.shape[-1])[rows] = np.uint8(0x48)
+    wl2.layers = [inputs.Layer(q=wl.layers[0].q, kv=kv, kv_dtype=wl.layers[0].kv_dtype), wl.layers[1]]
+    dw2 = runner.DeviceWorkload(wl2, DEV)
+    dw2.step()
+    torch.cuda.synchronize()
+    assert torch.equal(idx0, dw2.idx[0]) and torch.equal(out0, dw2.layers[0].out[0])

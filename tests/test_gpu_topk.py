@@ -1,0 +1,90 @@
+"""dsa_topk on the GPU is bit-exact against the oracle's top-k of the same fp32 rows."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dsa_sparse_attention_02_gb300 import _lib, inputs
+from gpu_helpers import DEV, geometry_for_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(rows, lengths, k):
+    lengths = np.asarray(lengths)
+    g = geometry_for_rows(lengths)
+    stride = int(-(-lengths.max() // 4) * 4)
+    sc = np.full((len(lengths), stride), np.float32(7.0e30), dtype=np.float32)   # junk past each row
+    for t, r in enumerate(rows):
+        sc[t, : len(r)] = r
+    scores = torch.from_numpy(sc).to(DEV)
+    idx = torch.full((len(lengths), k), -7, dtype=torch.int32, device=DEV)
+    ws = _lib.workspace(_lib.dsa_topk_workspace_size(g, k), DEV)
+    _lib.dsa_topk(g, scores, k, idx, ws)
+    assert _lib.dsa_get_error(ws) == 0
+    got = idx.cpu().numpy()
+    for t, r in enumerate(rows):
+        exp = oracle.topk_row(np.asarray(r, dtype=np.float32).astype(np.float64), k)
+        assert np.array_equal(got[t], exp), (t, len(r), k)
+
+
+def test_random_rows_many_lengths():
+    rng = np.random.default_rng(1)
+    lengths = [1, 5, 63, 64, 65, 2047, 2048, 2049, 3000, 5000, 8192, 12345, 16384]
+    rows = [rng.standard_normal(n).astype(np.float32) for n in lengths]
+    _run(rows, lengths, 2048)
+    _run(rows, lengths, 64)
+    _run(rows, lengths, 1)
+
+
+def test_exact_ties_and_signed_zero():
+    rng = np.random.default_rng(2)
+    rows = [
+        inputs.tied_scores(rng, 1, 10000, k=2048)[0],
+        rng.integers(-3, 4, size=9000).astype(np.float32),          # massive ties
+        np.zeros(5000, dtype=np.float32),                           # all equal
+        np.where(rng.random(6000) < 0.5, np.float32(0.0), np.float32(-0.0)),
+        np.concatenate([np.full(3000, 2.5, np.float32), np.full(3000, -1.0, np.float32)]),
+        rng.standard_normal(7000).astype(np.float32) * np.float32(1e-30),   # subnormal-range values
+        np.concatenate([rng.standard_normal(4000).astype(np.float32) * 1e30,
+                        np.float32([3.0e38, -3.0e38, 3.0, -3.0])]),
+    ]
+    _run(rows, [len(r) for r in rows], 2048)
+
+
+def test_k_equal_to_and_just_below_row_length():
+    rng = np.random.default_rng(3)
+    rows = [rng.standard_normal(16384).astype(np.float32), rng.standard_normal(2048).astype(np.float32)]
+    _run(rows, [16384, 2048], 2048)
+    _run(rows[:1], [16384], 16384)
+    _run(rows[:1], [16384], 16383)
+
+
+def test_long_rows_two_level_with_ties():
+    rng = np.random.default_rng(5)
+    # the long-context top-k workload: 131072 scores ~N(0,1) with 1% injected exact ties,
+    # including several copies of the k-th value
+    rows = list(inputs.tied_scores(rng, 3, 131072, k=2048))
+    rows += [rng.standard_normal(16385).astype(np.float32), rng.standard_normal(40000).astype(np.float32),
+             rng.integers(0, 5, size=100000).astype(np.float32), rng.standard_normal(300).astype(np.float32)]
+    _run(rows, [len(r) for r in rows], 2048)
+
+
+def test_rows_longer_than_context_are_read_only_up_to_position():
+    # multi-query requests: row t reads only s <= pos(t)
+    rng = np.random.default_rng(6)
+    L, nq, k = 3000, 4, 2048
+    sc = rng.standard_normal((nq, L)).astype(np.float32)
+    seq = torch.tensor([L], dtype=torch.int32, device=DEV)
+    cu = torch.tensor([0, nq], dtype=torch.int32, device=DEV)
+    bt = torch.zeros(1, (L + 63) // 64, dtype=torch.int32, device=DEV)
+    g = _lib.Geometry(seq, cu, bt, num_pages=bt.shape[1], max_seq_len=L, T=nq)
+    scores = torch.from_numpy(sc).to(DEV)
+    idx = torch.empty(nq, k, dtype=torch.int32, device=DEV)
+    ws = _lib.workspace(_lib.dsa_topk_workspace_size(g, k), DEV)
+    _lib.dsa_topk(g, scores, k, idx, ws)
+    got = idx.cpu().numpy()
+    for j in range(nq):
+        pos = L - nq + j
+        exp = oracle.topk_row(sc[j, : pos + 1].astype(np.float64), k)
+        assert np.array_equal(got[j], exp)
