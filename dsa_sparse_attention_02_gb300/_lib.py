@@ -21,7 +21,7 @@ DSA_BF16, DSA_E4M3 = 0, 1
 EXPORTED = (
     "dsa_indexer_scores", "dsa_indexer_scores_workspace_size",
     "dsa_topk", "dsa_topk_workspace_size",
-    "dsa_sparse_mla_attend", "dsa_sparse_mla_attend_workspace_size",
+    "dsa_sparse_mla_attend", "dsa_sparse_mla_attend_workspace_size", "dsa_sparse_mla_attend_static",
     "dsa_decode_step", "dsa_decode_step_workspace_size",
     "dsa_get_error", "dsa_clear_error", "dsa_status_string", "dsa_last_error", "dsa_abi_version",
 )
@@ -31,7 +31,7 @@ class DsaError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
         detail = ""
-        if status == DSA_ERR_CUDA:
+        if status in (DSA_ERR_CUDA, DSA_ERR_WORKSPACE):
             try:
                 detail = " [" + load().dsa_last_error().decode() + "]"
             except ImportError:
@@ -77,6 +77,7 @@ def load(path: str = LIB_PATH):
         "dsa_topk_workspace_size": (SZ, [G, I32]),
         "dsa_sparse_mla_attend": (C.c_int, [G, C.c_int, I32, P, P, P, I32, F, P, P, P, SZ, P]),
         "dsa_sparse_mla_attend_workspace_size": (SZ, [G, I32, I32]),
+        "dsa_sparse_mla_attend_static": (C.c_int, [G, C.c_int, I32, P, P, P, I32, F, P, P, P, P]),
         "dsa_decode_step": (C.c_int, [S, P, SZ, P]),
         "dsa_decode_step_workspace_size": (SZ, [S]),
         "dsa_get_error": (C.c_int, [P, P]),
@@ -176,6 +177,17 @@ def dsa_sparse_mla_attend(geom: Geometry, kv_dtype: int, q, kv_cache, idx, k: in
                                       int(k), float(sm_scale), _ptr(out), _ptr(lse),
                                       _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "dsa_sparse_mla_attend")
+
+
+def dsa_sparse_mla_attend_static(geom: Geometry, kv_dtype: int, q, kv_cache, idx, k: int,
+                                 sm_scale: float, out, lse, err_word=None, stream=None):
+    """dsa_sparse_mla_attend without a workspace, for callers that cannot allocate device
+    memory at call time; its partials use the library's static per-GPU buffer."""
+    H = int(q.shape[1])
+    st = load().dsa_sparse_mla_attend_static(geom.ref, kv_dtype, H, _ptr(q), _ptr(kv_cache), _ptr(idx),
+                                             int(k), float(sm_scale), _ptr(out), _ptr(lse),
+                                             _ptr(err_word), _stream(stream))
+    _check(st, "dsa_sparse_mla_attend_static")
 
 
 def make_step_args(geom: Geometry, topk: int, *, qk_dtype=DSA_E4M3, q_idx=None, q_scale=None,

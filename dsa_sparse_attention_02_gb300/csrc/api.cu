@@ -13,30 +13,12 @@
 
 using namespace dsa;
 
-namespace {
-
-constexpr size_t kHeaderBytes = 256;
-constexpr int kMaxTopk = 16384;
-constexpr int kTopkCap = 16384;
+namespace dsa {
 
 thread_local char g_last_error[256] = "";
 
-void set_error(const char* what, const char* detail) {
+void set_last_error(const char* what, const char* detail) {
   snprintf(g_last_error, sizeof(g_last_error), "%s: %s", what, detail);
-}
-
-size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-int num_sms() {
-  static int cache[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
-  int n = 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-  if (dev >= 0 && dev < 64) cache[dev] = n;
-  return n;
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -56,10 +38,10 @@ EncodeTiledFn encode_fn() {
 }
 
 // 2-D row-major tensor [rows, cols] with a 128-byte-swizzled box of box_cols x box_rows.
-bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t cols, uint64_t rows,
+bool encode_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t cols, uint64_t rows,
                uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();
-  if (!fn) { set_error("cudaGetDriverEntryPointByVersion", "cuTensorMapEncodeTiled unavailable"); return false; }
+  if (!fn) { set_last_error("cudaGetDriverEntryPointByVersion", "cuTensorMapEncodeTiled unavailable"); return false; }
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {row_bytes};
   cuuint32_t box[2] = {box_cols, box_rows};
@@ -71,10 +53,32 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_
     char buf[96];
     snprintf(buf, sizeof(buf), "CUresult %d (dims %llu x %llu, box %u x %u)", (int)r, (unsigned long long)cols,
              (unsigned long long)rows, box_cols, box_rows);
-    set_error("cuTensorMapEncodeTiled", buf);
+    set_last_error("cuTensorMapEncodeTiled", buf);
     return false;
   }
   return true;
+}
+
+}  // namespace dsa
+
+namespace {
+
+constexpr size_t kHeaderBytes = 256;
+constexpr int kMaxTopk = 16384;
+constexpr int kTopkCap = 16384;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
 }
 
 dsa_status_t check_geom(const dsa_geom_t* g) {
@@ -97,7 +101,7 @@ GeomDev to_dev(const dsa_geom_t* g) {
 
 dsa_status_t from_cuda(cudaError_t e, const char* what = "kernel launch") {
   if (e == cudaSuccess) return DSA_OK;
-  set_error(what, cudaGetErrorString(e));
+  set_last_error(what, cudaGetErrorString(e));
   return DSA_ERR_CUDA;
 }
 
@@ -126,8 +130,8 @@ dsa_status_t run_indexer(const dsa_geom_t* g, dsa_dtype_t dt, int Hi, const void
   const CUtensorMapDataType tdt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const uint32_t box_cols = fp8 ? 128 : 64;
   const uint64_t row_bytes = fp8 ? 128 : 256;
-  if (!encode_2d(&mk, tdt, kc, 128, (uint64_t)g->num_pages * 64, row_bytes, box_cols, 64)) return DSA_ERR_CUDA;
-  if (!encode_2d(&mq, tdt, q_idx, 128, (uint64_t)g->T * Hi, row_bytes, box_cols, (uint32_t)Hi)) return DSA_ERR_CUDA;
+  if (!encode_tensor_map_2d(&mk, tdt, kc, 128, (uint64_t)g->num_pages * 64, row_bytes, box_cols, 64)) return DSA_ERR_CUDA;
+  if (!encode_tensor_map_2d(&mq, tdt, q_idx, 128, (uint64_t)g->T * Hi, row_bytes, box_cols, (uint32_t)Hi)) return DSA_ERR_CUDA;
   IndexerArgs A;
   A.g = to_dev(g); A.Hi = Hi; A.q_scale = q_scale; A.w = w; A.k_scale = ks; A.scores = scores; A.stride = stride;
   A.err = err;
@@ -175,7 +179,7 @@ dsa_status_t run_attend(const dsa_geom_t* g, dsa_dtype_t dt, int H, const void* 
                         int k, float sm_scale, void* out, float* lse, void* scratch, int* err, cudaStream_t st) {
   CUtensorMap mq;
   const uint32_t box_rows = H < 16 ? (uint32_t)H : 16u;
-  if (!encode_2d(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, 576, (uint64_t)g->T * H, 1152, 64, box_rows))
+  if (!encode_tensor_map_2d(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, 576, (uint64_t)g->T * H, 1152, 64, box_rows))
     return DSA_ERR_CUDA;
   MlaArgs A;
   A.g = to_dev(g); A.H = H; A.k = k; A.C = (k + 127) / 128; A.n_chunks = (int64_t)g->T * A.C;

@@ -48,4 +48,9 @@ int mla_grid(int64_t n_chunks, int num_sms);
 size_t mla_partial_bytes(int T, int H, int grid);
 cudaError_t mla_launch(bool fp8_kv, const CUtensorMap& map_q, MlaArgs A, int grid, cudaStream_t st);
 
+// ---- host helpers defined in api.cu
+bool encode_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t cols,
+                          uint64_t rows, uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows);
+void set_last_error(const char* what, const char* detail);
+
 }  // namespace dsa

@@ -136,6 +136,33 @@ dsa_status_t dsa_sparse_mla_attend(const dsa_geom_t* geom, dsa_dtype_t kv_dtype,
                                    void* ws, size_t ws_bytes, void* stream);
 size_t dsa_sparse_mla_attend_workspace_size(const dsa_geom_t* geom, int32_t H, int32_t k);
 
+/*
+ * dsa_sparse_mla_attend_static -- dsa_sparse_mla_attend for callers that cannot
+ *   provide device memory at call time: a runtime that plans and reserves all of
+ *   its device memory up front, a plugin host that offers no workspace, or code
+ *   at a point where an allocation would synchronize the device or disturb a
+ *   memory pool. It takes no workspace and allocates nothing; the split-softmax
+ *   partials live in a library-owned static device buffer of
+ *   DSA_STATIC_SCRATCH_BYTES per GPU, which every GPU that loads the library
+ *   holds until the process exits. (The pages have no counterpart to this entry
+ *   point.)
+ *   Arguments, layouts and results are those of dsa_sparse_mla_attend, except:
+ *   err_word: optional device int32 (NULL allowed) that receives device-side data
+ *     errors (DSA_ERR_BAD_INDEX, DSA_ERR_TIMEOUT); the caller zeroes it.
+ *   The call needs (T + G) * H * 2056 bytes of the buffer (G = min(SM count,
+ *   T * ceil(k/128))); a larger call returns DSA_ERR_WORKSPACE and
+ *   dsa_last_error() says how much was needed.
+ *   The first call on a device looks up the buffer's address on that device;
+ *   make that first call before any stream capture. Every call shares the buffer
+ *   and it keeps the last call's contents (nothing in it must start at zero);
+ *   calls whose work overlaps on the GPU race on it.
+ */
+#define DSA_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
+dsa_status_t dsa_sparse_mla_attend_static(const dsa_geom_t* geom, dsa_dtype_t kv_dtype, int32_t H,
+                                          const void* q, const void* kv_cache, const int32_t* idx,
+                                          int32_t k, float sm_scale, void* out, float* lse,
+                                          int32_t* err_word, void* stream);
+
 /* Arguments of the fused step. */
 typedef struct {
   dsa_geom_t geom;
