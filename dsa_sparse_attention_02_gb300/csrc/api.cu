@@ -59,6 +59,11 @@ bool encode_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* ba
   return true;
 }
 
+bool encode_mla_q_map(CUtensorMap* map_q, const void* q, int T, int H) {
+  const uint32_t box_rows = H < 16 ? (uint32_t)H : 16u;
+  return encode_tensor_map_2d(map_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, 576, (uint64_t)T * H, 1152, 64, box_rows);
+}
+
 }  // namespace dsa
 
 namespace {
@@ -178,9 +183,7 @@ size_t attend_scratch_bytes(const dsa_geom_t* g, int H, int k) {
 dsa_status_t run_attend(const dsa_geom_t* g, dsa_dtype_t dt, int H, const void* q, const void* kv, const int* idx,
                         int k, float sm_scale, void* out, float* lse, void* scratch, int* err, cudaStream_t st) {
   CUtensorMap mq;
-  const uint32_t box_rows = H < 16 ? (uint32_t)H : 16u;
-  if (!encode_tensor_map_2d(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, 576, (uint64_t)g->T * H, 1152, 64, box_rows))
-    return DSA_ERR_CUDA;
+  if (!encode_mla_q_map(&mq, q, g->T, H)) return DSA_ERR_CUDA;
   MlaArgs A;
   A.g = to_dev(g); A.H = H; A.k = k; A.C = (k + 127) / 128; A.n_chunks = (int64_t)g->T * A.C;
   A.kv = reinterpret_cast<const uint8_t*>(kv); A.idx = idx; A.scale_log2 = sm_scale * 1.4426950408889634f;

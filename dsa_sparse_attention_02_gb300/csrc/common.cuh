@@ -48,6 +48,33 @@ __device__ __forceinline__ QueryInfo query_info(const GeomDev& g, int t) {
   return qi;
 }
 
+// query_info computed by a whole warp: the request search probes 32 entries of
+// cu_q per round (one round for B <= 32, two for B <= 1024) instead of a serial
+// binary search. Every lane returns the same result.
+__device__ __forceinline__ QueryInfo query_info_warp(const GeomDev& g, int t) {
+  const int lane = threadIdx.x & 31;
+  int lo = 0, n = g.B;                       // answer in [lo, lo + n)
+  while (n > 32) {
+    const int step = (n + 31) / 32;
+    const int idx = lo + lane * step;
+    const bool le = idx < lo + n && __ldg(g.cu_q + idx) <= t;
+    const unsigned m = __ballot_sync(0xffffffffu, le);
+    const int last = m ? 31 - __clz(m) : 0;
+    lo += last * step;
+    n = min(step, n - last * step);
+  }
+  const int idx = lo + lane;
+  const bool le = lane < n && __ldg(g.cu_q + idx) <= t;
+  const unsigned m = __ballot_sync(0xffffffffu, le);
+  QueryInfo qi;
+  qi.b = lo + (m ? 31 - __clz(m) : 0);
+  const int q0 = __ldg(g.cu_q + qi.b), q1 = __ldg(g.cu_q + qi.b + 1);
+  qi.len = __ldg(g.seq_lens + qi.b);
+  qi.pos = qi.len - (q1 - q0) + (t - q0);
+  qi.ok = (t >= q0) && (t < q1) && (qi.len <= g.max_seq_len) && (qi.pos >= 0) && (qi.pos < qi.len);
+  return qi;
+}
+
 // Physical row (page*64 + s%64) of request b's logical token s, or -1 if the page id
 // is out of range.
 __device__ __forceinline__ int64_t physical_row(const GeomDev& g, int b, int s) {

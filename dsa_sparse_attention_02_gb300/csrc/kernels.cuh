@@ -46,7 +46,9 @@ struct MlaArgs {
 };
 int mla_grid(int64_t n_chunks, int num_sms);
 size_t mla_partial_bytes(int T, int H, int grid);
+// map_q: [T*H, 576] bf16 query rows, 64 x min(H,16) box, 128-byte swizzle.
 cudaError_t mla_launch(bool fp8_kv, const CUtensorMap& map_q, MlaArgs A, int grid, cudaStream_t st);
+bool encode_mla_q_map(CUtensorMap* map_q, const void* q, int T, int H);
 
 // ---- host helpers defined in api.cu
 bool encode_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t cols,

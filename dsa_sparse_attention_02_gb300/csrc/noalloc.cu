@@ -88,9 +88,7 @@ extern "C" dsa_status_t dsa_sparse_mla_attend_static(const dsa_geom_t* geom, dsa
     return DSA_ERR_CUDA;
   }
   CUtensorMap mq;
-  if (!encode_tensor_map_2d(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, 576, (uint64_t)geom->T * H, 1152, 64,
-                            H < 16 ? (uint32_t)H : 16u))
-    return DSA_ERR_CUDA;
+  if (!encode_mla_q_map(&mq, q, geom->T, H)) return DSA_ERR_CUDA;
   A.g.B = geom->B; A.g.T = geom->T; A.g.max_seq_len = geom->max_seq_len; A.g.num_pages = geom->num_pages;
   A.g.bt_stride = geom->bt_stride; A.g.seq_lens = geom->seq_lens; A.g.cu_q = geom->cu_q;
   A.g.block_table = geom->block_table;

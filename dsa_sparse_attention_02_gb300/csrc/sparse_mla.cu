@@ -9,20 +9,32 @@
 //   out[t,h,:] = sum_i softmax(z)_i kv[s_i, 0:512],  lse[t,h] = ln sum_i exp(z_i)
 //
 // Work: the T x C list of (query, 128-key chunk) pairs, C = ceil(k/128), split
-// evenly over a persistent grid. Per chunk:
-//   * 3 producer warps resolve logical positions through the block table and
-//     gather the 128 selected rows straight from the paged cache into one
-//     128-byte-swizzled K-major tile (9 column atoms of 64 bf16): cp.async for
-//     bf16 rows; for e4m3 rows a load, dequantize (code * per-128 scale) and
-//     store of bf16. Padding rows are zero-filled.
-//   * one MMA thread computes S^T = KV . Q^T on tcgen05 (M = 128 keys, N = 16
-//     heads, K = 576) into TMEM, then, once P is ready, O^T = V^T . P^T (M = 128
-//     latent columns x 4 blocks, N = 16, K = 128 keys) reading V^T MN-major
-//     from the same smem tile.
-//   * 4 softmax warps (TMEM lane = key) run the online softmax per head in the
-//     exp2 domain, write P^T as bf16 into smem for the second MMA, and add the
-//     chunk's O^T (TMEM lane = latent column) into fp32 registers after
-//     rescaling.
+// evenly over a persistent grid. A chunk's 128 selected rows live in shared
+// memory as 128-byte-swizzled K-major atoms of 64 bf16 columns: four "pair"
+// slots of two atoms (latent columns 0..511) and one RoPE atom (512..575). The
+// slots form rings (5 pair slots, 2 RoPE slots), so the next chunk's RoPE atom
+// and first pair load while the current chunk computes, and its other pairs
+// load as soon as the current chunk's PV MMAs release theirs.
+//   * a resolver warp maps each chunk's 128 logical positions to physical cache
+//     rows through the block table (-1 for padding or out-of-range entries) up
+//     to four chunks ahead, into a shared-memory row table that the producer
+//     and the softmax warps read.
+//   * bf16 cache: two producer warps copy the rows with 16-byte cp.async, slot
+//     by slot (RoPE atom, then the four pairs), each warp half of every slot;
+//     padding rows are zero-filled. Each producer thread ends a slot with
+//     cp.async.mbarrier.arrive.noinc, so the slot's full barrier completes when
+//     the copies have landed and producers never wait on their own copies; the
+//     MMA thread fences the generic->async proxy after each wait. (TMA
+//     tile::gather4 of 4 x 128-byte row pieces measured at half the bandwidth
+//     of this on the same access pattern.)
+//   * e4m3 cache: three producer warps load the 656-byte records, dequantize
+//     (code * per-128 scale) to bf16 and store into the same slots.
+//   * one MMA thread: S^T = KV . Q^T on tcgen05 (M = 128 keys, N = 16 heads,
+//     K = 576) into TMEM, then O^T = V^T . P^T (M = 128 latent columns x 4
+//     blocks, N = 16, K = 128 keys), V^T read MN-major from the pair slots.
+//   * 4 softmax warps (TMEM lane = key for S, = latent column for O) run the
+//     online softmax per head in the exp2 domain, write P^T as bf16 for the
+//     second MMA, and accumulate O in fp32 registers.
 // A CTA that holds every chunk of a query writes the final bf16 output; other
 // segments write (unnormalized O, running max, sum) partials that the combine
 // kernel merges with log-sum-exp weights.
@@ -34,20 +46,26 @@ namespace dsa {
 
 constexpr int kMlaHeads = 16;                       // heads per CTA (MMA N)
 constexpr int kMlaKeys = 128;                       // keys per chunk (MMA M)
-constexpr int kKvAtomBytes = kMlaKeys * 128;        // 16 KB: 128 rows x 64 bf16
-constexpr int kKvTileBytes = 9 * kKvAtomBytes;      // 144 KB
+constexpr int kAtomBytes = kMlaKeys * 128;          // 16 KB: 128 rows x 64 bf16
+constexpr int kPairBytes = 2 * kAtomBytes;          // 32 KB
+constexpr int kPairSlots = 5;
+constexpr int kRopeSlots = 2;
 constexpr int kQAtomBytes = kMlaHeads * 128;        // 2 KB
 constexpr int kQBufBytes = 9 * kQAtomBytes;         // 18 KB
 constexpr int kPBufBytes = 2 * kQAtomBytes;         // P^T: 16 heads x 128 keys bf16 = 4 KB
-constexpr int kMlaSmemBytes = 1024 + kKvTileBytes + 2 * kQBufBytes + 2 * kPBufBytes;
-// 8 warps: 0-3 softmax (one per TMEM lane quarter), 4-6 producers, 7 MMA. Eight
-// warps put two on each SM sub-partition, which leaves room for ~200 registers.
+constexpr int kMlaSmemBytes =
+    1024 + kPairSlots * kPairBytes + kRopeSlots * kAtomBytes + kQBufBytes + 2 * kPBufBytes;
+// Warps 0-3 softmax (one per TMEM lane quarter), 4 and 6 producers with 5 the row
+// resolver (bf16), or 4-6 producers (e4m3); 7 MMA. Two warps per SM sub-partition
+// leave room for ~200 registers.
 constexpr int kMlaThreads = 256;
-constexpr int kProdWarps = 3;
+constexpr int kFp8ProdWarps = 3;
+constexpr int kBf16ProdWarps = 2;
+constexpr int kResolverWarp = 5;
 constexpr int kMmaWarp = 7;
+constexpr int kRowBufs = 4;                         // row-table ring depth (chunks)
 constexpr int kMlaTmemCols = 256;                   // S: 2 x 16, O: 2 x 64
 constexpr float kLn2 = 0.6931471805599453f;
-
 
 // Bounded group barrier over the 4 softmax warps (one arrive per warp).
 struct GroupSync {
@@ -86,20 +104,35 @@ struct ChunkPos {
   bool first, last;
 };
 
+// Physical cache row of the selected position at offset e of query t's index row,
+// or -1 for padding / out-of-range entries (reported).
+__device__ __forceinline__ int64_t selected_row(const MlaArgs& A, const QueryInfo& qi, int t, int e) {
+  if (!qi.ok || e >= A.k) return -1;
+  const int s = __ldg(A.idx + (int64_t)t * A.k + e);
+  if (s < 0) return -1;
+  const int64_t row = s < qi.len ? physical_row(A.g, qi.b, s) : -1;
+  if (row < 0) record_error(A.err, kDevBadIndex);
+  return row;
+}
+
 template <bool kFp8Kv>
 __global__ void __launch_bounds__(kMlaThreads, 1)
     sparse_mla_kernel(const __grid_constant__ CUtensorMap map_q, const MlaArgs A) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* kv_tile = smem;
-  uint8_t* q_buf = smem + kKvTileBytes;                 // 2 x 18 KB
-  uint8_t* p_buf = q_buf + 2 * kQBufBytes;              // 2 x 4 KB
+  uint8_t* pair_buf = smem;                                         // 5 x 32 KB
+  uint8_t* rope_buf = pair_buf + kPairSlots * kPairBytes;           // 2 x 16 KB
+  uint8_t* q_buf = rope_buf + kRopeSlots * kAtomBytes;              // 18 KB
+  uint8_t* p_buf = q_buf + kQBufBytes;                              // 2 x 4 KB
 
-  __shared__ uint64_t kv_full, kv_empty, q_full[2], q_empty[2];
+  __shared__ uint64_t pair_full[kPairSlots], pair_empty[kPairSlots], rope_full[kRopeSlots], rope_empty[kRopeSlots];
+  __shared__ uint64_t q_full, q_empty;
   __shared__ uint64_t s_full[2], s_empty[2], p_full[2], p_empty[2], o_full[2], o_empty[2], grp_bar;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
   __shared__ float red[2][4][kMlaHeads];
+  __shared__ __align__(16) int rows_s[kRowBufs][kMlaKeys];   // physical row per key of a chunk, -1 = none
+  __shared__ uint64_t rows_full[kRowBufs], rows_empty[kRowBufs];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const GeomDev& g = A.g;
@@ -109,6 +142,8 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
   const int64_t c_begin = split_begin(blockIdx.x, A.n_chunks, G);
   const int64_t c_end = split_begin(blockIdx.x + 1, A.n_chunks, G);
   const int n_mine = (int)(c_end - c_begin);
+  const int slot_producers = kFp8Kv ? kFp8ProdWarps : 32 * kBf16ProdWarps;   // arrivals per slot fill
+  const bool is_producer = kFp8Kv ? (warp >= 4 && warp < 4 + kFp8ProdWarps) : (warp == 4 || warp == 6);
 
   auto chunk_pos = [&](int i) {
     ChunkPos cp;
@@ -122,11 +157,11 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
 
   if (tid == 0) {
     abort_flag = 0;
-    mbar_init(smem_u32(&kv_full), kProdWarps * 32);
-    mbar_init(smem_u32(&kv_empty), 1);
+    for (int j = 0; j < kPairSlots; ++j) { mbar_init(smem_u32(&pair_full[j]), slot_producers); mbar_init(smem_u32(&pair_empty[j]), 1); }
+    for (int j = 0; j < kRopeSlots; ++j) { mbar_init(smem_u32(&rope_full[j]), slot_producers); mbar_init(smem_u32(&rope_empty[j]), 1); }
+    mbar_init(smem_u32(&q_full), 1);
+    mbar_init(smem_u32(&q_empty), 1);
     for (int j = 0; j < 2; ++j) {
-      mbar_init(smem_u32(&q_full[j]), 1);
-      mbar_init(smem_u32(&q_empty[j]), 1);
       mbar_init(smem_u32(&s_full[j]), 1);
       mbar_init(smem_u32(&s_empty[j]), 4);
       mbar_init(smem_u32(&p_full[j]), 4);
@@ -135,11 +170,16 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       mbar_init(smem_u32(&o_empty[j]), 4);
     }
     mbar_init(smem_u32(&grp_bar), 4);
+    for (int j = 0; j < kRowBufs; ++j) {
+      // bf16: written by the resolver warp, read by the producer and the 4 softmax warps;
+      // e4m3: written by the 3 producer warps, read by the softmax warps.
+      mbar_init(smem_u32(&rows_full[j]), kFp8Kv ? kFp8ProdWarps : 1);
+      mbar_init(smem_u32(&rows_empty[j]), kFp8Kv ? 4 : 4 + kBf16ProdWarps);
+    }
     fence_mbar_init();
   }
   // Query rows >= h_eff stay zero (TMA writes h_eff rows per atom).
-  for (int i = tid; i < 2 * kQBufBytes / 16; i += kMlaThreads)
-    reinterpret_cast<int4*>(q_buf)[i] = make_int4(0, 0, 0, 0);
+  for (int i = tid; i < kQBufBytes / 16; i += kMlaThreads) reinterpret_cast<int4*>(q_buf)[i] = make_int4(0, 0, 0, 0);
   fence_proxy_async_smem();
   if (warp == kMmaWarp) { tmem_alloc(smem_u32(&tmem_base_s), kMlaTmemCols); tmem_relinquish(); }
   tc_fence_before();
@@ -149,150 +189,245 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
   const uint32_t tmem_s = tmem;          // + 16 * buf
   const uint32_t tmem_o = tmem + 32;     // + 64 * buf, + 16 * mb
 
-  if (warp >= 4 && warp < 4 + kProdWarps) {
+  if (is_producer) {
     // ================================================================ producers
-    // Warp pw gathers rows [r0, r1) of the chunk (43, 43, 42 rows); lane l resolves
-    // rows r0 + l and r0 + 32 + l.
-    const int pw = warp - 4;
-    const int r0 = pw * 43, r1 = min(kMlaKeys, r0 + 43), nrows = r1 - r0;
+    const int pw = kFp8Kv ? warp - 4 : (warp == 4 ? 0 : 1);
     int seg = 0;
+    // Warp-uniform bounded wait (lane 0 waits, the result is broadcast).
+    auto slot_acquire = [&](uint32_t bar, uint32_t parity) -> bool {
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(bar, parity, &abort_flag, A.err) ? 1 : 0;
+      return __shfl_sync(0xffffffffu, ok, 0) != 0;
+    };
     for (int i = 0; i < n_mine; ++i) {
       const ChunkPos cp = chunk_pos(i);
       if (cp.first) {
-        const int qb = seg & 1;
-        if (pw == 0 && lane == 0) {
-          if (!mbar_wait(smem_u32(&q_empty[qb]), ((seg >> 1) & 1) ^ 1, &abort_flag, A.err)) break;
-          const uint32_t bar = smem_u32(&q_full[qb]);
-          mbar_arrive_expect_tx(bar, 9 * h_eff * 128);
-          for (int a = 0; a < 9; ++a)
-            tma_load_2d(smem_u32(q_buf + qb * kQBufBytes + a * kQAtomBytes), &map_q, bar, a * 64,
-                        cp.t * A.H + hg * kMlaHeads);
+        if (pw == 0) {
+          if (!slot_acquire(smem_u32(&q_empty), (seg & 1) ^ 1)) break;
+          if (lane == 0) {
+            const uint32_t bar = smem_u32(&q_full);
+            mbar_arrive_expect_tx(bar, 9 * h_eff * 128);
+            for (int a = 0; a < 9; ++a)
+              tma_load_2d(smem_u32(q_buf + a * kQAtomBytes), &map_q, bar, a * 64, cp.t * A.H + hg * kMlaHeads);
+          }
         }
         ++seg;
       }
-      // resolve this lane's two key rows
-      const QueryInfo qi = query_info(g, cp.t);
-      int64_t rowv[2] = {-1, -1};
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        const int r = r0 + h2 * 32 + lane;
-        const int e = cp.cq * kMlaKeys + r;
-        if (r < r1 && qi.ok && e < A.k) {
-          const int s = __ldg(A.idx + (int64_t)cp.t * A.k + e);
-          if (s >= 0) {
-            if (s < qi.len) rowv[h2] = physical_row(g, qi.b, s);
-            if (rowv[h2] < 0) record_error(A.err, kDevBadIndex);
-          }
-        }
-      }
-      if (!mbar_wait(smem_u32(&kv_empty), (i & 1) ^ 1, &abort_flag, A.err)) break;
+      const int rs = i % kRopeSlots;
       if (!kFp8Kv) {
-        const uint8_t* base = A.kv;
-        for (int j = 0; j < nrows; ++j) {
-          const int key = r0 + j;
-          const int64_t pr = __shfl_sync(0xffffffffu, j < 32 ? rowv[0] : rowv[1], j & 31);
-          const uint8_t* src = base + (pr >= 0 ? pr : 0) * (int64_t)(kDimQK * 2);
-          const uint32_t nbytes = pr >= 0 ? 16u : 0u;
+        const int rb = i % kRowBufs;
+        if (!slot_acquire(smem_u32(&rows_full[rb]), (i / kRowBufs) & 1)) break;
+        mbar_try_wait(smem_u32(&rows_full[rb]), (i / kRowBufs) & 1);   // acquire in every lane (phase is complete)
+        const int* rows = rows_s[rb];
+        const uint8_t* kv = A.kv;
+        bool stop = false;
+        // RoPE atom: 8 lanes per row (128 B), 4 rows per instruction; this warp's 64 rows
+        if (!slot_acquire(smem_u32(&rope_empty[rs]), ((i / kRopeSlots) & 1) ^ 1)) break;
+        {
+          const uint32_t dst0 = smem_u32(rope_buf + rs * kAtomBytes);
+#pragma unroll 4
+          for (int j = 0; j < 16; ++j) {
+            const int ri = 64 * pw + 4 * j + (lane >> 3);
+            const int row = rows[ri];
+            const int cb = (lane & 7) * 16;
+            cp_async_16(dst0 + sw128_offset(ri, cb, 0), kv + (int64_t)(row >= 0 ? row : 0) * (kDimQK * 2) + kDimLatent * 2 + cb,
+                        row >= 0 ? 16u : 0u);
+          }
+          cp_async_arrive_noinc(smem_u32(&rope_full[rs]));
+        }
+        // four pairs: 16 lanes per row (256 B), 2 rows per instruction
+        for (int j = 0; j < 4; ++j) {
+          const int gidx = 4 * i + j, ps = gidx % kPairSlots;
+          if (!slot_acquire(smem_u32(&pair_empty[ps]), ((gidx / kPairSlots) & 1) ^ 1)) { stop = true; break; }
+          const uint32_t dst0 = smem_u32(pair_buf + ps * kPairBytes);
+#pragma unroll 4
+          for (int jj = 0; jj < 32; ++jj) {
+            const int ri = 64 * pw + 2 * jj + (lane >> 4);
+            const int row = rows[ri];
+            const int cb = (lane & 15) * 16;
+            cp_async_16(dst0 + sw128_offset(ri, cb, kAtomBytes), kv + (int64_t)(row >= 0 ? row : 0) * (kDimQK * 2) + j * 256 + cb,
+                        row >= 0 ? 16u : 0u);
+          }
+          cp_async_arrive_noinc(smem_u32(&pair_full[ps]));
+        }
+        if (stop) break;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&rows_empty[rb]));
+      } else {
+        // e4m3 records: warp pw handles 4-row groups g4 = pw, pw+3, ...; 8 lanes per row,
+        // lane part p covers 16 latent codes of the pair and 16 bytes of the RoPE part.
+        const QueryInfo qi = query_info_warp(g, cp.t);
+        const int part = lane & 7, sub = lane >> 3;
+        constexpr int kMaxGroups = 11;
+        int64_t rrow[kMaxGroups];
+        int ng = 0;
 #pragma unroll
-          for (int part = 0; part < 3; ++part) {
-            const int c16 = part * 32 + lane;       // 16-byte chunk of the 1152-byte row
-            if (c16 < 72)
-              cp_async_16(smem_u32(kv_tile + sw128_offset(key, c16 * 16, kKvAtomBytes)), src + c16 * 16, nbytes);
+        for (int gi = 0; gi < kMaxGroups; ++gi) {
+          const int g4 = pw + kFp8ProdWarps * gi;
+          rrow[gi] = -1;
+          if (g4 < 32) {
+            rrow[gi] = selected_row(A, qi, cp.t, cp.cq * kMlaKeys + 4 * g4 + sub);
+            ng = gi + 1;
           }
         }
-        cp_async_commit();
-        cp_async_wait<0>();
-      } else {
-        // e4m3 record: 512 latent codes | 4 fp32 scales | 64 bf16 RoPE values
-        constexpr int kBatch = 8;
-        for (int j0 = 0; j0 < nrows; j0 += kBatch) {
-          uint4 lat[kBatch];
-          float sc[kBatch];
-          uint4 rope[kBatch];
+        bool stop = false;
+        // publish this warp's rows to the softmax warps' row table
+        {
+          const int rb = i % kRowBufs;
+          if (lane == 0 && !mbar_wait(smem_u32(&rows_empty[rb]), ((i / kRowBufs) & 1) ^ 1, &abort_flag, A.err))
+            abort_flag = 1;
+          __syncwarp();
+          if (abort_flag) break;
+          if (part == 0) {
 #pragma unroll
-          for (int jj = 0; jj < kBatch; ++jj) {
-            const int j = j0 + jj;
-            const int64_t pr = __shfl_sync(0xffffffffu, j < 32 ? rowv[0] : rowv[1], j & 31);
-            lat[jj] = make_uint4(0, 0, 0, 0); sc[jj] = 0.f; rope[jj] = make_uint4(0, 0, 0, 0);
-            if (j < nrows && pr >= 0) {
-              const uint8_t* rec = A.kv + pr * (int64_t)kFp8Record;
-              lat[jj] = __ldg(reinterpret_cast<const uint4*>(rec) + lane);
-              sc[jj] = __ldg(reinterpret_cast<const float*>(rec + kDimLatent) + (lane >> 3));
-              if (lane < 8) rope[jj] = __ldg(reinterpret_cast<const uint4*>(rec + kDimLatent + 16) + lane);
+            for (int gi = 0; gi < kMaxGroups; ++gi)
+              if (gi < ng) rows_s[rb][4 * (pw + kFp8ProdWarps * gi) + sub] = (int)rrow[gi];
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&rows_full[rb]));
+        }
+        // RoPE atom (plain copy of 16 bytes per lane)
+        if (lane == 0 && !mbar_wait(smem_u32(&rope_empty[rs]), ((i / kRopeSlots) & 1) ^ 1, &abort_flag, A.err))
+          abort_flag = 1;
+        __syncwarp();
+        if (abort_flag) break;
+        {
+          uint4 v[kMaxGroups];
+#pragma unroll
+          for (int gi = 0; gi < kMaxGroups; ++gi) {
+            v[gi] = make_uint4(0, 0, 0, 0);
+            if (gi < ng && rrow[gi] >= 0)
+              v[gi] = __ldg(reinterpret_cast<const uint4*>(A.kv + rrow[gi] * (int64_t)kFp8Record + kDimLatent + 16) + part);
+          }
+#pragma unroll
+          for (int gi = 0; gi < kMaxGroups; ++gi) {
+            if (gi >= ng) break;
+            const int key = 4 * (pw + kFp8ProdWarps * gi) + sub;
+            *reinterpret_cast<uint4*>(rope_buf + rs * kAtomBytes + sw128_offset(key, part * 16, 0)) = v[gi];
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&rope_full[rs]));
+        for (int j = 0; j < 4; ++j) {
+          const int gidx = 4 * i + j, ps = gidx % kPairSlots;
+          if (lane == 0 && !mbar_wait(smem_u32(&pair_empty[ps]), ((gidx / kPairSlots) & 1) ^ 1, &abort_flag, A.err))
+            abort_flag = 1;
+          __syncwarp();
+          if (abort_flag) { stop = true; break; }
+          uint4 c[kMaxGroups];
+          float sc[kMaxGroups];
+#pragma unroll
+          for (int gi = 0; gi < kMaxGroups; ++gi) {
+            c[gi] = make_uint4(0, 0, 0, 0);
+            sc[gi] = 0.f;
+            if (gi < ng && rrow[gi] >= 0) {
+              const uint8_t* rec = A.kv + rrow[gi] * (int64_t)kFp8Record;
+              c[gi] = __ldg(reinterpret_cast<const uint4*>(rec + 128 * j) + part);
+              sc[gi] = __ldg(reinterpret_cast<const float*>(rec + kDimLatent) + j);
             }
           }
+          uint8_t* slot = pair_buf + ps * kPairBytes;
 #pragma unroll
-          for (int jj = 0; jj < kBatch; ++jj) {
-            if (j0 + jj >= nrows) break;
-            const int key = r0 + j0 + jj;
-            const uint32_t w4[4] = {lat[jj].x, lat[jj].y, lat[jj].z, lat[jj].w};
-            uint32_t packed[8];
+          for (int gi = 0; gi < kMaxGroups; ++gi) {
+            if (gi >= ng) break;
+            const int key = 4 * (pw + kFp8ProdWarps * gi) + sub;
+            const uint32_t w4[4] = {c[gi].x, c[gi].y, c[gi].z, c[gi].w};
+            uint32_t pk[8];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const uint32_t wv = w4[q];
-              packed[2 * q] = pack_bf16x2(e4m3_to_f32(wv & 0xFF) * sc[jj], e4m3_to_f32((wv >> 8) & 0xFF) * sc[jj]);
-              packed[2 * q + 1] = pack_bf16x2(e4m3_to_f32((wv >> 16) & 0xFF) * sc[jj], e4m3_to_f32(wv >> 24) * sc[jj]);
+              pk[2 * q] = pack_bf16x2(e4m3_to_f32(wv & 0xFF) * sc[gi], e4m3_to_f32((wv >> 8) & 0xFF) * sc[gi]);
+              pk[2 * q + 1] = pack_bf16x2(e4m3_to_f32((wv >> 16) & 0xFF) * sc[gi], e4m3_to_f32(wv >> 24) * sc[gi]);
             }
-            // latent elements 16*lane .. 16*lane+15 = bytes 32*lane .. +31 of the bf16 row
-            uint8_t* d0 = kv_tile + sw128_offset(key, lane * 32, kKvAtomBytes);
-            uint8_t* d1 = kv_tile + sw128_offset(key, lane * 32 + 16, kKvAtomBytes);
-            *reinterpret_cast<uint4*>(d0) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-            *reinterpret_cast<uint4*>(d1) = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-            if (lane < 8)
-              *reinterpret_cast<uint4*>(kv_tile + sw128_offset(key, kDimLatent * 2 + lane * 16, kKvAtomBytes)) = rope[jj];
+            // pair column 16*part .. 16*part+15 -> atom part/4, bytes 32*(part%4) .. +31
+            const int col_byte = (part >> 2) * 128 + (part & 3) * 32;
+            *reinterpret_cast<uint4*>(slot + sw128_offset(key, col_byte, kAtomBytes)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            *reinterpret_cast<uint4*>(slot + sw128_offset(key, col_byte + 16, kAtomBytes)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
           }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&pair_full[ps]));
         }
+        if (stop) break;
       }
-      fence_proxy_async_smem();
-      mbar_arrive(smem_u32(&kv_full));
+    }
+  } else if (!kFp8Kv && warp == kResolverWarp) {
+    // ================================================================ row resolver (bf16)
+    int t_cached = -1;
+    QueryInfo qi{};
+    for (int i = 0; i < n_mine; ++i) {
+      const ChunkPos cp = chunk_pos(i);
+      if (cp.t != t_cached) { qi = query_info_warp(g, cp.t); t_cached = cp.t; }
+      const int rb = i % kRowBufs;
+      int rr[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) rr[m] = (int)selected_row(A, qi, cp.t, cp.cq * kMlaKeys + 4 * lane + m);
+      if (!mbar_wait(smem_u32(&rows_empty[rb]), ((i / kRowBufs) & 1) ^ 1, &abort_flag, A.err)) break;
+      *reinterpret_cast<int4*>(&rows_s[rb][4 * lane]) = make_int4(rr[0], rr[1], rr[2], rr[3]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&rows_full[rb]));
     }
   } else if (warp == kMmaWarp) {
     // ================================================================ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = make_idesc(128, kMlaHeads, kFmtBF16, kFmtBF16, 0, 0);
       constexpr uint32_t idesc_o = make_idesc(128, kMlaHeads, kFmtBF16, kFmtBF16, 1, 0);
-      const uint32_t kv0 = smem_u32(kv_tile);
+      const uint32_t pair0 = smem_u32(pair_buf), rope0 = smem_u32(rope_buf), q0 = smem_u32(q_buf);
       int seg = -1;
       for (int i = 0; i < n_mine; ++i) {
         const ChunkPos cp = chunk_pos(i);
         if (cp.first) ++seg;
-        const int qb = seg & 1, sb = i & 1;
+        const int sb = i & 1, rs = i % kRopeSlots;
         const uint32_t ph2 = (i >> 1) & 1;
-        if (!mbar_wait(smem_u32(&kv_full), i & 1, &abort_flag, A.err)) break;
-        if (cp.first && !mbar_wait(smem_u32(&q_full[qb]), (seg >> 1) & 1, &abort_flag, A.err)) break;
         if (!mbar_wait(smem_u32(&s_empty[sb]), ph2 ^ 1, &abort_flag, A.err)) break;
+        if (cp.first && !mbar_wait(smem_u32(&q_full), seg & 1, &abort_flag, A.err)) break;
+        if (!mbar_wait(smem_u32(&rope_full[rs]), (i / kRopeSlots) & 1, &abort_flag, A.err)) break;
+        fence_proxy_async_smem();   // slot filled through the generic proxy (cp.async / st.shared)
         tc_fence_after();
-        const uint32_t q0 = smem_u32(q_buf + qb * kQBufBytes);
-#pragma unroll 1
-        for (int a = 0; a < 9; ++a) {
+        const uint32_t d_s = tmem_s + sb * 16;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = smem_desc(kv0 + a * kKvAtomBytes + kk * 32, 0, 1024, kSwizzle128B);
-            const uint64_t bd = smem_desc(q0 + a * kQAtomBytes + kk * 32, 0, 1024, kSwizzle128B);
-            mma_f16_ss(tmem_s + sb * 16, ad, bd, idesc_s, (a | kk) != 0);
+        for (int kk = 0; kk < 4; ++kk)
+          mma_f16_ss(d_s, smem_desc(rope0 + rs * kAtomBytes + kk * 32, 0, 1024, kSwizzle128B),
+                     smem_desc(q0 + 8 * kQAtomBytes + kk * 32, 0, 1024, kSwizzle128B), idesc_s, kk != 0);
+        mma_commit(smem_u32(&rope_empty[rs]));
+        bool stop = false;
+        for (int j = 0; j < 4; ++j) {
+          const int gidx = 4 * i + j, ps = gidx % kPairSlots;
+          if (!mbar_wait(smem_u32(&pair_full[ps]), (gidx / kPairSlots) & 1, &abort_flag, A.err)) { stop = true; break; }
+          fence_proxy_async_smem();
+          tc_fence_after();
+#pragma unroll
+          for (int a2 = 0; a2 < 2; ++a2) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f16_ss(d_s, smem_desc(pair0 + ps * kPairBytes + a2 * kAtomBytes + kk * 32, 0, 1024, kSwizzle128B),
+                         smem_desc(q0 + (2 * j + a2) * kQAtomBytes + kk * 32, 0, 1024, kSwizzle128B), idesc_s, 1);
           }
         }
+        if (stop) break;
         mma_commit(smem_u32(&s_full[sb]));
-        if (cp.last) mma_commit(smem_u32(&q_empty[qb]));
+        if (cp.last) mma_commit(smem_u32(&q_empty));
         if (!mbar_wait(smem_u32(&p_full[sb]), ph2, &abort_flag, A.err)) break;
         if (!mbar_wait(smem_u32(&o_empty[sb]), ph2 ^ 1, &abort_flag, A.err)) break;
         tc_fence_after();
         const uint32_t p0 = smem_u32(p_buf + sb * kPBufBytes);
 #pragma unroll 1
         for (int mb = 0; mb < 4; ++mb) {
+          const int ps = (4 * i + mb) % kPairSlots;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
-            const uint64_t ad = smem_desc(kv0 + 2 * mb * kKvAtomBytes + ks * 2048, kKvAtomBytes, 1024, kSwizzle128B);
+            const uint64_t ad = smem_desc(pair0 + ps * kPairBytes + ks * 2048, kAtomBytes, 1024, kSwizzle128B);
             const uint64_t bd = smem_desc(p0 + (ks >> 2) * kQAtomBytes + (ks & 3) * 32, 0, 1024, kSwizzle128B);
             mma_f16_ss(tmem_o + sb * 64 + mb * 16, ad, bd, idesc_o, ks != 0);
           }
+          mma_commit(smem_u32(&pair_empty[ps]));
         }
         mma_commit(smem_u32(&o_full[sb]));
         mma_commit(smem_u32(&p_empty[sb]));
-        mma_commit(smem_u32(&kv_empty));
       }
     }
-  } else {
+  } else if (warp < 4) {
     // ================================================================ softmax warps 0-3
     GroupSync gs{smem_u32(&grp_bar), 0};
     int red_i = 0;
@@ -311,14 +446,12 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
           for (int mb = 0; mb < 4; ++mb) o[mb][h] = 0.f;
         }
       }
-      // validity of this thread's key (same test as the producers)
-      const QueryInfo qi = query_info(g, cp.t);
-      const int e = cp.cq * kMlaKeys + tid;
-      bool valid = false;
-      if (qi.ok && e < A.k) {
-        const int s = __ldg(A.idx + (int64_t)cp.t * A.k + e);
-        valid = s >= 0 && s < qi.len && physical_row(g, qi.b, s) >= 0;
-      }
+      // validity of this thread's key from the row table
+      const int rb = i % kRowBufs;
+      if (!mbar_wait(smem_u32(&rows_full[rb]), (i / kRowBufs) & 1, &abort_flag, A.err)) break;
+      const bool valid = rows_s[rb][tid] >= 0;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&rows_empty[rb]));
       if (!mbar_wait(smem_u32(&s_full[sb]), ph2, &abort_flag, A.err)) break;
       tc_fence_after();
       float z[kMlaHeads];
