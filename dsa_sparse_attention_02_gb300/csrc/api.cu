@@ -116,14 +116,15 @@ dsa_status_t check_indexer(const dsa_geom_t* g, dsa_dtype_t dt, int Hi, const vo
   dsa_status_t s = check_geom(g);
   if (s != DSA_OK) return s;
   if (dt != DSA_BF16 && dt != DSA_E4M3) return DSA_ERR_INVALID_ARG;
-  if (Hi < 1 || Hi > 64) return DSA_ERR_INVALID_ARG;
+  if (Hi < 4 || Hi > 64 || Hi % 4 != 0) return DSA_ERR_INVALID_ARG;
   if (g->B > indexer_max_requests()) return DSA_ERR_UNSUPPORTED;
   if (stride < g->max_seq_len) return DSA_ERR_INVALID_ARG;
   if (g->T == 0) return DSA_OK;
   if (!q_idx || !w || !kc || !scores) return DSA_ERR_INVALID_ARG;
   if (dt == DSA_E4M3 && (!q_scale || !ks)) return DSA_ERR_INVALID_ARG;
   if (dt == DSA_BF16 && (q_scale || ks)) return DSA_ERR_INVALID_ARG;
-  if (!aligned16(q_idx) || !aligned16(kc)) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q_idx) || !aligned16(kc) || !aligned16(w)) return DSA_ERR_INVALID_ARG;
+  if (dt == DSA_E4M3 && (!aligned16(q_scale) || !aligned16(ks))) return DSA_ERR_INVALID_ARG;
   return DSA_OK;
 }
 

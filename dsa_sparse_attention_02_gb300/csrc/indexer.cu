@@ -15,10 +15,13 @@
 // the head sum within its own registers, multiplies the key's scale and writes
 // one score per query, -inf past the query's causal position.
 //
-// Roles: warp P issues TMA into an S-stage smem ring; warp M issues the MMAs into
-// two TMEM accumulators; 4*EW epilogue warps drain them. Units are split
-// contiguously over a persistent grid, key-tile major so that consecutive units
-// of a multi-query request reuse the same key tile.
+// Roles: warp P decodes 32 units at a time (one per lane) and fills an S-stage
+// smem ring by TMA: the two key pages, the group's query rows, and by bulk copy
+// the pages' key scales and the queries' w and q_scale rows, plus a small unit
+// descriptor; warp M issues the MMAs into two TMEM accumulators; 4*EW epilogue
+// warps drain them reading only TMEM and the stage, and release the stage with
+// the MMA. Units are split contiguously over a persistent grid, key-tile major
+// so that consecutive units of a multi-query request reuse the same key tile.
 #include <cstdint>
 #include "kernels.cuh"
 
@@ -31,19 +34,31 @@ struct IndexerCfg {
   static constexpr int kN = kQG * kHp;                         // MMA N
   static constexpr int kKeyBytes = 128 * 128 * kAtoms;         // one 128-key tile
   static constexpr int kQBytes = kN * 128 * kAtoms;
-  static constexpr int kStageBytes = kKeyBytes + kQBytes;
-  static constexpr int kStages = (196608 / kStageBytes) < 8 ? (196608 / kStageBytes) : 8;
+  // per-stage side data: key scales (2 pages x 64), w and q_scale rows, unit descriptor
+  static constexpr int kKsOff = kKeyBytes + kQBytes;
+  static constexpr int kWOff = kKsOff + 512;
+  static constexpr int kQsOff = kWOff + kN * 4;
+  static constexpr int kDescOff = kQsOff + kN * 4;
+  static constexpr int kSideBytes = ((512 + 2 * kN * 4 + 64) + 1023) / 1024 * 1024;
+  static constexpr int kStageBytes = kKeyBytes + kQBytes + kSideBytes;
+  static constexpr int kStages = (204800 / kStageBytes) < 8 ? (204800 / kStageBytes) : 8;
   static constexpr int kEW = kQG >= 2 ? 2 : 1;                 // epilogue warp groups
   static constexpr int kEpiWarps = 4 * kEW;
   static constexpr int kThreads = 32 * (kEpiWarps + 2);
   static constexpr int kProdWarp = kEpiWarps, kMmaWarp = kEpiWarps + 1;
   static constexpr int kTmemCols = (2 * kN) <= 32 ? 32 : (2 * kN) <= 64 ? 64 : (2 * kN) <= 128 ? 128
                                    : (2 * kN) <= 256 ? 256 : 512;
-  static constexpr int kMaxB = 4096;
+  static constexpr int kMaxB = 2048;                           // requests per call
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes;
   static constexpr int kKSteps = kFp8 ? 4 : 8;
   static_assert(kN <= 256 && kN % 16 == 0, "MMA N");
   static_assert(kStages >= 2, "stages");
+};
+
+// What the epilogue needs about a unit; written by the producer into the stage.
+struct UnitDesc {
+  int b, tile, q_start, q_count, len, pos0, page_ok;   // pos0 = position of the unit's first query
+  int pad;
 };
 
 struct UnitInfo {
@@ -85,7 +100,6 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kThreads, 1)
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
   __shared__ int prefix[C::kMaxB + 1];
-  __shared__ float wq_s[C::kEpiWarps][kQG * kHp];   // per-warp copy of w*q_scale
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const GeomDev& g = A.g;
@@ -117,18 +131,20 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kThreads, 1)
   }
   if (tid == 0) {
     abort_flag = 0;
-    for (int s = 0; s < C::kStages; ++s) { mbar_init(smem_u32(&full_bar[s]), 1); mbar_init(smem_u32(&empty_bar[s]), 1); }
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), 1 + C::kEpiWarps);   // MMA commit + every epilogue warp
+    }
     for (int a = 0; a < 2; ++a) { mbar_init(smem_u32(&tfull_bar[a]), 1); mbar_init(smem_u32(&tempty_bar[a]), C::kEpiWarps); }
     fence_mbar_init();
   }
-  if (kHp > 0) {
-    // Query rows beyond Hi stay zero for the whole kernel (TMA writes rows < Hi only).
-    for (int s = 0; s < C::kStages; ++s) {
-      int4* qz = reinterpret_cast<int4*>(smem + s * C::kStageBytes + C::kKeyBytes);
-      for (int i = tid; i < C::kQBytes / 16; i += C::kThreads) qz[i] = make_int4(0, 0, 0, 0);
-    }
-    fence_proxy_async_smem();
+  // Query rows beyond Hi and w / q_scale entries beyond Hi stay zero for the whole
+  // kernel (TMA and the bulk copies write only the first Hi of them).
+  for (int s = 0; s < C::kStages; ++s) {
+    int4* z = reinterpret_cast<int4*>(smem + s * C::kStageBytes + C::kKeyBytes);
+    for (int i = tid; i < (C::kQBytes + C::kSideBytes) / 16; i += C::kThreads) z[i] = make_int4(0, 0, 0, 0);
   }
+  fence_proxy_async_smem();
   if (warp == C::kMmaWarp) { tmem_alloc(smem_u32(&tmem_base_s), C::kTmemCols); tmem_relinquish(); }
   tc_fence_before();
   __syncthreads();
@@ -138,44 +154,76 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kThreads, 1)
   const int U = prefix[B];
   const int G = gridDim.x;
   const int u_begin = (int)split_begin(blockIdx.x, U, G), u_end = (int)split_begin(blockIdx.x + 1, U, G);
+  const int Hi = A.Hi;
 
   if (warp == C::kProdWarp) {
-    if (lane == 0) {
-      tma_prefetch_desc(&map_k);
-      tma_prefetch_desc(&map_q);
-      for (int u = u_begin, i = 0; u < u_end; ++u, ++i) {
+    // ================================================================ producer
+    // 32 units are decoded at a time, one per lane, so their global lookups
+    // overlap; lane 0 then fills one stage per unit.
+    if (lane == 0) { tma_prefetch_desc(&map_k); tma_prefetch_desc(&map_q); }
+    bool stop = false;
+    for (int u_base = u_begin; u_base < u_end && !stop; u_base += 32) {
+      const int u = u_base + lane;
+      UnitInfo ui{};
+      int pg0 = -1, pg1 = -1;
+      if (u < u_end) {
+        ui = decode_unit<kQG>(prefix, B, u, g);
+        const int s0 = ui.tile * 128;
+        const int* bt = g.block_table + (int64_t)ui.b * g.bt_stride;
+        if (s0 < ui.len) pg0 = __ldg(bt + (s0 >> 6));
+        if (s0 + 64 < ui.len) pg1 = __ldg(bt + ((s0 + 64) >> 6));
+        const bool bad0 = s0 < ui.len && (pg0 < 0 || pg0 >= g.num_pages);
+        const bool bad1 = s0 + 64 < ui.len && (pg1 < 0 || pg1 >= g.num_pages);
+        if (bad0 || bad1) record_error(A.err, kDevBadIndex);
+        if (bad0) pg0 = -1;
+        if (bad1) pg1 = -1;
+      }
+      const int cnt = min(32, u_end - u_base);
+      for (int jj = 0; jj < cnt; ++jj) {
+        const int b = __shfl_sync(0xffffffffu, ui.b, jj), tile = __shfl_sync(0xffffffffu, ui.tile, jj);
+        const int q_start = __shfl_sync(0xffffffffu, ui.q_start, jj), q_count = __shfl_sync(0xffffffffu, ui.q_count, jj);
+        const int len = __shfl_sync(0xffffffffu, ui.len, jj);
+        const int pos0 = __shfl_sync(0xffffffffu, ui.pos0 + (ui.q_start - ui.q0), jj);
+        const int p0 = __shfl_sync(0xffffffffu, pg0, jj), p1 = __shfl_sync(0xffffffffu, pg1, jj);
+        const int i = u_base + jj - u_begin;
         const int s = i % C::kStages;
         const uint32_t ph = (i / C::kStages) & 1;
-        if (!mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1, &abort_flag, A.err)) break;
-        const UnitInfo ui = decode_unit<kQG>(prefix, B, u, g);
-        uint8_t* kdst = smem + s * C::kStageBytes;
-        uint8_t* qdst = kdst + C::kKeyBytes;
-        int pages[2], np = 0;
-        for (int hp = 0; hp < 2; ++hp) {
-          const int s0 = ui.tile * 128 + hp * 64;
-          pages[hp] = -1;
-          if (s0 < ui.len) {
-            const int pg = __ldg(g.block_table + (int64_t)ui.b * g.bt_stride + (s0 >> 6));
-            if (pg >= 0 && pg < g.num_pages) { pages[hp] = pg; ++np; }
-            else record_error(A.err, kDevBadIndex);
+        if (lane == 0) {
+          if (!mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1, &abort_flag, A.err)) {
+            stop = true;
+          } else {
+            uint8_t* st = smem + s * C::kStageBytes;
+            UnitDesc* d = reinterpret_cast<UnitDesc*>(st + C::kDescOff);
+            d->b = b; d->tile = tile; d->q_start = q_start; d->q_count = q_count; d->len = len; d->pos0 = pos0;
+            d->page_ok = (p0 >= 0 ? 1 : 0) | (p1 >= 0 ? 2 : 0);
+            const int np = (p0 >= 0) + (p1 >= 0);
+            uint32_t bytes = np * 64 * 128 * C::kAtoms + q_count * Hi * 128 * C::kAtoms + q_count * Hi * 4;
+            if (kFp8) bytes += np * 256 + q_count * Hi * 4;
+            const uint32_t bar = smem_u32(&full_bar[s]);
+            mbar_arrive_expect_tx(bar, bytes);
+            const int pages[2] = {p0, p1};
+            for (int hp = 0; hp < 2; ++hp) {
+              if (pages[hp] < 0) continue;
+              for (int a = 0; a < C::kAtoms; ++a)
+                tma_load_2d(smem_u32(st + a * 16384 + hp * 8192), &map_k, bar, a * (kFp8 ? 128 : 64), pages[hp] * 64);
+              if (kFp8) bulk_load(smem_u32(st + C::kKsOff + hp * 256), A.k_scale + (int64_t)pages[hp] * 64, 256, bar);
+            }
+            for (int j = 0; j < q_count; ++j) {
+              const int t = q_start + j;
+              for (int a = 0; a < C::kAtoms; ++a)
+                tma_load_2d(smem_u32(st + C::kKeyBytes + a * (C::kN * 128) + j * kHp * 128), &map_q, bar,
+                            a * (kFp8 ? 128 : 64), t * Hi);
+              bulk_load(smem_u32(st + C::kWOff + j * kHp * 4), A.w + (int64_t)t * Hi, Hi * 4, bar);
+              if (kFp8) bulk_load(smem_u32(st + C::kQsOff + j * kHp * 4), A.q_scale + (int64_t)t * Hi, Hi * 4, bar);
+            }
           }
         }
-        const uint32_t bytes = np * 64 * 128 * C::kAtoms + ui.q_count * A.Hi * 128 * C::kAtoms;
-        const uint32_t bar = smem_u32(&full_bar[s]);
-        mbar_arrive_expect_tx(bar, bytes);
-        for (int hp = 0; hp < 2; ++hp) {
-          if (pages[hp] < 0) continue;
-          for (int a = 0; a < C::kAtoms; ++a)
-            tma_load_2d(smem_u32(kdst + a * 16384 + hp * 8192), &map_k, bar, a * (kFp8 ? 128 : 64), pages[hp] * 64);
-        }
-        for (int j = 0; j < ui.q_count; ++j) {
-          for (int a = 0; a < C::kAtoms; ++a)
-            tma_load_2d(smem_u32(qdst + a * (C::kN * 128) + j * kHp * 128), &map_q, bar,
-                        a * (kFp8 ? 128 : 64), (ui.q_start + j) * A.Hi);
-        }
+        stop = __shfl_sync(0xffffffffu, stop ? 1 : 0, 0) != 0;
+        if (stop) break;
       }
     }
   } else if (warp == C::kMmaWarp) {
+    // ================================================================ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = make_idesc(128, C::kN, kFp8 ? kFmtE4M3 : kFmtBF16, kFp8 ? kFmtE4M3 : kFmtBF16, 0, 0);
       for (int u = u_begin, i = 0; u < u_end; ++u, ++i) {
@@ -202,35 +250,31 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kThreads, 1)
       }
     }
   } else {
-    // ---- epilogue warps
+    // ================================================================ epilogue warps
+    // Lane = key of the tile; reads the accumulator, the key scale, w and q_scale
+    // from TMEM / the stage only.
     const int quarter = warp & 3, half = warp >> 2;
-    float* wq = wq_s[warp];
+    const int key = quarter * 32 + lane;
+    const float neg_inf = -__int_as_float(0x7f800000);
     for (int u = u_begin, i = 0; u < u_end; ++u, ++i) {
+      const int s = i % C::kStages;
+      const uint32_t ph = (i / C::kStages) & 1;
       const int acc = i & 1;
       const uint32_t aph = (i >> 1) & 1;
-      const UnitInfo ui = decode_unit<kQG>(prefix, B, u, g);
-      // this warp's copy of w*q_scale for the group's queries (warp-local, no CTA barrier)
-      __syncwarp();
-      for (int e = lane; e < kQG * kHp; e += 32) {
-        const int j = e / kHp, h = e % kHp;
-        float v = 0.f;
-        if (j < ui.q_count && h < A.Hi) {
-          const int64_t o = (int64_t)(ui.q_start + j) * A.Hi + h;
-          v = __ldg(A.w + o);
-          if (kFp8) v *= __ldg(A.q_scale + o);
-        }
-        wq[e] = v;
-      }
-      __syncwarp();
-      const int s = ui.tile * 128 + quarter * 32 + lane;
-      int64_t row = -1;
-      if (s < ui.len) row = physical_row(g, ui.b, s);
-      const float ks = (kFp8 && row >= 0) ? __ldg(A.k_scale + row) : 1.f;
       if (!mbar_wait(smem_u32(&tfull_bar[acc]), aph, &abort_flag, A.err)) break;
+      if (!mbar_wait(smem_u32(&full_bar[s]), ph, &abort_flag, A.err)) break;   // stage data visible here
       tc_fence_after();
+      const uint8_t* st = smem + s * C::kStageBytes;
+      const UnitDesc d = *reinterpret_cast<const UnitDesc*>(st + C::kDescOff);
+      const float* wv = reinterpret_cast<const float*>(st + C::kWOff);
+      const float* qv = reinterpret_cast<const float*>(st + C::kQsOff);
+      const int sidx = d.tile * 128 + key;
+      const bool in_ctx = sidx < d.len;
+      const bool page_ok = (d.page_ok >> (key >> 6)) & 1;
+      const float ks = kFp8 ? reinterpret_cast<const float*>(st + C::kKsOff)[key] : 1.f;
 #pragma unroll 1
       for (int j = half; j < kQG; j += C::kEW) {
-        if (j >= ui.q_count) break;
+        if (j >= d.q_count) break;
         float sum = 0.f;
 #pragma unroll
         for (int hc = 0; hc < kHp / 16; ++hc) {
@@ -238,19 +282,35 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kThreads, 1)
           tmem_ld16(tmem + acc * C::kN + j * kHp + hc * 16 + ((uint32_t)(quarter * 32) << 16), v);
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 16; ++e) sum = fmaf(wq[j * kHp + hc * 16 + e], fmaxf(v[e], 0.f), sum);
+          for (int e = 0; e < 16; e += 4) {
+            const float4 w4 = *reinterpret_cast<const float4*>(wv + j * kHp + hc * 16 + e);
+            if (kFp8) {
+              const float4 q4 = *reinterpret_cast<const float4*>(qv + j * kHp + hc * 16 + e);
+              sum = fmaf(w4.x * q4.x, fmaxf(v[e], 0.f), sum);
+              sum = fmaf(w4.y * q4.y, fmaxf(v[e + 1], 0.f), sum);
+              sum = fmaf(w4.z * q4.z, fmaxf(v[e + 2], 0.f), sum);
+              sum = fmaf(w4.w * q4.w, fmaxf(v[e + 3], 0.f), sum);
+            } else {
+              sum = fmaf(w4.x, fmaxf(v[e], 0.f), sum);
+              sum = fmaf(w4.y, fmaxf(v[e + 1], 0.f), sum);
+              sum = fmaf(w4.z, fmaxf(v[e + 2], 0.f), sum);
+              sum = fmaf(w4.w, fmaxf(v[e + 3], 0.f), sum);
+            }
+          }
         }
-        if (s < ui.len) {
-          const int t = ui.q_start + j;
-          const int pos = ui.pos0 + (t - ui.q0);
-          float out = sum * ks;
-          if (s > pos || row < 0) out = -__int_as_float(0x7f800000);
-          A.scores[(int64_t)t * A.stride + s] = out;
+        if (in_ctx) {
+          const int t = d.q_start + j;
+          const int pos = d.pos0 + j;
+          const float out = (sidx <= pos && page_ok) ? sum * ks : neg_inf;
+          A.scores[(int64_t)t * A.stride + sidx] = out;
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[acc]));
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&tempty_bar[acc]));
+        mbar_arrive(smem_u32(&empty_bar[s]));
+      }
     }
   }
 
@@ -274,7 +334,7 @@ static cudaError_t launch_indexer_t(const CUtensorMap& mk, const CUtensorMap& mq
   return cudaGetLastError();
 }
 
-int indexer_max_requests() { return 4096; }
+int indexer_max_requests() { return IndexerCfg<true, 64, 1>::kMaxB; }
 
 cudaError_t indexer_launch(bool fp8, int Hi, bool multi_query, const CUtensorMap& mk, const CUtensorMap& mq,
                            const IndexerArgs& A, int grid, cudaStream_t st) {

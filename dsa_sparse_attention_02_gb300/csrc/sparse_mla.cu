@@ -32,9 +32,13 @@
 //   * one MMA thread: S^T = KV . Q^T on tcgen05 (M = 128 keys, N = 16 heads,
 //     K = 576) into TMEM, then O^T = V^T . P^T (M = 128 latent columns x 4
 //     blocks, N = 16, K = 128 keys), V^T read MN-major from the pair slots.
-//   * 4 softmax warps (TMEM lane = key for S, = latent column for O) run the
-//     online softmax per head in the exp2 domain, write P^T as bf16 for the
-//     second MMA, and accumulate O in fp32 registers.
+//   * 4 softmax warps (TMEM lane = key for S) run the online softmax per head in
+//     the exp2 domain and write P^T as bf16 for the second MMA. O^T accumulates
+//     in TMEM across a query's chunks. The reference max moves only when a
+//     chunk's max exceeds it by more than 2^8 (p <= 256 otherwise); then the
+//     softmax warps rescale O in TMEM (lane = latent column) before releasing P.
+//     S(i) completing implies PV(i-1) completed (a commit tracks every earlier
+//     MMA of the issuing thread), so that rescale needs no further wait.
 // A CTA that holds every chunk of a query writes the final bf16 output; other
 // segments write (unnormalized O, running max, sum) partials that the combine
 // kernel merges with log-sum-exp weights.
@@ -55,16 +59,18 @@ constexpr int kQBufBytes = 9 * kQAtomBytes;         // 18 KB
 constexpr int kPBufBytes = 2 * kQAtomBytes;         // P^T: 16 heads x 128 keys bf16 = 4 KB
 constexpr int kMlaSmemBytes =
     1024 + kPairSlots * kPairBytes + kRopeSlots * kAtomBytes + kQBufBytes + 2 * kPBufBytes;
-// Warps 0-3 softmax (one per TMEM lane quarter), 4 and 6 producers with 5 the row
-// resolver (bf16), or 4-6 producers (e4m3); 7 MMA. Two warps per SM sub-partition
-// leave room for ~200 registers.
-constexpr int kMlaThreads = 256;
-constexpr int kFp8ProdWarps = 3;
-constexpr int kBf16ProdWarps = 2;
-constexpr int kResolverWarp = 5;
-constexpr int kMmaWarp = 7;
+// Twelve warps, 168 registers each (three per SM sub-partition):
+//   warps 0-3   softmax (one per TMEM lane quarter)
+//   warps 4-7   producers (one per sub-partition, so that copy issue runs on all four)
+//   warp  8     MMA issuer; warp 9 row resolver; warps 10-11 idle
+constexpr int kMlaThreads = 384;
+constexpr int kProdWarp0 = 4;
+constexpr int kProdWarps = 4;
+constexpr int kMmaWarp = 8;
+constexpr int kResolverWarp = 9;
 constexpr int kRowBufs = 4;                         // row-table ring depth (chunks)
-constexpr int kMlaTmemCols = 256;                   // S: 2 x 16, O: 2 x 64
+constexpr int kMlaTmemCols = 128;                   // S: 2 x 16, O: 64
+constexpr float kRescaleLog2 = 8.f;                 // lazy rescale threshold (log2 units)
 constexpr float kLn2 = 0.6931471805599453f;
 
 // Bounded group barrier over the 4 softmax warps (one arrive per warp).
@@ -98,6 +104,57 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
   return __uint_as_float(__float_as_uint(v) | sign);
 }
 
+// 2^x with the MUFU ex2 instruction (inputs here are <= 8 or -inf).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Max over the 32 lanes of 16 values at once (a transposing butterfly: 16 shuffles
+// instead of 80). On return, lanes h and h+16 hold the max of value h.
+__device__ __forceinline__ float warp_max16(const float (&v)[16]) {
+  const int lane = threadIdx.x & 31;
+  float a[8];
+  {
+    const bool up = lane & 16;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float send = up ? v[k] : v[k + 8];
+      const float keep = up ? v[k + 8] : v[k];
+      a[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+    }
+  }
+  float b[4];
+  {
+    const bool up = lane & 8;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float send = up ? a[k] : a[k + 4];
+      const float keep = up ? a[k + 4] : a[k];
+      b[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+    }
+  }
+  float c[2];
+  {
+    const bool up = lane & 4;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const float send = up ? b[k] : b[k + 2];
+      const float keep = up ? b[k + 2] : b[k];
+      c[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+    }
+  }
+  float d;
+  {
+    const bool up = lane & 2;
+    const float send = up ? c[0] : c[1];
+    const float keep = up ? c[1] : c[0];
+    d = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 2));
+  }
+  return fmaxf(d, __shfl_xor_sync(0xffffffffu, d, 1));
+}
+
 struct ChunkPos {
   int64_t chunk;
   int t, cq;
@@ -127,10 +184,10 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
 
   __shared__ uint64_t pair_full[kPairSlots], pair_empty[kPairSlots], rope_full[kRopeSlots], rope_empty[kRopeSlots];
   __shared__ uint64_t q_full, q_empty;
-  __shared__ uint64_t s_full[2], s_empty[2], p_full[2], p_empty[2], o_full[2], o_empty[2], grp_bar;
+  __shared__ uint64_t s_full[2], s_empty[2], p_full[2], p_empty[2], o_full, o_free, grp_bar;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
-  __shared__ float red[2][4][kMlaHeads];
+  __shared__ __align__(16) float red[2][4][kMlaHeads];
   __shared__ __align__(16) int rows_s[kRowBufs][kMlaKeys];   // physical row per key of a chunk, -1 = none
   __shared__ uint64_t rows_full[kRowBufs], rows_empty[kRowBufs];
 
@@ -142,8 +199,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
   const int64_t c_begin = split_begin(blockIdx.x, A.n_chunks, G);
   const int64_t c_end = split_begin(blockIdx.x + 1, A.n_chunks, G);
   const int n_mine = (int)(c_end - c_begin);
-  const int slot_producers = kFp8Kv ? kFp8ProdWarps : 32 * kBf16ProdWarps;   // arrivals per slot fill
-  const bool is_producer = kFp8Kv ? (warp >= 4 && warp < 4 + kFp8ProdWarps) : (warp == 4 || warp == 6);
+  const int slot_producers = 32 * kProdWarps;   // one arrival per producer thread per slot fill
 
   auto chunk_pos = [&](int i) {
     ChunkPos cp;
@@ -166,15 +222,14 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       mbar_init(smem_u32(&s_empty[j]), 4);
       mbar_init(smem_u32(&p_full[j]), 4);
       mbar_init(smem_u32(&p_empty[j]), 1);
-      mbar_init(smem_u32(&o_full[j]), 1);
-      mbar_init(smem_u32(&o_empty[j]), 4);
     }
+    mbar_init(smem_u32(&o_full), 1);     // one phase per chunk's PV
+    mbar_init(smem_u32(&o_free), 4);     // softmax warps have read O at a segment end
     mbar_init(smem_u32(&grp_bar), 4);
     for (int j = 0; j < kRowBufs; ++j) {
-      // bf16: written by the resolver warp, read by the producer and the 4 softmax warps;
-      // e4m3: written by the 3 producer warps, read by the softmax warps.
-      mbar_init(smem_u32(&rows_full[j]), kFp8Kv ? kFp8ProdWarps : 1);
-      mbar_init(smem_u32(&rows_empty[j]), kFp8Kv ? 4 : 4 + kBf16ProdWarps);
+      // written by the resolver warp, read by the producer and softmax warps
+      mbar_init(smem_u32(&rows_full[j]), 1);
+      mbar_init(smem_u32(&rows_empty[j]), 4 + kProdWarps);
     }
     fence_mbar_init();
   }
@@ -187,18 +242,23 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
   const uint32_t tmem_s = tmem;          // + 16 * buf
-  const uint32_t tmem_o = tmem + 32;     // + 64 * buf, + 16 * mb
+  const uint32_t tmem_o = tmem + 32;     // + 16 * mb
 
-  if (is_producer) {
+  if (warp >= kProdWarp0 && warp < kProdWarp0 + kProdWarps) {
     // ================================================================ producers
-    const int pw = kFp8Kv ? warp - 4 : (warp == 4 ? 0 : 1);
+    // Warp pw copies rows [32*pw, 32*pw+32) of every slot. bf16: 16-byte cp.async
+    // (zero-fill for padding), slot completion through cp.async.mbarrier.arrive.noinc.
+    // e4m3: the RoPE atom by cp.async as well; the latent pairs are loaded,
+    // dequantized to bf16 and stored, then each thread arrives.
+    const int pw = warp - kProdWarp0;
     int seg = 0;
-    // Warp-uniform bounded wait (lane 0 waits, the result is broadcast).
-    auto slot_acquire = [&](uint32_t bar, uint32_t parity) -> bool {
+    auto slot_acquire = [&](uint32_t bar, uint32_t parity) -> bool {   // warp-uniform bounded wait
       int ok = 1;
       if (lane == 0) ok = mbar_wait(bar, parity, &abort_flag, A.err) ? 1 : 0;
       return __shfl_sync(0xffffffffu, ok, 0) != 0;
     };
+    const size_t row_bytes = kFp8Kv ? (size_t)kFp8Record : (size_t)(kDimQK * 2);
+    const size_t rope_off = kFp8Kv ? (size_t)(kDimLatent + 16) : (size_t)(kDimLatent * 2);
     for (int i = 0; i < n_mine; ++i) {
       const ChunkPos cp = chunk_pos(i);
       if (cp.first) {
@@ -213,132 +273,68 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         }
         ++seg;
       }
-      const int rs = i % kRopeSlots;
-      if (!kFp8Kv) {
-        const int rb = i % kRowBufs;
-        if (!slot_acquire(smem_u32(&rows_full[rb]), (i / kRowBufs) & 1)) break;
-        mbar_try_wait(smem_u32(&rows_full[rb]), (i / kRowBufs) & 1);   // acquire in every lane (phase is complete)
-        const int* rows = rows_s[rb];
-        const uint8_t* kv = A.kv;
-        bool stop = false;
-        // RoPE atom: 8 lanes per row (128 B), 4 rows per instruction; this warp's 64 rows
-        if (!slot_acquire(smem_u32(&rope_empty[rs]), ((i / kRopeSlots) & 1) ^ 1)) break;
-        {
-          const uint32_t dst0 = smem_u32(rope_buf + rs * kAtomBytes);
-#pragma unroll 4
-          for (int j = 0; j < 16; ++j) {
-            const int ri = 64 * pw + 4 * j + (lane >> 3);
-            const int row = rows[ri];
-            const int cb = (lane & 7) * 16;
-            cp_async_16(dst0 + sw128_offset(ri, cb, 0), kv + (int64_t)(row >= 0 ? row : 0) * (kDimQK * 2) + kDimLatent * 2 + cb,
-                        row >= 0 ? 16u : 0u);
-          }
-          cp_async_arrive_noinc(smem_u32(&rope_full[rs]));
+      const int rb = i % kRowBufs, rs = i % kRopeSlots;
+      if (!slot_acquire(smem_u32(&rows_full[rb]), (i / kRowBufs) & 1)) break;
+      mbar_try_wait(smem_u32(&rows_full[rb]), (i / kRowBufs) & 1);   // acquire in every lane (phase is complete)
+      const int* rows = rows_s[rb];
+      const uint8_t* kv = A.kv;
+      // RoPE atom: 8 lanes per row (128 B), 4 rows per instruction
+      if (!slot_acquire(smem_u32(&rope_empty[rs]), ((i / kRopeSlots) & 1) ^ 1)) break;
+      {
+        const uint32_t dst0 = smem_u32(rope_buf + rs * kAtomBytes);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int ri = 32 * pw + 4 * j + (lane >> 3);
+          const int row = rows[ri];
+          const int cb = (lane & 7) * 16;
+          cp_async_16(dst0 + sw128_offset(ri, cb, 0), kv + (int64_t)(row >= 0 ? row : 0) * row_bytes + rope_off + cb,
+                      row >= 0 ? 16u : 0u);
         }
-        // four pairs: 16 lanes per row (256 B), 2 rows per instruction
-        for (int j = 0; j < 4; ++j) {
-          const int gidx = 4 * i + j, ps = gidx % kPairSlots;
-          if (!slot_acquire(smem_u32(&pair_empty[ps]), ((gidx / kPairSlots) & 1) ^ 1)) { stop = true; break; }
-          const uint32_t dst0 = smem_u32(pair_buf + ps * kPairBytes);
+        cp_async_arrive_noinc(smem_u32(&rope_full[rs]));
+      }
+      bool stop = false;
+      for (int j = 0; j < 4; ++j) {
+        const int gidx = 4 * i + j, ps = gidx % kPairSlots;
+        if (!slot_acquire(smem_u32(&pair_empty[ps]), ((gidx / kPairSlots) & 1) ^ 1)) { stop = true; break; }
+        uint8_t* slot = pair_buf + ps * kPairBytes;
+        if (!kFp8Kv) {
+          // 16 lanes per row (256 B of the pair), 2 rows per instruction
+          const uint32_t dst0 = smem_u32(slot);
 #pragma unroll 4
-          for (int jj = 0; jj < 32; ++jj) {
-            const int ri = 64 * pw + 2 * jj + (lane >> 4);
+          for (int jj = 0; jj < 16; ++jj) {
+            const int ri = 32 * pw + 2 * jj + (lane >> 4);
             const int row = rows[ri];
             const int cb = (lane & 15) * 16;
-            cp_async_16(dst0 + sw128_offset(ri, cb, kAtomBytes), kv + (int64_t)(row >= 0 ? row : 0) * (kDimQK * 2) + j * 256 + cb,
+            cp_async_16(dst0 + sw128_offset(ri, cb, kAtomBytes), kv + (int64_t)(row >= 0 ? row : 0) * row_bytes + j * 256 + cb,
                         row >= 0 ? 16u : 0u);
           }
           cp_async_arrive_noinc(smem_u32(&pair_full[ps]));
-        }
-        if (stop) break;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&rows_empty[rb]));
-      } else {
-        // e4m3 records: warp pw handles 4-row groups g4 = pw, pw+3, ...; 8 lanes per row,
-        // lane part p covers 16 latent codes of the pair and 16 bytes of the RoPE part.
-        const QueryInfo qi = query_info_warp(g, cp.t);
-        const int part = lane & 7, sub = lane >> 3;
-        constexpr int kMaxGroups = 11;
-        int64_t rrow[kMaxGroups];
-        int ng = 0;
+        } else {
+          // 8 lanes per row: lane part p dequantizes codes 16p..16p+15 of the pair's 128
+          const int part = lane & 7, sub = lane >> 3;
+          uint4 c[8];
+          float sc[8];
 #pragma unroll
-        for (int gi = 0; gi < kMaxGroups; ++gi) {
-          const int g4 = pw + kFp8ProdWarps * gi;
-          rrow[gi] = -1;
-          if (g4 < 32) {
-            rrow[gi] = selected_row(A, qi, cp.t, cp.cq * kMlaKeys + 4 * g4 + sub);
-            ng = gi + 1;
-          }
-        }
-        bool stop = false;
-        // publish this warp's rows to the softmax warps' row table
-        {
-          const int rb = i % kRowBufs;
-          if (lane == 0 && !mbar_wait(smem_u32(&rows_empty[rb]), ((i / kRowBufs) & 1) ^ 1, &abort_flag, A.err))
-            abort_flag = 1;
-          __syncwarp();
-          if (abort_flag) break;
-          if (part == 0) {
-#pragma unroll
-            for (int gi = 0; gi < kMaxGroups; ++gi)
-              if (gi < ng) rows_s[rb][4 * (pw + kFp8ProdWarps * gi) + sub] = (int)rrow[gi];
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&rows_full[rb]));
-        }
-        // RoPE atom (plain copy of 16 bytes per lane)
-        if (lane == 0 && !mbar_wait(smem_u32(&rope_empty[rs]), ((i / kRopeSlots) & 1) ^ 1, &abort_flag, A.err))
-          abort_flag = 1;
-        __syncwarp();
-        if (abort_flag) break;
-        {
-          uint4 v[kMaxGroups];
-#pragma unroll
-          for (int gi = 0; gi < kMaxGroups; ++gi) {
-            v[gi] = make_uint4(0, 0, 0, 0);
-            if (gi < ng && rrow[gi] >= 0)
-              v[gi] = __ldg(reinterpret_cast<const uint4*>(A.kv + rrow[gi] * (int64_t)kFp8Record + kDimLatent + 16) + part);
-          }
-#pragma unroll
-          for (int gi = 0; gi < kMaxGroups; ++gi) {
-            if (gi >= ng) break;
-            const int key = 4 * (pw + kFp8ProdWarps * gi) + sub;
-            *reinterpret_cast<uint4*>(rope_buf + rs * kAtomBytes + sw128_offset(key, part * 16, 0)) = v[gi];
-          }
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&rope_full[rs]));
-        for (int j = 0; j < 4; ++j) {
-          const int gidx = 4 * i + j, ps = gidx % kPairSlots;
-          if (lane == 0 && !mbar_wait(smem_u32(&pair_empty[ps]), ((gidx / kPairSlots) & 1) ^ 1, &abort_flag, A.err))
-            abort_flag = 1;
-          __syncwarp();
-          if (abort_flag) { stop = true; break; }
-          uint4 c[kMaxGroups];
-          float sc[kMaxGroups];
-#pragma unroll
-          for (int gi = 0; gi < kMaxGroups; ++gi) {
-            c[gi] = make_uint4(0, 0, 0, 0);
-            sc[gi] = 0.f;
-            if (gi < ng && rrow[gi] >= 0) {
-              const uint8_t* rec = A.kv + rrow[gi] * (int64_t)kFp8Record;
-              c[gi] = __ldg(reinterpret_cast<const uint4*>(rec + 128 * j) + part);
-              sc[gi] = __ldg(reinterpret_cast<const float*>(rec + kDimLatent) + j);
+          for (int jj = 0; jj < 8; ++jj) {
+            const int row = rows[32 * pw + 4 * jj + sub];
+            c[jj] = make_uint4(0, 0, 0, 0);
+            sc[jj] = 0.f;
+            if (row >= 0) {
+              const uint8_t* rec = kv + (int64_t)row * kFp8Record;
+              c[jj] = __ldg(reinterpret_cast<const uint4*>(rec + 128 * j) + part);
+              sc[jj] = __ldg(reinterpret_cast<const float*>(rec + kDimLatent) + j);
             }
           }
-          uint8_t* slot = pair_buf + ps * kPairBytes;
 #pragma unroll
-          for (int gi = 0; gi < kMaxGroups; ++gi) {
-            if (gi >= ng) break;
-            const int key = 4 * (pw + kFp8ProdWarps * gi) + sub;
-            const uint32_t w4[4] = {c[gi].x, c[gi].y, c[gi].z, c[gi].w};
+          for (int jj = 0; jj < 8; ++jj) {
+            const int key = 32 * pw + 4 * jj + sub;
+            const uint32_t w4[4] = {c[jj].x, c[jj].y, c[jj].z, c[jj].w};
             uint32_t pk[8];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const uint32_t wv = w4[q];
-              pk[2 * q] = pack_bf16x2(e4m3_to_f32(wv & 0xFF) * sc[gi], e4m3_to_f32((wv >> 8) & 0xFF) * sc[gi]);
-              pk[2 * q + 1] = pack_bf16x2(e4m3_to_f32((wv >> 16) & 0xFF) * sc[gi], e4m3_to_f32(wv >> 24) * sc[gi]);
+              pk[2 * q] = pack_bf16x2(e4m3_to_f32(wv & 0xFF) * sc[jj], e4m3_to_f32((wv >> 8) & 0xFF) * sc[jj]);
+              pk[2 * q + 1] = pack_bf16x2(e4m3_to_f32((wv >> 16) & 0xFF) * sc[jj], e4m3_to_f32(wv >> 24) * sc[jj]);
             }
             // pair column 16*part .. 16*part+15 -> atom part/4, bytes 32*(part%4) .. +31
             const int col_byte = (part >> 2) * 128 + (part & 3) * 32;
@@ -346,14 +342,15 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
             *reinterpret_cast<uint4*>(slot + sw128_offset(key, col_byte + 16, kAtomBytes)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
           }
           fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&pair_full[ps]));
+          mbar_arrive(smem_u32(&pair_full[ps]));
         }
-        if (stop) break;
       }
+      if (stop) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&rows_empty[rb]));
     }
-  } else if (!kFp8Kv && warp == kResolverWarp) {
-    // ================================================================ row resolver (bf16)
+  } else if (warp == kResolverWarp) {
+    // ================================================================ row resolver
     int t_cached = -1;
     QueryInfo qi{};
     for (int i = 0; i < n_mine; ++i) {
@@ -409,7 +406,8 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         mma_commit(smem_u32(&s_full[sb]));
         if (cp.last) mma_commit(smem_u32(&q_empty));
         if (!mbar_wait(smem_u32(&p_full[sb]), ph2, &abort_flag, A.err)) break;
-        if (!mbar_wait(smem_u32(&o_empty[sb]), ph2 ^ 1, &abort_flag, A.err)) break;
+        // a new segment's first PV overwrites O: the previous segment's O must have been read
+        if (cp.first && seg > 0 && !mbar_wait(smem_u32(&o_free), (seg - 1) & 1, &abort_flag, A.err)) break;
         tc_fence_after();
         const uint32_t p0 = smem_u32(p_buf + sb * kPBufBytes);
 #pragma unroll 1
@@ -419,11 +417,11 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
           for (int ks = 0; ks < 8; ++ks) {
             const uint64_t ad = smem_desc(pair0 + ps * kPairBytes + ks * 2048, kAtomBytes, 1024, kSwizzle128B);
             const uint64_t bd = smem_desc(p0 + (ks >> 2) * kQAtomBytes + (ks & 3) * 32, 0, 1024, kSwizzle128B);
-            mma_f16_ss(tmem_o + sb * 64 + mb * 16, ad, bd, idesc_o, ks != 0);
+            mma_f16_ss(tmem_o + mb * 16, ad, bd, idesc_o, (ks != 0 || !cp.first) ? 1u : 0u);
           }
           mma_commit(smem_u32(&pair_empty[ps]));
         }
-        mma_commit(smem_u32(&o_full[sb]));
+        mma_commit(smem_u32(&o_full));
         mma_commit(smem_u32(&p_empty[sb]));
       }
     }
@@ -433,18 +431,14 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     int red_i = 0;
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     const float neg_inf = -__int_as_float(0x7f800000);
-    float m[kMlaHeads], l[kMlaHeads], o[4][kMlaHeads];
+    float m[kMlaHeads], l[kMlaHeads];
     for (int i = 0; i < n_mine; ++i) {
       const ChunkPos cp = chunk_pos(i);
       const int sb = i & 1;
       const uint32_t ph2 = (i >> 1) & 1;
       if (cp.first) {
 #pragma unroll
-        for (int h = 0; h < kMlaHeads; ++h) {
-          m[h] = neg_inf; l[h] = 0.f;
-#pragma unroll
-          for (int mb = 0; mb < 4; ++mb) o[mb][h] = 0.f;
-        }
+        for (int h = 0; h < kMlaHeads; ++h) { m[h] = neg_inf; l[h] = 0.f; }
       }
       // validity of this thread's key from the row table
       const int rb = i % kRowBufs;
@@ -462,23 +456,60 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       if (lane == 0) mbar_arrive(smem_u32(&s_empty[sb]));
       // chunk max per head across the 128 keys
 #pragma unroll
-      for (int h = 0; h < kMlaHeads; ++h) {
-        z[h] = valid ? z[h] * A.scale_log2 : neg_inf;
-        const float wm = warp_max(z[h]);
-        if (lane == 0) red[red_i][warp][h] = wm;
+      for (int h = 0; h < kMlaHeads; ++h) z[h] = valid ? z[h] * A.scale_log2 : neg_inf;
+      {
+        // after the butterfly, lanes 2h' and 2h'+1 hold the warp max of head hidx below
+        // (exchange distances 16, 8, 4, 2 select head bits 3, 2, 1, 0)
+        const float wm = warp_max16(z);
+        const int hidx = ((lane >> 4) & 1) << 3 | ((lane >> 3) & 1) << 2 | ((lane >> 2) & 1) << 1 | ((lane >> 1) & 1);
+        if ((lane & 1) == 0) red[red_i][warp][hidx] = wm;
       }
       if (!gs.sync(&abort_flag, A.err)) break;
+      // move the reference max only where this chunk exceeds it by more than 2^8
       float alpha[kMlaHeads];
+      bool any_raise = false;
+      {
+        float cmv[kMlaHeads];
 #pragma unroll
-      for (int h = 0; h < kMlaHeads; ++h) {
-        const float cm = fmaxf(fmaxf(red[red_i][0][h], red[red_i][1][h]), fmaxf(red[red_i][2][h], red[red_i][3][h]));
-        const float mn = fmaxf(m[h], cm);
-        alpha[h] = (mn == neg_inf) ? 1.f : exp2f(m[h] - mn);
-        z[h] = (z[h] == neg_inf) ? 0.f : exp2f(z[h] - mn);   // z now holds p
-        l[h] = l[h] * alpha[h] + z[h];
-        m[h] = mn;
+        for (int q4 = 0; q4 < kMlaHeads / 4; ++q4) {
+          const float4 r0 = *reinterpret_cast<const float4*>(&red[red_i][0][4 * q4]);
+          const float4 r1 = *reinterpret_cast<const float4*>(&red[red_i][1][4 * q4]);
+          const float4 r2 = *reinterpret_cast<const float4*>(&red[red_i][2][4 * q4]);
+          const float4 r3 = *reinterpret_cast<const float4*>(&red[red_i][3][4 * q4]);
+          cmv[4 * q4 + 0] = fmaxf(fmaxf(r0.x, r1.x), fmaxf(r2.x, r3.x));
+          cmv[4 * q4 + 1] = fmaxf(fmaxf(r0.y, r1.y), fmaxf(r2.y, r3.y));
+          cmv[4 * q4 + 2] = fmaxf(fmaxf(r0.z, r1.z), fmaxf(r2.z, r3.z));
+          cmv[4 * q4 + 3] = fmaxf(fmaxf(r0.w, r1.w), fmaxf(r2.w, r3.w));
+        }
+#pragma unroll
+        for (int h = 0; h < kMlaHeads; ++h) {
+          const float cm = cmv[h];
+          alpha[h] = 1.f;
+          if (cm > m[h] + kRescaleLog2) {       // also true for the first finite max (m = -inf)
+            alpha[h] = (m[h] == neg_inf) ? 0.f : fast_exp2(m[h] - cm);
+            any_raise = true;
+            m[h] = cm;
+          }
+          l[h] *= alpha[h];
+          z[h] = (z[h] == neg_inf) ? 0.f : fast_exp2(z[h] - m[h]);   // z now holds p <= 256
+          l[h] += z[h];
+        }
       }
       red_i ^= 1;
+      if (any_raise && !cp.first) {
+        // O in TMEM holds this segment's earlier chunks (their PVs are complete: S(i)
+        // was committed after them); scale the raised heads' columns by alpha.
+#pragma unroll
+        for (int mb = 0; mb < 4; ++mb) {
+          float ov[16];
+          tmem_ld16(tmem_o + mb * 16 + lane_off, ov);
+          tmem_ld_wait();
+#pragma unroll
+          for (int h = 0; h < kMlaHeads; ++h) ov[h] *= alpha[h];
+          tmem_st16(tmem_o + mb * 16 + lane_off, ov);
+        }
+        tmem_st_wait();
+      }
       // P^T (K-major: row = head, 128 keys = 2 atoms) for the second MMA
       if (!mbar_wait(smem_u32(&p_empty[sb]), ph2 ^ 1, &abort_flag, A.err)) break;
       uint8_t* pb = p_buf + sb * kPBufBytes;
@@ -486,22 +517,9 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       for (int h = 0; h < kMlaHeads; ++h)
         *reinterpret_cast<__nv_bfloat16*>(pb + sw128_offset(h, tid * 2, kQAtomBytes)) = __float2bfloat16_rn(z[h]);
       fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&p_full[sb]));
-      // add this chunk's O^T (lane = latent column within a 128-block)
-      if (!mbar_wait(smem_u32(&o_full[sb]), ph2, &abort_flag, A.err)) break;
-      tc_fence_after();
-#pragma unroll
-      for (int mb = 0; mb < 4; ++mb) {
-        float ov[16];
-        tmem_ld16(tmem_o + sb * 64 + mb * 16 + lane_off, ov);
-        tmem_ld_wait();
-#pragma unroll
-        for (int h = 0; h < kMlaHeads; ++h) o[mb][h] = fmaf(o[mb][h], alpha[h], ov[h]);
-      }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&o_empty[sb]));
+      if (lane == 0) mbar_arrive(smem_u32(&p_full[sb]));
 
       if (cp.last) {
         // total sum per head over the 128 key lanes
@@ -516,30 +534,47 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         for (int h = 0; h < kMlaHeads; ++h)
           lt[h] = red[red_i][0][h] + red[red_i][1][h] + red[red_i][2][h] + red[red_i][3][h];
         red_i ^= 1;
+        // O^T after this chunk's PV (lane = latent column within a 128-block),
+        // streamed out one 16-column block of TMEM at a time
+        if (!mbar_wait(smem_u32(&o_full), i & 1, &abort_flag, A.err)) break;
+        tc_fence_after();
         const int64_t c_first = split_owner((int64_t)cp.t * A.C, A.n_chunks, G);
         const int64_t c_last = split_owner((int64_t)cp.t * A.C + A.C - 1, A.n_chunks, G);
+        const bool whole = c_first == c_last;
         const int hbase = hg * kMlaHeads;
-        if (c_first == c_last) {
+        const int64_t row0 = whole ? (int64_t)cp.t * A.H + hbase : ((int64_t)cp.t + blockIdx.x) * A.H + hbase;
 #pragma unroll
-          for (int h = 0; h < kMlaHeads; ++h) {
-            if (h >= h_eff) break;
-            const float inv = lt[h] > 0.f ? 1.f / lt[h] : 0.f;
-            __nv_bfloat16* orow = A.out + ((int64_t)cp.t * A.H + hbase + h) * kDimLatent;
+        for (int h = 0; h < kMlaHeads; ++h) lt[h] = lt[h] > 0.f ? 1.f / lt[h] : 0.f;   // now 1/l
+#pragma unroll 1
+        for (int mb = 0; mb < 4; ++mb) {
+          float ov[16];
+          tmem_ld16(tmem_o + mb * 16 + lane_off, ov);
+          tmem_ld_wait();
+          if (whole) {
+            __nv_bfloat16* op = A.out + row0 * kDimLatent + mb * 128 + tid;
 #pragma unroll
-            for (int mb = 0; mb < 4; ++mb) orow[mb * 128 + tid] = __float2bfloat16_rn(o[mb][h] * inv);
-            if (A.lse && tid == h)
-              A.lse[(int64_t)cp.t * A.H + hbase + h] = lt[h] > 0.f ? (m[h] + log2f(lt[h])) * kLn2 : -__int_as_float(0x7f800000);
+            for (int h = 0; h < kMlaHeads; ++h)
+              if (h < h_eff) op[(int64_t)h * kDimLatent] = __float2bfloat16_rn(ov[h] * lt[h]);
+          } else {
+            float* op = A.o_part + row0 * kDimLatent + mb * 128 + tid;
+#pragma unroll
+            for (int h = 0; h < kMlaHeads; ++h)
+              if (h < h_eff) op[(int64_t)h * kDimLatent] = ov[h];
           }
-        } else {
-          const int64_t seg_id = (int64_t)cp.t + blockIdx.x;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&o_free));
+        if (tid < h_eff) {
+          float mh = m[0], inv = lt[0];
 #pragma unroll
-          for (int h = 0; h < kMlaHeads; ++h) {
-            if (h >= h_eff) break;
-            const int64_t r = seg_id * A.H + hbase + h;
-            float* orow = A.o_part + r * kDimLatent;
-#pragma unroll
-            for (int mb = 0; mb < 4; ++mb) orow[mb * 128 + tid] = o[mb][h];
-            if (tid == h) { A.ml_part[2 * r] = m[h]; A.ml_part[2 * r + 1] = lt[h]; }
+          for (int h = 1; h < kMlaHeads; ++h)
+            if (tid == h) { mh = m[h]; inv = lt[h]; }
+          if (whole) {
+            if (A.lse) A.lse[row0 + tid] = inv > 0.f ? (mh - log2f(inv)) * kLn2 : neg_inf;
+          } else {
+            A.ml_part[2 * (row0 + tid)] = mh;
+            A.ml_part[2 * (row0 + tid) + 1] = inv > 0.f ? 1.f / inv : 0.f;
           }
         }
       }

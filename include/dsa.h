@@ -90,11 +90,11 @@ typedef struct {
  *     (one scale per token); the scores use q = code*q_scale, k = code*k_scale.
  *   qk_dtype DSA_BF16: q_idx [T, Hi, 128] bf16, idx_k_cache [num_pages, 64, 128]
  *     bf16; q_scale and idx_k_scale must be NULL.
- *   w [T, Hi] fp32 head weights. 1 <= Hi <= 64.
+ *   w [T, Hi] fp32 head weights. Hi is a multiple of 4, 4 <= Hi <= 64.
  *   scores [T, score_stride] fp32 (device, written): for query t and s <= pos(t),
  *     scores[t*score_stride + s] = I[t,s]; entries pos(t) < s < seq_len are set to
  *     -inf; entries s >= seq_len are not written. score_stride >= max_seq_len.
- *   All pointers device, 16-byte aligned; the caches are contiguous.
+ *   All pointers device, 16-byte aligned; tensors are contiguous.
  */
 dsa_status_t dsa_indexer_scores(const dsa_geom_t* geom, dsa_dtype_t qk_dtype, int32_t Hi,
                                 const void* q_idx, const float* q_scale, const float* w,

@@ -66,7 +66,9 @@ def test_host_validation(lib):
     # zero work: OK without touching the device
     assert _topk(lib, _geom(T=0)) == _lib.DSA_OK
     g = _geom()
-    # indexer: Hi out of range, bf16 with a scale pointer, misaligned cache
+    # indexer: Hi out of range or not a multiple of 4, bf16 with a scale pointer, misaligned cache
+    assert lib.dsa_indexer_scores(C.byref(g), _lib.DSA_E4M3, 6, 16, 16, 16, 16, 16, 16, 128, 256,
+                                  4096, None) == _lib.DSA_ERR_INVALID_ARG
     assert lib.dsa_indexer_scores(C.byref(g), _lib.DSA_E4M3, 65, 16, 16, 16, 16, 16, 16, 128, 256,
                                   4096, None) == _lib.DSA_ERR_INVALID_ARG
     assert lib.dsa_indexer_scores(C.byref(g), _lib.DSA_BF16, 4, 16, 16, 16, 16, None, 16, 128, 256,
