@@ -4,10 +4,11 @@
 //
 // One CTA of 1024 threads per row segment of at most 16384 entries, held in
 // registers (entry e is item e/1024 of thread e%1024). Scores map to 32-bit keys
-// whose unsigned order is the float order (-0 folded onto +0). Four 8-bit MSB-first
-// passes build a shared-memory histogram of the keys still matching the prefix
-// (warp-aggregated with match.any) and narrow the prefix to the bin holding the
-// k-th largest key; the passes stop early once that bin is taken whole. An
+// whose unsigned order is the float order (-0 folded onto +0). Three MSB-first
+// passes (11, 11 and 10 bits) build a shared-memory histogram of the keys still
+// matching the prefix and narrow the prefix to the bin holding the k-th largest
+// key; the passes stop early once that bin is taken whole. After the first pass
+// only that bin's elements take part, so the later passes touch few elements. An
 // element is then taken if its masked key is above the prefix, or equal to it and
 // among the first `rem` equal ones by position (ties to the lower position). The
 // output positions come from one ordered ballot/prefix scan, so indices leave in
@@ -49,7 +50,8 @@ struct TopkLaunch {
 };
 
 __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkLaunch L) {
-  __shared__ int hist[256];
+  __shared__ int hist[2048];
+  __shared__ int wsum[32];
   __shared__ int sel_bin, sel_above, sel_cnt;
   __shared__ int wt_gt[kTopkItems][32], wt_eq[kTopkItems][32];
   __shared__ int row_len_s;
@@ -120,52 +122,62 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkLaunch 
     }
   }
 
-  // ---- radix passes
+  // ---- radix passes: digits of 11, 11 and 10 bits (MSB first). The first pass
+  // histograms every element; later passes only the elements still matching the
+  // selected prefix, which are few, so plain shared-memory atomics suffice.
   uint32_t prefix = 0u, pmask = 0u;
   int rem = k;
 #pragma unroll 1
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    if (tid < 256) hist[tid] = 0;
+  for (int pass = 0; pass < 3; ++pass) {
+    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+    const int nbits = pass == 2 ? 10 : 11;
+    const int nb = 1 << nbits;
+    const uint32_t dmask = (uint32_t)nb - 1u;
+    for (int j = tid; j < nb; j += kTopkThreads) hist[j] = 0;
     if (tid == 0) { sel_bin = 0; sel_above = 0; sel_cnt = -1; }
     __syncthreads();
 #pragma unroll
     for (int i = 0; i < kTopkItems; ++i) {
-      const bool cand = ((valid_bits >> i) & 1u) && ((key[i] & pmask) == prefix);
-      const uint32_t bin = cand ? ((key[i] >> shift) & 0xFFu) : 0x100u;
-      const unsigned peers = __match_any_sync(0xffffffffu, bin);
-      if (cand && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+      if (((valid_bits >> i) & 1u) && ((key[i] & pmask) == prefix)) atomicAdd(&hist[(key[i] >> shift) & dmask], 1);
     }
     __syncthreads();
-    if (warp == 0) {
-      int cnt[8], s = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) { cnt[j] = hist[255 - 8 * lane - j]; s += cnt[j]; }
-      int incl = s;
+    // suffix search over the bins, highest bin first: thread t owns bins nb-1-2t and nb-2-2t
+    {
+      const int hi_bin = nb - 1 - 2 * tid;
+      const int c0 = hi_bin >= 0 ? hist[hi_bin] : 0;
+      const int c1 = hi_bin - 1 >= 0 ? hist[hi_bin - 1] : 0;
+      const int own = c0 + c1;
+      int incl = own;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int v = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += v;
       }
-      const int excl = incl - s;
-      if (excl < rem && rem <= incl) {
-        int acc = excl;
+      if (lane == 31) wsum[warp] = incl;
+      __syncthreads();
+      if (warp == 0) {
+        const int v = wsum[lane];
+        int iv = v;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (acc + cnt[j] >= rem) {
-            sel_bin = 255 - 8 * lane - j; sel_above = acc; sel_cnt = cnt[j];
-            break;
-          }
-          acc += cnt[j];
+        for (int o = 1; o < 32; o <<= 1) {
+          const int u = __shfl_up_sync(0xffffffffu, iv, o);
+          if (lane >= o) iv += u;
         }
+        wsum[lane] = iv - v;   // exclusive prefix of warp totals
+      }
+      __syncthreads();
+      const int excl = wsum[warp] + incl - own;
+      if (own > 0 && excl < rem && rem <= excl + own) {
+        if (excl + c0 >= rem) { sel_bin = hi_bin; sel_above = excl; sel_cnt = c0; }
+        else { sel_bin = hi_bin - 1; sel_above = excl + c0; sel_cnt = c1; }
       }
     }
     __syncthreads();
     rem -= sel_above;
     prefix |= (uint32_t)sel_bin << shift;
-    pmask |= 0xFFu << shift;
+    pmask |= dmask << shift;
     const bool whole = (sel_cnt == rem);
-    __syncthreads();   // sel_* are rewritten by the next pass
+    __syncthreads();   // sel_* and wsum are rewritten by the next pass
     if (whole) break;
   }
 
