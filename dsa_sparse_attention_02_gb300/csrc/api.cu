@@ -182,7 +182,8 @@ size_t attend_scratch_bytes(const dsa_geom_t* g, int H, int k) {
 }
 
 dsa_status_t run_attend(const dsa_geom_t* g, dsa_dtype_t dt, int H, const void* q, const void* kv, const int* idx,
-                        int k, float sm_scale, void* out, float* lse, void* scratch, int* err, cudaStream_t st) {
+                        int k, float sm_scale, void* out, float* lse, void* scratch, int* err, bool pdl,
+                        cudaStream_t st) {
   CUtensorMap mq;
   if (!encode_mla_q_map(&mq, q, g->T, H)) return DSA_ERR_CUDA;
   MlaArgs A;
@@ -194,7 +195,7 @@ dsa_status_t run_attend(const dsa_geom_t* g, dsa_dtype_t dt, int H, const void* 
   A.o_part = reinterpret_cast<float*>(scratch);
   A.ml_part = A.o_part + rows * 512;
   A.err = err;
-  return from_cuda(mla_launch(dt == DSA_E4M3, mq, A, grid, st));
+  return from_cuda(mla_launch(dt == DSA_E4M3, mq, A, grid, pdl, st));
 }
 
 int64_t step_score_stride(const dsa_geom_t* g) { return (int64_t)align_up((size_t)g->max_seq_len, 64); }
@@ -247,7 +248,7 @@ dsa_status_t dsa_topk(const dsa_geom_t* geom, const float* scores, int64_t score
     return DSA_ERR_WORKSPACE;
   if (geom->T == 0) return DSA_OK;
   return from_cuda(topk_launch(to_dev(geom), scores, score_stride, k, idx,
-                               reinterpret_cast<uint8_t*>(ws) + kHeaderBytes, reinterpret_cast<int*>(ws),
+                               reinterpret_cast<uint8_t*>(ws) + kHeaderBytes, reinterpret_cast<int*>(ws), false,
                                reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -265,7 +266,7 @@ dsa_status_t dsa_sparse_mla_attend(const dsa_geom_t* geom, dsa_dtype_t kv_dtype,
     return DSA_ERR_WORKSPACE;
   if (geom->T == 0) return DSA_OK;
   return run_attend(geom, kv_dtype, H, q, kv_cache, idx, k, sm_scale, out, lse,
-                    reinterpret_cast<uint8_t*>(ws) + kHeaderBytes, reinterpret_cast<int*>(ws),
+                    reinterpret_cast<uint8_t*>(ws) + kHeaderBytes, reinterpret_cast<int*>(ws), false,
                     reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -319,11 +320,14 @@ dsa_status_t dsa_decode_step(const dsa_step_args_t* a, void* ws, size_t ws_bytes
     s = run_indexer(g, a->qk_dtype, a->Hi, a->q_idx, a->q_scale, a->w, a->idx_k_cache, a->idx_k_scale, scores, stride,
                     err, st);
     if (s != DSA_OK) return s;
-    s = from_cuda(topk_launch(to_dev(g), scores, stride, a->topk, idx_buf, p, err, st));
+    // The top-k and attention kernels follow this call's own kernels, so they may
+    // launch early (programmatic dependent launch) and wait for their inputs inside.
+    s = from_cuda(topk_launch(to_dev(g), scores, stride, a->topk, idx_buf, p, err, true, st));
     if (s != DSA_OK) return s;
     idx = idx_buf;
   }
-  return run_attend(g, a->kv_dtype, a->H, a->q, a->kv_cache, idx, a->topk, a->sm_scale, a->out, a->lse, p, err, st);
+  return run_attend(g, a->kv_dtype, a->H, a->q, a->kv_cache, idx, a->topk, a->sm_scale, a->out, a->lse, p, err,
+                    a->reuse_idx == nullptr, st);
 }
 
 dsa_status_t dsa_get_error(void* ws, void* stream) {

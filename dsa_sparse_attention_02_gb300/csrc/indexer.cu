@@ -150,6 +150,9 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
+  // The top-k grid that follows may start launching (it waits for these scores).
+  griddep_launch_dependents();
+  griddep_wait();   // a no-op unless this grid itself was launched programmatically
 
   const int U = prefix[B];
   const int G = gridDim.x;

@@ -25,8 +25,11 @@ int indexer_max_requests();
 
 // ---- radix top-k (topk.cu)
 size_t topk_workspace_bytes(int T, int max_seq_len, int k);
+// pdl: the launch may overlap the tail of the kernel just before it on the stream
+// (programmatic dependent launch); set only when that kernel is one of this library's
+// and the geometry was complete before it started.
 cudaError_t topk_launch(const GeomDev& g, const float* scores, int64_t stride, int k, int* idx,
-                        void* scratch, int* err, cudaStream_t st);
+                        void* scratch, int* err, bool pdl, cudaStream_t st);
 
 // ---- sparse MLA + combine (sparse_mla.cu)
 struct MlaArgs {
@@ -44,10 +47,11 @@ struct MlaArgs {
   float* ml_part;      // [T + G, H, 2]  (running max in log2 units, sum)
   int* err;
 };
+// Number of two-CTA clusters of the persistent attention grid.
 int mla_grid(int64_t n_chunks, int num_sms);
 size_t mla_partial_bytes(int T, int H, int grid);
 // map_q: [T*H, 576] bf16 query rows, 64 x min(H,16) box, 128-byte swizzle.
-cudaError_t mla_launch(bool fp8_kv, const CUtensorMap& map_q, MlaArgs A, int grid, cudaStream_t st);
+cudaError_t mla_launch(bool fp8_kv, const CUtensorMap& map_q, MlaArgs A, int grid, bool pdl, cudaStream_t st);
 bool encode_mla_q_map(CUtensorMap* map_q, const void* q, int T, int H);
 
 // ---- host helpers defined in api.cu

@@ -97,7 +97,7 @@ extern "C" dsa_status_t dsa_sparse_mla_attend_static(const dsa_geom_t* geom, dsa
   A.o_part = reinterpret_cast<float*>(scratch);
   A.ml_part = A.o_part + (size_t)(geom->T + grid) * H * 512;
   A.err = reinterpret_cast<int*>(err_word);
-  const cudaError_t le = mla_launch(kv_dtype == DSA_E4M3, mq, A, grid, reinterpret_cast<cudaStream_t>(stream));
+  const cudaError_t le = mla_launch(kv_dtype == DSA_E4M3, mq, A, grid, false, reinterpret_cast<cudaStream_t>(stream));
   if (le != cudaSuccess) {
     set_last_error("kernel launch", cudaGetErrorString(le));
     return DSA_ERR_CUDA;

@@ -9,39 +9,37 @@
 //   out[t,h,:] = sum_i softmax(z)_i kv[s_i, 0:512],  lse[t,h] = ln sum_i exp(z_i)
 //
 // Work: the T x C list of (query, 128-key chunk) pairs, C = ceil(k/128), split
-// evenly over a persistent grid. A chunk's 128 selected rows live in shared
-// memory as 128-byte-swizzled K-major atoms of 64 bf16 columns: four "pair"
-// slots of two atoms (latent columns 0..511) and one RoPE atom (512..575). The
-// slots form rings (5 pair slots, 2 RoPE slots), so the next chunk's RoPE atom
-// and first pair load while the current chunk computes, and its other pairs
-// load as soon as the current chunk's PV MMAs release theirs.
+// evenly over a persistent grid of two-CTA clusters. The two CTAs of a cluster
+// walk the same chunks and split every selected row by columns: CTA r holds
+// latent columns 256r..256r+255 (two "pairs" of 64-column atoms) and RoPE
+// columns 512+32r..512+32r+31, i.e. half of each 1152-byte row. Each CTA's share
+// of a chunk (72 KB) is small enough that two chunks are resident at once, so the
+// next chunk streams in while the current one is scored and reduced.
 //   * a resolver warp maps each chunk's 128 logical positions to physical cache
 //     rows through the block table (-1 for padding or out-of-range entries) up
-//     to four chunks ahead, into a shared-memory row table that the producer
-//     and the softmax warps read.
-//   * bf16 cache: two producer warps copy the rows with 16-byte cp.async, slot
-//     by slot (RoPE atom, then the four pairs), each warp half of every slot;
-//     padding rows are zero-filled. Each producer thread ends a slot with
-//     cp.async.mbarrier.arrive.noinc, so the slot's full barrier completes when
-//     the copies have landed and producers never wait on their own copies; the
-//     MMA thread fences the generic->async proxy after each wait. (TMA
-//     tile::gather4 of 4 x 128-byte row pieces measured at half the bandwidth
-//     of this on the same access pattern.)
-//   * e4m3 cache: three producer warps load the 656-byte records, dequantize
-//     (code * per-128 scale) to bf16 and store into the same slots.
-//   * one MMA thread: S^T = KV . Q^T on tcgen05 (M = 128 keys, N = 16 heads,
-//     K = 576) into TMEM, then O^T = V^T . P^T (M = 128 latent columns x 4
+//     to four chunks ahead, into a shared-memory row table.
+//   * four producer warps copy the CTA's columns of the rows with 16-byte
+//     cp.async into 128-byte-swizzled K-major atoms (zero-fill for padding), and
+//     end each slot with cp.async.mbarrier.arrive.noinc, so a slot's full barrier
+//     completes when its copies have landed. e4m3 cache: the latent codes are
+//     loaded, dequantized (code * per-128 scale) to bf16 and stored instead.
+//   * one MMA thread (issuing S steps and PVs as they become ready, so that
+//     S(i+1) overlaps the softmax of chunk i): partial S^T = KV . Q^T over the CTA's 288 columns on
+//     tcgen05 (M = 128 keys, N = 16 heads) into TMEM, then, once P is known,
+//     O^T = V^T . P^T for the CTA's 256 latent columns (M = 128 columns x 2
 //     blocks, N = 16, K = 128 keys), V^T read MN-major from the pair slots.
-//   * 4 softmax warps (TMEM lane = key for S) run the online softmax per head in
-//     the exp2 domain and write P^T as bf16 for the second MMA. O^T accumulates
-//     in TMEM across a query's chunks. The reference max moves only when a
-//     chunk's max exceeds it by more than 2^8 (p <= 256 otherwise); then the
-//     softmax warps rescale O in TMEM (lane = latent column) before releasing P.
-//     S(i) completing implies PV(i-1) completed (a commit tracks every earlier
-//     MMA of the issuing thread), so that rescale needs no further wait.
-// A CTA that holds every chunk of a query writes the final bf16 output; other
-// segments write (unnormalized O, running max, sum) partials that the combine
-// kernel merges with log-sum-exp weights.
+//   * 4 softmax warps (TMEM lane = key) exchange the partial scores with the
+//     other CTA through distributed shared memory (8 KB per chunk each way), add
+//     them (the same sum in both CTAs, since fp32 addition commutes), and run the
+//     online softmax per head in the exp2 domain; both CTAs obtain bit-identical
+//     P and statistics. O^T accumulates in TMEM across a query's chunks. The
+//     reference max moves only when a chunk's max exceeds it by more than 2^8
+//     (p <= 256 otherwise); then the softmax warps wait for PV(i-1) and rescale
+//     O in TMEM before releasing P. The partial scores go out with st.async,
+//     counted on the receiver's mbarrier; buffer release is a plain signal.
+// A cluster that holds every chunk of a query writes the final bf16 output (each
+// CTA its 256 columns); other segments write (unnormalized O, running max, sum)
+// partials that the combine kernel merges with log-sum-exp weights.
 #include <cstdint>
 #include <cuda_bf16.h>
 #include "kernels.cuh"
@@ -52,13 +50,15 @@ constexpr int kMlaHeads = 16;                       // heads per CTA (MMA N)
 constexpr int kMlaKeys = 128;                       // keys per chunk (MMA M)
 constexpr int kAtomBytes = kMlaKeys * 128;          // 16 KB: 128 rows x 64 bf16
 constexpr int kPairBytes = 2 * kAtomBytes;          // 32 KB
-constexpr int kPairSlots = 5;
-constexpr int kRopeSlots = 2;
+constexpr int kPairSlots = 5;                       // two and a half chunks of the CTA's two pairs
+constexpr int kRopeSlots = 2;                       // halves of one RoPE atom (chunk parity)
 constexpr int kQAtomBytes = kMlaHeads * 128;        // 2 KB
-constexpr int kQBufBytes = 9 * kQAtomBytes;         // 18 KB
+constexpr int kQAtoms = 6;                          // the CTA's 4 latent atoms + 2 RoPE atoms
+constexpr int kQBufBytes = kQAtoms * kQAtomBytes;   // 12 KB
 constexpr int kPBufBytes = 2 * kQAtomBytes;         // P^T: 16 heads x 128 keys bf16 = 4 KB
-constexpr int kMlaSmemBytes =
-    1024 + kPairSlots * kPairBytes + kRopeSlots * kAtomBytes + kQBufBytes + 2 * kPBufBytes;
+constexpr int kXBufBytes = kMlaKeys * kMlaHeads * 4;  // partial scores from the other CTA: 8 KB
+constexpr int kMlaSmemBytes = 1024 + kPairSlots * kPairBytes + kAtomBytes + kQBufBytes +
+                              2 * kPBufBytes + 2 * kXBufBytes;
 // Twelve warps, 168 registers each (three per SM sub-partition):
 //   warps 0-3   softmax (one per TMEM lane quarter)
 //   warps 4-7   producers (one per sub-partition, so that copy issue runs on all four)
@@ -69,7 +69,7 @@ constexpr int kProdWarps = 4;
 constexpr int kMmaWarp = 8;
 constexpr int kResolverWarp = 9;
 constexpr int kRowBufs = 4;                         // row-table ring depth (chunks)
-constexpr int kMlaTmemCols = 128;                   // S: 2 x 16, O: 64
+constexpr int kMlaTmemCols = 64;                    // S: 2 x 16, O: 2 x 16
 constexpr float kRescaleLog2 = 8.f;                 // lazy rescale threshold (log2 units)
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -177,27 +177,33 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     sparse_mla_kernel(const __grid_constant__ CUtensorMap map_q, const MlaArgs A) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* pair_buf = smem;                                         // 5 x 32 KB
-  uint8_t* rope_buf = pair_buf + kPairSlots * kPairBytes;           // 2 x 16 KB
-  uint8_t* q_buf = rope_buf + kRopeSlots * kAtomBytes;              // 18 KB
+  uint8_t* pair_buf = smem;                                         // 4 x 32 KB
+  uint8_t* rope_buf = pair_buf + kPairSlots * kPairBytes;           // 16 KB
+  uint8_t* q_buf = rope_buf + kAtomBytes;                           // 12 KB
   uint8_t* p_buf = q_buf + kQBufBytes;                              // 2 x 4 KB
+  float4* x_buf = reinterpret_cast<float4*>(p_buf + 2 * kPBufBytes);  // 2 x [4 head quads][128 keys]
 
   __shared__ uint64_t pair_full[kPairSlots], pair_empty[kPairSlots], rope_full[kRopeSlots], rope_empty[kRopeSlots];
   __shared__ uint64_t q_full, q_empty;
   __shared__ uint64_t s_full[2], s_empty[2], p_full[2], p_empty[2], o_full, o_free, grp_bar;
+  __shared__ uint64_t x_full[2], x_free[2];   // partial-score exchange with the other CTA
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
   __shared__ __align__(16) float red[2][4][kMlaHeads];
+  __shared__ __align__(16) int over_s[2][4];   // per softmax warp: a key exceeds the reference by > 2^8
   __shared__ __align__(16) int rows_s[kRowBufs][kMlaKeys];   // physical row per key of a chunk, -1 = none
   __shared__ uint64_t rows_full[kRowBufs], rows_empty[kRowBufs];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const GeomDev& g = A.g;
-  const int G = gridDim.x;
+  const int rank = (int)cluster_ctarank();            // column half of this CTA
+  const int peer = rank ^ 1;
+  const int G = (int)cluster_count_x();               // clusters (work splits over clusters)
+  const int cid = (int)cluster_id_x();
   const int hg = blockIdx.y;
   const int h_eff = min(kMlaHeads, A.H - hg * kMlaHeads);
-  const int64_t c_begin = split_begin(blockIdx.x, A.n_chunks, G);
-  const int64_t c_end = split_begin(blockIdx.x + 1, A.n_chunks, G);
+  const int64_t c_begin = split_begin(cid, A.n_chunks, G);
+  const int64_t c_end = split_begin(cid + 1, A.n_chunks, G);
   const int n_mine = (int)(c_end - c_begin);
   const int slot_producers = 32 * kProdWarps;   // one arrival per producer thread per slot fill
 
@@ -209,6 +215,27 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     cp.first = (i == 0) || (cp.cq == 0);
     cp.last = (i == n_mine - 1) || (cp.cq == A.C - 1);
     return cp;
+  };
+  // The same walked one chunk at a time, without a division per step.
+  auto chunk_next = [&](ChunkPos& cp, int i_next) {
+    ++cp.chunk;
+    if (++cp.cq == A.C) { cp.cq = 0; ++cp.t; }
+    cp.first = (cp.cq == 0);
+    cp.last = (i_next == n_mine - 1) || (cp.cq == A.C - 1);
+  };
+  // Q atoms of this CTA: latent columns 256*rank + 64a (a = 0..3); then two RoPE
+  // atoms. The CTA's RoPE columns 32*rank..32*rank+31 sit in 16-byte chunks
+  // 4p..4p+3 of the KV RoPE atom for chunk parity p, and must sit at the same
+  // chunks of the Q atom the MMA pairs them with: atom 4 starts at column 512
+  // (its chunks 4*rank.. hold them), atom 5 at 480 + 64*rank (its chunks
+  // 4*(1-rank).. hold them; columns past 575 are zero-filled by TMA).
+  auto load_q = [&](int t) {
+    const uint32_t bar = smem_u32(&q_full);
+    mbar_arrive_expect_tx(bar, kQAtoms * h_eff * 128);   // out-of-range columns are zero-filled and counted
+    for (int a = 0; a < kQAtoms; ++a)
+      tma_load_2d(smem_u32(q_buf + a * kQAtomBytes), &map_q, bar,
+                  a < 4 ? 256 * rank + 64 * a : (a == 4 ? kDimLatent : kDimLatent - 32 + 64 * rank),
+                  t * A.H + hg * kMlaHeads);
   };
 
   if (tid == 0) {
@@ -222,6 +249,8 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       mbar_init(smem_u32(&s_empty[j]), 4);
       mbar_init(smem_u32(&p_full[j]), 4);
       mbar_init(smem_u32(&p_empty[j]), 1);
+      mbar_init(smem_u32(&x_full[j]), 1);     // local expect_tx + 8 KB of st.async from the other CTA
+      mbar_init(smem_u32(&x_free[j]), 4);     // one signal per softmax warp of the other CTA
     }
     mbar_init(smem_u32(&o_full), 1);     // one phase per chunk's PV
     mbar_init(smem_u32(&o_free), 4);     // softmax warps have read O at a segment end
@@ -240,15 +269,21 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // The other CTA's barriers are initialized before any remote arrival.
+  cluster_sync();
   const uint32_t tmem = tmem_base_s;
   const uint32_t tmem_s = tmem;          // + 16 * buf
-  const uint32_t tmem_o = tmem + 32;     // + 16 * mb
+  const uint32_t tmem_o = tmem + 32;     // + 16 * block
+  // The query rows are inputs of this call, not results of the preceding kernel.
+  if (warp == kProdWarp0 && lane == 0 && n_mine > 0) { tma_prefetch_desc(&map_q); load_q(chunk_pos(0).t); }
+  // Everything below may read what the preceding kernel wrote (the index rows).
+  griddep_wait();
 
   if (warp >= kProdWarp0 && warp < kProdWarp0 + kProdWarps) {
     // ================================================================ producers
     // Warp pw copies rows [32*pw, 32*pw+32) of every slot. bf16: 16-byte cp.async
     // (zero-fill for padding), slot completion through cp.async.mbarrier.arrive.noinc.
-    // e4m3: the RoPE atom by cp.async as well; the latent pairs are loaded,
+    // e4m3: the RoPE half by cp.async as well; the latent pairs are loaded,
     // dequantized to bf16 and stored, then each thread arrives.
     const int pw = warp - kProdWarp0;
     int seg = 0;
@@ -258,18 +293,13 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       return __shfl_sync(0xffffffffu, ok, 0) != 0;
     };
     const size_t row_bytes = kFp8Kv ? (size_t)kFp8Record : (size_t)(kDimQK * 2);
-    const size_t rope_off = kFp8Kv ? (size_t)(kDimLatent + 16) : (size_t)(kDimLatent * 2);
-    for (int i = 0; i < n_mine; ++i) {
-      const ChunkPos cp = chunk_pos(i);
+    const size_t rope_off = (kFp8Kv ? (size_t)(kDimLatent + 16) : (size_t)(kDimLatent * 2)) + 64 * rank;
+    ChunkPos cp = chunk_pos(0);
+    for (int i = 0; i < n_mine; chunk_next(cp, ++i)) {
       if (cp.first) {
-        if (pw == 0) {
+        if (pw == 0 && seg > 0) {
           if (!slot_acquire(smem_u32(&q_empty), (seg & 1) ^ 1)) break;
-          if (lane == 0) {
-            const uint32_t bar = smem_u32(&q_full);
-            mbar_arrive_expect_tx(bar, 9 * h_eff * 128);
-            for (int a = 0; a < 9; ++a)
-              tma_load_2d(smem_u32(q_buf + a * kQAtomBytes), &map_q, bar, a * 64, cp.t * A.H + hg * kMlaHeads);
-          }
+          if (lane == 0) load_q(cp.t);
         }
         ++seg;
       }
@@ -278,23 +308,25 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       mbar_try_wait(smem_u32(&rows_full[rb]), (i / kRowBufs) & 1);   // acquire in every lane (phase is complete)
       const int* rows = rows_s[rb];
       const uint8_t* kv = A.kv;
-      // RoPE atom: 8 lanes per row (128 B), 4 rows per instruction
+      // RoPE columns of this CTA: 4 lanes per row (64 B), 8 rows per instruction,
+      // into logical 16-byte chunks 4*rs..4*rs+3 of the shared RoPE atom's rows
       if (!slot_acquire(smem_u32(&rope_empty[rs]), ((i / kRopeSlots) & 1) ^ 1)) break;
       {
-        const uint32_t dst0 = smem_u32(rope_buf + rs * kAtomBytes);
+        const uint32_t dst0 = smem_u32(rope_buf);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int ri = 32 * pw + 4 * j + (lane >> 3);
+        for (int j = 0; j < 4; ++j) {
+          const int ri = 32 * pw + 8 * j + (lane >> 2);
           const int row = rows[ri];
-          const int cb = (lane & 7) * 16;
-          cp_async_16(dst0 + sw128_offset(ri, cb, 0), kv + (int64_t)(row >= 0 ? row : 0) * row_bytes + rope_off + cb,
-                      row >= 0 ? 16u : 0u);
+          const int cb = (lane & 3) * 16;
+          cp_async_16(dst0 + sw128_offset(ri, 64 * rs + cb, 0),
+                      kv + (int64_t)(row >= 0 ? row : 0) * row_bytes + rope_off + cb, row >= 0 ? 16u : 0u);
         }
         cp_async_arrive_noinc(smem_u32(&rope_full[rs]));
       }
       bool stop = false;
-      for (int j = 0; j < 4; ++j) {
-        const int gidx = 4 * i + j, ps = gidx % kPairSlots;
+      for (int jl = 0; jl < 2; ++jl) {
+        const int j = 2 * rank + jl;                 // pair of the row: latent columns 128j..128j+127
+        const int gidx = 2 * i + jl, ps = gidx % kPairSlots;
         if (!slot_acquire(smem_u32(&pair_empty[ps]), ((gidx / kPairSlots) & 1) ^ 1)) { stop = true; break; }
         uint8_t* slot = pair_buf + ps * kPairBytes;
         if (!kFp8Kv) {
@@ -353,8 +385,8 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     // ================================================================ row resolver
     int t_cached = -1;
     QueryInfo qi{};
-    for (int i = 0; i < n_mine; ++i) {
-      const ChunkPos cp = chunk_pos(i);
+    ChunkPos cp = chunk_pos(0);
+    for (int i = 0; i < n_mine; chunk_next(cp, ++i)) {
       if (cp.t != t_cached) { qi = query_info_warp(g, cp.t); t_cached = cp.t; }
       const int rb = i % kRowBufs;
       int rr[4];
@@ -367,62 +399,105 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ================================================================ MMA issuer
+    // Issues, in order within each kind, the S steps of chunk s_i (RoPE, pair 0,
+    // pair 1 as each lands) and the PV of chunk pv_i < s_i (once its P is
+    // written), whichever is ready first, so that S(i+1) overlaps softmax(i) and
+    // PV(i) never waits behind the next chunk's loads. A PV is preferred when both
+    // are ready, since it releases ring slots.
     if (lane == 0) {
       constexpr uint32_t idesc_s = make_idesc(128, kMlaHeads, kFmtBF16, kFmtBF16, 0, 0);
       constexpr uint32_t idesc_o = make_idesc(128, kMlaHeads, kFmtBF16, kFmtBF16, 1, 0);
       const uint32_t pair0 = smem_u32(pair_buf), rope0 = smem_u32(rope_buf), q0 = smem_u32(q_buf);
-      int seg = -1;
-      for (int i = 0; i < n_mine; ++i) {
-        const ChunkPos cp = chunk_pos(i);
-        if (cp.first) ++seg;
-        const int sb = i & 1, rs = i % kRopeSlots;
-        const uint32_t ph2 = (i >> 1) & 1;
-        if (!mbar_wait(smem_u32(&s_empty[sb]), ph2 ^ 1, &abort_flag, A.err)) break;
-        if (cp.first && !mbar_wait(smem_u32(&q_full), seg & 1, &abort_flag, A.err)) break;
-        if (!mbar_wait(smem_u32(&rope_full[rs]), (i / kRopeSlots) & 1, &abort_flag, A.err)) break;
-        fence_proxy_async_smem();   // slot filled through the generic proxy (cp.async / st.shared)
-        tc_fence_after();
-        const uint32_t d_s = tmem_s + sb * 16;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_f16_ss(d_s, smem_desc(rope0 + rs * kAtomBytes + kk * 32, 0, 1024, kSwizzle128B),
-                     smem_desc(q0 + 8 * kQAtomBytes + kk * 32, 0, 1024, kSwizzle128B), idesc_s, kk != 0);
-        mma_commit(smem_u32(&rope_empty[rs]));
-        bool stop = false;
-        for (int j = 0; j < 4; ++j) {
-          const int gidx = 4 * i + j, ps = gidx % kPairSlots;
-          if (!mbar_wait(smem_u32(&pair_full[ps]), (gidx / kPairSlots) & 1, &abort_flag, A.err)) { stop = true; break; }
-          fence_proxy_async_smem();
-          tc_fence_after();
-#pragma unroll
-          for (int a2 = 0; a2 < 2; ++a2) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_f16_ss(d_s, smem_desc(pair0 + ps * kPairBytes + a2 * kAtomBytes + kk * 32, 0, 1024, kSwizzle128B),
-                         smem_desc(q0 + (2 * j + a2) * kQAtomBytes + kk * 32, 0, 1024, kSwizzle128B), idesc_s, 1);
-          }
-        }
-        if (stop) break;
-        mma_commit(smem_u32(&s_full[sb]));
-        if (cp.last) mma_commit(smem_u32(&q_empty));
-        if (!mbar_wait(smem_u32(&p_full[sb]), ph2, &abort_flag, A.err)) break;
-        // a new segment's first PV overwrites O: the previous segment's O must have been read
-        if (cp.first && seg > 0 && !mbar_wait(smem_u32(&o_free), (seg - 1) & 1, &abort_flag, A.err)) break;
-        tc_fence_after();
-        const uint32_t p0 = smem_u32(p_buf + sb * kPBufBytes);
+      int s_i = 0, s_step = 0, s_seg = -1;   // s_step: 0 = RoPE next, 1 = pair 0 next, 2 = pair 1 next
+      int pv_i = 0, pv_seg = -1;
+      ChunkPos s_cp = chunk_pos(0), pv_cp = s_cp;
+      uint64_t t_idle = globaltimer_ns();
+      while (pv_i < n_mine) {
+        bool progress = false;
+        if (pv_i < s_i) {
+          const ChunkPos& cp = pv_cp;
+          const int sb = pv_i & 1;
+          // a new segment's first PV overwrites O: the previous segment's O must have been read
+          const bool o_ok = !cp.first || pv_seg < 0 || mbar_test_wait(smem_u32(&o_free), pv_seg & 1);
+          if (o_ok && mbar_test_wait(smem_u32(&p_full[sb]), (pv_i >> 1) & 1)) {
+            if (cp.first) ++pv_seg;
+            tc_fence_after();
+            const uint32_t p0 = smem_u32(p_buf + sb * kPBufBytes);
 #pragma unroll 1
-        for (int mb = 0; mb < 4; ++mb) {
-          const int ps = (4 * i + mb) % kPairSlots;
+            for (int mb = 0; mb < 2; ++mb) {
+              const int ps = (2 * pv_i + mb) % kPairSlots;
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint64_t ad = smem_desc(pair0 + ps * kPairBytes + ks * 2048, kAtomBytes, 1024, kSwizzle128B);
-            const uint64_t bd = smem_desc(p0 + (ks >> 2) * kQAtomBytes + (ks & 3) * 32, 0, 1024, kSwizzle128B);
-            mma_f16_ss(tmem_o + mb * 16, ad, bd, idesc_o, (ks != 0 || !cp.first) ? 1u : 0u);
+              for (int ks = 0; ks < 8; ++ks) {
+                const uint64_t ad = smem_desc(pair0 + ps * kPairBytes + ks * 2048, kAtomBytes, 1024, kSwizzle128B);
+                const uint64_t bd = smem_desc(p0 + (ks >> 2) * kQAtomBytes + (ks & 3) * 32, 0, 1024, kSwizzle128B);
+                mma_f16_ss(tmem_o + mb * 16, ad, bd, idesc_o, (ks != 0 || !cp.first) ? 1u : 0u);
+              }
+              mma_commit(smem_u32(&pair_empty[ps]));
+            }
+            mma_commit(smem_u32(&o_full));
+            mma_commit(smem_u32(&p_empty[sb]));
+            chunk_next(pv_cp, ++pv_i);
+            progress = true;
           }
-          mma_commit(smem_u32(&pair_empty[ps]));
         }
-        mma_commit(smem_u32(&o_full));
-        mma_commit(smem_u32(&p_empty[sb]));
+        if (s_i < n_mine) {
+          const ChunkPos& cp = s_cp;
+          const int sb = s_i & 1, rs = s_i % kRopeSlots;
+          const uint32_t d_s = tmem_s + sb * 16;
+          if (s_step == 0) {
+            if ((!cp.first || mbar_test_wait(smem_u32(&q_full), (s_seg + 1) & 1)) &&
+                mbar_test_wait(smem_u32(&s_empty[sb]), ((s_i >> 1) & 1) ^ 1) &&
+                mbar_test_wait(smem_u32(&rope_full[rs]), (s_i / kRopeSlots) & 1)) {
+              if (cp.first) ++s_seg;
+              fence_proxy_async_smem();   // slot filled through the generic proxy (cp.async / st.shared)
+              tc_fence_after();
+              // RoPE columns 32*rank..32*rank+31: K-steps 2*rs and 2*rs+1 of the atom,
+              // against the Q RoPE atom that holds the same columns at the same chunks
+              const uint32_t q_rope = q0 + (rs == rank ? 4 : 5) * kQAtomBytes;
+#pragma unroll
+              for (int kk = 0; kk < 2; ++kk) {
+                const uint32_t off = (2 * rs + kk) * 32;
+                mma_f16_ss(d_s, smem_desc(rope0 + off, 0, 1024, kSwizzle128B),
+                           smem_desc(q_rope + off, 0, 1024, kSwizzle128B), idesc_s, kk != 0);
+              }
+              mma_commit(smem_u32(&rope_empty[rs]));
+              s_step = 1;
+              progress = true;
+            }
+          } else {
+            const int jl = s_step - 1, gidx = 2 * s_i + jl, ps = gidx % kPairSlots;
+            if (mbar_test_wait(smem_u32(&pair_full[ps]), (gidx / kPairSlots) & 1)) {
+              fence_proxy_async_smem();
+              tc_fence_after();
+#pragma unroll
+              for (int a2 = 0; a2 < 2; ++a2) {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                  mma_f16_ss(d_s, smem_desc(pair0 + ps * kPairBytes + a2 * kAtomBytes + kk * 32, 0, 1024, kSwizzle128B),
+                             smem_desc(q0 + (2 * jl + a2) * kQAtomBytes + kk * 32, 0, 1024, kSwizzle128B), idesc_s, 1);
+              }
+              if (jl == 1) {
+                mma_commit(smem_u32(&s_full[sb]));
+                if (cp.last) mma_commit(smem_u32(&q_empty));
+                chunk_next(s_cp, ++s_i);
+                s_step = 0;
+              } else {
+                s_step = 2;
+              }
+              progress = true;
+            }
+          }
+        }
+        if (progress) {
+          t_idle = globaltimer_ns();
+        } else {
+          if (abort_flag) break;
+          if (globaltimer_ns() - t_idle > kWaitLimitNs) {
+            abort_flag = 1;
+            record_error(A.err, kDevTimeout);
+            break;
+          }
+        }
       }
     }
   } else if (warp < 4) {
@@ -432,8 +507,13 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     const float neg_inf = -__int_as_float(0x7f800000);
     float m[kMlaHeads], l[kMlaHeads];
-    for (int i = 0; i < n_mine; ++i) {
-      const ChunkPos cp = chunk_pos(i);
+    // exchange addresses: this thread's float4 slot per head quad, locally and in the other CTA
+    const uint32_t x_local = smem_u32(x_buf) + tid * 16;
+    const uint32_t x_remote = mapa_shared(x_local, peer);
+    const uint32_t xfull_remote = mapa_shared(smem_u32(&x_full[0]), peer);
+    const uint32_t xfree_remote = mapa_shared(smem_u32(&x_free[0]), peer);
+    ChunkPos cp = chunk_pos(0);
+    for (int i = 0; i < n_mine; chunk_next(cp, ++i)) {
       const int sb = i & 1;
       const uint32_t ph2 = (i >> 1) & 1;
       if (cp.first) {
@@ -454,21 +534,50 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&s_empty[sb]));
-      // chunk max per head across the 128 keys
+      // ---- exchange the partial scores with the other CTA (buffer sb, layout [quad][key]):
+      // st.async into its buffer, counted on its x_full; it signals x_free once read.
+      if (!mbar_wait(smem_u32(&x_free[sb]), ph2 ^ 1, &abort_flag, A.err)) break;   // it has read buffer sb
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4)
+        st_async_v4(x_remote + (uint32_t)(sb * kXBufBytes + q4 * kMlaKeys * 16), z[4 * q4], z[4 * q4 + 1],
+                    z[4 * q4 + 2], z[4 * q4 + 3], xfull_remote + sb * 8);
+      if (tid == 0) mbar_arrive_expect_tx(smem_u32(&x_full[sb]), kXBufBytes);
+      if (!mbar_wait<true>(smem_u32(&x_full[sb]), ph2, &abort_flag, A.err)) break;
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const float4 v = x_buf[sb * (kXBufBytes / 16) + q4 * kMlaKeys + tid];
+        z[4 * q4] += v.x; z[4 * q4 + 1] += v.y; z[4 * q4 + 2] += v.z; z[4 * q4 + 3] += v.w;
+      }
+      __syncwarp();   // the warp's reads of the buffer are done (their sums are in registers)
+      if (lane == 0) mbar_arrive_remote_signal(xfree_remote + sb * 8);
 #pragma unroll
       for (int h = 0; h < kMlaHeads; ++h) z[h] = valid ? z[h] * A.scale_log2 : neg_inf;
+      // The reference max of a head moves only where this chunk exceeds it by more
+      // than 2^8. Usually no key does: one flag per warp settles that, and only
+      // otherwise is the chunk max per head reduced across the 128 keys.
+      bool over = false;
+#pragma unroll
+      for (int h = 0; h < kMlaHeads; ++h) over |= z[h] > m[h] + kRescaleLog2;   // also true for m = -inf
       {
-        // after the butterfly, lanes 2h' and 2h'+1 hold the warp max of head hidx below
-        // (exchange distances 16, 8, 4, 2 select head bits 3, 2, 1, 0)
-        const float wm = warp_max16(z);
-        const int hidx = ((lane >> 4) & 1) << 3 | ((lane >> 3) & 1) << 2 | ((lane >> 2) & 1) << 1 | ((lane >> 1) & 1);
-        if ((lane & 1) == 0) red[red_i][warp][hidx] = wm;
+        const bool warp_over = __any_sync(0xffffffffu, over);
+        if (lane == 0) over_s[red_i][warp] = warp_over ? 1 : 0;
       }
       if (!gs.sync(&abort_flag, A.err)) break;
-      // move the reference max only where this chunk exceeds it by more than 2^8
+      const int4 ov4 = *reinterpret_cast<const int4*>(over_s[red_i]);
+      red_i ^= 1;
       float alpha[kMlaHeads];
       bool any_raise = false;
-      {
+#pragma unroll
+      for (int h = 0; h < kMlaHeads; ++h) alpha[h] = 1.f;
+      if (ov4.x | ov4.y | ov4.z | ov4.w) {   // uniform over the four warps
+        {
+          // after the butterfly, lanes 2h' and 2h'+1 hold the warp max of head hidx below
+          // (exchange distances 16, 8, 4, 2 select head bits 3, 2, 1, 0)
+          const float wm = warp_max16(z);
+          const int hidx = ((lane >> 4) & 1) << 3 | ((lane >> 3) & 1) << 2 | ((lane >> 2) & 1) << 1 | ((lane >> 1) & 1);
+          if ((lane & 1) == 0) red[red_i][warp][hidx] = wm;
+        }
+        if (!gs.sync(&abort_flag, A.err)) break;
         float cmv[kMlaHeads];
 #pragma unroll
         for (int q4 = 0; q4 < kMlaHeads / 4; ++q4) {
@@ -481,26 +590,30 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
           cmv[4 * q4 + 2] = fmaxf(fmaxf(r0.z, r1.z), fmaxf(r2.z, r3.z));
           cmv[4 * q4 + 3] = fmaxf(fmaxf(r0.w, r1.w), fmaxf(r2.w, r3.w));
         }
+        red_i ^= 1;
 #pragma unroll
         for (int h = 0; h < kMlaHeads; ++h) {
           const float cm = cmv[h];
-          alpha[h] = 1.f;
           if (cm > m[h] + kRescaleLog2) {       // also true for the first finite max (m = -inf)
             alpha[h] = (m[h] == neg_inf) ? 0.f : fast_exp2(m[h] - cm);
             any_raise = true;
             m[h] = cm;
           }
-          l[h] *= alpha[h];
-          z[h] = (z[h] == neg_inf) ? 0.f : fast_exp2(z[h] - m[h]);   // z now holds p <= 256
-          l[h] += z[h];
         }
       }
-      red_i ^= 1;
-      if (any_raise && !cp.first) {
-        // O in TMEM holds this segment's earlier chunks (their PVs are complete: S(i)
-        // was committed after them); scale the raised heads' columns by alpha.
 #pragma unroll
-        for (int mb = 0; mb < 4; ++mb) {
+      for (int h = 0; h < kMlaHeads; ++h) {
+        l[h] *= alpha[h];
+        z[h] = (z[h] == neg_inf) ? 0.f : fast_exp2(z[h] - m[h]);   // z now holds p <= 256
+        l[h] += z[h];
+      }
+      if (any_raise && !cp.first) {
+        // O in TMEM holds this segment's earlier chunks; once PV(i-1) has completed,
+        // scale the raised heads' columns by alpha (PV(i) waits for this chunk's P).
+        if (!mbar_wait(smem_u32(&o_full), (i - 1) & 1, &abort_flag, A.err)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int mb = 0; mb < 2; ++mb) {
           float ov[16];
           tmem_ld16(tmem_o + mb * 16 + lane_off, ov);
           tmem_ld_wait();
@@ -542,21 +655,22 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         const int64_t c_last = split_owner((int64_t)cp.t * A.C + A.C - 1, A.n_chunks, G);
         const bool whole = c_first == c_last;
         const int hbase = hg * kMlaHeads;
-        const int64_t row0 = whole ? (int64_t)cp.t * A.H + hbase : ((int64_t)cp.t + blockIdx.x) * A.H + hbase;
+        const int64_t row0 = whole ? (int64_t)cp.t * A.H + hbase : ((int64_t)cp.t + cid) * A.H + hbase;
+        const int col0 = 256 * rank + tid;
 #pragma unroll
         for (int h = 0; h < kMlaHeads; ++h) lt[h] = lt[h] > 0.f ? 1.f / lt[h] : 0.f;   // now 1/l
 #pragma unroll 1
-        for (int mb = 0; mb < 4; ++mb) {
+        for (int mb = 0; mb < 2; ++mb) {
           float ov[16];
           tmem_ld16(tmem_o + mb * 16 + lane_off, ov);
           tmem_ld_wait();
           if (whole) {
-            __nv_bfloat16* op = A.out + row0 * kDimLatent + mb * 128 + tid;
+            __nv_bfloat16* op = A.out + row0 * kDimLatent + mb * 128 + col0;
 #pragma unroll
             for (int h = 0; h < kMlaHeads; ++h)
               if (h < h_eff) op[(int64_t)h * kDimLatent] = __float2bfloat16_rn(ov[h] * lt[h]);
           } else {
-            float* op = A.o_part + row0 * kDimLatent + mb * 128 + tid;
+            float* op = A.o_part + row0 * kDimLatent + mb * 128 + col0;
 #pragma unroll
             for (int h = 0; h < kMlaHeads; ++h)
               if (h < h_eff) op[(int64_t)h * kDimLatent] = ov[h];
@@ -565,7 +679,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&o_free));
-        if (tid < h_eff) {
+        if (rank == 0 && tid < h_eff) {   // the statistics are identical in both CTAs
           float mh = m[0], inv = lt[0];
 #pragma unroll
           for (int h = 1; h < kMlaHeads; ++h)
@@ -581,16 +695,21 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     }
   }
 
+  // The combine kernel may start launching; it waits for this grid to finish.
+  griddep_launch_dependents();
   tc_fence_before();
   __syncthreads();
+  // Neither CTA leaves while the other may still write into its shared memory.
+  cluster_sync();
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kMlaTmemCols);
   }
 }
 
-// Merge the partial segments of every query that more than one CTA worked on.
+// Merge the partial segments of every query that more than one cluster worked on.
 __global__ void __launch_bounds__(128) mla_combine_kernel(const MlaArgs A, int G) {
+  griddep_wait();   // the partials come from the attention grid just before
   const int t = blockIdx.x;
   const int h = blockIdx.y;
   const int64_t c_first = split_owner((int64_t)t * A.C, A.n_chunks, G);
@@ -617,8 +736,36 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(const MlaArgs A, int G
 }
 
 // ------------------------------------------------------------------ host side
+// Clusters of two CTAs that can be resident at once (the grid is persistent),
+// cached per device; the cluster placement limit can be below half the SM count.
+static int mla_max_clusters(int num_sms) {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return num_sms / 2;
+  if (cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaFuncSetAttribute(sparse_mla_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMlaSmemBytes) ==
+      cudaSuccess) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+    cfg.blockDim = dim3(kMlaThreads, 1, 1);
+    cfg.dynamicSmemBytes = kMlaSmemBytes;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2; at[0].val.clusterDim.y = 1; at[0].val.clusterDim.z = 1;
+    cfg.attrs = at; cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, sparse_mla_kernel<false>, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();
+  if (n <= 0 || n > num_sms / 2) n = num_sms / 2;
+  if (n < 1) n = 1;
+  cache[dev] = n;
+  return n;
+}
+
 int mla_grid(int64_t n_chunks, int num_sms) {
-  return (int)(n_chunks < num_sms ? n_chunks : num_sms);
+  const int clusters = mla_max_clusters(num_sms);
+  return (int)(n_chunks < clusters ? n_chunks : clusters);
 }
 
 size_t mla_partial_bytes(int T, int H, int grid) {
@@ -626,17 +773,32 @@ size_t mla_partial_bytes(int T, int H, int grid) {
   return rows * kDimLatent * sizeof(float) + rows * 2 * sizeof(float);
 }
 
-cudaError_t mla_launch(bool fp8_kv, const CUtensorMap& map_q, MlaArgs A, int grid, cudaStream_t st) {
+cudaError_t mla_launch(bool fp8_kv, const CUtensorMap& map_q, MlaArgs A, int grid, bool pdl, cudaStream_t st) {
   const int hgroups = (A.H + kMlaHeads - 1) / kMlaHeads;
   auto kern = fp8_kv ? sparse_mla_kernel<true> : sparse_mla_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMlaSmemBytes);
   if (e != cudaSuccess) return e;
-  kern<<<dim3(grid, hgroups), kMlaThreads, kMlaSmemBytes, st>>>(map_q, A);
-  e = cudaGetLastError();
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2; at[0].val.clusterDim.y = 1; at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(2 * grid, hgroups, 1);
+  cfg.blockDim = dim3(kMlaThreads, 1, 1);
+  cfg.dynamicSmemBytes = kMlaSmemBytes;
+  cfg.stream = st;
+  cfg.attrs = at; cfg.numAttrs = 2;
+  e = cudaLaunchKernelEx(&cfg, kern, map_q, A);
   if (e != cudaSuccess) return e;
-  if (A.C > 1) {  // a query with several chunks may span CTAs
-    mla_combine_kernel<<<dim3(A.g.T, A.H), 128, 0, st>>>(A, grid);
-    e = cudaGetLastError();
+  if (A.C > 1) {  // a query with several chunks may span clusters
+    cudaLaunchConfig_t cc{};
+    cc.gridDim = dim3(A.g.T, A.H, 1);
+    cc.blockDim = dim3(128, 1, 1);
+    cc.stream = st;
+    cc.attrs = &at[1]; cc.numAttrs = 1;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
+    e = cudaLaunchKernelEx(&cc, mla_combine_kernel, A, grid);
   }
   return e;
 }

@@ -61,22 +61,27 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkLaunch 
   if (L.mode == 1) { t = blockIdx.x / L.nchunks; c = blockIdx.x % L.nchunks; }
   else t = blockIdx.x;
 
-  if (tid == 0) {
-    int n;
-    if (L.mode == 2) {
-      // A row with no more valid keys than k keeps all of them: its candidates are
-      // exactly positions 0..pos, so it takes the short path below with n = pos+1.
-      const QueryInfo qi = query_info(L.g, t);
-      const int valid = qi.ok ? qi.pos + 1 : 0;
-      n = valid <= L.k ? valid : L.nchunks * L.k;
-    } else {
-      const QueryInfo qi = query_info(L.g, t);
-      if (!qi.ok) { record_error(L.err, kDevBadIndex); n = 0; }
-      else n = qi.pos + 1;
-      if (L.mode == 1) n = max(0, min(L.chunk, n - c * L.chunk));
+  // Row length from the geometry (an input of the call, not of the preceding
+  // kernel), found by one warp while the scores may still be in flight.
+  if (warp == 0) {
+    const QueryInfo qi = query_info_warp(L.g, t);
+    if (lane == 0) {
+      int n;
+      if (L.mode == 2) {
+        // A row with no more valid keys than k keeps all of them: its candidates are
+        // exactly positions 0..pos, so it takes the short path below with n = pos+1.
+        const int valid = qi.ok ? qi.pos + 1 : 0;
+        n = valid <= L.k ? valid : L.nchunks * L.k;
+      } else {
+        if (!qi.ok) { record_error(L.err, kDevBadIndex); n = 0; }
+        else n = qi.pos + 1;
+        if (L.mode == 1) n = max(0, min(L.chunk, n - c * L.chunk));
+      }
+      row_len_s = n;
     }
-    row_len_s = n;
   }
+  griddep_launch_dependents();
+  griddep_wait();   // scores (or candidates) come from the preceding kernel
   __syncthreads();
   const int n = row_len_s;
   const int k = L.k;
@@ -264,25 +269,34 @@ size_t topk_workspace_bytes(int T, int max_seq_len, int k) {
   return (size_t)T * p.nchunks * k * (sizeof(uint32_t) + sizeof(int));
 }
 
+static cudaError_t launch_topk_kernel(const TopkLaunch& L, int grid, bool pdl, cudaStream_t st) {
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kTopkThreads, 1, 1);
+  cfg.stream = st;
+  cfg.attrs = at; cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, topk_kernel, L);
+}
+
 cudaError_t topk_launch(const GeomDev& g, const float* scores, int64_t stride, int k, int* idx,
-                        void* scratch, int* err, cudaStream_t st) {
+                        void* scratch, int* err, bool pdl, cudaStream_t st) {
   const TopkPlan p = topk_plan(g.max_seq_len, k);
   TopkLaunch L{};
   L.g = g; L.k = k; L.scores = scores; L.score_stride = stride; L.idx_out = idx; L.err = err;
   if (p.levels == 1) {
     L.mode = 0;
-    topk_kernel<<<g.T, kTopkThreads, 0, st>>>(L);
-    return cudaGetLastError();
+    return launch_topk_kernel(L, g.T, pdl, st);
   }
   uint32_t* ck = reinterpret_cast<uint32_t*>(scratch);
   int* ci = reinterpret_cast<int*>(ck + (size_t)g.T * p.nchunks * k);
   L.mode = 1; L.chunk = p.chunk; L.nchunks = p.nchunks; L.cand_key_out = ck; L.cand_idx_out = ci;
-  topk_kernel<<<g.T * p.nchunks, kTopkThreads, 0, st>>>(L);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_topk_kernel(L, g.T * p.nchunks, pdl, st);
   if (e != cudaSuccess) return e;
   L.mode = 2; L.cand_key_in = ck; L.cand_idx_in = ci;
-  topk_kernel<<<g.T, kTopkThreads, 0, st>>>(L);
-  return cudaGetLastError();
+  return launch_topk_kernel(L, g.T, true, st);   // follows the chunk pass just launched
 }
 
 }  // namespace dsa
