@@ -15,13 +15,16 @@
 // the head sum within its own registers, multiplies the key's scale and writes
 // one score per query, -inf past the query's causal position.
 //
-// Roles: warp P decodes 32 units at a time (one per lane) and fills an S-stage
-// smem ring by TMA: the two key pages, the group's query rows, and by bulk copy
-// the pages' key scales and the queries' w and q_scale rows, plus a small unit
-// descriptor; warp M issues the MMAs into two TMEM accumulators; 4*EW epilogue
-// warps drain them reading only TMEM and the stage, and release the stage with
-// the MMA. Units are split contiguously over a persistent grid, key-tile major
-// so that consecutive units of a multi-query request reuse the same key tile.
+// Roles: warp P decodes 32 units at a time (one per lane) and, per unit, loads
+// only what changed since the previous unit: a new key tile (two pages by TMA,
+// their key scales by bulk copy) into a ring of key stages, and a new query group
+// (the QG x Hp query rows by TMA, w and q_scale by bulk copy) into a ring of query
+// slots; a small descriptor per unit names the stage and slot it uses. In decode
+// a request's query is loaded once for all its key tiles; in prefill a key tile is
+// loaded once for the run of query groups that follow it. Warp M issues the MMAs
+// into two TMEM accumulators; 4*EW epilogue warps drain them (one 64-column TMEM
+// load per query) reading only TMEM, the stage and the slot. Units are split
+// contiguously over a persistent grid, key-tile major.
 #include <cstdint>
 #include "kernels.cuh"
 
@@ -33,40 +36,48 @@ struct IndexerCfg {
   static constexpr int kAtoms = kFp8 ? 1 : 2;                  // 128-byte column blocks per row
   static constexpr int kN = kQG * kHp;                         // MMA N
   static constexpr int kKeyBytes = 128 * 128 * kAtoms;         // one 128-key tile
-  static constexpr int kQBytes = kN * 128 * kAtoms;
-  // per-stage side data: key scales (2 pages x 64), w and q_scale rows, unit descriptor
-  static constexpr int kKsOff = kKeyBytes + kQBytes;
-  static constexpr int kWOff = kKsOff + 512;
-  static constexpr int kQsOff = kWOff + kN * 4;
-  static constexpr int kDescOff = kQsOff + kN * 4;
-  static constexpr int kSideBytes = ((512 + 2 * kN * 4 + 64) + 1023) / 1024 * 1024;
-  static constexpr int kStageBytes = kKeyBytes + kQBytes + kSideBytes;
-  static constexpr int kStages = (204800 / kStageBytes) < 8 ? (204800 / kStageBytes) : 8;
+  static constexpr int kKStageBytes = kKeyBytes + 1024;        // + key scales of its two pages (512 B)
+  static constexpr int kQBytes = kN * 128 * kAtoms;            // the group's query rows
+  static constexpr int kWOff = kQBytes, kQsOff = kQBytes + kN * 4;
+  static constexpr int kQSlotBytes = (kQBytes + 2 * kN * 4 + 1023) / 1024 * 1024;
+  static constexpr int kQSlots = (kQG >= 2 && kFp8) ? 4 : 2;
+  static constexpr int kBudget = 204800;
+  static constexpr int kKStagesFit = (kBudget - kQSlots * kQSlotBytes) / kKStageBytes;
+  static constexpr int kKStages = kKStagesFit < 8 ? kKStagesFit : 8;
+  static constexpr int kDescs = 16;                            // unit descriptor ring
   static constexpr int kEW = kQG >= 2 ? 2 : 1;                 // epilogue warp groups
   static constexpr int kEpiWarps = 4 * kEW;
-  static constexpr int kThreads = 32 * (kEpiWarps + 2);
-  static constexpr int kProdWarp = kEpiWarps, kMmaWarp = kEpiWarps + 1;
+  static constexpr int kProdWarps = 1;
+  static constexpr int kThreads = 32 * (kEpiWarps + kProdWarps + 1);
+  // Register bound: warps are spread over the four SM sub-partitions, each with a
+  // quarter of the register file, so the cap is set by the busiest one.
+  static constexpr int kBoundThreads = 128 * ((kEpiWarps + kProdWarps + 1 + 3) / 4);
+  static constexpr int kProdWarp = kEpiWarps, kMmaWarp = kEpiWarps + kProdWarps;
   static constexpr int kTmemCols = (2 * kN) <= 32 ? 32 : (2 * kN) <= 64 ? 64 : (2 * kN) <= 128 ? 128
                                    : (2 * kN) <= 256 ? 256 : 512;
-  static constexpr int kMaxB = 2048;                           // requests per call
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes;
+  static constexpr int kMaxB = 1024;                           // requests per call
+  static constexpr int kSmemBytes = 1024 + kQSlots * kQSlotBytes + kKStages * kKStageBytes;
   static constexpr int kKSteps = kFp8 ? 4 : 8;
   static_assert(kN <= 256 && kN % 16 == 0, "MMA N");
-  static_assert(kStages >= 2, "stages");
+  static_assert(kKStages >= 2, "key stages");
 };
 
-// What the epilogue needs about a unit; written by the producer into the stage.
+// What the MMA and epilogue warps need about a unit; written by the producer.
 struct UnitDesc {
-  int b, tile, q_start, q_count, len, pos0, page_ok;   // pos0 = position of the unit's first query
-  int pad;
+  int b, tile, q_start, q_count, len, pos0;   // pos0 = position of the unit's first query
+  int page0, page1;                            // physical pages of the tile, -1 if unmapped
+  int kstage, qslot;                           // key stage and query slot the unit reads
+  int flags;                                   // bit 0: new key stage, bit 1: new query slot
 };
+constexpr int kNewKey = 1, kNewQuery = 2;
 
 struct UnitInfo {
   int b, tile, q_start, q_count, len, q0, pos0;  // pos0 = position of the request's first query
 };
 
 template <int kQG>
-__device__ __forceinline__ UnitInfo decode_unit(const int* prefix, int B, int u, const GeomDev& g) {
+// prefix, cuq and lens are shared-memory copies of the unit prefix, cu_q and seq_lens.
+__device__ __forceinline__ UnitInfo decode_unit(const int* prefix, const int* cuq, const int* lens, int B, int u) {
   int lo = 0, hi = B - 1;
   while (lo < hi) {  // last b with prefix[b] <= u
     const int mid = (lo + hi + 1) >> 1;
@@ -74,7 +85,7 @@ __device__ __forceinline__ UnitInfo decode_unit(const int* prefix, int B, int u,
   }
   UnitInfo ui;
   ui.b = lo;
-  const int q0 = __ldg(g.cu_q + lo), q1 = __ldg(g.cu_q + lo + 1);
+  const int q0 = cuq[lo], q1 = cuq[lo + 1];
   const int nq = q1 - q0;
   const int ngroups = (nq + kQG - 1) / kQG;
   const int local = u - prefix[lo];
@@ -82,24 +93,29 @@ __device__ __forceinline__ UnitInfo decode_unit(const int* prefix, int B, int u,
   const int grp = local - ui.tile * ngroups;
   ui.q_start = q0 + grp * kQG;
   ui.q_count = min(kQG, nq - grp * kQG);
-  ui.len = __ldg(g.seq_lens + lo);
+  ui.len = lens[lo];
   ui.q0 = q0;
   ui.pos0 = ui.len - nq;
   return ui;
 }
 
 template <bool kFp8, int kHp, int kQG>
-__global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kThreads, 1)
+__global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_q,
                    const IndexerArgs A) {
   using C = IndexerCfg<kFp8, kHp, kQG>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t full_bar[C::kStages], empty_bar[C::kStages];
+  uint8_t* q_slots = smem;                                       // kQSlots x kQSlotBytes
+  uint8_t* k_stages = smem + C::kQSlots * C::kQSlotBytes;        // kKStages x kKStageBytes
+  __shared__ uint64_t key_full[C::kKStages], key_empty[C::kKStages];
+  __shared__ uint64_t q_full[C::kQSlots], q_empty[C::kQSlots];
+  __shared__ uint64_t desc_full[C::kDescs], desc_empty[C::kDescs];
   __shared__ uint64_t tfull_bar[2], tempty_bar[2];
+  __shared__ UnitDesc descs[C::kDescs];
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
-  __shared__ int prefix[C::kMaxB + 1];
+  __shared__ int prefix[C::kMaxB + 1], cuq_s[C::kMaxB + 1], lens_s[C::kMaxB];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const GeomDev& g = A.g;
@@ -113,6 +129,9 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kThreads, 1)
       int units = 0;
       if (b < B) {
         const int q0 = __ldg(g.cu_q + b), q1 = __ldg(g.cu_q + b + 1), len = __ldg(g.seq_lens + b);
+        cuq_s[b + 1] = q1;
+        lens_s[b] = len;
+        if (b == 0) cuq_s[0] = q0;
         const int nq = q1 - q0;
         const bool ok = nq >= 0 && nq <= len && len <= g.max_seq_len && q1 <= g.T;
         if (!ok) record_error(A.err, kDevBadIndex);
@@ -131,19 +150,18 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kThreads, 1)
   }
   if (tid == 0) {
     abort_flag = 0;
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(smem_u32(&full_bar[s]), 1);
-      mbar_init(smem_u32(&empty_bar[s]), 1 + C::kEpiWarps);   // MMA commit + every epilogue warp
-    }
+    // a stage / slot is released by the MMA thread's commit and every epilogue
+    // warp once they have moved on to the next one
+    for (int s = 0; s < C::kKStages; ++s) { mbar_init(smem_u32(&key_full[s]), 1); mbar_init(smem_u32(&key_empty[s]), 1 + C::kEpiWarps); }
+    for (int s = 0; s < C::kQSlots; ++s) { mbar_init(smem_u32(&q_full[s]), 1); mbar_init(smem_u32(&q_empty[s]), 1 + C::kEpiWarps); }
+    for (int s = 0; s < C::kDescs; ++s) { mbar_init(smem_u32(&desc_full[s]), 1); mbar_init(smem_u32(&desc_empty[s]), 1 + C::kEpiWarps); }
     for (int a = 0; a < 2; ++a) { mbar_init(smem_u32(&tfull_bar[a]), 1); mbar_init(smem_u32(&tempty_bar[a]), C::kEpiWarps); }
     fence_mbar_init();
   }
   // Query rows beyond Hi and w / q_scale entries beyond Hi stay zero for the whole
   // kernel (TMA and the bulk copies write only the first Hi of them).
-  for (int s = 0; s < C::kStages; ++s) {
-    int4* z = reinterpret_cast<int4*>(smem + s * C::kStageBytes + C::kKeyBytes);
-    for (int i = tid; i < (C::kQBytes + C::kSideBytes) / 16; i += C::kThreads) z[i] = make_int4(0, 0, 0, 0);
-  }
+  for (int i = tid; i < C::kQSlots * C::kQSlotBytes / 16; i += C::kThreads)
+    reinterpret_cast<int4*>(q_slots)[i] = make_int4(0, 0, 0, 0);
   fence_proxy_async_smem();
   if (warp == C::kMmaWarp) { tmem_alloc(smem_u32(&tmem_base_s), C::kTmemCols); tmem_relinquish(); }
   tc_fence_before();
@@ -162,15 +180,18 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kThreads, 1)
   if (warp == C::kProdWarp) {
     // ================================================================ producer
     // 32 units are decoded at a time, one per lane, so their global lookups
-    // overlap; lane 0 then fills one stage per unit.
+    // overlap; lane 0 then publishes one descriptor per unit, loading a key tile
+    // or a query group only when it differs from the previous unit's.
     if (lane == 0) { tma_prefetch_desc(&map_k); tma_prefetch_desc(&map_q); }
     bool stop = false;
+    int kcount = 0, qcount = 0;                       // key stages / query slots opened so far
+    int prev_b = -1, prev_tile = -1, prev_q = -1;
     for (int u_base = u_begin; u_base < u_end && !stop; u_base += 32) {
       const int u = u_base + lane;
       UnitInfo ui{};
       int pg0 = -1, pg1 = -1;
       if (u < u_end) {
-        ui = decode_unit<kQG>(prefix, B, u, g);
+        ui = decode_unit<kQG>(prefix, cuq_s, lens_s, B, u);
         const int s0 = ui.tile * 128;
         const int* bt = g.block_table + (int64_t)ui.b * g.bt_stride;
         if (s0 < ui.len) pg0 = __ldg(bt + (s0 >> 6));
@@ -189,37 +210,58 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kThreads, 1)
         const int pos0 = __shfl_sync(0xffffffffu, ui.pos0 + (ui.q_start - ui.q0), jj);
         const int p0 = __shfl_sync(0xffffffffu, pg0, jj), p1 = __shfl_sync(0xffffffffu, pg1, jj);
         const int i = u_base + jj - u_begin;
-        const int s = i % C::kStages;
-        const uint32_t ph = (i / C::kStages) & 1;
         if (lane == 0) {
-          if (!mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1, &abort_flag, A.err)) {
-            stop = true;
-          } else {
-            uint8_t* st = smem + s * C::kStageBytes;
-            UnitDesc* d = reinterpret_cast<UnitDesc*>(st + C::kDescOff);
-            d->b = b; d->tile = tile; d->q_start = q_start; d->q_count = q_count; d->len = len; d->pos0 = pos0;
-            d->page_ok = (p0 >= 0 ? 1 : 0) | (p1 >= 0 ? 2 : 0);
-            const int np = (p0 >= 0) + (p1 >= 0);
-            uint32_t bytes = np * 64 * 128 * C::kAtoms + q_count * Hi * 128 * C::kAtoms + q_count * Hi * 4;
-            if (kFp8) bytes += np * 256 + q_count * Hi * 4;
-            const uint32_t bar = smem_u32(&full_bar[s]);
-            mbar_arrive_expect_tx(bar, bytes);
-            const int pages[2] = {p0, p1};
-            for (int hp = 0; hp < 2; ++hp) {
-              if (pages[hp] < 0) continue;
-              for (int a = 0; a < C::kAtoms; ++a)
-                tma_load_2d(smem_u32(st + a * 16384 + hp * 8192), &map_k, bar, a * (kFp8 ? 128 : 64), pages[hp] * 64);
-              if (kFp8) bulk_load(smem_u32(st + C::kKsOff + hp * 256), A.k_scale + (int64_t)pages[hp] * 64, 256, bar);
-            }
-            for (int j = 0; j < q_count; ++j) {
-              const int t = q_start + j;
-              for (int a = 0; a < C::kAtoms; ++a)
-                tma_load_2d(smem_u32(st + C::kKeyBytes + a * (C::kN * 128) + j * kHp * 128), &map_q, bar,
-                            a * (kFp8 ? 128 : 64), t * Hi);
-              bulk_load(smem_u32(st + C::kWOff + j * kHp * 4), A.w + (int64_t)t * Hi, Hi * 4, bar);
-              if (kFp8) bulk_load(smem_u32(st + C::kQsOff + j * kHp * 4), A.q_scale + (int64_t)t * Hi, Hi * 4, bar);
+          const int r = i % C::kDescs;
+          const bool new_k = (b != prev_b) || (tile != prev_tile);
+          const bool new_q = (b != prev_b) || (q_start != prev_q);
+          // a descriptor slot is fresh on the ring's first lap
+          bool ok = i < C::kDescs || mbar_wait(smem_u32(&desc_empty[r]), ((i / C::kDescs) & 1) ^ 1, &abort_flag, A.err);
+          if (ok && new_k) {
+            const int ks = kcount % C::kKStages;
+            ok = mbar_wait(smem_u32(&key_empty[ks]), ((kcount / C::kKStages) & 1) ^ 1, &abort_flag, A.err);
+            if (ok) {
+              uint8_t* st = k_stages + ks * C::kKStageBytes;
+              const uint32_t bar = smem_u32(&key_full[ks]);
+              const int np = (p0 >= 0) + (p1 >= 0);
+              mbar_arrive_expect_tx(bar, np * 64 * 128 * C::kAtoms + (kFp8 ? np * 256 : 0));
+              const int pages[2] = {p0, p1};
+              for (int hp = 0; hp < 2; ++hp) {
+                if (pages[hp] < 0) continue;
+                for (int a = 0; a < C::kAtoms; ++a)
+                  tma_load_2d(smem_u32(st + a * 16384 + hp * 8192), &map_k, bar, a * (kFp8 ? 128 : 64), pages[hp] * 64);
+                if (kFp8) bulk_load(smem_u32(st + C::kKeyBytes + hp * 256), A.k_scale + (int64_t)pages[hp] * 64, 256, bar);
+              }
+              ++kcount;
             }
           }
+          if (ok && new_q) {
+            const int qs = qcount % C::kQSlots;
+            ok = mbar_wait(smem_u32(&q_empty[qs]), ((qcount / C::kQSlots) & 1) ^ 1, &abort_flag, A.err);
+            if (ok) {
+              uint8_t* sl = q_slots + qs * C::kQSlotBytes;
+              const uint32_t bar = smem_u32(&q_full[qs]);
+              mbar_arrive_expect_tx(bar, q_count * Hi * (128 * C::kAtoms + 4 + (kFp8 ? 4 : 0)));
+              for (int j = 0; j < q_count; ++j) {
+                const int t = q_start + j;
+                for (int a = 0; a < C::kAtoms; ++a)
+                  tma_load_2d(smem_u32(sl + a * (C::kN * 128) + j * kHp * 128), &map_q, bar, a * (kFp8 ? 128 : 64), t * Hi);
+                bulk_load(smem_u32(sl + C::kWOff + j * kHp * 4), A.w + (int64_t)t * Hi, Hi * 4, bar);
+                if (kFp8) bulk_load(smem_u32(sl + C::kQsOff + j * kHp * 4), A.q_scale + (int64_t)t * Hi, Hi * 4, bar);
+              }
+              ++qcount;
+            }
+          }
+          if (ok) {
+            UnitDesc& d = descs[r];
+            d.b = b; d.tile = tile; d.q_start = q_start; d.q_count = q_count; d.len = len; d.pos0 = pos0;
+            d.page0 = p0; d.page1 = p1;
+            d.kstage = (kcount - 1) % C::kKStages;
+            d.qslot = (qcount - 1) % C::kQSlots;
+            d.flags = (new_k ? kNewKey : 0) | (new_q ? kNewQuery : 0);
+            mbar_arrive(smem_u32(&desc_full[r]));
+            prev_b = b; prev_tile = tile; prev_q = q_start;
+          }
+          stop = !ok;
         }
         stop = __shfl_sync(0xffffffffu, stop ? 1 : 0, 0) != 0;
         if (stop) break;
@@ -229,91 +271,125 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kThreads, 1)
     // ================================================================ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = make_idesc(128, C::kN, kFp8 ? kFmtE4M3 : kFmtBF16, kFp8 ? kFmtE4M3 : kFmtBF16, 0, 0);
+      int kc = 0, qc = 0, cur_k = -1, cur_q = -1;
       for (int u = u_begin, i = 0; u < u_end; ++u, ++i) {
-        const int s = i % C::kStages;
-        const uint32_t ph = (i / C::kStages) & 1;
+        const int r = i % C::kDescs;
+        if (!mbar_wait(smem_u32(&desc_full[r]), (i / C::kDescs) & 1, &abort_flag, A.err)) break;
+        const UnitDesc d = descs[r];
+        mbar_arrive(smem_u32(&desc_empty[r]));
+        if (d.flags & kNewKey) {
+          if (cur_k >= 0) mma_commit(smem_u32(&key_empty[cur_k]));   // after every MMA that read it
+          cur_k = d.kstage;
+          if (!mbar_wait(smem_u32(&key_full[cur_k]), (kc / C::kKStages) & 1, &abort_flag, A.err)) break;
+          ++kc;
+        }
+        if (d.flags & kNewQuery) {
+          if (cur_q >= 0) mma_commit(smem_u32(&q_empty[cur_q]));
+          cur_q = d.qslot;
+          if (!mbar_wait(smem_u32(&q_full[cur_q]), (qc / C::kQSlots) & 1, &abort_flag, A.err)) break;
+          ++qc;
+        }
         const int acc = i & 1;
-        const uint32_t aph = (i >> 1) & 1;
-        if (!mbar_wait(smem_u32(&full_bar[s]), ph, &abort_flag, A.err)) break;
-        if (!mbar_wait(smem_u32(&tempty_bar[acc]), aph ^ 1, &abort_flag, A.err)) break;
+        if (!mbar_wait(smem_u32(&tempty_bar[acc]), ((i >> 1) & 1) ^ 1, &abort_flag, A.err)) break;
         tc_fence_after();
-        const uint32_t kbase = smem_u32(smem + s * C::kStageBytes);
-        const uint32_t qbase = kbase + C::kKeyBytes;
-        const uint32_t d = tmem + acc * C::kN;
+        const uint32_t kbase = smem_u32(k_stages + cur_k * C::kKStageBytes);
+        const uint32_t qbase = smem_u32(q_slots + cur_q * C::kQSlotBytes);
+        const uint32_t dt = tmem + acc * C::kN;
 #pragma unroll
         for (int kk = 0; kk < C::kKSteps; ++kk) {
           const uint32_t atom = kk / 4, within = (kk % 4) * 32;
           const uint64_t ad = smem_desc(kbase + atom * 16384 + within, 0, 1024, kSwizzle128B);
           const uint64_t bd = smem_desc(qbase + atom * (C::kN * 128) + within, 0, 1024, kSwizzle128B);
-          if (kFp8) mma_f8_ss(d, ad, bd, idesc, kk > 0);
-          else mma_f16_ss(d, ad, bd, idesc, kk > 0);
+          if (kFp8) mma_f8_ss(dt, ad, bd, idesc, kk > 0);
+          else mma_f16_ss(dt, ad, bd, idesc, kk > 0);
         }
-        mma_commit(smem_u32(&empty_bar[s]));
         mma_commit(smem_u32(&tfull_bar[acc]));
       }
     }
   } else {
     // ================================================================ epilogue warps
-    // Lane = key of the tile; reads the accumulator, the key scale, w and q_scale
-    // from TMEM / the stage only.
+    // Lane = key of the tile; reads the accumulator (TMEM), w and q_scale (the
+    // query slot) and its key's scale (global, fetched before the accumulator
+    // is ready). With one query per unit the products w*q_scale stay in
+    // registers for as long as the query slot does.
     const int quarter = warp & 3, half = warp >> 2;
     const int key = quarter * 32 + lane;
     const float neg_inf = -__int_as_float(0x7f800000);
+    int kc = 0, qc = 0, cur_k = -1, cur_q = -1;
+    float wq[kQG == 1 ? kHp : 1];
     for (int u = u_begin, i = 0; u < u_end; ++u, ++i) {
-      const int s = i % C::kStages;
-      const uint32_t ph = (i / C::kStages) & 1;
+      const int r = i % C::kDescs;
+      if (!mbar_wait(smem_u32(&desc_full[r]), (i / C::kDescs) & 1, &abort_flag, A.err)) break;
+      const UnitDesc d = descs[r];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&desc_empty[r]));
+      const int page = (key < 64) ? d.page0 : d.page1;
+      // moving to a new stage / slot releases the previous one (this warp is done with it)
+      if (d.flags & kNewKey) {
+        if (cur_k >= 0 && lane == 0) mbar_arrive(smem_u32(&key_empty[cur_k]));
+        cur_k = d.kstage;
+        if (!mbar_wait(smem_u32(&key_full[cur_k]), (kc / C::kKStages) & 1, &abort_flag, A.err)) break;   // key scales visible
+        ++kc;
+      }
+      if (d.flags & kNewQuery) {
+        if (cur_q >= 0 && lane == 0) mbar_arrive(smem_u32(&q_empty[cur_q]));
+        cur_q = d.qslot;
+        if (!mbar_wait(smem_u32(&q_full[cur_q]), (qc / C::kQSlots) & 1, &abort_flag, A.err)) break;   // w, q_scale visible
+        ++qc;
+        if constexpr (kQG == 1) {
+          const uint8_t* sl = q_slots + cur_q * C::kQSlotBytes;
+#pragma unroll
+          for (int e = 0; e < kHp; e += 4) {
+            const float4 w4 = *reinterpret_cast<const float4*>(sl + C::kWOff + e * 4);
+            float4 q4 = make_float4(1.f, 1.f, 1.f, 1.f);
+            if (kFp8) q4 = *reinterpret_cast<const float4*>(sl + C::kQsOff + e * 4);
+            wq[e] = w4.x * q4.x; wq[e + 1] = w4.y * q4.y; wq[e + 2] = w4.z * q4.z; wq[e + 3] = w4.w * q4.w;
+          }
+        }
+      }
       const int acc = i & 1;
-      const uint32_t aph = (i >> 1) & 1;
-      if (!mbar_wait(smem_u32(&tfull_bar[acc]), aph, &abort_flag, A.err)) break;
-      if (!mbar_wait(smem_u32(&full_bar[s]), ph, &abort_flag, A.err)) break;   // stage data visible here
+      if (!mbar_wait(smem_u32(&tfull_bar[acc]), (i >> 1) & 1, &abort_flag, A.err)) break;
       tc_fence_after();
-      const uint8_t* st = smem + s * C::kStageBytes;
-      const UnitDesc d = *reinterpret_cast<const UnitDesc*>(st + C::kDescOff);
-      const float* wv = reinterpret_cast<const float*>(st + C::kWOff);
-      const float* qv = reinterpret_cast<const float*>(st + C::kQsOff);
+      const uint8_t* sl = q_slots + cur_q * C::kQSlotBytes;
+      const float* wv = reinterpret_cast<const float*>(sl + C::kWOff);
+      const float* qv = reinterpret_cast<const float*>(sl + C::kQsOff);
       const int sidx = d.tile * 128 + key;
       const bool in_ctx = sidx < d.len;
-      const bool page_ok = (d.page_ok >> (key >> 6)) & 1;
-      const float ks = kFp8 ? reinterpret_cast<const float*>(st + C::kKsOff)[key] : 1.f;
+      const float ks = kFp8 ? reinterpret_cast<const float*>(k_stages + cur_k * C::kKStageBytes + C::kKeyBytes)[key] : 1.f;
 #pragma unroll 1
       for (int j = half; j < kQG; j += C::kEW) {
         if (j >= d.q_count) break;
-        float sum = 0.f;
+        float v[kHp];
+        if constexpr (kHp == 64) tmem_ld64(tmem + acc * C::kN + j * kHp + ((uint32_t)(quarter * 32) << 16), v);
+        else tmem_ld16(tmem + acc * C::kN + j * kHp + ((uint32_t)(quarter * 32) << 16), v);
+        tmem_ld_wait();
+        // four partial sums (heads e, e+1, e+2, e+3 mod 4), added at the end
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int hc = 0; hc < kHp / 16; ++hc) {
-          float v[16];
-          tmem_ld16(tmem + acc * C::kN + j * kHp + hc * 16 + ((uint32_t)(quarter * 32) << 16), v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 16; e += 4) {
-            const float4 w4 = *reinterpret_cast<const float4*>(wv + j * kHp + hc * 16 + e);
-            if (kFp8) {
-              const float4 q4 = *reinterpret_cast<const float4*>(qv + j * kHp + hc * 16 + e);
-              sum = fmaf(w4.x * q4.x, fmaxf(v[e], 0.f), sum);
-              sum = fmaf(w4.y * q4.y, fmaxf(v[e + 1], 0.f), sum);
-              sum = fmaf(w4.z * q4.z, fmaxf(v[e + 2], 0.f), sum);
-              sum = fmaf(w4.w * q4.w, fmaxf(v[e + 3], 0.f), sum);
-            } else {
-              sum = fmaf(w4.x, fmaxf(v[e], 0.f), sum);
-              sum = fmaf(w4.y, fmaxf(v[e + 1], 0.f), sum);
-              sum = fmaf(w4.z, fmaxf(v[e + 2], 0.f), sum);
-              sum = fmaf(w4.w, fmaxf(v[e + 3], 0.f), sum);
-            }
+        for (int e = 0; e < kHp; e += 4) {
+          float c[4];
+          if constexpr (kQG == 1) {
+            c[0] = wq[e]; c[1] = wq[e + 1]; c[2] = wq[e + 2]; c[3] = wq[e + 3];
+          } else {
+            const float4 w4 = *reinterpret_cast<const float4*>(wv + j * kHp + e);
+            float4 q4 = make_float4(1.f, 1.f, 1.f, 1.f);
+            if (kFp8) q4 = *reinterpret_cast<const float4*>(qv + j * kHp + e);
+            c[0] = w4.x * q4.x; c[1] = w4.y * q4.y; c[2] = w4.z * q4.z; c[3] = w4.w * q4.w;
           }
+#pragma unroll
+          for (int x = 0; x < 4; ++x) s4[x] = fmaf(c[x], fmaxf(v[e + x], 0.f), s4[x]);
         }
+        const float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
         if (in_ctx) {
           const int t = d.q_start + j;
           const int pos = d.pos0 + j;
-          const float out = (sidx <= pos && page_ok) ? sum * ks : neg_inf;
+          const float out = (sidx <= pos && page >= 0) ? sum * ks : neg_inf;
           A.scores[(int64_t)t * A.stride + sidx] = out;
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(smem_u32(&tempty_bar[acc]));
-        mbar_arrive(smem_u32(&empty_bar[s]));
-      }
+      if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[acc]));
     }
   }
 

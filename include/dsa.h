@@ -91,6 +91,7 @@ typedef struct {
  *   qk_dtype DSA_BF16: q_idx [T, Hi, 128] bf16, idx_k_cache [num_pages, 64, 128]
  *     bf16; q_scale and idx_k_scale must be NULL.
  *   w [T, Hi] fp32 head weights. Hi is a multiple of 4, 4 <= Hi <= 64.
+ *   At most 1024 requests per call (B > 1024 returns DSA_ERR_UNSUPPORTED).
  *   scores [T, score_stride] fp32 (device, written): for query t and s <= pos(t),
  *     scores[t*score_stride + s] = I[t,s]; entries pos(t) < s < seq_len are set to
  *     -inf; entries s >= seq_len are not written. score_stride >= max_seq_len.
