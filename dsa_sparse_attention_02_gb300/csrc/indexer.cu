@@ -41,7 +41,10 @@ struct IndexerCfg {
   static constexpr int kWOff = kQBytes, kQsOff = kQBytes + kN * 4;
   static constexpr int kQSlotBytes = (kQBytes + 2 * kN * 4 + 1023) / 1024 * 1024;
   static constexpr int kQSlots = (kQG >= 2 && kFp8) ? 4 : 2;
-  static constexpr int kBudget = 204800;
+  // One-query e4m3 units run two CTAs per SM (two producers per SM), each with
+  // half the shared memory; the other variants one CTA with the whole budget.
+  static constexpr int kCtasPerSm = (kQG == 1 && kFp8) ? 2 : 1;
+  static constexpr int kBudget = kCtasPerSm == 2 ? 90112 : 204800;
   static constexpr int kKStagesFit = (kBudget - kQSlots * kQSlotBytes) / kKStageBytes;
   static constexpr int kKStages = kKStagesFit < 8 ? kKStagesFit : 8;
   static constexpr int kDescs = 16;                            // unit descriptor ring
@@ -52,6 +55,8 @@ struct IndexerCfg {
   // Register bound: warps are spread over the four SM sub-partitions, each with a
   // quarter of the register file, so the cap is set by the busiest one.
   static constexpr int kBoundThreads = 128 * ((kEpiWarps + kProdWarps + 1 + 3) / 4);
+  // registers: kCtasPerSm CTAs of kBoundThreads share the register file
+  static constexpr int kBoundCtas = kCtasPerSm;
   static constexpr int kProdWarp = kEpiWarps, kMmaWarp = kEpiWarps + kProdWarps;
   static constexpr int kTmemCols = (2 * kN) <= 32 ? 32 : (2 * kN) <= 64 ? 64 : (2 * kN) <= 128 ? 128
                                    : (2 * kN) <= 256 ? 256 : 512;
@@ -100,7 +105,7 @@ __device__ __forceinline__ UnitInfo decode_unit(const int* prefix, const int* cu
 }
 
 template <bool kFp8, int kHp, int kQG>
-__global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, 1)
+__global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, IndexerCfg<kFp8, kHp, kQG>::kBoundCtas)
     indexer_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_q,
                    const IndexerArgs A) {
   using C = IndexerCfg<kFp8, kHp, kQG>;
@@ -310,13 +315,14 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, 1)
     // ================================================================ epilogue warps
     // Lane = key of the tile; reads the accumulator (TMEM), w and q_scale (the
     // query slot) and its key's scale (global, fetched before the accumulator
-    // is ready). With one query per unit the products w*q_scale stay in
-    // registers for as long as the query slot does.
+    // is ready).
     const int quarter = warp & 3, half = warp >> 2;
     const int key = quarter * 32 + lane;
     const float neg_inf = -__int_as_float(0x7f800000);
     int kc = 0, qc = 0, cur_k = -1, cur_q = -1;
-    float wq[kQG == 1 ? kHp : 1];
+    // with one query per unit and one CTA per SM, w*q_scale stays in registers
+    constexpr bool kWqRegs = kQG == 1 && C::kCtasPerSm == 1;
+    float wq[kWqRegs ? kHp : 1];
     for (int u = u_begin, i = 0; u < u_end; ++u, ++i) {
       const int r = i % C::kDescs;
       if (!mbar_wait(smem_u32(&desc_full[r]), (i / C::kDescs) & 1, &abort_flag, A.err)) break;
@@ -336,7 +342,7 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, 1)
         cur_q = d.qslot;
         if (!mbar_wait(smem_u32(&q_full[cur_q]), (qc / C::kQSlots) & 1, &abort_flag, A.err)) break;   // w, q_scale visible
         ++qc;
-        if constexpr (kQG == 1) {
+        if constexpr (kWqRegs) {
           const uint8_t* sl = q_slots + cur_q * C::kQSlotBytes;
 #pragma unroll
           for (int e = 0; e < kHp; e += 4) {
@@ -368,7 +374,7 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, 1)
 #pragma unroll
         for (int e = 0; e < kHp; e += 4) {
           float c[4];
-          if constexpr (kQG == 1) {
+          if constexpr (kWqRegs) {
             c[0] = wq[e]; c[1] = wq[e + 1]; c[2] = wq[e + 2]; c[3] = wq[e + 3];
           } else {
             const float4 w4 = *reinterpret_cast<const float4*>(wv + j * kHp + e);
@@ -409,7 +415,7 @@ static cudaError_t launch_indexer_t(const CUtensorMap& mk, const CUtensorMap& mq
   auto kern = indexer_kernel<kFp8, kHp, kQG>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(mk, mq, A);
+  kern<<<grid * C::kCtasPerSm, C::kThreads, C::kSmemBytes, st>>>(mk, mq, A);
   return cudaGetLastError();
 }
 
