@@ -3,15 +3,17 @@
 // "glm5.3-flash support", Operator-level gains).
 //
 // One CTA of 1024 threads per row segment of at most 16384 entries, held in
-// registers (entry e is item e/1024 of thread e%1024). Scores map to 32-bit keys
-// whose unsigned order is the float order (-0 folded onto +0). Three MSB-first
-// passes (11, 11 and 10 bits) build a shared-memory histogram of the keys still
-// matching the prefix and narrow the prefix to the bin holding the k-th largest
-// key; the passes stop early once that bin is taken whole. After the first pass
-// only that bin's elements take part, so the later passes touch few elements. An
-// element is then taken if its masked key is above the prefix, or equal to it and
-// among the first `rem` equal ones by position (ties to the lower position). The
-// output positions come from one ordered ballot/prefix scan, so indices leave in
+// registers (thread t holds entries 16t..16t+15, read as four 16-byte loads where
+// the row is aligned). Scores map to 32-bit keys whose unsigned order is the
+// float order (-0 folded onto +0). Three MSB-first passes (11, 11 and 10 bits)
+// build a shared-memory histogram of the keys still matching the prefix and
+// narrow the prefix to the bin holding the k-th largest key; the passes stop
+// early once that bin is taken whole. After the first pass only that bin's
+// elements take part, so the later passes touch few elements. An element is then
+// taken if its masked key is above the prefix, or equal to it and among the first
+// `rem` equal ones by position (ties to the lower position). Output positions come
+// from one block-wide exclusive scan of every thread's (above, equal) counts, in
+// position order since each thread holds a contiguous run, so indices leave in
 // ascending order.
 //
 // Rows longer than one CTA's capacity are split into chunks whose exact top-k
@@ -53,7 +55,6 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkLaunch 
   __shared__ int hist[2048];
   __shared__ int wsum[32];
   __shared__ int sel_bin, sel_above, sel_cnt;
-  __shared__ int wt_gt[kTopkItems][32], wt_eq[kTopkItems][32];
   __shared__ int row_len_s;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -109,20 +110,32 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkLaunch 
     return;
   }
 
-  // ---- load keys (n > k here, n <= capacity)
+  // ---- load keys (n > k here, n <= capacity): thread t holds entries 16t..16t+15
   uint32_t key[kTopkItems];
   uint32_t valid_bits = 0;
+  const int e0 = tid * kTopkItems;
+  if (L.mode != 2 && e0 + kTopkItems <= n && ((reinterpret_cast<uintptr_t>(L.scores + in_base) & 15) == 0)) {
+    const float4* src = reinterpret_cast<const float4*>(L.scores + in_base + e0);
 #pragma unroll
-  for (int i = 0; i < kTopkItems; ++i) {
-    const int e = i * kTopkThreads + tid;
-    key[i] = 0u;
-    if (e < n) {
-      if (L.mode == 2) {
-        key[i] = L.cand_key_in[in_base + e];
-        if (L.cand_idx_in[in_base + e] >= 0) valid_bits |= 1u << i;
-      } else {
-        key[i] = orderable_key(L.scores[in_base + e]);
-        valid_bits |= 1u << i;
+    for (int q = 0; q < kTopkItems / 4; ++q) {
+      const float4 v = src[q];
+      key[4 * q] = orderable_key(v.x); key[4 * q + 1] = orderable_key(v.y);
+      key[4 * q + 2] = orderable_key(v.z); key[4 * q + 3] = orderable_key(v.w);
+    }
+    valid_bits = 0xffffu;
+  } else {
+#pragma unroll
+    for (int i = 0; i < kTopkItems; ++i) {
+      const int e = e0 + i;
+      key[i] = 0u;
+      if (e < n) {
+        if (L.mode == 2) {
+          key[i] = L.cand_key_in[in_base + e];
+          if (L.cand_idx_in[in_base + e] >= 0) valid_bits |= 1u << i;
+        } else {
+          key[i] = orderable_key(L.scores[in_base + e]);
+          valid_bits |= 1u << i;
+        }
       }
     }
   }
@@ -186,56 +199,47 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkLaunch 
     if (whole) break;
   }
 
-  // ---- ordered compaction: ranks among "above" and "equal" elements
+  // ---- ordered compaction: one block-wide exclusive scan of (above, equal)
+  // counts packed as above << 16 | equal (each total <= 16384, so no carry)
+  uint32_t gt_bits = 0, eq_bits = 0;
 #pragma unroll
   for (int i = 0; i < kTopkItems; ++i) {
     const bool v = (valid_bits >> i) & 1u;
     const uint32_t m = key[i] & pmask;
-    const unsigned gb = __ballot_sync(0xffffffffu, v && m > prefix);
-    const unsigned eb = __ballot_sync(0xffffffffu, v && m == prefix);
-    if (lane == 0) { wt_gt[i][warp] = __popc(gb); wt_eq[i][warp] = __popc(eb); }
+    if (v && m > prefix) gt_bits |= 1u << i;
+    if (v && m == prefix) eq_bits |= 1u << i;
   }
-  __syncthreads();
-  if (warp < 2) {
-    // Exclusive scan of the per-(item, warp) counts in (item, warp) order, which is
-    // position order; warp 0 scans the "above" counts, warp 1 the "equal" counts.
-    int (*tab)[32] = warp == 0 ? wt_gt : wt_eq;
-    int lv[16], sv = 0;
+  const int own = (__popc(gt_bits) << 16) | __popc(eq_bits);
+  int incl = own;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int e = lane * 16 + j;
-      lv[j] = tab[e >> 5][e & 31];
-      sv += lv[j];
-    }
-    int iv = sv;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int v = wsum[lane];
+    int iv = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, iv, o);
-      if (lane >= o) iv += v;
+      const int u = __shfl_up_sync(0xffffffffu, iv, o);
+      if (lane >= o) iv += u;
     }
-    int av = iv - sv;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int e = lane * 16 + j;
-      tab[e >> 5][e & 31] = av;
-      av += lv[j];
-    }
+    wsum[lane] = iv - v;   // exclusive prefix of warp totals
   }
   __syncthreads();
-  const unsigned lt = (1u << lane) - 1u;
+  const int excl = wsum[warp] + incl - own;
+  int rg = excl >> 16, re = excl & 0xffff;
 #pragma unroll
   for (int i = 0; i < kTopkItems; ++i) {
-    const bool v = (valid_bits >> i) & 1u;
-    const uint32_t m = key[i] & pmask;
-    const bool is_gt = v && m > prefix, is_eq = v && m == prefix;
-    const unsigned gb = __ballot_sync(0xffffffffu, is_gt);
-    const unsigned eb = __ballot_sync(0xffffffffu, is_eq);
+    const bool is_gt = (gt_bits >> i) & 1u, is_eq = (eq_bits >> i) & 1u;
     if (!is_gt && !is_eq) continue;
-    const int rg = wt_gt[i][warp] + __popc(gb & lt);
-    const int re = wt_eq[i][warp] + __popc(eb & lt);
-    if (is_eq && re >= rem) continue;
+    const bool take = is_gt || re < rem;
     const int pos = rg + min(re, rem);
-    const int e = i * kTopkThreads + tid;
+    if (is_gt) ++rg; else ++re;
+    if (!take) continue;
+    const int e = e0 + i;
     if (L.mode == 1) {
       L.cand_key_out[out_base + pos] = key[i];
       L.cand_idx_out[out_base + pos] = idx_offset + e;
