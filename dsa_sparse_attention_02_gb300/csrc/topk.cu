@@ -114,6 +114,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkLaunch 
   uint32_t key[kTopkItems];
   uint32_t valid_bits = 0;
   const int e0 = tid * kTopkItems;
+  const bool has_data = e0 < n;
   if (L.mode != 2 && e0 + kTopkItems <= n && ((reinterpret_cast<uintptr_t>(L.scores + in_base) & 15) == 0)) {
     const float4* src = reinterpret_cast<const float4*>(L.scores + in_base + e0);
 #pragma unroll
@@ -154,9 +155,11 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkLaunch 
     for (int j = tid; j < nb; j += kTopkThreads) hist[j] = 0;
     if (tid == 0) { sel_bin = 0; sel_above = 0; sel_cnt = -1; }
     __syncthreads();
+    if (has_data) {   // whole warps past the row's end skip the item loops
 #pragma unroll
-    for (int i = 0; i < kTopkItems; ++i) {
-      if (((valid_bits >> i) & 1u) && ((key[i] & pmask) == prefix)) atomicAdd(&hist[(key[i] >> shift) & dmask], 1);
+      for (int i = 0; i < kTopkItems; ++i) {
+        if (((valid_bits >> i) & 1u) && ((key[i] & pmask) == prefix)) atomicAdd(&hist[(key[i] >> shift) & dmask], 1);
+      }
     }
     __syncthreads();
     // suffix search over the bins, highest bin first: thread t owns bins nb-1-2t and nb-2-2t
@@ -202,12 +205,14 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkLaunch 
   // ---- ordered compaction: one block-wide exclusive scan of (above, equal)
   // counts packed as above << 16 | equal (each total <= 16384, so no carry)
   uint32_t gt_bits = 0, eq_bits = 0;
+  if (has_data) {
 #pragma unroll
-  for (int i = 0; i < kTopkItems; ++i) {
-    const bool v = (valid_bits >> i) & 1u;
-    const uint32_t m = key[i] & pmask;
-    if (v && m > prefix) gt_bits |= 1u << i;
-    if (v && m == prefix) eq_bits |= 1u << i;
+    for (int i = 0; i < kTopkItems; ++i) {
+      const bool v = (valid_bits >> i) & 1u;
+      const uint32_t m = key[i] & pmask;
+      if (v && m > prefix) gt_bits |= 1u << i;
+      if (v && m == prefix) eq_bits |= 1u << i;
+    }
   }
   const int own = (__popc(gt_bits) << 16) | __popc(eq_bits);
   int incl = own;
@@ -231,8 +236,12 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkLaunch 
   __syncthreads();
   const int excl = wsum[warp] + incl - own;
   int rg = excl >> 16, re = excl & 0xffff;
+  // The k outputs are placed in shared memory first, then written out coalesced.
+  extern __shared__ int out_s[];                       // [k] indices (+ [k] keys in mode 1)
+  uint32_t* key_s = reinterpret_cast<uint32_t*>(out_s + k);
 #pragma unroll
   for (int i = 0; i < kTopkItems; ++i) {
+    if ((gt_bits | eq_bits) >> i == 0) break;
     const bool is_gt = (gt_bits >> i) & 1u, is_eq = (eq_bits >> i) & 1u;
     if (!is_gt && !is_eq) continue;
     const bool take = is_gt || re < rem;
@@ -241,13 +250,22 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkLaunch 
     if (!take) continue;
     const int e = e0 + i;
     if (L.mode == 1) {
-      L.cand_key_out[out_base + pos] = key[i];
-      L.cand_idx_out[out_base + pos] = idx_offset + e;
+      out_s[pos] = idx_offset + e;
+      key_s[pos] = key[i];
     } else if (L.mode == 0) {
-      L.idx_out[out_base + pos] = e;
+      out_s[pos] = e;
     } else {
-      L.idx_out[out_base + pos] = L.cand_idx_in[in_base + e];
+      out_s[pos] = L.cand_idx_in[in_base + e];
     }
+  }
+  __syncthreads();
+  if (L.mode == 1) {
+    for (int j = tid; j < k; j += kTopkThreads) {
+      L.cand_idx_out[out_base + j] = out_s[j];
+      L.cand_key_out[out_base + j] = key_s[j];
+    }
+  } else {
+    for (int j = tid; j < k; j += kTopkThreads) L.idx_out[out_base + j] = out_s[j];
   }
 }
 
@@ -273,13 +291,22 @@ size_t topk_workspace_bytes(int T, int max_seq_len, int k) {
   return (size_t)T * p.nchunks * k * (sizeof(uint32_t) + sizeof(int));
 }
 
+// Dynamic shared memory of one launch: the staged outputs (indices, and keys in mode 1).
+static size_t topk_smem_bytes(const TopkLaunch& L) { return (size_t)L.k * (L.mode == 1 ? 8 : 4); }
+
 static cudaError_t launch_topk_kernel(const TopkLaunch& L, int grid, bool pdl, cudaStream_t st) {
+  const size_t smem = topk_smem_bytes(L);
+  if (smem > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kTopkThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = at; cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, topk_kernel, L);
