@@ -276,8 +276,9 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
   const uint32_t tmem_o = tmem + 32;     // + 16 * block
   // The query rows are inputs of this call, not results of the preceding kernel.
   if (warp == kProdWarp0 && lane == 0 && n_mine > 0) { tma_prefetch_desc(&map_q); load_q(chunk_pos(0).t); }
-  // Everything below may read what the preceding kernel wrote (the index rows).
-  griddep_wait();
+  // Only the resolver reads what the preceding kernel wrote (the index rows); it
+  // waits for that kernel (griddepcontrol.wait) before its first index load, and
+  // every other role depends on the resolver's row table.
 
   if (warp >= kProdWarp0 && warp < kProdWarp0 + kProdWarps) {
     // ================================================================ producers
@@ -383,9 +384,11 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     }
   } else if (warp == kResolverWarp) {
     // ================================================================ row resolver
-    int t_cached = -1;
-    QueryInfo qi{};
     ChunkPos cp = chunk_pos(0);
+    // the request geometry is an input of the call: looked up before the wait
+    QueryInfo qi = query_info_warp(g, cp.t);
+    int t_cached = cp.t;
+    griddep_wait();
     for (int i = 0; i < n_mine; chunk_next(cp, ++i)) {
       if (cp.t != t_cached) { qi = query_info_warp(g, cp.t); t_cached = cp.t; }
       const int rb = i % kRowBufs;
