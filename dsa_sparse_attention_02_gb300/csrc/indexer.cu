@@ -297,14 +297,14 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, Ind
         const int acc = i & 1;
         if (!mbar_wait(smem_u32(&tempty_bar[acc]), ((i >> 1) & 1) ^ 1, &abort_flag, A.err)) break;
         tc_fence_after();
-        const uint32_t kbase = smem_u32(k_stages + cur_k * C::kKStageBytes);
-        const uint32_t qbase = smem_u32(q_slots + cur_q * C::kQSlotBytes);
+        const uint64_t a0 = smem_desc(smem_u32(k_stages + cur_k * C::kKStageBytes), 0, 1024, kSwizzle128B);
+        const uint64_t b0 = smem_desc(smem_u32(q_slots + cur_q * C::kQSlotBytes), 0, 1024, kSwizzle128B);
         const uint32_t dt = tmem + acc * C::kN;
 #pragma unroll
         for (int kk = 0; kk < C::kKSteps; ++kk) {
           const uint32_t atom = kk / 4, within = (kk % 4) * 32;
-          const uint64_t ad = smem_desc(kbase + atom * 16384 + within, 0, 1024, kSwizzle128B);
-          const uint64_t bd = smem_desc(qbase + atom * (C::kN * 128) + within, 0, 1024, kSwizzle128B);
+          const uint64_t ad = desc_add(a0, atom * 16384 + within);
+          const uint64_t bd = desc_add(b0, atom * (C::kN * 128) + within);
           if (kFp8) mma_f8_ss(dt, ad, bd, idesc, kk > 0);
           else mma_f16_ss(dt, ad, bd, idesc, kk > 0);
         }

@@ -305,6 +305,14 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
          ((uint64_t)((sbo & 0x3FFFFu) >> 4) << 32) | (1ull << 46) | (swz << 61);
 }
 
+// The descriptor of the same layout starting `byte_offset` bytes further: the start
+// address sits in the low 14 bits (address >> 4), and shared-memory addresses stay
+// below 2^18 bytes, so adding offset >> 4 never carries into the other fields.
+// Building descriptors once and offsetting them keeps the MMA issue loop short.
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t byte_offset) {
+  return desc + (uint64_t)(byte_offset >> 4);
+}
+
 // Instruction descriptor: fp32 accumulator (bits 4-5 = 1), A/B formats (bits 7-9,
 // 10-12), transpose flags (bit 15 for A, 16 for B: 0 = K-major), N>>3 at bit 17,
 // M>>4 at bit 24.

@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
 
   if (tid == 0) {
     abort_flag = 0;
-    for (int j = 0; j < kPairSlots; ++j) { mbar_init(smem_u32(&pair_full[j]), slot_producers); mbar_init(smem_u32(&pair_empty[j]), 1); }
+    for (int j = 0; j < kPairSlots; ++j) { mbar_init(smem_u32(&pair_full[j]), 64); mbar_init(smem_u32(&pair_empty[j]), 1); }
     for (int j = 0; j < kRopeSlots; ++j) { mbar_init(smem_u32(&rope_full[j]), slot_producers); mbar_init(smem_u32(&rope_empty[j]), 1); }
     mbar_init(smem_u32(&q_full), 1);
     mbar_init(smem_u32(&q_empty), 1);
@@ -282,11 +282,16 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
 
   if (warp >= kProdWarp0 && warp < kProdWarp0 + kProdWarps) {
     // ================================================================ producers
-    // Warp pw copies rows [32*pw, 32*pw+32) of every slot. bf16: 16-byte cp.async
-    // (zero-fill for padding), slot completion through cp.async.mbarrier.arrive.noinc.
-    // e4m3: the RoPE half by cp.async as well; the latent pairs are loaded,
-    // dequantized to bf16 and stored, then each thread arrives.
+    // Two groups of two warps: group jl (warps 4-5: jl = 0; warps 6-7: jl = 1) fills
+    // latent pair jl of every chunk, so that both pairs of a chunk are requested at
+    // once; warp wg of a group copies rows [64*wg, 64*wg+64) of the pair. Every
+    // producer warp also copies the RoPE columns of rows [32*pw, 32*pw+32). bf16:
+    // 16-byte cp.async (zero-fill for padding), slot completion through
+    // cp.async.mbarrier.arrive.noinc. e4m3: the latent codes are loaded, dequantized
+    // to bf16 and stored, then each thread arrives.
     const int pw = warp - kProdWarp0;
+    const int jl = pw >> 1, wg = pw & 1;
+    const int j = 2 * rank + jl;                 // pair of the row: latent columns 128j..128j+127
     int seg = 0;
     auto slot_acquire = [&](uint32_t bar, uint32_t parity) -> bool {   // warp-uniform bounded wait
       int ok = 1;
@@ -315,8 +320,8 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       {
         const uint32_t dst0 = smem_u32(rope_buf);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int ri = 32 * pw + 8 * j + (lane >> 2);
+        for (int q = 0; q < 4; ++q) {
+          const int ri = 32 * pw + 8 * q + (lane >> 2);
           const int row = rows[ri];
           const int cb = (lane & 3) * 16;
           cp_async_16(dst0 + sw128_offset(ri, 64 * rs + cb, 0),
@@ -324,32 +329,40 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         }
         cp_async_arrive_noinc(smem_u32(&rope_full[rs]));
       }
-      bool stop = false;
-      for (int jl = 0; jl < 2; ++jl) {
-        const int j = 2 * rank + jl;                 // pair of the row: latent columns 128j..128j+127
-        const int gidx = 2 * i + jl, ps = gidx % kPairSlots;
-        if (!slot_acquire(smem_u32(&pair_empty[ps]), ((gidx / kPairSlots) & 1) ^ 1)) { stop = true; break; }
-        uint8_t* slot = pair_buf + ps * kPairBytes;
-        if (!kFp8Kv) {
-          // 16 lanes per row (256 B of the pair), 2 rows per instruction
-          const uint32_t dst0 = smem_u32(slot);
-#pragma unroll 4
-          for (int jj = 0; jj < 16; ++jj) {
-            const int ri = 32 * pw + 2 * jj + (lane >> 4);
-            const int row = rows[ri];
-            const int cb = (lane & 15) * 16;
-            cp_async_16(dst0 + sw128_offset(ri, cb, kAtomBytes), kv + (int64_t)(row >= 0 ? row : 0) * row_bytes + j * 256 + cb,
-                        row >= 0 ? 16u : 0u);
-          }
-          cp_async_arrive_noinc(smem_u32(&pair_full[ps]));
-        } else {
-          // 8 lanes per row: lane part p dequantizes codes 16p..16p+15 of the pair's 128
-          const int part = lane & 7, sub = lane >> 3;
+      const int gidx = 2 * i + jl, ps = gidx % kPairSlots;
+      if (!slot_acquire(smem_u32(&pair_empty[ps]), ((gidx / kPairSlots) & 1) ^ 1)) break;
+      uint8_t* slot = pair_buf + ps * kPairBytes;
+      if (!kFp8Kv) {
+        // 16 lanes per row (256 B of the pair), 2 rows per instruction: lane half h
+        // takes rows r0 .. r0+31, r0 = 64*wg + 32*h, whose indices it reads up front
+        const int r0 = 64 * wg + 32 * (lane >> 4);
+        const int cb = (lane & 15) * 16;
+        int rr[32];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int4 v = *reinterpret_cast<const int4*>(rows + r0 + 4 * q);
+          rr[4 * q] = v.x; rr[4 * q + 1] = v.y; rr[4 * q + 2] = v.z; rr[4 * q + 3] = v.w;
+        }
+        const uint32_t dst0 = smem_u32(slot);
+        const uint8_t* src0 = kv + j * 256 + cb;
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          const int row = rr[jj];
+          cp_async_16(dst0 + sw128_offset(r0 + jj, cb, kAtomBytes), src0 + (int64_t)(row >= 0 ? row : 0) * row_bytes,
+                      row >= 0 ? 16u : 0u);
+        }
+        cp_async_arrive_noinc(smem_u32(&pair_full[ps]));
+      } else {
+        // 8 lanes per row: lane part p dequantizes codes 16p..16p+15 of the pair's 128
+        const int part = lane & 7, sub = lane >> 3;
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          const int rbase = 64 * wg + 32 * half;
           uint4 c[8];
           float sc[8];
 #pragma unroll
           for (int jj = 0; jj < 8; ++jj) {
-            const int row = rows[32 * pw + 4 * jj + sub];
+            const int row = rows[rbase + 4 * jj + sub];
             c[jj] = make_uint4(0, 0, 0, 0);
             sc[jj] = 0.f;
             if (row >= 0) {
@@ -360,7 +373,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
           }
 #pragma unroll
           for (int jj = 0; jj < 8; ++jj) {
-            const int key = 32 * pw + 4 * jj + sub;
+            const int key = rbase + 4 * jj + sub;
             const uint32_t w4[4] = {c[jj].x, c[jj].y, c[jj].z, c[jj].w};
             uint32_t pk[8];
 #pragma unroll
@@ -374,11 +387,10 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
             *reinterpret_cast<uint4*>(slot + sw128_offset(key, col_byte, kAtomBytes)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             *reinterpret_cast<uint4*>(slot + sw128_offset(key, col_byte + 16, kAtomBytes)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
           }
-          fence_proxy_async_smem();
-          mbar_arrive(smem_u32(&pair_full[ps]));
         }
+        fence_proxy_async_smem();
+        mbar_arrive(smem_u32(&pair_full[ps]));
       }
-      if (stop) break;
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&rows_empty[rb]));
     }
@@ -410,7 +422,12 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = make_idesc(128, kMlaHeads, kFmtBF16, kFmtBF16, 0, 0);
       constexpr uint32_t idesc_o = make_idesc(128, kMlaHeads, kFmtBF16, kFmtBF16, 1, 0);
-      const uint32_t pair0 = smem_u32(pair_buf), rope0 = smem_u32(rope_buf), q0 = smem_u32(q_buf);
+      // descriptors built once; each MMA offsets them by a byte distance
+      const uint64_t dk_pair = smem_desc(smem_u32(pair_buf), 0, 1024, kSwizzle128B);            // K-major (S)
+      const uint64_t dmn_pair = smem_desc(smem_u32(pair_buf), kAtomBytes, 1024, kSwizzle128B);  // MN-major (PV)
+      const uint64_t dk_rope = smem_desc(smem_u32(rope_buf), 0, 1024, kSwizzle128B);
+      const uint64_t dk_q = smem_desc(smem_u32(q_buf), 0, 1024, kSwizzle128B);
+      const uint64_t dk_p = smem_desc(smem_u32(p_buf), 0, 1024, kSwizzle128B);
       int s_i = 0, s_step = 0, s_seg = -1;   // s_step: 0 = RoPE next, 1 = pair 0 next, 2 = pair 1 next
       int pv_i = 0, pv_seg = -1;
       ChunkPos s_cp = chunk_pos(0), pv_cp = s_cp;
@@ -425,16 +442,16 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
           if (o_ok && mbar_test_wait(smem_u32(&p_full[sb]), (pv_i >> 1) & 1)) {
             if (cp.first) ++pv_seg;
             tc_fence_after();
-            const uint32_t p0 = smem_u32(p_buf + sb * kPBufBytes);
-#pragma unroll 1
+            const uint64_t bd0 = desc_add(dk_p, sb * kPBufBytes);
+#pragma unroll
             for (int mb = 0; mb < 2; ++mb) {
               const int ps = (2 * pv_i + mb) % kPairSlots;
+              const uint64_t ad0 = desc_add(dmn_pair, ps * kPairBytes);
 #pragma unroll
-              for (int ks = 0; ks < 8; ++ks) {
-                const uint64_t ad = smem_desc(pair0 + ps * kPairBytes + ks * 2048, kAtomBytes, 1024, kSwizzle128B);
-                const uint64_t bd = smem_desc(p0 + (ks >> 2) * kQAtomBytes + (ks & 3) * 32, 0, 1024, kSwizzle128B);
-                mma_f16_ss(tmem_o + mb * 16, ad, bd, idesc_o, (ks != 0 || !cp.first) ? 1u : 0u);
-              }
+              for (int ks = 0; ks < 8; ++ks)
+                mma_f16_ss(tmem_o + mb * 16, desc_add(ad0, ks * 2048),
+                           desc_add(bd0, (ks >> 2) * kQAtomBytes + (ks & 3) * 32), idesc_o,
+                           (ks != 0 || !cp.first) ? 1u : 0u);
               mma_commit(smem_u32(&pair_empty[ps]));
             }
             mma_commit(smem_u32(&o_full));
@@ -456,12 +473,11 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
               tc_fence_after();
               // RoPE columns 32*rank..32*rank+31: K-steps 2*rs and 2*rs+1 of the atom,
               // against the Q RoPE atom that holds the same columns at the same chunks
-              const uint32_t q_rope = q0 + (rs == rank ? 4 : 5) * kQAtomBytes;
+              const uint64_t q_rope = desc_add(dk_q, (rs == rank ? 4 : 5) * kQAtomBytes);
 #pragma unroll
               for (int kk = 0; kk < 2; ++kk) {
                 const uint32_t off = (2 * rs + kk) * 32;
-                mma_f16_ss(d_s, smem_desc(rope0 + off, 0, 1024, kSwizzle128B),
-                           smem_desc(q_rope + off, 0, 1024, kSwizzle128B), idesc_s, kk != 0);
+                mma_f16_ss(d_s, desc_add(dk_rope, off), desc_add(q_rope, off), idesc_s, kk != 0);
               }
               mma_commit(smem_u32(&rope_empty[rs]));
               s_step = 1;
@@ -472,12 +488,14 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
             if (mbar_test_wait(smem_u32(&pair_full[ps]), (gidx / kPairSlots) & 1)) {
               fence_proxy_async_smem();
               tc_fence_after();
+              const uint64_t a0 = desc_add(dk_pair, ps * kPairBytes);
+              const uint64_t b0 = desc_add(dk_q, 2 * jl * kQAtomBytes);
 #pragma unroll
               for (int a2 = 0; a2 < 2; ++a2) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                  mma_f16_ss(d_s, smem_desc(pair0 + ps * kPairBytes + a2 * kAtomBytes + kk * 32, 0, 1024, kSwizzle128B),
-                             smem_desc(q0 + (2 * jl + a2) * kQAtomBytes + kk * 32, 0, 1024, kSwizzle128B), idesc_s, 1);
+                  mma_f16_ss(d_s, desc_add(a0, a2 * kAtomBytes + kk * 32), desc_add(b0, a2 * kQAtomBytes + kk * 32),
+                             idesc_s, 1);
               }
               if (jl == 1) {
                 mma_commit(smem_u32(&s_full[sb]));

@@ -72,6 +72,38 @@ def test_step_full_size_sampled(name, nsample):
     _verify(wl, dw, ts)
 
 
+SELECTION = [
+    ("tiny", dict()),
+    ("decode", dict()),                            # the bench configuration, 64 queries
+    ("decode", dict(batch=5, ctx_scale=0.25)),     # rows no longer than index_topk
+    ("longctx", dict(batch=2, ctx_scale=1 / 16)),  # 8192-entry rows with exact score ties
+]
+
+
+@pytest.mark.parametrize("name,kw", SELECTION, ids=["tiny", "decode", "decode-short", "longctx-ties"])
+def test_step_selection_bit_exact_on_gpu_scores(name, kw):
+    """The step's selection equals the oracle's top-k of the GPU's own fp32 scores bit
+    for bit (the indexer is deterministic, so a standalone indexer call reproduces the
+    scores the step ranked)."""
+    wl = inputs.make_config(name, **kw)
+    dw = runner.DeviceWorkload(wl, DEV)
+    dw.step()
+    torch.cuda.synchronize()
+    assert dw.check_error() == 0
+    stride = int(-(-wl.max_seq_len // 64) * 64)
+    scores = torch.empty((wl.T, stride), dtype=torch.float32, device=DEV)
+    ws = _lib.workspace(_lib.dsa_indexer_scores_workspace_size(dw.geom), DEV)
+    _lib.dsa_indexer_scores(dw.geom, dw.qk_dtype, dw.q_idx, dw.q_scale, dw.w, dw.idx_k, dw.idx_k_scale,
+                            scores, ws)
+    assert _lib.dsa_get_error(ws) == 0
+    sc = scores.cpu().numpy()
+    idx = dw.idx.cpu().numpy()
+    _, pos = oracle.query_positions(wl.seq_lens, wl.n_q)
+    for t in range(wl.T):
+        p = int(pos[t])
+        assert np.array_equal(idx[t], oracle.topk_row(sc[t, : p + 1].astype(np.float64), wl.topk)), t
+
+
 def test_indexshare_layer_reuses_full_layer_selection():
     wl = inputs.make_config("mtp", batch=2, ctx_scale=0.3)
     dw = runner.DeviceWorkload(wl, DEV)
