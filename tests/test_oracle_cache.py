@@ -1,0 +1,156 @@
+"""Pins of the oracle's cache append (oracle/cache.py) against things fixed outside it:
+torch's e4m3 cast over a dense sweep, hand-worked encodings and a hand-worked record
+(tests/golden/), round-trip error bounds, the row mapping the attention reads, and
+that no other row changes."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import cache as oc
+from oracle.fp8 import E4M3_TABLE, decode_bf16, decode_e4m3, decode_f32le
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def torch_e4m3(v):
+    t = torch.tensor(np.asarray(v, dtype=np.float32)).clamp(-448.0, 448.0)
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def test_encoder_equals_torch_cast_on_values_midpoints_and_neighbours():
+    vals = E4M3_TABLE[:0x7F]
+    mids = (vals[:-1] + vals[1:]) / 2
+    base = np.concatenate([vals, mids, -vals, -mids, [0.0, -0.0, 449.0, 470.0, -1e30, 1e-30, -1e-30]])
+    f32 = base.astype(np.float32)
+    rng = np.random.default_rng(7)
+    wide = (rng.standard_normal(20000) * np.exp2(rng.uniform(-14, 9, 20000))).astype(np.float32)
+    allv = np.concatenate([f32, np.nextafter(f32, np.float32(np.inf)), np.nextafter(f32, np.float32(-np.inf)), wide])
+    assert np.array_equal(oc.encode_e4m3(allv.astype(np.float64)), torch_e4m3(allv))
+
+
+def test_encoder_hand_cases():
+    with open(os.path.join(GOLDEN, "e4m3_encode.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        assert oc.encode_e4m3(np.array([c["value"]]))[0] == int(c["code"], 16), c
+
+
+def test_encoder_round_trip_is_nearest():
+    rng = np.random.default_rng(3)
+    v = rng.uniform(-448, 448, 5000)
+    codes = oc.encode_e4m3(v)
+    back = decode_e4m3(codes)
+    finite = E4M3_TABLE[np.isfinite(E4M3_TABLE)]
+    best = np.abs(v[:, None] - finite[None, :]).min(axis=1)
+    assert np.allclose(np.abs(back - v), best, rtol=0, atol=1e-12)
+
+
+def _one_token_geometry(pos):
+    """One request whose last (new) token sits at `pos`; block table [2, 0, 1]."""
+    bt = np.array([[2, 0, 1]], dtype=np.int32)
+    return np.array([pos + 1], dtype=np.int32), np.array([1], dtype=np.int32), bt
+
+
+def test_hand_worked_e4m3_record():
+    with open(os.path.join(GOLDEN, "cache_record_hand.json")) as f:
+        g = json.load(f)
+    x = np.zeros(576, dtype=np.float32)
+    for k, v in g["latent_nonzero"].items():
+        x[int(k)] = v
+    x[512:] = np.where(np.arange(64) % 2 == 0, 1.0, -2.0)
+    bits = (x.view(np.uint32) >> 16).astype(np.uint16)          # exact in bf16
+    assert np.array_equal(decode_bf16(bits), x.astype(np.float64))
+    seq, nq, bt = _one_token_geometry(pos=70)   # logical page 1 -> physical page bt[0][1] = 0, slot 6
+    kv = np.zeros((3, 64, 656), dtype=np.uint8)
+    out, _, _ = oc.cache_append(kv, "e4m3", bits[None], None, None, "e4m3", None, seq, nq, bt)
+    row = out.reshape(-1, 656)[0 * 64 + 70 % 64]
+    for k, code in g["expected_codes"].items():
+        assert row[int(k)] == int(code, 16), (k, hex(row[int(k)]))
+    scales = decode_f32le(row[512:528])
+    for c, s in enumerate(g["expected_scales_exact"]):
+        if s is None:
+            assert scales[c] == float(np.float32(3.0) / np.float32(448.0))
+        else:
+            assert scales[c] == s
+    assert np.array_equal(decode_bf16(row[528:].view(np.uint16)), x[512:].astype(np.float64))
+    # every other row is untouched
+    rest = np.delete(out.reshape(-1, 656), 6, axis=0)
+    assert not rest.any()
+
+
+def _random_append_case(rng, kv_dtype, qk_dtype):
+    seq = np.array([130, 64, 200], dtype=np.int32)
+    nq = np.array([2, 1, 4], dtype=np.int32)
+    P = 12
+    bt = rng.permutation(P)[:12].reshape(3, 4).astype(np.int32)
+    T = int(nq.sum())
+    x = (rng.standard_normal((T, 576)) * 0.5).astype(np.float32)
+    x[0, 128:256] = 0.0                                           # an all-zero group
+    x[1, :128] *= np.float32(2.0 ** -20)                          # tiny values
+    bits = (x.view(np.uint32) >> 16).astype(np.uint16)
+    k = rng.standard_normal((T, 128)).astype(np.float32)
+    kbits = (k.view(np.uint32) >> 16).astype(np.uint16)
+    if kv_dtype == "bf16":
+        kv = rng.integers(0, 2 ** 16, size=(P, 64, 576), dtype=np.uint16)
+    else:
+        kv = rng.integers(0, 256, size=(P, 64, 656), dtype=np.uint8)
+    if qk_dtype == "bf16":
+        ik = rng.integers(0, 2 ** 16, size=(P, 64, 128), dtype=np.uint16)
+        isc = None
+    else:
+        ik = rng.integers(0, 256, size=(P, 64, 128), dtype=np.uint8)
+        isc = rng.standard_normal((P, 64)).astype(np.float32)
+    return seq, nq, bt, bits, kbits, kv, ik, isc
+
+
+@pytest.mark.parametrize("kv_dtype,qk_dtype", [("bf16", "e4m3"), ("e4m3", "e4m3"), ("bf16", "bf16")])
+def test_append_rows_round_trip_and_untouched_rows(kv_dtype, qk_dtype):
+    rng = np.random.default_rng(11)
+    seq, nq, bt, bits, kbits, kv, ik, isc = _random_append_case(rng, kv_dtype, qk_dtype)
+    out, ok_, os_ = oc.cache_append(kv, kv_dtype, bits, ik, isc, qk_dtype, kbits, seq, nq, bt)
+    # rows follow the attention's position rule: query j of request b is at L_b - n_b + j
+    req, pos = oracle.query_positions(seq, nq)
+    rows = np.array([bt[b][p // 64] * 64 + p % 64 for b, p in zip(req, pos)])
+    assert np.array_equal(rows, oc.token_rows(seq, nq, bt))
+    width = out.shape[-1]
+    touched = np.zeros(out.shape[0] * 64, dtype=bool)
+    touched[rows] = True
+    assert np.array_equal(out.reshape(-1, width)[~touched], kv.reshape(-1, width)[~touched])
+    assert np.array_equal(ok_.reshape(-1, 128)[~touched], ik.reshape(-1, 128)[~touched])
+    x = decode_bf16(bits)
+    for t, r in enumerate(rows):
+        rec = out.reshape(-1, width)[r]
+        if kv_dtype == "bf16":
+            assert np.array_equal(rec, bits[t])
+        else:
+            scales = decode_f32le(rec[512:528])
+            deq = decode_e4m3(rec[:512]) * np.repeat(scales, 128)
+            amax = np.abs(x[t, :512]).reshape(4, 128).max(axis=1)
+            # scale = amax/448 in fp32; round trip within half an e4m3 step (2^-4 relative,
+            # 2^-10 * scale absolute in the subnormal range)
+            assert np.all(scales[amax > 0] == (amax[amax > 0].astype(np.float32) / np.float32(448)))
+            assert np.all(scales[amax == 0] == 1.0)
+            bound = np.abs(x[t, :512]) * 2.0 ** -4 + np.repeat(scales, 128) * 2.0 ** -10
+            assert np.all(np.abs(deq - x[t, :512]) <= bound * (1 + 1e-6))
+            assert np.array_equal(rec[528:].view(np.uint16), bits[t, 512:])
+        krow = ok_.reshape(-1, 128)[r]
+        if qk_dtype == "bf16":
+            assert np.array_equal(krow, kbits[t])
+        else:
+            kx = decode_bf16(kbits[t])
+            s = os_.reshape(-1)[r]
+            assert s == np.float32(np.abs(kx).max()) / np.float32(448)
+            assert np.all(np.abs(decode_e4m3(krow) * s - kx) <= np.abs(kx) * 2.0 ** -4 + s * 2.0 ** -10 + 1e-12)
+
+
+def test_append_is_idempotent_and_bf16_rope_passes_through():
+    rng = np.random.default_rng(5)
+    seq, nq, bt, bits, kbits, kv, ik, isc = _random_append_case(rng, "e4m3", "e4m3")
+    a = oc.cache_append(kv, "e4m3", bits, ik, isc, "e4m3", kbits, seq, nq, bt)
+    b = oc.cache_append(a[0], "e4m3", bits, a[1], a[2], "e4m3", kbits, seq, nq, bt)
+    for u, v in zip(a, b):
+        assert np.array_equal(u, v)
