@@ -288,6 +288,8 @@ def main():
     e2e = measure_e2e(dw, graph, flush, stream, max(20, min(args.steps, 200)))
     # ---- per-kernel breakdown for the roofline of the dominant kernel
     comp = measure_components(dw, flush, stream, max(20, min(args.steps, 200)))
+    # ---- next row beyond the step: the cache update (timed alone; not part of `value`)
+    append = measure_cache_append(dw, flush, stream, max(20, min(args.steps, 100)))
 
     idx_b, lat_b, selected = algorithmic_bytes(wl)
     peak, peak_kind = load_peaks()
@@ -314,6 +316,7 @@ def main():
                      "avg_launch_ms": comp["attend_ms"],
                      "traffic": load_traffic("sparse_mla_kernel")},
         "components_ms": comp,
+        "next_rows": {"cache_append": append},
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
@@ -389,6 +392,54 @@ def measure_components(dw, flush, stream, n):
         acc["topk_ms"] += ev[1].elapsed_time(ev[2])
         acc["attend_ms"] += ev3.elapsed_time(ev[3])
     return {k: v / n for k, v in acc.items()}
+
+
+def measure_cache_append(dw, flush, stream, n):
+    """Device time of dsa_cache_append (the cache-update row), launched alone with the
+    GPU kept busy while the host enqueues, L2 flushed before each: (a) the decode
+    batch's 64 new tokens into its bf16 latent and e4m3 index caches, (b) a 2048-token
+    prefill chunk into e4m3 latent and index caches. Algorithmic bytes: the new rows
+    read (1152 + 256 B per token) and the cache rows written."""
+    wl = dw.wl
+    dev = dw.device
+    rng = np.random.default_rng(99)
+
+    def bits(shape):
+        x = rng.standard_normal(shape).astype(np.float32)
+        return torch.from_numpy((x.view(np.uint32) >> 16).astype(np.uint16).view(np.int16)).to(dev)
+
+    ws = _lib.workspace(256, dev)
+    cases = {}
+    lay = dw.layers[0]
+    cases["decode_64_tokens_bf16_latent"] = (
+        dw.geom, lay.kv_dtype, bits((wl.T, 576)), lay.kv, bits((wl.T, 128)), wl.T * (1152 + 256 + 1152 + 132))
+    L, m = 4096, 2048
+    P = L // 64
+    seq = torch.tensor([L], dtype=torch.int32, device=dev)
+    cu = torch.tensor([0, m], dtype=torch.int32, device=dev)
+    bt = torch.from_numpy(rng.permutation(P).astype(np.int32).reshape(1, P)).to(dev)
+    g2 = _lib.Geometry(seq, cu, bt, num_pages=P, max_seq_len=L, T=m)
+    kv2 = torch.zeros(P, 64, 656, dtype=torch.uint8, device=dev)
+    ik2 = torch.zeros(P, 64, 128, dtype=torch.uint8, device=dev)
+    is2 = torch.zeros(P, 64, dtype=torch.float32, device=dev)
+    cases["prefill_2048_tokens_e4m3_latent"] = (g2, _lib.DSA_E4M3, bits((m, 576)), kv2, bits((m, 128)),
+                                                m * (1152 + 256 + 656 + 132))
+    out = {}
+    for name, (g, kvd, kv_new, kv, k_new, nbytes) in cases.items():
+        ik, isc = (dw.idx_k, dw.idx_k_scale) if g is dw.geom else (ik2, is2)
+        tot = 0.0
+        for i in range(n):
+            flush.fill_(i & 0xFF)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda._sleep(200_000)
+            a.record(stream)
+            _lib.dsa_cache_append(g, kvd, kv_new, kv, _lib.DSA_E4M3, k_new, ik, isc, ws)
+            b.record(stream)
+            b.synchronize()
+            tot += a.elapsed_time(b)
+        ms = tot / n
+        out[name] = {"ms": ms, "algorithmic_bytes": nbytes, "achieved_gbs": nbytes / (ms / 1000.0) / 1e9}
+    return out
 
 
 if __name__ == "__main__":

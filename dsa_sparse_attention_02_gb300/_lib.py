@@ -23,6 +23,7 @@ EXPORTED = (
     "dsa_topk", "dsa_topk_workspace_size",
     "dsa_sparse_mla_attend", "dsa_sparse_mla_attend_workspace_size", "dsa_sparse_mla_attend_static",
     "dsa_decode_step", "dsa_decode_step_workspace_size",
+    "dsa_cache_append", "dsa_cache_append_workspace_size",
     "dsa_get_error", "dsa_clear_error", "dsa_status_string", "dsa_last_error", "dsa_abi_version",
 )
 
@@ -80,6 +81,8 @@ def load(path: str = LIB_PATH):
         "dsa_sparse_mla_attend_static": (C.c_int, [G, C.c_int, I32, P, P, P, I32, F, P, P, P, P]),
         "dsa_decode_step": (C.c_int, [S, P, SZ, P]),
         "dsa_decode_step_workspace_size": (SZ, [S]),
+        "dsa_cache_append": (C.c_int, [G, C.c_int, P, P, C.c_int, P, P, P, P, SZ, P]),
+        "dsa_cache_append_workspace_size": (SZ, [G]),
         "dsa_get_error": (C.c_int, [P, P]),
         "dsa_clear_error": (C.c_int, [P, P]),
         "dsa_status_string": (C.c_char_p, [C.c_int]),
@@ -188,6 +191,19 @@ def dsa_sparse_mla_attend_static(geom: Geometry, kv_dtype: int, q, kv_cache, idx
                                              int(k), float(sm_scale), _ptr(out), _ptr(lse),
                                              _ptr(err_word), _stream(stream))
     _check(st, "dsa_sparse_mla_attend_static")
+
+
+def dsa_cache_append_workspace_size(geom: Geometry) -> int:
+    return int(load().dsa_cache_append_workspace_size(geom.ref))
+
+
+def dsa_cache_append(geom: Geometry, kv_dtype: int, kv_new, kv_cache, qk_dtype: int = DSA_E4M3, k_new=None,
+                     idx_k_cache=None, idx_k_scale=None, ws=None, stream=None):
+    """Writes the geom.T new tokens (flattened like queries) into the paged caches."""
+    st = load().dsa_cache_append(geom.ref, kv_dtype, _ptr(kv_new), _ptr(kv_cache), qk_dtype, _ptr(k_new),
+                                 _ptr(idx_k_cache), _ptr(idx_k_scale), _ptr(ws), ws.numel() if ws is not None else 0,
+                                 _stream(stream))
+    _check(st, "dsa_cache_append")
 
 
 def make_step_args(geom: Geometry, topk: int, *, qk_dtype=DSA_E4M3, q_idx=None, q_scale=None,

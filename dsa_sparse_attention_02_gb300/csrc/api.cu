@@ -330,6 +330,36 @@ dsa_status_t dsa_decode_step(const dsa_step_args_t* a, void* ws, size_t ws_bytes
                     a->reuse_idx == nullptr, st);
 }
 
+size_t dsa_cache_append_workspace_size(const dsa_geom_t*) { return kHeaderBytes; }
+
+dsa_status_t dsa_cache_append(const dsa_geom_t* geom, dsa_dtype_t kv_dtype, const void* kv_new, void* kv_cache,
+                              dsa_dtype_t qk_dtype, const void* k_new, void* idx_k_cache, float* idx_k_scale,
+                              void* ws, size_t ws_bytes, void* stream) {
+  dsa_status_t s = check_geom(geom);
+  if (s != DSA_OK) return s;
+  if (kv_dtype != DSA_BF16 && kv_dtype != DSA_E4M3) return DSA_ERR_INVALID_ARG;
+  if (k_new) {
+    if (qk_dtype != DSA_BF16 && qk_dtype != DSA_E4M3) return DSA_ERR_INVALID_ARG;
+    if (!idx_k_cache || !aligned16(k_new) || !aligned16(idx_k_cache)) return DSA_ERR_INVALID_ARG;
+    if (qk_dtype == DSA_E4M3 && !idx_k_scale) return DSA_ERR_INVALID_ARG;
+    if (qk_dtype == DSA_BF16 && idx_k_scale) return DSA_ERR_INVALID_ARG;
+  }
+  if (!ws || ws_bytes < kHeaderBytes || (reinterpret_cast<uintptr_t>(ws) & 255u)) return DSA_ERR_WORKSPACE;
+  if (geom->T == 0) return DSA_OK;
+  if (!kv_new || !kv_cache || !aligned16(kv_new) || !aligned16(kv_cache)) return DSA_ERR_INVALID_ARG;
+  AppendArgs A;
+  A.g = to_dev(geom);
+  A.kv_fp8 = kv_dtype == DSA_E4M3;
+  A.kv_new = kv_new;
+  A.kv_cache = reinterpret_cast<uint8_t*>(kv_cache);
+  A.k_fp8 = qk_dtype == DSA_E4M3;
+  A.k_new = k_new;
+  A.k_cache = reinterpret_cast<uint8_t*>(idx_k_cache);
+  A.k_scale = idx_k_scale;
+  A.err = reinterpret_cast<int*>(ws);
+  return from_cuda(cache_append_launch(A, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 dsa_status_t dsa_get_error(void* ws, void* stream) {
   if (!ws) return DSA_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

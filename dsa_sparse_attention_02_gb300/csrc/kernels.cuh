@@ -54,6 +54,20 @@ size_t mla_partial_bytes(int T, int H, int grid);
 cudaError_t mla_launch(bool fp8_kv, const CUtensorMap& map_q, MlaArgs A, int grid, bool pdl, cudaStream_t st);
 bool encode_mla_q_map(CUtensorMap* map_q, const void* q, int T, int H);
 
+// ---- cache append (cache_append.cu)
+struct AppendArgs {
+  GeomDev g;
+  bool kv_fp8;                  // latent cache: e4m3 656-byte records (else bf16 576)
+  const void* kv_new;           // [T, 576] bf16
+  uint8_t* kv_cache;            // [P*64] rows
+  bool k_fp8;                   // index keys: e4m3 + per-token scale (else bf16)
+  const void* k_new;            // [T, 128] bf16, or null to leave the index cache alone
+  uint8_t* k_cache;             // [P*64] rows of 128 e4m3 codes or 128 bf16
+  float* k_scale;               // [P*64] (e4m3 keys)
+  int* err;
+};
+cudaError_t cache_append_launch(const AppendArgs& A, cudaStream_t st);
+
 // ---- host helpers defined in api.cu
 bool encode_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t cols,
                           uint64_t rows, uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows);

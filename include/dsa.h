@@ -164,6 +164,37 @@ dsa_status_t dsa_sparse_mla_attend_static(const dsa_geom_t* geom, dsa_dtype_t kv
                                           int32_t k, float sm_scale, void* out, float* lse,
                                           int32_t* err_word, void* stream);
 
+/*
+ * dsa_cache_append -- write the new tokens' latent rows and index keys into the
+ *   paged caches (the cache update that runs before each decode / draft step's
+ *   attention; lmdeploy "feat: support GLM-5.2", Changes: BF16/FP8 sparse
+ *   FlashMLA cache paths, MLA cache dtype policy; lmdeploy "glm5.3-flash
+ *   support": cache updates still run on every draft step).
+ *   The new tokens are flattened like queries: token j of request b is the
+ *     request's position seq_lens[b] - n_b + j (n_b from cu_q), written to page
+ *     block_table[b][pos/64], row pos%64 -- the row the indexer and attention
+ *     read for that position. geom->T is the number of new tokens.
+ *   kv_new [T, 576] bf16 (device): latent (512) then RoPE (64) of each token.
+ *   kv_dtype DSA_BF16: kv_cache [num_pages, 64, 576] bf16 receives kv_new as is.
+ *   kv_dtype DSA_E4M3: kv_cache [num_pages, 64, 656] bytes receives, per token,
+ *     for each group c of 128 latent values scale_c = amax_c / 448 (fp32; 1 for
+ *     an all-zero group) and code = e4m3(x / scale_c) (quotient in fp32, round
+ *     to nearest even, saturating at +-448): 512 codes, the 4 scales as
+ *     little-endian fp32, then the 64 RoPE values as bf16.
+ *   k_new [T, 128] bf16 (device) or NULL to leave the index cache alone.
+ *   qk_dtype DSA_E4M3: idx_k_cache [num_pages, 64, 128] e4m3 and idx_k_scale
+ *     [num_pages, 64] fp32 receive codes and one scale per token, same rule.
+ *   qk_dtype DSA_BF16: idx_k_cache [num_pages, 64, 128] bf16 receives k_new as
+ *     is; idx_k_scale must be NULL.
+ *   No other row changes. All pointers 16-byte aligned. A page id out of range
+ *   skips that token and sets DSA_ERR_BAD_INDEX in the error word.
+ */
+dsa_status_t dsa_cache_append(const dsa_geom_t* geom, dsa_dtype_t kv_dtype, const void* kv_new,
+                              void* kv_cache, dsa_dtype_t qk_dtype, const void* k_new,
+                              void* idx_k_cache, float* idx_k_scale, void* ws, size_t ws_bytes,
+                              void* stream);
+size_t dsa_cache_append_workspace_size(const dsa_geom_t* geom);
+
 /* Arguments of the fused step. */
 typedef struct {
   dsa_geom_t geom;

@@ -84,6 +84,18 @@ def test_host_validation(lib):
                                      256, 1 << 24, None) == _lib.DSA_ERR_INVALID_ARG
     assert lib.dsa_sparse_mla_attend(C.byref(g), _lib.DSA_BF16, 16, 16, 16, 16, 64, float("inf"),
                                      16, None, 256, 1 << 24, None) == _lib.DSA_ERR_INVALID_ARG
+    # cache append: bad dtypes, e4m3 keys without scales, bf16 keys with scales,
+    # misaligned buffers, no workspace; zero tokens is a no-op
+    ca = lib.dsa_cache_append
+    assert ca(C.byref(g), 9, 16, 16, _lib.DSA_E4M3, None, None, None, 256, 256, None) == _lib.DSA_ERR_INVALID_ARG
+    assert ca(C.byref(g), _lib.DSA_BF16, 16, 16, 9, 16, 16, 16, 256, 256, None) == _lib.DSA_ERR_INVALID_ARG
+    assert ca(C.byref(g), _lib.DSA_BF16, 16, 16, _lib.DSA_E4M3, 16, 16, None, 256, 256, None) == _lib.DSA_ERR_INVALID_ARG
+    assert ca(C.byref(g), _lib.DSA_BF16, 16, 16, _lib.DSA_BF16, 16, 16, 16, 256, 256, None) == _lib.DSA_ERR_INVALID_ARG
+    assert ca(C.byref(g), _lib.DSA_BF16, 24, 16, _lib.DSA_E4M3, None, None, None, 256, 256, None) == _lib.DSA_ERR_INVALID_ARG
+    assert ca(C.byref(g), _lib.DSA_BF16, 16, 16, _lib.DSA_E4M3, None, None, None, None, 0, None) == _lib.DSA_ERR_WORKSPACE
+    g0 = _geom(T=0)
+    assert ca(C.byref(g0), _lib.DSA_BF16, None, None, _lib.DSA_E4M3, None, None, None, 256, 256, None) == _lib.DSA_OK
+    assert lib.dsa_cache_append_workspace_size(C.byref(g)) == 256
     assert lib.dsa_get_error(None, None) == _lib.DSA_ERR_INVALID_ARG
 
 
