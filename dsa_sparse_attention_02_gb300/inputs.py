@@ -56,7 +56,7 @@ class Layer:
     """One attention layer's MLA inputs."""
     q: np.ndarray            # [T, H, 576] uint16 (bf16 bits)
     kv: np.ndarray           # [P, 64, 576] uint16 (bf16) or [P, 64, 656] uint8 (e4m3 record)
-    kv_dtype: str            # "bf16" or "e4m3"
+    kv_dtype: str            # "bf16", "e4m3" or "int8"
 
 
 @dataclass
@@ -169,6 +169,22 @@ def make_kv_e4m3(rng, num_pages: int) -> np.ndarray:
     return rec
 
 
+def make_kv_int8(rng, num_pages: int) -> np.ndarray:
+    """Latent KV rows ~ N(0, 0.5^2) as 656-byte records: the 512 latent values as int8
+    with one fp32 scale (amax/127) per 128 of them, then the 64 RoPE values in bf16."""
+    x = _normal(rng, (num_pages, PAGE, D_QK), 0.5)
+    g = x[..., :D_LATENT].reshape(num_pages, PAGE, 4, 128)
+    amax = np.abs(g).max(axis=-1)
+    scales = np.where(amax > 0, amax / np.float32(127.0), np.float32(1.0)).astype(np.float32)
+    codes = np.clip(np.rint(g / scales[..., None]), -127, 127).astype(np.int8).view(np.uint8)
+    rope = to_bf16_bits(x[..., D_LATENT:])
+    rec = np.empty((num_pages, PAGE, FP8_RECORD), dtype=np.uint8)
+    rec[..., :D_LATENT] = codes.reshape(num_pages, PAGE, D_LATENT)
+    rec[..., D_LATENT:D_LATENT + 16] = np.ascontiguousarray(scales, dtype="<f4").view(np.uint8).reshape(num_pages, PAGE, 16)
+    rec[..., D_LATENT + 16:] = np.ascontiguousarray(rope, dtype="<u2").view(np.uint8)
+    return rec
+
+
 def make_workload(name: str, seq_lens, n_q, topk: int, hi: int, qk_dtype: str,
                   kv_dtypes=("bf16",), heads: int = 16, seed: int = 0,
                   dup_key_frac: float = 0.0, spare_frac: float = 0.05) -> Workload:
@@ -212,7 +228,7 @@ def make_workload(name: str, seq_lens, n_q, topk: int, hi: int, qk_dtype: str,
     layers = []
     for kd in kv_dtypes:
         q = to_bf16_bits(_normal(rng, (T, heads, D_QK)))
-        kv = make_kv_bf16(rng, P) if kd == "bf16" else make_kv_e4m3(rng, P)
+        kv = make_kv_bf16(rng, P) if kd == "bf16" else (make_kv_e4m3(rng, P) if kd == "e4m3" else make_kv_int8(rng, P))
         layers.append(Layer(q=q, kv=kv, kv_dtype=kd))
 
     return Workload(name=name, seq_lens=seq_lens, n_q=n_q, cu_q=cu_q, block_table=bt,
@@ -224,9 +240,15 @@ def make_workload(name: str, seq_lens, n_q, topk: int, hi: int, qk_dtype: str,
 
 
 def make_config(name: str, batch: int | None = None, seed: int | None = None,
-                ctx_scale: float = 1.0) -> Workload:
+                ctx_scale: float = 1.0, latent: str | None = None) -> Workload:
     """The five configurations, optionally with a smaller batch or shorter contexts
-    (`ctx_scale` < 1 shrinks the context range; used for quick parity runs)."""
+    (`ctx_scale` < 1 shrinks the context range; used for quick parity runs), or with
+    every layer's latent cache in another format (`latent`: "bf16", "e4m3", "int8")."""
+    wl = _make_config(name, batch, seed, ctx_scale, latent)
+    return wl
+
+
+def _make_config(name, batch, seed, ctx_scale, latent):
     s = CONFIG_SEEDS[name] if seed is None else seed
     rng = np.random.Generator(np.random.PCG64(s + 1000))
 
@@ -237,24 +259,28 @@ def make_config(name: str, batch: int | None = None, seed: int | None = None,
     if name == "tiny":
         B = 2 if batch is None else batch
         lens = ([200, 256] * B)[:B]
-        return make_workload(name, lens, [1] * B, 64, 4, "bf16", ("bf16",), seed=s)
+        return make_workload(name, lens, [1] * B, 64, 4, "bf16", _lat(("bf16",), latent), seed=s)
     if name == "decode":
         B = 64 if batch is None else batch
-        return make_workload(name, U(2048, 8192, B), [1] * B, 2048, 64, "e4m3", ("bf16",), seed=s)
+        return make_workload(name, U(2048, 8192, B), [1] * B, 2048, 64, "e4m3", _lat(("bf16",), latent), seed=s)
     if name == "mtp":
         B = 32 if batch is None else batch
         return make_workload(name, U(4096, 16384, B), [4] * B, 2048, 64, "e4m3",
-                             ("e4m3", "e4m3"), seed=s)
+                             _lat(("e4m3", "e4m3"), latent), seed=s)
     if name == "prefill":
         L = int(16384 * ctx_scale)
         nq = min(2048, L) if batch is None else batch
-        return make_workload(name, [L], [nq], 2048, 64, "e4m3", ("bf16",), seed=s)
+        return make_workload(name, [L], [nq], 2048, 64, "e4m3", _lat(("bf16",), latent), seed=s)
     if name == "longctx":
         B = 8 if batch is None else batch
         L = int(131072 * ctx_scale)
-        return make_workload(name, [L] * B, [1] * B, 2048, 64, "e4m3", ("bf16",), seed=s,
+        return make_workload(name, [L] * B, [1] * B, 2048, 64, "e4m3", _lat(("bf16",), latent), seed=s,
                              dup_key_frac=0.01)
     raise KeyError(name)
+
+
+def _lat(kv_dtypes, latent):
+    return kv_dtypes if latent is None else tuple(latent for _ in kv_dtypes)
 
 
 def tied_scores(rng: np.random.Generator, rows: int, n: int, frac: float = 0.01,

@@ -12,6 +12,10 @@ print no layout or rounding, so this follows the layouts the attention reads:
   * token j of request b (flattened like the queries) sits at position
     L_b - n_b + j, physical row block_table[b][pos // 64] * 64 + pos % 64;
   * bf16 latent cache: the 576 bf16 values as given;
+  * int8 latent record (mlx-lm "GLM-5.2 (glm_moe_dsa) inference": int8 MLA latent
+    KV, only the compressed latent quantized): the e4m3 record's layout with
+    two's-complement int8 codes, scale_c = amax_c / 127 and the quotient rounded to
+    the nearest integer (ties to even), clamped to +-127;
   * e4m3 latent record (656 bytes): for each group c of 128 latent values,
     scale_c = amax_c / 448 in fp32 (1 for an all-zero group) and
     code = e4m3(x / scale_c), the quotient taken in fp32 and rounded to the nearest
@@ -74,6 +78,33 @@ def quantize_groups(x32: np.ndarray, group: int) -> tuple[np.ndarray, np.ndarray
     return encode_e4m3(q.astype(np.float64)).reshape(x32.shape), scale
 
 
+I8_MAX = 127.0
+
+
+def encode_int8(v: np.ndarray) -> np.ndarray:
+    """Round values (held exactly in float64) to the nearest integer, ties to even,
+    clamp to [-127, 127], and return the two's-complement bytes."""
+    v = np.asarray(v, dtype=np.float64)
+    if not np.all(np.isfinite(v)):
+        raise ValueError("int8 encoding expects finite values")
+    fl = np.floor(v)
+    frac = v - fl
+    up = (frac > 0.5) | ((frac == 0.5) & (np.mod(fl, 2) == 1))
+    q = np.clip(fl + up, -I8_MAX, I8_MAX).astype(np.int64)
+    return q.astype(np.int8).view(np.uint8)
+
+
+def quantize_groups_int8(x32: np.ndarray, group: int) -> tuple[np.ndarray, np.ndarray]:
+    """int8 codes of x / scale (fp32 quotient), scale = amax / 127 in fp32 (1 for an
+    all-zero group), per run of `group` values along the last axis."""
+    x32 = np.asarray(x32, dtype=np.float32)
+    g = x32.reshape(*x32.shape[:-1], x32.shape[-1] // group, group)
+    amax = np.abs(g).max(axis=-1)
+    scale = np.where(amax > 0, amax / np.float32(I8_MAX), np.float32(1.0)).astype(np.float32)
+    q = (g / scale[..., None]).astype(np.float32)
+    return encode_int8(q.astype(np.float64)).reshape(x32.shape), scale
+
+
 def token_rows(seq_lens, n_q, block_table) -> np.ndarray:
     """Physical cache row of every new token (flattened like the queries)."""
     rows = []
@@ -93,7 +124,7 @@ def cache_append(kv_cache, kv_dtype, kv_new_bits, idx_k_cache, idx_k_scale, qk_d
                  seq_lens, n_q, block_table):
     """Return updated copies of the caches after appending the new tokens.
 
-    kv_cache: [P, 64, 576] uint16 (bf16 bits) or [P, 64, 656] uint8 (e4m3 records).
+    kv_cache: [P, 64, 576] uint16 (bf16 bits) or [P, 64, 656] uint8 (e4m3 / int8 records).
     kv_new_bits: [T, 576] uint16 bf16 bits.
     idx_k_cache: [P, 64, 128] uint8 (e4m3) or uint16 (bf16 bits), or None;
     idx_k_scale: [P, 64] float32 or None; k_new_bits: [T, 128] uint16 or None.
@@ -106,7 +137,8 @@ def cache_append(kv_cache, kv_dtype, kv_new_bits, idx_k_cache, idx_k_scale, qk_d
         if kv_dtype == "bf16":
             flat[r] = np.asarray(kv_new_bits[t], dtype=np.uint16)
         else:
-            codes, scales = quantize_groups(x[t, :512], 128)
+            quant = quantize_groups if kv_dtype == "e4m3" else quantize_groups_int8
+            codes, scales = quant(x[t, :512], 128)
             flat[r, :512] = codes
             flat[r, 512:528] = np.ascontiguousarray(scales, dtype="<f4").view(np.uint8)
             flat[r, 528:656] = np.ascontiguousarray(np.asarray(kv_new_bits[t, 512:], dtype=np.uint16),

@@ -38,7 +38,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .fp8 import decode_bf16, decode_e4m3, decode_f32le
+from .fp8 import decode_bf16, decode_e4m3, decode_f32le, decode_int8
 
 PAGE = 64
 D_LATENT = 512
@@ -82,13 +82,16 @@ def decode_index_keys(idx_k, idx_k_scale, qk_dtype, rows):
 def decode_kv_rows(kv, kv_dtype, rows):
     """Selected rows of the paged latent cache -> float64 [len(rows), 576].
 
-    bf16: the 576 stored values. e4m3 (656-byte record): element 128c+e of the
-    latent is code[128c+e] * scale[c] for c = 0..3, followed by the 64 bf16 RoPE values.
+    bf16: the 576 stored values. e4m3 or int8 (656-byte record): element 128c+e of
+    the latent is code[128c+e] * scale[c] for c = 0..3, followed by the 64 bf16 RoPE
+    values. The int8 latent cache is mlx-lm "GLM-5.2 (glm_moe_dsa) inference",
+    int8 MLA latent KV (only the compressed latent is quantized, dequantized on read);
+    its code layout is the e4m3 record's with two's-complement int8 codes.
     """
     flat = kv.reshape(-1, kv.shape[-1])[rows]
     if kv_dtype == "bf16":
         return decode_bf16(flat)
-    lat = decode_e4m3(flat[:, :D_LATENT])
+    lat = decode_e4m3(flat[:, :D_LATENT]) if kv_dtype == "e4m3" else decode_int8(flat[:, :D_LATENT])
     scales = decode_f32le(flat[:, D_LATENT:D_LATENT + 16])           # [n, 4]
     lat = lat * np.repeat(scales, 128, axis=1)
     rope = decode_bf16(np.ascontiguousarray(flat[:, D_LATENT + 16:]).view("<u2").astype(np.uint16))

@@ -50,3 +50,11 @@ def decode_f32le(raw: np.ndarray) -> np.ndarray:
     """Little-endian fp32 stored as raw bytes (last axis a multiple of 4) -> float64."""
     raw = np.ascontiguousarray(raw, dtype=np.uint8)
     return raw.view("<f4").astype(np.float64)
+
+
+def decode_int8(codes: np.ndarray) -> np.ndarray:
+    """uint8 bytes holding two's-complement int8 codes -> float64 values (exact)."""
+    codes = np.asarray(codes)
+    if codes.dtype != np.uint8:
+        raise TypeError("int8 codes must be stored as uint8 bytes")
+    return codes.view(np.int8).astype(np.float64)

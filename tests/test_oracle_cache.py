@@ -154,3 +154,30 @@ def test_append_is_idempotent_and_bf16_rope_passes_through():
     b = oc.cache_append(a[0], "e4m3", bits, a[1], a[2], "e4m3", kbits, seq, nq, bt)
     for u, v in zip(a, b):
         assert np.array_equal(u, v)
+
+
+def test_int8_encoder_hand_cases_and_rint():
+    with open(os.path.join(GOLDEN, "int8_encode.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        assert oc.encode_int8(np.array([c["value"]]))[0] == int(c["byte"], 16), c
+    rng = np.random.default_rng(9)
+    v = np.concatenate([rng.uniform(-140, 140, 20000), np.arange(-130, 130) + 0.5])
+    ref = np.clip(np.rint(v), -127, 127).astype(np.int8).view(np.uint8)   # library round-half-even
+    assert np.array_equal(oc.encode_int8(v), ref)
+
+
+def test_int8_append_round_trip_within_half_a_step():
+    rng = np.random.default_rng(12)
+    seq, nq, bt, bits, kbits, kv, ik, isc = _random_append_case(rng, "e4m3", "e4m3")
+    out, _, _ = oc.cache_append(kv, "int8", bits, None, None, "e4m3", None, seq, nq, bt)
+    rows = oc.token_rows(seq, nq, bt)
+    x = decode_bf16(bits)
+    for t, r in enumerate(rows):
+        rec = out.reshape(-1, 656)[r]
+        scales = decode_f32le(rec[512:528])
+        amax = np.abs(x[t, :512]).reshape(4, 128).max(axis=1)
+        assert np.all(scales[amax > 0] == amax[amax > 0].astype(np.float32) / np.float32(127))
+        deq = rec[:512].view(np.int8).astype(np.float64) * np.repeat(scales, 128)
+        assert np.all(np.abs(deq - x[t, :512]) <= np.repeat(scales, 128) * (0.5 + 1e-6))
+        assert np.array_equal(rec[528:].view(np.uint16), bits[t, 512:])

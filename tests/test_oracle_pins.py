@@ -14,6 +14,7 @@ import pytest
 import torch
 
 import oracle
+from oracle.fp8 import decode_bf16
 from dsa_sparse_attention_02_gb300 import inputs as synth
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -327,3 +328,33 @@ def test_fp8_latent_dequant_is_exact_product():
     np.testing.assert_array_equal(dec[:, :512], ref)
     # the quantized latent stays within half an e4m3 step (2^-4 relative) of amax-scaled data
     assert np.all(np.abs(dec[:, :512]).max(axis=1) <= 448 * scales.max(axis=1) + 1e-12)
+
+
+def test_int8_latent_record_decodes_like_the_bf16_rows_it_stands_for():
+    """An int8 record whose codes times scales are exact bf16 values gives the same
+    attention as the bf16 cache holding those values (mlx-lm int8 MLA latent KV:
+    dequantized on read)."""
+    rng = np.random.default_rng(31)
+    P, T, H = 3, 2, 4
+    scales = np.float32(2.0) ** rng.integers(-6, -2, size=(P, 64, 4)).astype(np.float32)
+    codes = rng.integers(-127, 128, size=(P, 64, 512)).astype(np.int8)
+    rope = rng.standard_normal((P, 64, 64)).astype(np.float32)
+    rope_bits = (rope.view(np.uint32) >> 16).astype(np.uint16)
+    rec = np.empty((P, 64, 656), dtype=np.uint8)
+    rec[..., :512] = codes.view(np.uint8)
+    rec[..., 512:528] = np.ascontiguousarray(scales, dtype="<f4").view(np.uint8).reshape(P, 64, 16)
+    rec[..., 528:] = np.ascontiguousarray(rope_bits, dtype="<u2").view(np.uint8)
+    lat = codes.astype(np.float32) * np.repeat(scales, 128, axis=-1)          # exact in bf16 (8-bit codes x 2^k)
+    full = np.concatenate([lat, decode_bf16(rope_bits).astype(np.float32)], axis=-1)
+    kv_bf16 = (full.view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal(decode_bf16(kv_bf16), full.astype(np.float64))
+    seq = np.array([150, 40], dtype=np.int32)
+    nq = np.array([1, 1], dtype=np.int32)
+    bt = np.array([[2, 0, 1], [1, 0, 0]], dtype=np.int32)
+    q = (rng.standard_normal((T, H, 576)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    idx = {0: np.array([0, 5, 64, 149, -1], dtype=np.int32), 1: np.array([3, 39, -1, -1, -1], dtype=np.int32)}
+    a = oracle.sparse_mla(q, rec, "int8", idx, seq, nq, bt, 0.07, [0, 1])
+    b = oracle.sparse_mla(q, kv_bf16, "bf16", idx, seq, nq, bt, 0.07, [0, 1])
+    for t in (0, 1):
+        assert np.allclose(a[t][0], b[t][0], rtol=0, atol=1e-12)
+        assert np.allclose(a[t][1], b[t][1], rtol=0, atol=1e-12)
