@@ -290,6 +290,7 @@ def main():
     comp = measure_components(dw, flush, stream, max(20, min(args.steps, 200)))
     # ---- next row beyond the step: the cache update (timed alone; not part of `value`)
     append = measure_cache_append(dw, flush, stream, max(20, min(args.steps, 100)))
+    int8_attend = measure_int8_attend(dw, flush, stream, max(20, min(args.steps, 100)))
 
     idx_b, lat_b, selected = algorithmic_bytes(wl)
     peak, peak_kind = load_peaks()
@@ -316,7 +317,7 @@ def main():
                      "avg_launch_ms": comp["attend_ms"],
                      "traffic": load_traffic("sparse_mla_kernel")},
         "components_ms": comp,
-        "next_rows": {"cache_append": append},
+        "next_rows": {"cache_append": append, "int8_latent_attend": int8_attend},
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
@@ -440,6 +441,46 @@ def measure_cache_append(dw, flush, stream, n):
         ms = tot / n
         out[name] = {"ms": ms, "algorithmic_bytes": nbytes, "achieved_gbs": nbytes / (ms / 1000.0) / 1e9}
     return out
+
+
+def measure_int8_attend(dw, flush, stream, n):
+    """Device time of dsa_sparse_mla_attend over an int8 latent cache (next row f4):
+    the decode workload's bf16 latent cache re-encoded as int8 records by
+    dsa_cache_append (every row, as one request with an identity block table), then
+    attended with the step's own selection. Algorithmic bytes: the selected 656-byte
+    records."""
+    wl = dw.wl
+    dev = dw.device
+    lay = dw.layers[0]
+    P = wl.num_pages
+    rows = P * 64
+    seq = torch.tensor([rows], dtype=torch.int32, device=dev)
+    cu = torch.tensor([0, rows], dtype=torch.int32, device=dev)
+    bt = torch.arange(P, dtype=torch.int32, device=dev).view(1, P)
+    g_all = _lib.Geometry(seq, cu, bt, num_pages=P, max_seq_len=rows, T=rows)
+    kv8 = torch.empty(P, 64, 656, dtype=torch.uint8, device=dev)
+    ws = _lib.workspace(max(256, _lib.dsa_sparse_mla_attend_workspace_size(dw.geom, lay.q.shape[1], wl.topk)), dev)
+    _lib.dsa_cache_append(g_all, _lib.DSA_I8, lay.kv.view(rows, 576), kv8, _lib.DSA_E4M3, None, None, None, ws)
+    dw.step()
+    torch.cuda.synchronize()
+    _, pos = _positions(wl)
+    selected = int(np.minimum(pos + 1, wl.topk).sum())
+    out = torch.empty_like(lay.out)
+    lse = torch.empty_like(lay.lse)
+    tot = 0.0
+    for i in range(n):
+        flush.fill_(i & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(400_000)
+        a.record(stream)
+        _lib.dsa_sparse_mla_attend(dw.geom, _lib.DSA_I8, lay.q, kv8, dw.idx, wl.topk, wl.sm_scale, out, lse, ws)
+        b.record(stream)
+        b.synchronize()
+        tot += a.elapsed_time(b)
+    ms = tot / n
+    nbytes = selected * 656
+    return {"ms": ms, "algorithmic_bytes": nbytes, "achieved_gbs": nbytes / (ms / 1000.0) / 1e9,
+            "cache": "the decode cache re-encoded as int8 records (per-128 amax/127 scales, bf16 RoPE)"}
 
 
 if __name__ == "__main__":

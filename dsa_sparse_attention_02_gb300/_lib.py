@@ -16,7 +16,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdsa.so")
 
 DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_CUDA = 0, 1, 2, 3
 DSA_ERR_TIMEOUT, DSA_ERR_WORKSPACE, DSA_ERR_BAD_INDEX = 4, 5, 6
-DSA_BF16, DSA_E4M3 = 0, 1
+DSA_BF16, DSA_E4M3, DSA_I8 = 0, 1, 2
 
 EXPORTED = (
     "dsa_indexer_scores", "dsa_indexer_scores_workspace_size",

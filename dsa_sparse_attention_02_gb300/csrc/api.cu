@@ -74,6 +74,7 @@ constexpr int kTopkCap = 16384;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+int kv_format_of(dsa_dtype_t dt) { return dt == DSA_E4M3 ? kKvE4m3 : dt == DSA_I8 ? kKvInt8 : kKvBf16; }
 
 int num_sms() {
   static int cache[64] = {0};
@@ -165,7 +166,7 @@ dsa_status_t check_attend(const dsa_geom_t* g, dsa_dtype_t dt, int H, const void
                           int k, float sm_scale, const void* out) {
   dsa_status_t s = check_geom(g);
   if (s != DSA_OK) return s;
-  if (dt != DSA_BF16 && dt != DSA_E4M3) return DSA_ERR_INVALID_ARG;
+  if (dt != DSA_BF16 && dt != DSA_E4M3 && dt != DSA_I8) return DSA_ERR_INVALID_ARG;
   if (H < 1 || H > 128 || (H > 16 && H % 16 != 0)) return DSA_ERR_INVALID_ARG;
   if (k < 1 || k > kMaxTopk) return DSA_ERR_INVALID_ARG;
   if (!std::isfinite(sm_scale)) return DSA_ERR_INVALID_ARG;
@@ -195,7 +196,7 @@ dsa_status_t run_attend(const dsa_geom_t* g, dsa_dtype_t dt, int H, const void* 
   A.o_part = reinterpret_cast<float*>(scratch);
   A.ml_part = A.o_part + rows * 512;
   A.err = err;
-  return from_cuda(mla_launch(dt == DSA_E4M3, mq, A, grid, pdl, st));
+  return from_cuda(mla_launch(kv_format_of(dt), mq, A, grid, pdl, st));
 }
 
 int64_t step_score_stride(const dsa_geom_t* g) { return (int64_t)align_up((size_t)g->max_seq_len, 64); }
@@ -337,7 +338,7 @@ dsa_status_t dsa_cache_append(const dsa_geom_t* geom, dsa_dtype_t kv_dtype, cons
                               void* ws, size_t ws_bytes, void* stream) {
   dsa_status_t s = check_geom(geom);
   if (s != DSA_OK) return s;
-  if (kv_dtype != DSA_BF16 && kv_dtype != DSA_E4M3) return DSA_ERR_INVALID_ARG;
+  if (kv_dtype != DSA_BF16 && kv_dtype != DSA_E4M3 && kv_dtype != DSA_I8) return DSA_ERR_INVALID_ARG;
   if (k_new) {
     if (qk_dtype != DSA_BF16 && qk_dtype != DSA_E4M3) return DSA_ERR_INVALID_ARG;
     if (!idx_k_cache || !aligned16(k_new) || !aligned16(idx_k_cache)) return DSA_ERR_INVALID_ARG;
@@ -349,7 +350,7 @@ dsa_status_t dsa_cache_append(const dsa_geom_t* geom, dsa_dtype_t kv_dtype, cons
   if (!kv_new || !kv_cache || !aligned16(kv_new) || !aligned16(kv_cache)) return DSA_ERR_INVALID_ARG;
   AppendArgs A;
   A.g = to_dev(geom);
-  A.kv_fp8 = kv_dtype == DSA_E4M3;
+  A.kv_format = kv_format_of(kv_dtype);
   A.kv_new = kv_new;
   A.kv_cache = reinterpret_cast<uint8_t*>(kv_cache);
   A.k_fp8 = qk_dtype == DSA_E4M3;

@@ -7,6 +7,9 @@
 // L_b - n_b + j, physical row block_table[b][pos / 64] * 64 + pos % 64 -- the rows
 // the indexer and the attention read for it. One warp per token:
 //   * bf16 latent cache: the 1152-byte row copied as given;
+//   * int8 latent record (mlx-lm "GLM-5.2 (glm_moe_dsa) inference": int8 MLA latent
+//     KV): as the e4m3 record with scale = amax / 127 and codes rounded to the
+//     nearest integer (ties to even), clamped to +-127;
 //   * e4m3 latent record (656 B): lane l quantizes latent values 16l..16l+15; the
 //     eight lanes of a 128-value group reduce its amax, scale = amax / 448 (1 for an
 //     all-zero group), code = e4m3(x / scale) with the quotient in fp32 and the
@@ -25,12 +28,25 @@ namespace dsa {
 
 constexpr int kAppendWarps = 4;
 constexpr float kE4m3Max = 448.f;
+constexpr float kI8Max = 127.f;
 
 // Four e4m3 codes (byte i from value i): round to nearest even, saturate at +-448.
 __device__ __forceinline__ uint32_t e4m3_pack4(float a, float b, float c, float d) {
   const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
   const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
   return (lo & 0xFFFFu) | (hi << 16);
+}
+
+// Four int8 codes (byte i from value i): round to nearest even, clamp to +-127.
+__device__ __forceinline__ uint32_t i8_pack4(float a, float b, float c, float d) {
+  const float f[4] = {a, b, c, d};
+  uint32_t r = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int q = max(-127, min(127, __float2int_rn(f[i])));
+    r |= (uint32_t)(q & 0xFF) << (8 * i);
+  }
+  return r;
 }
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float (&f)[8]) {
@@ -50,7 +66,8 @@ __global__ void __launch_bounds__(32 * kAppendWarps) cache_append_kernel(const A
   // the row lookup (request search, block table), so the two latencies overlap.
   const uint4* src = reinterpret_cast<const uint4*>(A.kv_new) + (int64_t)t * 72;   // 576 bf16 = 72 x 16 B
   uint4 d0 = make_uint4(0, 0, 0, 0), d1 = d0, d2 = d0;
-  if (!A.kv_fp8) {
+  const bool record = A.kv_format != kKvBf16;
+  if (!record) {
     d0 = __ldg(src + lane);
     d1 = __ldg(src + 32 + lane);
     if (lane < 8) d2 = __ldg(src + 64 + lane);
@@ -69,7 +86,7 @@ __global__ void __launch_bounds__(32 * kAppendWarps) cache_append_kernel(const A
     return;
   }
   // ---- latent row
-  if (!A.kv_fp8) {
+  if (!record) {
     uint4* dst = reinterpret_cast<uint4*>(A.kv_cache + row * (kDimQK * 2));
     dst[lane] = d0;
     dst[32 + lane] = d1;
@@ -90,12 +107,17 @@ __global__ void __launch_bounds__(32 * kAppendWarps) cache_append_kernel(const A
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));   // amax of the lane's 128-value group
-    const float scale = m > 0.f ? m / kE4m3Max : 1.f;
+    const bool i8 = A.kv_format == kKvInt8;
+    const float scale = m > 0.f ? m / (i8 ? kI8Max : kE4m3Max) : 1.f;
     uint4 codes;
-    codes.x = e4m3_pack4(v[0] / scale, v[1] / scale, v[2] / scale, v[3] / scale);
-    codes.y = e4m3_pack4(v[4] / scale, v[5] / scale, v[6] / scale, v[7] / scale);
-    codes.z = e4m3_pack4(v[8] / scale, v[9] / scale, v[10] / scale, v[11] / scale);
-    codes.w = e4m3_pack4(v[12] / scale, v[13] / scale, v[14] / scale, v[15] / scale);
+    auto pack4 = [&](int i) {
+      const float a = v[i] / scale, b = v[i + 1] / scale, c = v[i + 2] / scale, d = v[i + 3] / scale;
+      return i8 ? i8_pack4(a, b, c, d) : e4m3_pack4(a, b, c, d);
+    };
+    codes.x = pack4(0);
+    codes.y = pack4(4);
+    codes.z = pack4(8);
+    codes.w = pack4(12);
     *reinterpret_cast<uint4*>(rec + 16 * lane) = codes;
     if ((lane & 7) == 0) *reinterpret_cast<float*>(rec + kDimLatent + 4 * (lane >> 3)) = scale;
     if (lane < 8) *reinterpret_cast<uint4*>(rec + kDimLatent + 16 + 16 * lane) = d2;

@@ -59,7 +59,7 @@ extern "C" dsa_status_t dsa_sparse_mla_attend_static(const dsa_geom_t* geom, dsa
   if (geom->page_size != 64) return DSA_ERR_UNSUPPORTED;
   if (geom->T > 0 && geom->B < 1) return DSA_ERR_INVALID_ARG;
   if (geom->bt_stride < (geom->max_seq_len + 63) / 64) return DSA_ERR_INVALID_ARG;
-  if (kv_dtype != DSA_BF16 && kv_dtype != DSA_E4M3) return DSA_ERR_INVALID_ARG;
+  if (kv_dtype != DSA_BF16 && kv_dtype != DSA_E4M3 && kv_dtype != DSA_I8) return DSA_ERR_INVALID_ARG;
   if (H < 1 || H > 128 || (H > 16 && H % 16 != 0)) return DSA_ERR_INVALID_ARG;
   if (k < 1 || k > 16384) return DSA_ERR_INVALID_ARG;
   if (!std::isfinite(sm_scale)) return DSA_ERR_INVALID_ARG;
@@ -97,7 +97,8 @@ extern "C" dsa_status_t dsa_sparse_mla_attend_static(const dsa_geom_t* geom, dsa
   A.o_part = reinterpret_cast<float*>(scratch);
   A.ml_part = A.o_part + (size_t)(geom->T + grid) * H * 512;
   A.err = reinterpret_cast<int*>(err_word);
-  const cudaError_t le = mla_launch(kv_dtype == DSA_E4M3, mq, A, grid, false, reinterpret_cast<cudaStream_t>(stream));
+  const int kv_format = kv_dtype == DSA_E4M3 ? kKvE4m3 : kv_dtype == DSA_I8 ? kKvInt8 : kKvBf16;
+  const cudaError_t le = mla_launch(kv_format, mq, A, grid, false, reinterpret_cast<cudaStream_t>(stream));
   if (le != cudaSuccess) {
     set_last_error("kernel launch", cudaGetErrorString(le));
     return DSA_ERR_CUDA;

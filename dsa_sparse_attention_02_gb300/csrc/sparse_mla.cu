@@ -21,8 +21,9 @@
 //   * four producer warps copy the CTA's columns of the rows with 16-byte
 //     cp.async into 128-byte-swizzled K-major atoms (zero-fill for padding), and
 //     end each slot with cp.async.mbarrier.arrive.noinc, so a slot's full barrier
-//     completes when its copies have landed. e4m3 cache: the latent codes are
-//     loaded, dequantized (code * per-128 scale) to bf16 and stored instead.
+//     completes when its copies have landed. e4m3 or int8 cache (mlx-lm "GLM-5.2
+//     (glm_moe_dsa) inference": int8 MLA latent KV, dequantized on read): the latent
+//     codes are loaded, dequantized (code * per-128 scale) to bf16 and stored instead.
 //   * one MMA thread (issuing S steps and PVs as they become ready, so that
 //     S(i+1) overlaps the softmax of chunk i): partial S^T = KV . Q^T over the CTA's 288 columns on
 //     tcgen05 (M = 128 keys, N = 16 heads) into TMEM, then, once P is known,
@@ -104,6 +105,13 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
   return __uint_as_float(__float_as_uint(v) | sign);
 }
 
+// A latent code byte -> fp32: e4m3 as above, or two's-complement int8 (exact).
+template <int kKv>
+__device__ __forceinline__ float code_to_f32(uint32_t c) {
+  if (kKv == kKvInt8) return (float)(int)(int8_t)(uint8_t)c;
+  return e4m3_to_f32(c);
+}
+
 // 2^x with the MUFU ex2 instruction (inputs here are <= 8 or -inf).
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
@@ -172,7 +180,7 @@ __device__ __forceinline__ int64_t selected_row(const MlaArgs& A, const QueryInf
   return row;
 }
 
-template <bool kFp8Kv>
+template <int kKv>
 __global__ void __launch_bounds__(kMlaThreads, 1)
     sparse_mla_kernel(const __grid_constant__ CUtensorMap map_q, const MlaArgs A) {
   extern __shared__ uint8_t smem_raw[];
@@ -298,8 +306,9 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       if (lane == 0) ok = mbar_wait(bar, parity, &abort_flag, A.err) ? 1 : 0;
       return __shfl_sync(0xffffffffu, ok, 0) != 0;
     };
-    const size_t row_bytes = kFp8Kv ? (size_t)kFp8Record : (size_t)(kDimQK * 2);
-    const size_t rope_off = (kFp8Kv ? (size_t)(kDimLatent + 16) : (size_t)(kDimLatent * 2)) + 64 * rank;
+    constexpr bool kRecord = kKv != kKvBf16;   // 656-byte record: codes, scales, RoPE
+    const size_t row_bytes = kRecord ? (size_t)kFp8Record : (size_t)(kDimQK * 2);
+    const size_t rope_off = (kRecord ? (size_t)(kDimLatent + 16) : (size_t)(kDimLatent * 2)) + 64 * rank;
     ChunkPos cp = chunk_pos(0);
     for (int i = 0; i < n_mine; chunk_next(cp, ++i)) {
       if (cp.first) {
@@ -332,7 +341,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       const int gidx = 2 * i + jl, ps = gidx % kPairSlots;
       if (!slot_acquire(smem_u32(&pair_empty[ps]), ((gidx / kPairSlots) & 1) ^ 1)) break;
       uint8_t* slot = pair_buf + ps * kPairBytes;
-      if (!kFp8Kv) {
+      if (!kRecord) {
         // 16 lanes per row (256 B of the pair), 2 rows per instruction: lane half h
         // takes rows r0 .. r0+31, r0 = 64*wg + 32*h, whose indices it reads up front
         const int r0 = 64 * wg + 32 * (lane >> 4);
@@ -379,8 +388,8 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const uint32_t wv = w4[q];
-              pk[2 * q] = pack_bf16x2(e4m3_to_f32(wv & 0xFF) * sc[jj], e4m3_to_f32((wv >> 8) & 0xFF) * sc[jj]);
-              pk[2 * q + 1] = pack_bf16x2(e4m3_to_f32((wv >> 16) & 0xFF) * sc[jj], e4m3_to_f32(wv >> 24) * sc[jj]);
+              pk[2 * q] = pack_bf16x2(code_to_f32<kKv>(wv & 0xFF) * sc[jj], code_to_f32<kKv>((wv >> 8) & 0xFF) * sc[jj]);
+              pk[2 * q + 1] = pack_bf16x2(code_to_f32<kKv>((wv >> 16) & 0xFF) * sc[jj], code_to_f32<kKv>(wv >> 24) * sc[jj]);
             }
             // pair column 16*part .. 16*part+15 -> atom part/4, bytes 32*(part%4) .. +31
             const int col_byte = (part >> 2) * 128 + (part & 3) * 32;
@@ -765,7 +774,7 @@ static int mla_max_clusters(int num_sms) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return num_sms / 2;
   if (cache[dev] > 0) return cache[dev];
   int n = 0;
-  if (cudaFuncSetAttribute(sparse_mla_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMlaSmemBytes) ==
+  if (cudaFuncSetAttribute(sparse_mla_kernel<kKvBf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMlaSmemBytes) ==
       cudaSuccess) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
@@ -775,7 +784,7 @@ static int mla_max_clusters(int num_sms) {
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = 2; at[0].val.clusterDim.y = 1; at[0].val.clusterDim.z = 1;
     cfg.attrs = at; cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&n, sparse_mla_kernel<false>, &cfg) != cudaSuccess) n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, sparse_mla_kernel<kKvBf16>, &cfg) != cudaSuccess) n = 0;
   }
   cudaGetLastError();
   if (n <= 0 || n > num_sms / 2) n = num_sms / 2;
@@ -794,9 +803,10 @@ size_t mla_partial_bytes(int T, int H, int grid) {
   return rows * kDimLatent * sizeof(float) + rows * 2 * sizeof(float);
 }
 
-cudaError_t mla_launch(bool fp8_kv, const CUtensorMap& map_q, MlaArgs A, int grid, bool pdl, cudaStream_t st) {
+cudaError_t mla_launch(int kv_format, const CUtensorMap& map_q, MlaArgs A, int grid, bool pdl, cudaStream_t st) {
   const int hgroups = (A.H + kMlaHeads - 1) / kMlaHeads;
-  auto kern = fp8_kv ? sparse_mla_kernel<true> : sparse_mla_kernel<false>;
+  auto kern = kv_format == kKvE4m3 ? sparse_mla_kernel<kKvE4m3>
+            : kv_format == kKvInt8 ? sparse_mla_kernel<kKvInt8> : sparse_mla_kernel<kKvBf16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMlaSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute at[2];

@@ -59,7 +59,7 @@ class DeviceWorkload:
             if L.kv_dtype == "bf16":
                 kv, kd = _dev(L.kv.view(np.int16), d, torch.bfloat16), _lib.DSA_BF16
             else:
-                kv, kd = _dev(L.kv, d), _lib.DSA_E4M3
+                kv, kd = _dev(L.kv, d), (_lib.DSA_E4M3 if L.kv_dtype == "e4m3" else _lib.DSA_I8)
             T, H = q.shape[0], q.shape[1]
             self.layers.append(DeviceLayer(q, kv, kd,
                                            torch.empty(T, H, 512, dtype=torch.bfloat16, device=d),

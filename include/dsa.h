@@ -67,7 +67,7 @@ typedef enum {
   DSA_ERR_BAD_INDEX = 6
 } dsa_status_t;
 
-typedef enum { DSA_BF16 = 0, DSA_E4M3 = 1 } dsa_dtype_t;
+typedef enum { DSA_BF16 = 0, DSA_E4M3 = 1, DSA_I8 = 2 } dsa_dtype_t;
 
 /* Request geometry shared by every entry point. */
 typedef struct {
@@ -123,6 +123,9 @@ size_t dsa_topk_workspace_size(const dsa_geom_t* geom, int32_t k);
  *   kv_dtype DSA_E4M3: kv_cache [num_pages, 64, 656] bytes per token: 512 e4m3
  *     latent codes, 4 little-endian fp32 scales (latent element 128c+e is
  *     code*scale[c]), 64 bf16 RoPE values.
+ *   kv_dtype DSA_I8: the same 656-byte record with two's-complement int8 codes
+ *     (the int8 latent cache of mlx-lm "GLM-5.2 (glm_moe_dsa) inference": only
+ *     the compressed latent is quantized; dequantized on read).
  *   idx [T, k] int32 (device): logical positions of the request's tokens; -1 is
  *     padding and is skipped.
  *   For each (t, h): z_i = sm_scale * q[t,h,:] . kv[s_i,:] over the selected s_i,
@@ -181,6 +184,8 @@ dsa_status_t dsa_sparse_mla_attend_static(const dsa_geom_t* geom, dsa_dtype_t kv
  *     an all-zero group) and code = e4m3(x / scale_c) (quotient in fp32, round
  *     to nearest even, saturating at +-448): 512 codes, the 4 scales as
  *     little-endian fp32, then the 64 RoPE values as bf16.
+ *   kv_dtype DSA_I8: the same record with scale_c = amax_c / 127 and int8 codes
+ *     round-to-nearest-even(x / scale_c) clamped to +-127.
  *   k_new [T, 128] bf16 (device) or NULL to leave the index cache alone.
  *   qk_dtype DSA_E4M3: idx_k_cache [num_pages, 64, 128] e4m3 and idx_k_scale
  *     [num_pages, 64] fp32 receive codes and one scale per token, same rule.

@@ -14,7 +14,7 @@ from gpu_helpers import DEV
 
 pytestmark = pytest.mark.gpu
 
-DT = {"bf16": _lib.DSA_BF16, "e4m3": _lib.DSA_E4M3}
+DT = {"bf16": _lib.DSA_BF16, "e4m3": _lib.DSA_E4M3, "int8": _lib.DSA_I8}
 
 
 def _bits(x32):
@@ -85,7 +85,8 @@ def _host(t, dtype):
     return a.view(dtype) if a.dtype != dtype else a
 
 
-@pytest.mark.parametrize("kv_dtype,qk_dtype", [("bf16", "e4m3"), ("e4m3", "e4m3"), ("e4m3", "bf16"), ("bf16", "bf16")])
+@pytest.mark.parametrize("kv_dtype,qk_dtype", [("bf16", "e4m3"), ("e4m3", "e4m3"), ("e4m3", "bf16"), ("bf16", "bf16"),
+                                               ("int8", "e4m3"), ("int8", "bf16")])
 def test_append_bit_exact_against_oracle(kv_dtype, qk_dtype):
     rng = np.random.default_rng(21)
     seq, nq, bt, bits, kbits, kv, ik, isc = _case(rng, kv_dtype, qk_dtype)

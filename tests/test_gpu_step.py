@@ -11,7 +11,7 @@ from gpu_helpers import DEV, assert_close, index_set_parity
 
 pytestmark = pytest.mark.gpu
 
-TOL = {"bf16": 2e-2, "e4m3": 5e-2}
+TOL = {"bf16": 2e-2, "e4m3": 5e-2, "int8": 5e-2}
 
 
 def _verify(wl, dw, ts):
@@ -36,13 +36,14 @@ def _verify(wl, dw, ts):
 SMALL = [
     ("tiny", dict()),
     ("decode", dict(batch=6)),
+    ("decode", dict(batch=6, latent="int8")),      # the int8 latent cache (next row f4)
     ("mtp", dict(batch=3, ctx_scale=0.25)),
     ("prefill", dict(ctx_scale=1 / 8)),
     ("longctx", dict(batch=2, ctx_scale=1 / 16)),
 ]
 
 
-@pytest.mark.parametrize("name,kw", SMALL, ids=[c[0] for c in SMALL])
+@pytest.mark.parametrize("name,kw", SMALL, ids=[c[0] + ("-" + c[1]["latent"] if "latent" in c[1] else "") for c in SMALL])
 def test_step_small_configs(name, kw):
     wl = inputs.make_config(name, **kw)
     dw = runner.DeviceWorkload(wl, DEV)
@@ -55,6 +56,7 @@ def test_step_small_configs(name, kw):
 
 FULL = [
     ("decode", 64),   # the bench configuration: every query checked
+    ("decode-int8", 16),
     ("mtp", 10),
     ("prefill", 8),
     ("longctx", 4),
@@ -63,7 +65,7 @@ FULL = [
 
 @pytest.mark.parametrize("name,nsample", FULL, ids=[c[0] for c in FULL])
 def test_step_full_size_sampled(name, nsample):
-    wl = inputs.make_config(name)
+    wl = inputs.make_config("decode", latent="int8") if name == "decode-int8" else inputs.make_config(name)
     dw = runner.DeviceWorkload(wl, DEV)
     dw.step()
     torch.cuda.synchronize()
