@@ -43,6 +43,8 @@
 // partials that the combine kernel merges with log-sum-exp weights.
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include "kernels.cuh"
 
 namespace dsa {
@@ -93,23 +95,22 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-// e4m3 code -> fp32, exact (sign, 4-bit exponent with bias 7, 3-bit mantissa;
-// exponent 0 encodes subnormals m * 2^-9; S.1111.111 is NaN).
-__device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
-  const uint32_t sign = (c & 0x80u) << 24;
-  const uint32_t em = c & 0x7Fu;
-  float v;
-  if (em == 0x7Fu) v = __uint_as_float(0x7FC00000u);
-  else if ((em >> 3) == 0) v = (float)(em & 7u) * 0.001953125f;            // m * 2^-9
-  else v = __uint_as_float((((em >> 3) + 120u) << 23) | ((em & 7u) << 20));  // rebias 7 -> 127
-  return __uint_as_float(__float_as_uint(v) | sign);
-}
-
-// A latent code byte -> fp32: e4m3 as above, or two's-complement int8 (exact).
+// Four latent codes (byte i of w = code i) -> fp32 values, exact.
+//   e4m3: every e4m3 value (subnormals, the NaN code) is a half value, so the
+//   hardware's e4m3x2 -> f16x2 conversion followed by f16 -> f32 is exact;
+//   int8: the biased byte x + 128 placed in the mantissa of 2^23 gives the float
+//   2^23 + 128 + x exactly, and subtracting 2^23 + 128 leaves x.
 template <int kKv>
-__device__ __forceinline__ float code_to_f32(uint32_t c) {
-  if (kKv == kKvInt8) return (float)(int)(int8_t)(uint8_t)c;
-  return e4m3_to_f32(c);
+__device__ __forceinline__ void codes4_to_f32(uint32_t w, float (&f)[4]) {
+  if (kKv == kKvInt8) {
+    const uint32_t x = w ^ 0x80808080u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f[i] = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7540u + i)) - 8388736.f;
+  } else {
+    const float2 a = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xFFFFu), __NV_E4M3)));
+    const float2 b = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3)));
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+  }
 }
 
 // 2^x with the MUFU ex2 instruction (inputs here are <= 8 or -inf).
@@ -192,6 +193,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
   float4* x_buf = reinterpret_cast<float4*>(p_buf + 2 * kPBufBytes);  // 2 x [4 head quads][128 keys]
 
   __shared__ uint64_t pair_full[kPairSlots], pair_empty[kPairSlots], rope_full[kRopeSlots], rope_empty[kRopeSlots];
+  __shared__ __align__(16) float scale_stage[kKv != kKvBf16 ? kPairSlots : 1][kMlaKeys];   // record caches
   __shared__ uint64_t q_full, q_empty;
   __shared__ uint64_t s_full[2], s_empty[2], p_full[2], p_empty[2], o_full, o_free, grp_bar;
   __shared__ uint64_t x_full[2], x_free[2];   // partial-score exchange with the other CTA
@@ -295,18 +297,76 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     // once; warp wg of a group copies rows [64*wg, 64*wg+64) of the pair. Every
     // producer warp also copies the RoPE columns of rows [32*pw, 32*pw+32). bf16:
     // 16-byte cp.async (zero-fill for padding), slot completion through
-    // cp.async.mbarrier.arrive.noinc. e4m3: the latent codes are loaded, dequantized
-    // to bf16 and stored, then each thread arrives.
+    // cp.async.mbarrier.arrive.noinc. e4m3 / int8 records: the codes and scales are
+    // staged by cp.async, and dequantized to bf16 in the slot one chunk later, so that
+    // the next chunk's loads are in flight during the conversion; each thread then
+    // arrives.
     const int pw = warp - kProdWarp0;
     const int jl = pw >> 1, wg = pw & 1;
     const int j = 2 * rank + jl;                 // pair of the row: latent columns 128j..128j+127
     int seg = 0;
-    auto slot_acquire = [&](uint32_t bar, uint32_t parity) -> bool {   // warp-uniform bounded wait
+    constexpr bool kRecord = kKv != kKvBf16;   // 656-byte record: codes, scales, RoPE
+    // Record caches: dequantizes the codes staged in the second atom of pair slot fps
+    // (this warp's 64 rows; lane part p = lane % 8 holds codes 16p..16p+15 of a row) to
+    // bf16 in the slot's swizzled layout, then marks the warp's share of the slot full.
+    // The bf16 row's second atom overwrites the staging of the same row, so all eight
+    // lanes of a row read before any writes. newer: the copies of one newer chunk may
+    // still be in flight.
+    int pend_ps = -1;
+    auto finish_record = [&](int fps, bool newer) {
+      if (newer) cp_async_wait<1>();
+      else cp_async_wait<0>();
+      __syncwarp();                               // the scale of a row is staged by its part-0 lane
+      uint8_t* fslot = pair_buf + fps * kPairBytes;
+      const uint8_t* stg = fslot + kAtomBytes;
+      const int part = lane & 7, sub = lane >> 3;
+      const int col_byte = (part >> 2) * 128 + (part & 3) * 32;   // pair columns 16p.. -> atom p/4
+#pragma unroll 1
+      for (int g = 0; g < 4; ++g) {
+        uint4 c[4];
+        float sc[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int r = 64 * wg + 16 * g + 4 * q + sub;
+          c[q] = *reinterpret_cast<const uint4*>(stg + r * 128 + 16 * part);
+          sc[q] = scale_stage[fps][r];
+        }
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int r = 64 * wg + 16 * g + 4 * q + sub;
+          const uint32_t w4[4] = {c[q].x, c[q].y, c[q].z, c[q].w};
+          uint32_t pk[8];
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            float f[4];
+            codes4_to_f32<kKv>(w4[h], f);
+            pk[2 * h] = pack_bf16x2(f[0] * sc[q], f[1] * sc[q]);
+            pk[2 * h + 1] = pack_bf16x2(f[2] * sc[q], f[3] * sc[q]);
+          }
+          *reinterpret_cast<uint4*>(fslot + sw128_offset(r, col_byte, kAtomBytes)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(fslot + sw128_offset(r, col_byte + 16, kAtomBytes)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(&pair_full[fps]));
+    };
+    // Warp-uniform bounded wait. A staged chunk is never held across a wait that is not
+    // already satisfied: every such wait may depend, through the MMA's order, on the
+    // staged chunk being converted (five pair slots cannot hold two pending chunks per
+    // group), so the chunk is converted first.
+    auto slot_acquire = [&](uint32_t bar, uint32_t parity) -> bool {
+      if (kRecord && pend_ps >= 0) {
+        const int ready = __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_test_wait(bar, parity) : 0, 0);
+        if (!ready) {
+          finish_record(pend_ps, false);
+          pend_ps = -1;
+        }
+      }
       int ok = 1;
       if (lane == 0) ok = mbar_wait(bar, parity, &abort_flag, A.err) ? 1 : 0;
       return __shfl_sync(0xffffffffu, ok, 0) != 0;
     };
-    constexpr bool kRecord = kKv != kKvBf16;   // 656-byte record: codes, scales, RoPE
     const size_t row_bytes = kRecord ? (size_t)kFp8Record : (size_t)(kDimQK * 2);
     const size_t rope_off = (kRecord ? (size_t)(kDimLatent + 16) : (size_t)(kDimLatent * 2)) + 64 * rank;
     ChunkPos cp = chunk_pos(0);
@@ -361,48 +421,31 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
                       row >= 0 ? 16u : 0u);
         }
         cp_async_arrive_noinc(smem_u32(&pair_full[ps]));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&rows_empty[rb]));
       } else {
-        // 8 lanes per row: lane part p dequantizes codes 16p..16p+15 of the pair's 128
+        // Record cache: the pair's 128 codes of each of this warp's 64 rows land by
+        // cp.async in the slot's second atom (row r at 16 KB + 128 r: exactly one atom),
+        // its scale in scale_stage[ps]; the codes are dequantized into the slot one
+        // iteration later, after the next chunk's copies are on their way.
+        const uint32_t stage = smem_u32(slot + kAtomBytes);
         const int part = lane & 7, sub = lane >> 3;
-#pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-          const int rbase = 64 * wg + 32 * half;
-          uint4 c[8];
-          float sc[8];
 #pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
-            const int row = rows[rbase + 4 * jj + sub];
-            c[jj] = make_uint4(0, 0, 0, 0);
-            sc[jj] = 0.f;
-            if (row >= 0) {
-              const uint8_t* rec = kv + (int64_t)row * kFp8Record;
-              c[jj] = __ldg(reinterpret_cast<const uint4*>(rec + 128 * j) + part);
-              sc[jj] = __ldg(reinterpret_cast<const float*>(rec + kDimLatent) + j);
-            }
-          }
-#pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
-            const int key = rbase + 4 * jj + sub;
-            const uint32_t w4[4] = {c[jj].x, c[jj].y, c[jj].z, c[jj].w};
-            uint32_t pk[8];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const uint32_t wv = w4[q];
-              pk[2 * q] = pack_bf16x2(code_to_f32<kKv>(wv & 0xFF) * sc[jj], code_to_f32<kKv>((wv >> 8) & 0xFF) * sc[jj]);
-              pk[2 * q + 1] = pack_bf16x2(code_to_f32<kKv>((wv >> 16) & 0xFF) * sc[jj], code_to_f32<kKv>(wv >> 24) * sc[jj]);
-            }
-            // pair column 16*part .. 16*part+15 -> atom part/4, bytes 32*(part%4) .. +31
-            const int col_byte = (part >> 2) * 128 + (part & 3) * 32;
-            *reinterpret_cast<uint4*>(slot + sw128_offset(key, col_byte, kAtomBytes)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            *reinterpret_cast<uint4*>(slot + sw128_offset(key, col_byte + 16, kAtomBytes)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-          }
+        for (int q = 0; q < 16; ++q) {
+          const int r = 64 * wg + 4 * q + sub;
+          const int row = rows[r];
+          const uint8_t* rec = kv + (int64_t)(row >= 0 ? row : 0) * kFp8Record;
+          cp_async_16(stage + r * 128 + 16 * part, rec + 128 * j + 16 * part, row >= 0 ? 16u : 0u);
+          if (part == 0) cp_async_4(smem_u32(&scale_stage[ps][r]), rec + kDimLatent + 4 * j, row >= 0 ? 4u : 0u);
         }
-        fence_proxy_async_smem();
-        mbar_arrive(smem_u32(&pair_full[ps]));
+        cp_async_commit();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&rows_empty[rb]));   // the staged chunk needs no row ids
+        if (pend_ps >= 0) finish_record(pend_ps, true);
+        pend_ps = ps;
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&rows_empty[rb]));
     }
+    if (kRecord && pend_ps >= 0) finish_record(pend_ps, false);   // no waits inside: safe after an abort too
   } else if (warp == kResolverWarp) {
     // ================================================================ row resolver
     ChunkPos cp = chunk_pos(0);
