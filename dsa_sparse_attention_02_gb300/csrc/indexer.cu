@@ -22,9 +22,11 @@
 // slots; a small descriptor per unit names the stage and slot it uses. In decode
 // a request's query is loaded once for all its key tiles; in prefill a key tile is
 // loaded once for the run of query groups that follow it. Warp M issues the MMAs
-// into two TMEM accumulators; 4*EW epilogue warps drain them (one 64-column TMEM
-// load per query) reading only TMEM, the stage and the slot. Units are split
-// contiguously over a persistent grid, key-tile major.
+// into a ring of up to four TMEM accumulators; 4*EW epilogue warps drain them (one
+// 64-column TMEM load per query). The epilogue takes what it needs from a key
+// stage (the key scales) and from a query slot (w * q_scale) when it first meets
+// it and releases it at once, so a stage is held only until its MMAs complete.
+// Units are split contiguously over a persistent grid, key-tile major.
 #include <cstdint>
 #include "kernels.cuh"
 
@@ -58,13 +60,18 @@ struct IndexerCfg {
   // registers: kCtasPerSm CTAs of kBoundThreads share the register file
   static constexpr int kBoundCtas = kCtasPerSm;
   static constexpr int kProdWarp = kEpiWarps, kMmaWarp = kEpiWarps + kProdWarps;
-  static constexpr int kTmemCols = (2 * kN) <= 32 ? 32 : (2 * kN) <= 64 ? 64 : (2 * kN) <= 128 ? 128
-                                   : (2 * kN) <= 256 ? 256 : 512;
+  // TMEM accumulators: up to four, within this CTA's share of the 512 columns, so
+  // that the MMA can run several units ahead of the epilogue.
+  static constexpr int kAccsFit = (512 / kCtasPerSm) / kN;
+  static constexpr int kAccs = kAccsFit >= 4 ? 4 : kAccsFit;
+  static constexpr int kTmemCols = (kAccs * kN) <= 32 ? 32 : (kAccs * kN) <= 64 ? 64 : (kAccs * kN) <= 128 ? 128
+                                   : (kAccs * kN) <= 256 ? 256 : 512;
   static constexpr int kMaxB = 1024;                           // requests per call
   static constexpr int kSmemBytes = 1024 + kQSlots * kQSlotBytes + kKStages * kKStageBytes;
   static constexpr int kKSteps = kFp8 ? 4 : 8;
   static_assert(kN <= 256 && kN % 16 == 0, "MMA N");
   static_assert(kKStages >= 2, "key stages");
+  static_assert(kAccs >= 2 && kAccs * kN <= 512 / kCtasPerSm, "TMEM accumulators");
 };
 
 // What the MMA and epilogue warps need about a unit; written by the producer.
@@ -116,7 +123,10 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, Ind
   __shared__ uint64_t key_full[C::kKStages], key_empty[C::kKStages];
   __shared__ uint64_t q_full[C::kQSlots], q_empty[C::kQSlots];
   __shared__ uint64_t desc_full[C::kDescs], desc_empty[C::kDescs];
-  __shared__ uint64_t tfull_bar[2], tempty_bar[2];
+  __shared__ uint64_t tfull_bar[C::kAccs], tempty_bar[C::kAccs];
+  // w * q_scale of the current query group, one copy per epilogue warp
+  constexpr bool kWqRegs = kQG == 1 && C::kCtasPerSm == 1;
+  __shared__ __align__(16) float wq_s[kWqRegs ? 1 : C::kEpiWarps][kWqRegs ? 4 : kQG * kHp];
   __shared__ UnitDesc descs[C::kDescs];
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
@@ -126,17 +136,27 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, Ind
   const GeomDev& g = A.g;
   const int B = g.B;
 
-  // ---- per-CTA unit table: prefix[b] = units before request b
+  // ---- per-CTA unit table: prefix[b] = units before request b. The request
+  // metadata is read in one round trip by every thread; meanwhile the CTAs warm the
+  // block table in L2 (a slice each), which the producer reads next.
+  {
+    const int64_t bt_lines = ((int64_t)B * g.bt_stride * 4 + 127) / 128;
+    if (tid >= 32 && tid < 64)
+      for (int64_t l = blockIdx.x + (int64_t)gridDim.x * (tid - 32); l < bt_lines; l += (int64_t)gridDim.x * 32)
+        prefetch_l2(reinterpret_cast<const uint8_t*>(g.block_table) + l * 128);
+    for (int b = tid; b <= B; b += C::kThreads) {
+      cuq_s[b] = __ldg(g.cu_q + b);
+      if (b < B) lens_s[b] = __ldg(g.seq_lens + b);
+    }
+  }
+  __syncthreads();
   if (warp == 0) {
     int run = 0;
     for (int base = 0; base < B; base += 32) {
       const int b = base + lane;
       int units = 0;
       if (b < B) {
-        const int q0 = __ldg(g.cu_q + b), q1 = __ldg(g.cu_q + b + 1), len = __ldg(g.seq_lens + b);
-        cuq_s[b + 1] = q1;
-        lens_s[b] = len;
-        if (b == 0) cuq_s[0] = q0;
+        const int q0 = cuq_s[b], q1 = cuq_s[b + 1], len = lens_s[b];
         const int nq = q1 - q0;
         const bool ok = nq >= 0 && nq <= len && len <= g.max_seq_len && q1 <= g.T;
         if (!ok) record_error(A.err, kDevBadIndex);
@@ -160,7 +180,7 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, Ind
     for (int s = 0; s < C::kKStages; ++s) { mbar_init(smem_u32(&key_full[s]), 1); mbar_init(smem_u32(&key_empty[s]), 1 + C::kEpiWarps); }
     for (int s = 0; s < C::kQSlots; ++s) { mbar_init(smem_u32(&q_full[s]), 1); mbar_init(smem_u32(&q_empty[s]), 1 + C::kEpiWarps); }
     for (int s = 0; s < C::kDescs; ++s) { mbar_init(smem_u32(&desc_full[s]), 1); mbar_init(smem_u32(&desc_empty[s]), 1 + C::kEpiWarps); }
-    for (int a = 0; a < 2; ++a) { mbar_init(smem_u32(&tfull_bar[a]), 1); mbar_init(smem_u32(&tempty_bar[a]), C::kEpiWarps); }
+    for (int a = 0; a < C::kAccs; ++a) { mbar_init(smem_u32(&tfull_bar[a]), 1); mbar_init(smem_u32(&tempty_bar[a]), C::kEpiWarps); }
     fence_mbar_init();
   }
   // Query rows beyond Hi and w / q_scale entries beyond Hi stay zero for the whole
@@ -294,8 +314,8 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, Ind
           if (!mbar_wait(smem_u32(&q_full[cur_q]), (qc / C::kQSlots) & 1, &abort_flag, A.err)) break;
           ++qc;
         }
-        const int acc = i & 1;
-        if (!mbar_wait(smem_u32(&tempty_bar[acc]), ((i >> 1) & 1) ^ 1, &abort_flag, A.err)) break;
+        const int acc = i % C::kAccs;
+        if (!mbar_wait(smem_u32(&tempty_bar[acc]), ((i / C::kAccs) & 1) ^ 1, &abort_flag, A.err)) break;
         tc_fence_after();
         const uint64_t a0 = smem_desc(smem_u32(k_stages + cur_k * C::kKStageBytes), 0, 1024, kSwizzle128B);
         const uint64_t b0 = smem_desc(smem_u32(q_slots + cur_q * C::kQSlotBytes), 0, 1024, kSwizzle128B);
@@ -313,16 +333,18 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, Ind
     }
   } else {
     // ================================================================ epilogue warps
-    // Lane = key of the tile; reads the accumulator (TMEM), w and q_scale (the
-    // query slot) and its key's scale (global, fetched before the accumulator
-    // is ready).
+    // Lane = key of the tile. A new key stage: the key's scale is read into a
+    // register and the stage released at once (the MMA's commit covers its own
+    // reads). A new query group: w * q_scale is formed once (registers for one query
+    // and one CTA per SM, else this warp's shared copy) and the slot released. Then
+    // per unit only the accumulator (TMEM) is read.
     const int quarter = warp & 3, half = warp >> 2;
     const int key = quarter * 32 + lane;
     const float neg_inf = -__int_as_float(0x7f800000);
     int kc = 0, qc = 0, cur_k = -1, cur_q = -1;
-    // with one query per unit and one CTA per SM, w*q_scale stays in registers
-    constexpr bool kWqRegs = kQG == 1 && C::kCtasPerSm == 1;
+    float ks = 1.f;
     float wq[kWqRegs ? kHp : 1];
+    const float* wqw = &wq_s[kWqRegs ? 0 : warp][0];
     for (int u = u_begin, i = 0; u < u_end; ++u, ++i) {
       const int r = i % C::kDescs;
       if (!mbar_wait(smem_u32(&desc_full[r]), (i / C::kDescs) & 1, &abort_flag, A.err)) break;
@@ -330,20 +352,20 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, Ind
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&desc_empty[r]));
       const int page = (key < 64) ? d.page0 : d.page1;
-      // moving to a new stage / slot releases the previous one (this warp is done with it)
       if (d.flags & kNewKey) {
-        if (cur_k >= 0 && lane == 0) mbar_arrive(smem_u32(&key_empty[cur_k]));
         cur_k = d.kstage;
         if (!mbar_wait(smem_u32(&key_full[cur_k]), (kc / C::kKStages) & 1, &abort_flag, A.err)) break;   // key scales visible
         ++kc;
+        if (kFp8) ks = reinterpret_cast<const float*>(k_stages + cur_k * C::kKStageBytes + C::kKeyBytes)[key];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&key_empty[cur_k]));
       }
       if (d.flags & kNewQuery) {
-        if (cur_q >= 0 && lane == 0) mbar_arrive(smem_u32(&q_empty[cur_q]));
         cur_q = d.qslot;
         if (!mbar_wait(smem_u32(&q_full[cur_q]), (qc / C::kQSlots) & 1, &abort_flag, A.err)) break;   // w, q_scale visible
         ++qc;
+        const uint8_t* sl = q_slots + cur_q * C::kQSlotBytes;
         if constexpr (kWqRegs) {
-          const uint8_t* sl = q_slots + cur_q * C::kQSlotBytes;
 #pragma unroll
           for (int e = 0; e < kHp; e += 4) {
             const float4 w4 = *reinterpret_cast<const float4*>(sl + C::kWOff + e * 4);
@@ -351,17 +373,20 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, Ind
             if (kFp8) q4 = *reinterpret_cast<const float4*>(sl + C::kQsOff + e * 4);
             wq[e] = w4.x * q4.x; wq[e + 1] = w4.y * q4.y; wq[e + 2] = w4.z * q4.z; wq[e + 3] = w4.w * q4.w;
           }
+        } else {
+          __syncwarp();   // the previous group's copy has been read by every lane
+          const float* wv = reinterpret_cast<const float*>(sl + C::kWOff);
+          const float* qv = reinterpret_cast<const float*>(sl + C::kQsOff);
+          for (int e = lane; e < kQG * kHp; e += 32) wq_s[warp][e] = wv[e] * (kFp8 ? qv[e] : 1.f);
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&q_empty[cur_q]));
       }
-      const int acc = i & 1;
-      if (!mbar_wait(smem_u32(&tfull_bar[acc]), (i >> 1) & 1, &abort_flag, A.err)) break;
+      const int acc = i % C::kAccs;
+      if (!mbar_wait(smem_u32(&tfull_bar[acc]), (i / C::kAccs) & 1, &abort_flag, A.err)) break;
       tc_fence_after();
-      const uint8_t* sl = q_slots + cur_q * C::kQSlotBytes;
-      const float* wv = reinterpret_cast<const float*>(sl + C::kWOff);
-      const float* qv = reinterpret_cast<const float*>(sl + C::kQsOff);
       const int sidx = d.tile * 128 + key;
       const bool in_ctx = sidx < d.len;
-      const float ks = kFp8 ? reinterpret_cast<const float*>(k_stages + cur_k * C::kKStageBytes + C::kKeyBytes)[key] : 1.f;
 #pragma unroll 1
       for (int j = half; j < kQG; j += C::kEW) {
         if (j >= d.q_count) break;
@@ -377,10 +402,8 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, Ind
           if constexpr (kWqRegs) {
             c[0] = wq[e]; c[1] = wq[e + 1]; c[2] = wq[e + 2]; c[3] = wq[e + 3];
           } else {
-            const float4 w4 = *reinterpret_cast<const float4*>(wv + j * kHp + e);
-            float4 q4 = make_float4(1.f, 1.f, 1.f, 1.f);
-            if (kFp8) q4 = *reinterpret_cast<const float4*>(qv + j * kHp + e);
-            c[0] = w4.x * q4.x; c[1] = w4.y * q4.y; c[2] = w4.z * q4.z; c[3] = w4.w * q4.w;
+            const float4 w4 = *reinterpret_cast<const float4*>(wqw + j * kHp + e);
+            c[0] = w4.x; c[1] = w4.y; c[2] = w4.z; c[3] = w4.w;
           }
 #pragma unroll
           for (int x = 0; x < 4; ++x) s4[x] = fmaf(c[x], fmaxf(v[e + x], 0.f), s4[x]);
