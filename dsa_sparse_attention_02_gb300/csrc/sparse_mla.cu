@@ -866,6 +866,10 @@ cudaError_t mla_launch(int kv_format, const CUtensorMap& map_q, MlaArgs A, int g
   e = cudaLaunchKernelEx(&cfg, kern, map_q, A);
   if (e != cudaSuccess) return e;
   if (A.C > 1) {  // a query with several chunks may span clusters
+    // the shared-memory configuration of the attention grid it follows
+    e = cudaFuncSetAttribute(mla_combine_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cc{};
     cc.gridDim = dim3(A.g.T, A.H, 1);
     cc.blockDim = dim3(128, 1, 1);

@@ -331,6 +331,11 @@ static cudaError_t launch_topk_kernel(const TopkLaunch& L, int grid, int seg_len
     const cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
+  // The attention kernel that follows needs the whole shared-memory carveout; an SM
+  // left in the same configuration takes its CTAs without reconfiguring.
+  cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                       (int)cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
