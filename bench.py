@@ -291,6 +291,8 @@ def main():
     # ---- next row beyond the step: the cache update (timed alone; not part of `value`)
     append = measure_cache_append(dw, flush, stream, max(20, min(args.steps, 100)))
     int8_attend = measure_int8_attend(dw, flush, stream, max(20, min(args.steps, 100)))
+    fp8_attend = measure_int8_attend(dw, flush, stream, max(20, min(args.steps, 100)), kv_dtype=_lib.DSA_E4M3)
+    prep = measure_indexer_prep(dw, flush, stream, max(20, min(args.steps, 100)))
 
     idx_b, lat_b, selected = algorithmic_bytes(wl)
     peak, peak_kind = load_peaks()
@@ -317,7 +319,8 @@ def main():
                      "avg_launch_ms": comp["attend_ms"],
                      "traffic": load_traffic("sparse_mla_kernel")},
         "components_ms": comp,
-        "next_rows": {"cache_append": append, "int8_latent_attend": int8_attend},
+        "next_rows": {"cache_append": append, "int8_latent_attend": int8_attend, "indexer_prep": prep},
+        "e4m3_latent_attend": fp8_attend,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
@@ -443,12 +446,66 @@ def measure_cache_append(dw, flush, stream, n):
     return out
 
 
-def measure_int8_attend(dw, flush, stream, n):
-    """Device time of dsa_sparse_mla_attend over an int8 latent cache (next row f4):
-    the decode workload's bf16 latent cache re-encoded as int8 records by
-    dsa_cache_append (every row, as one request with an identity block table), then
-    attended with the step's own selection. Algorithmic bytes: the selected 656-byte
-    records."""
+def measure_indexer_prep(dw, flush, stream, n):
+    """Device time of dsa_indexer_prepare (the indexer-preparation row), launched alone
+    with the GPU kept busy while the host enqueues, L2 flushed before each: (a) the
+    decode batch's 64 tokens x 64 indexer heads, keys into its e4m3 index cache, (b) a
+    2048-token prefill chunk. Algorithmic bytes: bf16 q and k read (256 B per head and
+    per key), e4m3 codes and fp32 scales written (132 B each), the RoPE table rows of
+    the tokens' positions read (256 B per token)."""
+    import types
+    wl = dw.wl
+    dev = dw.device
+    ws = _lib.workspace(256, dev)
+    hi = int(wl.q_idx.shape[1])
+
+    def dev_bits(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
+
+    cases = {}
+    pi = inputs.make_prep_inputs(wl, hi=hi, rope_dim=64, seed=7)
+    cases["decode_64_tokens_64_heads"] = (dw.geom, pi, dw.idx_k, dw.idx_k_scale, wl.T)
+    L, m = 4096, 2048
+    P = L // 64
+    rng = np.random.default_rng(98)
+    seq = torch.tensor([L], dtype=torch.int32, device=dev)
+    cu = torch.tensor([0, m], dtype=torch.int32, device=dev)
+    bt = torch.from_numpy(rng.permutation(P).astype(np.int32).reshape(1, P)).to(dev)
+    g2 = _lib.Geometry(seq, cu, bt, num_pages=P, max_seq_len=L, T=m)
+    pi2 = inputs.make_prep_inputs(types.SimpleNamespace(n_q=np.array([m]), max_seq_len=L), hi=hi, rope_dim=64, seed=8)
+    cases["prefill_2048_tokens_64_heads"] = (g2, pi2, torch.zeros(P, 64, 128, dtype=torch.uint8, device=dev),
+                                             torch.zeros(P, 64, dtype=torch.float32, device=dev), m)
+    out = {}
+    for name, (g, p, kc, ks, T) in cases.items():
+        q_in, k_in = dev_bits(p.q_in), dev_bits(p.k_in)
+        cos, sin = torch.from_numpy(p.rope_cos).to(dev), torch.from_numpy(p.rope_sin).to(dev)
+        gm, bt_ = torch.from_numpy(p.ln_gamma).to(dev), torch.from_numpy(p.ln_beta).to(dev)
+        q_out = torch.empty(T, hi, 128, dtype=torch.uint8, device=dev)
+        q_scale = torch.empty(T, hi, dtype=torch.float32, device=dev)
+        nbytes = T * (hi * (256 + 132) + 256 + 132 + 256)
+        tot = 0.0
+        for i in range(n):
+            flush.fill_(i & 0xFF)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda._sleep(200_000)
+            a.record(stream)
+            _lib.dsa_indexer_prepare(g, hi, p.rope_dim, q_in, k_in, cos, sin, gm, bt_, p.ln_eps, q_out, q_scale,
+                                     kc, ks, ws)
+            b.record(stream)
+            b.synchronize()
+            tot += a.elapsed_time(b)
+        ms = tot / n
+        out[name] = {"ms": ms, "algorithmic_bytes": nbytes, "achieved_gbs": nbytes / (ms / 1000.0) / 1e9}
+    return out
+
+
+def measure_int8_attend(dw, flush, stream, n, kv_dtype=None):
+    """Device time of dsa_sparse_mla_attend over an int8 (next row f4) or, with
+    kv_dtype=DSA_E4M3, an e4m3 latent record cache: the decode workload's bf16 latent
+    cache re-encoded as records by dsa_cache_append (every row, as one request with an
+    identity block table), then attended with the step's own selection. Algorithmic
+    bytes: the selected 656-byte records."""
+    kv_dtype = _lib.DSA_I8 if kv_dtype is None else kv_dtype
     wl = dw.wl
     dev = dw.device
     lay = dw.layers[0]
@@ -460,7 +517,7 @@ def measure_int8_attend(dw, flush, stream, n):
     g_all = _lib.Geometry(seq, cu, bt, num_pages=P, max_seq_len=rows, T=rows)
     kv8 = torch.empty(P, 64, 656, dtype=torch.uint8, device=dev)
     ws = _lib.workspace(max(256, _lib.dsa_sparse_mla_attend_workspace_size(dw.geom, lay.q.shape[1], wl.topk)), dev)
-    _lib.dsa_cache_append(g_all, _lib.DSA_I8, lay.kv.view(rows, 576), kv8, _lib.DSA_E4M3, None, None, None, ws)
+    _lib.dsa_cache_append(g_all, kv_dtype, lay.kv.view(rows, 576), kv8, _lib.DSA_E4M3, None, None, None, ws)
     dw.step()
     torch.cuda.synchronize()
     _, pos = _positions(wl)
@@ -473,14 +530,16 @@ def measure_int8_attend(dw, flush, stream, n):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda._sleep(400_000)
         a.record(stream)
-        _lib.dsa_sparse_mla_attend(dw.geom, _lib.DSA_I8, lay.q, kv8, dw.idx, wl.topk, wl.sm_scale, out, lse, ws)
+        _lib.dsa_sparse_mla_attend(dw.geom, kv_dtype, lay.q, kv8, dw.idx, wl.topk, wl.sm_scale, out, lse, ws)
         b.record(stream)
         b.synchronize()
         tot += a.elapsed_time(b)
     ms = tot / n
     nbytes = selected * 656
     return {"ms": ms, "algorithmic_bytes": nbytes, "achieved_gbs": nbytes / (ms / 1000.0) / 1e9,
-            "cache": "the decode cache re-encoded as int8 records (per-128 amax/127 scales, bf16 RoPE)"}
+            "cache": ("the decode cache re-encoded as int8 records (per-128 amax/127 scales, bf16 RoPE)"
+                      if kv_dtype == _lib.DSA_I8 else
+                      "the decode cache re-encoded as e4m3 records (per-128 amax/448 scales, bf16 RoPE)")}
 
 
 if __name__ == "__main__":

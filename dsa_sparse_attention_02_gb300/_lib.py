@@ -24,6 +24,7 @@ EXPORTED = (
     "dsa_sparse_mla_attend", "dsa_sparse_mla_attend_workspace_size", "dsa_sparse_mla_attend_static",
     "dsa_decode_step", "dsa_decode_step_workspace_size",
     "dsa_cache_append", "dsa_cache_append_workspace_size",
+    "dsa_indexer_prepare", "dsa_indexer_prepare_workspace_size",
     "dsa_get_error", "dsa_clear_error", "dsa_status_string", "dsa_last_error", "dsa_abi_version",
 )
 
@@ -83,6 +84,8 @@ def load(path: str = LIB_PATH):
         "dsa_decode_step_workspace_size": (SZ, [S]),
         "dsa_cache_append": (C.c_int, [G, C.c_int, P, P, C.c_int, P, P, P, P, SZ, P]),
         "dsa_cache_append_workspace_size": (SZ, [G]),
+        "dsa_indexer_prepare": (C.c_int, [G, I32, I32, P, P, P, P, P, P, F, P, P, P, P, P, SZ, P]),
+        "dsa_indexer_prepare_workspace_size": (SZ, [G]),
         "dsa_get_error": (C.c_int, [P, P]),
         "dsa_clear_error": (C.c_int, [P, P]),
         "dsa_status_string": (C.c_char_p, [C.c_int]),
@@ -204,6 +207,22 @@ def dsa_cache_append(geom: Geometry, kv_dtype: int, kv_new, kv_cache, qk_dtype: 
                                  _ptr(idx_k_cache), _ptr(idx_k_scale), _ptr(ws), ws.numel() if ws is not None else 0,
                                  _stream(stream))
     _check(st, "dsa_cache_append")
+
+
+def dsa_indexer_prepare_workspace_size(geom: Geometry) -> int:
+    return int(load().dsa_indexer_prepare_workspace_size(geom.ref))
+
+
+def dsa_indexer_prepare(geom: Geometry, Hi: int, rope_dim: int, q_in, k_in, rope_cos, rope_sin, ln_gamma,
+                        ln_beta, ln_eps: float, q_out, q_scale, idx_k_cache=None, idx_k_scale=None, ws=None,
+                        stream=None):
+    """RoPE + e4m3 of the indexer queries into q_out / q_scale; LayerNorm + RoPE + e4m3
+    of the new tokens' keys (k_in, or None) into the paged index cache."""
+    st = load().dsa_indexer_prepare(geom.ref, int(Hi), int(rope_dim), _ptr(q_in), _ptr(k_in), _ptr(rope_cos),
+                                    _ptr(rope_sin), _ptr(ln_gamma), _ptr(ln_beta), float(ln_eps), _ptr(q_out),
+                                    _ptr(q_scale), _ptr(idx_k_cache), _ptr(idx_k_scale), _ptr(ws),
+                                    ws.numel() if ws is not None else 0, _stream(stream))
+    _check(st, "dsa_indexer_prepare")
 
 
 def make_step_args(geom: Geometry, topk: int, *, qk_dtype=DSA_E4M3, q_idx=None, q_scale=None,

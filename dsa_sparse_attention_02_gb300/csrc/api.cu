@@ -361,6 +361,50 @@ dsa_status_t dsa_cache_append(const dsa_geom_t* geom, dsa_dtype_t kv_dtype, cons
   return from_cuda(cache_append_launch(A, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t dsa_indexer_prepare_workspace_size(const dsa_geom_t*) { return kHeaderBytes; }
+
+dsa_status_t dsa_indexer_prepare(const dsa_geom_t* geom, int32_t Hi, int32_t rope_dim, const void* q_in,
+                                 const void* k_in, const float* rope_cos, const float* rope_sin,
+                                 const float* ln_gamma, const float* ln_beta, float ln_eps, void* q_out,
+                                 float* q_scale, void* idx_k_cache, float* idx_k_scale, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  dsa_status_t s = check_geom(geom);
+  if (s != DSA_OK) return s;
+  if (Hi < 1 || Hi > 128) return DSA_ERR_INVALID_ARG;
+  if (rope_dim < 8 || rope_dim > 128 || rope_dim % 8 != 0) return DSA_ERR_INVALID_ARG;
+  if (!(ln_eps >= 0.f) || !std::isfinite(ln_eps)) return DSA_ERR_INVALID_ARG;
+  if (k_in && (!idx_k_cache || !idx_k_scale || !aligned16(k_in) || !aligned16(idx_k_cache))) return DSA_ERR_INVALID_ARG;
+  if ((ln_gamma && !aligned16(ln_gamma)) || (ln_beta && !aligned16(ln_beta))) return DSA_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < kHeaderBytes || (reinterpret_cast<uintptr_t>(ws) & 255u)) return DSA_ERR_WORKSPACE;
+  if (geom->T == 0) return DSA_OK;
+  if (!q_in || !q_out || !q_scale || !rope_cos || !rope_sin) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q_in) || !aligned16(q_out) || !aligned16(rope_cos) || !aligned16(rope_sin)) return DSA_ERR_INVALID_ARG;
+  PrepArgs A;
+  A.g = to_dev(geom);
+  A.Hi = Hi;
+  A.rope_dim = rope_dim;
+  // fewer tokens than two per SM: a token's heads are spread over up to 8 blocks
+  {
+    const int groups = (Hi + 3) / 4;
+    int split = (2 * num_sms() + geom->T - 1) / geom->T;
+    split = split < 1 ? 1 : (split > 8 ? 8 : split);
+    A.split = split < groups ? split : groups;
+  }
+  A.q_in = q_in;
+  A.k_in = k_in;
+  A.rope_cos = rope_cos;
+  A.rope_sin = rope_sin;
+  A.ln_gamma = ln_gamma;
+  A.ln_beta = ln_beta;
+  A.ln_eps = ln_eps;
+  A.q_out = reinterpret_cast<uint8_t*>(q_out);
+  A.q_scale = q_scale;
+  A.k_cache = reinterpret_cast<uint8_t*>(idx_k_cache);
+  A.k_scale = idx_k_scale;
+  A.err = reinterpret_cast<int*>(ws);
+  return from_cuda(indexer_prep_launch(A, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 dsa_status_t dsa_get_error(void* ws, void* stream) {
   if (!ws) return DSA_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

@@ -71,6 +71,27 @@ struct AppendArgs {
 };
 cudaError_t cache_append_launch(const AppendArgs& A, cudaStream_t st);
 
+// ---- indexer preparation (indexer_prep.cu)
+struct PrepArgs {
+  GeomDev g;
+  int Hi;                       // indexer heads
+  int rope_dim;                 // rotated values at the front of each 128 (multiple of 8)
+  int split;                    // blocks per token (each takes a run of whole 4-head groups)
+  const void* q_in;             // [T, Hi, 128] bf16
+  const void* k_in;             // [T, 128] bf16, or null (queries only)
+  const float* rope_cos;        // [max_seq_len, rope_dim/2]
+  const float* rope_sin;        // [max_seq_len, rope_dim/2]
+  const float* ln_gamma;        // [128] or null (1)
+  const float* ln_beta;         // [128] or null (0)
+  float ln_eps;
+  uint8_t* q_out;               // [T, Hi, 128] e4m3
+  float* q_scale;               // [T, Hi]
+  uint8_t* k_cache;             // [P*64, 128] e4m3
+  float* k_scale;               // [P*64]
+  int* err;
+};
+cudaError_t indexer_prep_launch(const PrepArgs& A, cudaStream_t st);
+
 // ---- host helpers defined in api.cu
 bool encode_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t cols,
                           uint64_t rows, uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows);

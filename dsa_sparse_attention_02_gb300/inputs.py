@@ -299,3 +299,35 @@ def tied_scores(rng: np.random.Generator, rows: int, n: int, frac: float = 0.01,
             where = rng.choice(n, size=kth_copies, replace=False)
             s[r, where] = kth
     return s
+
+
+@dataclass
+class PrepInputs:
+    """Raw indexer inputs of the new tokens, before RoPE / LayerNorm / quantization."""
+    q_in: np.ndarray         # [T, Hi, 128] uint16 (bf16 bits) ~N(0, 1)
+    k_in: np.ndarray         # [T, 128] uint16 (bf16 bits) ~N(0.3, 2^2)
+    rope_cos: np.ndarray     # [max_seq_len, rope_dim/2] fp32
+    rope_sin: np.ndarray     # [max_seq_len, rope_dim/2] fp32
+    ln_gamma: np.ndarray     # [128] fp32 ~1 + N(0, 0.1^2)
+    ln_beta: np.ndarray      # [128] fp32 ~N(0, 0.1^2)
+    ln_eps: float
+    rope_dim: int
+
+
+def make_prep_inputs(wl: Workload, hi: int = 64, rope_dim: int = 64, seed: int = 0,
+                     rope_base: float = 10000.0) -> PrepInputs:
+    """Seeded raw indexer q/k for the workload's query tokens and the model's RoPE
+    tables (angle p * base^(-2i/rope_dim) at position p, pair i), which are weights
+    of the model, not a step of the preparation."""
+    rng = np.random.default_rng(seed)
+    T = int(wl.n_q.sum())
+    q = _normal(rng, (T, hi, 128))
+    k = _normal(rng, (T, 128), std=2.0) + np.float32(0.3)
+    r = rope_dim // 2
+    inv = rope_base ** (-np.arange(r, dtype=np.float64) * 2.0 / rope_dim)
+    ang = np.arange(int(wl.max_seq_len), dtype=np.float64)[:, None] * inv[None, :]
+    return PrepInputs(q_in=to_bf16_bits(q), k_in=to_bf16_bits(k),
+                      rope_cos=np.cos(ang).astype(np.float32), rope_sin=np.sin(ang).astype(np.float32),
+                      ln_gamma=(1.0 + 0.1 * rng.standard_normal(128)).astype(np.float32),
+                      ln_beta=(0.1 * rng.standard_normal(128)).astype(np.float32),
+                      ln_eps=1e-6, rope_dim=rope_dim)

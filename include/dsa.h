@@ -200,6 +200,41 @@ dsa_status_t dsa_cache_append(const dsa_geom_t* geom, dsa_dtype_t kv_dtype, cons
                               void* stream);
 size_t dsa_cache_append_workspace_size(const dsa_geom_t* geom);
 
+/*
+ * dsa_indexer_prepare -- the indexer's query/key preparation, fused into one launch
+ *   (lmdeploy "feat: support GLM-5.2", Changes: fused indexer preparation;
+ *   mlx-lm "GLM-5.2 (glm_moe_dsa) inference", Changes: the indexer's RoPE is
+ *   non-interleaved and its LayerNorm eps is 1e-6). It produces the e4m3 queries
+ *   and scales dsa_indexer_scores takes, and writes each new token's key into the
+ *   e4m3 index cache, for query token t (flattened like the queries) at position
+ *   pos(t) = seq_lens[b] - n_b + j:
+ *     q_out[t,h,:] = e4m3(RoPE(q_in[t,h,:]) / s), q_scale[t,h] = s
+ *     idx_k_cache[row(pos(t)),:] = e4m3(RoPE(LayerNorm(k_in[t,:])) / s_k),
+ *     idx_k_scale[row(pos(t))] = s_k
+ *   RoPE (non-interleaved) on the first rope_dim values: for i < r = rope_dim/2,
+ *     y_i = x_i*cos[pos][i] - x_{i+r}*sin[pos][i], y_{i+r} = x_{i+r}*cos[pos][i] +
+ *     x_i*sin[pos][i]; values rope_dim..127 pass through.
+ *   LayerNorm: (x - mean) / sqrt(var + ln_eps) * gamma + beta over the 128 values,
+ *     var the biased variance; gamma NULL means 1, beta NULL means 0.
+ *   s = amax / 448 of the vector (1 if it is all zero); codes round to nearest
+ *   (ties to even) and saturate at +-448; everything is computed in fp32 from the
+ *   bf16 inputs.
+ *   Hi: 1..128 indexer heads. rope_dim: 8..128, a multiple of 8.
+ *   q_in [T, Hi, 128] bf16, k_in [T, 128] bf16 or NULL (queries only; then the
+ *     caches may be NULL); rope_cos, rope_sin [max_seq_len, rope_dim/2] fp32;
+ *     ln_gamma, ln_beta [128] fp32 or NULL; q_out [T, Hi, 128] e4m3 bytes;
+ *     q_scale [T, Hi] fp32; idx_k_cache [num_pages, 64, 128] e4m3 bytes;
+ *     idx_k_scale [num_pages, 64] fp32. All device, 16-byte aligned (scales 4).
+ *   Rows other than the new tokens' are untouched. A token whose page id is out
+ *   of range is skipped and sets DSA_ERR_BAD_INDEX in the error word.
+ */
+dsa_status_t dsa_indexer_prepare(const dsa_geom_t* geom, int32_t Hi, int32_t rope_dim, const void* q_in,
+                                 const void* k_in, const float* rope_cos, const float* rope_sin,
+                                 const float* ln_gamma, const float* ln_beta, float ln_eps, void* q_out,
+                                 float* q_scale, void* idx_k_cache, float* idx_k_scale, void* ws, size_t ws_bytes,
+                                 void* stream);
+size_t dsa_indexer_prepare_workspace_size(const dsa_geom_t* geom);
+
 /* Arguments of the fused step. */
 typedef struct {
   dsa_geom_t geom;

@@ -99,6 +99,27 @@ def test_host_validation(lib):
     assert lib.dsa_get_error(None, None) == _lib.DSA_ERR_INVALID_ARG
 
 
+def test_indexer_prepare_rejects_bad_arguments_before_launch(lib):
+    g = _geom(T=4)
+    pr = lib.dsa_indexer_prepare
+    ok = dict(Hi=64, rd=64, q=16, k=16, cs=16, sn=16, gm=None, bt=None, eps=1e-6, qo=16, qs=16, kc=16, ks=16,
+              ws=256, wb=256)
+
+    def call(geom=g, **kw):
+        a = dict(ok, **kw)
+        return pr(C.byref(geom), a["Hi"], a["rd"], a["q"], a["k"], a["cs"], a["sn"], a["gm"], a["bt"], a["eps"],
+                  a["qo"], a["qs"], a["kc"], a["ks"], a["ws"], a["wb"], None)
+
+    for bad in (dict(Hi=0), dict(Hi=129), dict(rd=0), dict(rd=12), dict(rd=136), dict(eps=-1.0),
+                dict(eps=float("nan")), dict(kc=None), dict(ks=None), dict(k=24), dict(gm=8),
+                dict(q=None), dict(cs=None), dict(qs=None), dict(q=24), dict(sn=20)):
+        assert call(**bad) == _lib.DSA_ERR_INVALID_ARG, bad
+    assert call(ws=None, wb=0) == _lib.DSA_ERR_WORKSPACE
+    assert call(ws=264) == _lib.DSA_ERR_WORKSPACE                   # not 256-byte aligned
+    assert call(geom=_geom(T=0), q=None, qo=None, qs=None, cs=None, sn=None) == _lib.DSA_OK
+    assert lib.dsa_indexer_prepare_workspace_size(C.byref(g)) == 256
+
+
 def test_workspace_sizes_are_consistent(lib):
     g = _geom(T=64, B=64, max_seq_len=131072, bt_stride=2048)
     assert lib.dsa_topk_workspace_size(C.byref(g), 2048) >= 256 + 64 * 8 * 2048 * 8
