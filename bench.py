@@ -293,6 +293,7 @@ def main():
     int8_attend = measure_int8_attend(dw, flush, stream, max(20, min(args.steps, 100)))
     fp8_attend = measure_int8_attend(dw, flush, stream, max(20, min(args.steps, 100)), kv_dtype=_lib.DSA_E4M3)
     prep = measure_indexer_prep(dw, flush, stream, max(20, min(args.steps, 100)))
+    bounded = measure_bounded_step(dw, flush, stream, max(20, min(args.steps, 100)))
 
     idx_b, lat_b, selected = algorithmic_bytes(wl)
     peak, peak_kind = load_peaks()
@@ -319,7 +320,8 @@ def main():
                      "avg_launch_ms": comp["attend_ms"],
                      "traffic": load_traffic("sparse_mla_kernel")},
         "components_ms": comp,
-        "next_rows": {"cache_append": append, "int8_latent_attend": int8_attend, "indexer_prep": prep},
+        "next_rows": {"cache_append": append, "int8_latent_attend": int8_attend, "indexer_prep": prep,
+                      "bounded_scoring": bounded},
         "e4m3_latent_attend": fp8_attend,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
@@ -497,6 +499,46 @@ def measure_indexer_prep(dw, flush, stream, n):
         ms = tot / n
         out[name] = {"ms": ms, "algorithmic_bytes": nbytes, "achieved_gbs": nbytes / (ms / 1000.0) / 1e9}
     return out
+
+
+def measure_bounded_step(dw, flush, stream, n, rows=16):
+    """The decode step through dsa_decode_step_bounded with a score budget of `rows`
+    queries (64 / rows ranges, each scored and reduced before the next), captured in
+    a CUDA graph and replayed like the main step; its score workspace against the
+    unbounded step's."""
+    wl = dw.wl
+    dev = dw.device
+    row_bytes = (-(-wl.max_seq_len // 64) * 64) * 4
+    budget = rows * row_bytes
+    a0 = dw.args[0]
+    ws = _lib.workspace(max([_lib.dsa_decode_step_bounded_workspace_size(a0, budget)] +
+                            [_lib.dsa_decode_step_workspace_size(a) for a in dw.args[1:]]), dev)
+
+    def enqueue():
+        for a in dw.args:
+            _lib.dsa_decode_step_bounded(a, budget, ws)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        enqueue()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        enqueue()
+    tot = 0.0
+    for i in range(n):
+        flush.fill_(i & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(200_000)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        b.synchronize()
+        tot += a.elapsed_time(b)
+    return {"budget_rows": rows, "ranges": -(-wl.T // rows), "ms_per_step": tot / n,
+            "score_workspace_bytes": budget, "unbounded_score_workspace_bytes": wl.T * row_bytes}
 
 
 def measure_int8_attend(dw, flush, stream, n, kv_dtype=None):

@@ -23,6 +23,7 @@ EXPORTED = (
     "dsa_topk", "dsa_topk_workspace_size",
     "dsa_sparse_mla_attend", "dsa_sparse_mla_attend_workspace_size", "dsa_sparse_mla_attend_static",
     "dsa_decode_step", "dsa_decode_step_workspace_size",
+    "dsa_decode_step_bounded", "dsa_decode_step_bounded_workspace_size",
     "dsa_cache_append", "dsa_cache_append_workspace_size",
     "dsa_indexer_prepare", "dsa_indexer_prepare_workspace_size",
     "dsa_get_error", "dsa_clear_error", "dsa_status_string", "dsa_last_error", "dsa_abi_version",
@@ -82,6 +83,8 @@ def load(path: str = LIB_PATH):
         "dsa_sparse_mla_attend_static": (C.c_int, [G, C.c_int, I32, P, P, P, I32, F, P, P, P, P]),
         "dsa_decode_step": (C.c_int, [S, P, SZ, P]),
         "dsa_decode_step_workspace_size": (SZ, [S]),
+        "dsa_decode_step_bounded": (C.c_int, [S, SZ, P, SZ, P]),
+        "dsa_decode_step_bounded_workspace_size": (SZ, [S, SZ]),
         "dsa_cache_append": (C.c_int, [G, C.c_int, P, P, C.c_int, P, P, P, P, SZ, P]),
         "dsa_cache_append_workspace_size": (SZ, [G]),
         "dsa_indexer_prepare": (C.c_int, [G, I32, I32, P, P, P, P, P, P, F, P, P, P, P, P, SZ, P]),
@@ -244,6 +247,17 @@ def dsa_decode_step_workspace_size(args: dsa_step_args_t) -> int:
 def dsa_decode_step(args: dsa_step_args_t, ws: torch.Tensor, stream=None):
     st = load().dsa_decode_step(C.byref(args), _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "dsa_decode_step")
+
+
+def dsa_decode_step_bounded_workspace_size(args: dsa_step_args_t, score_budget_bytes: int) -> int:
+    return int(load().dsa_decode_step_bounded_workspace_size(C.byref(args), int(score_budget_bytes)))
+
+
+def dsa_decode_step_bounded(args: dsa_step_args_t, score_budget_bytes: int, ws: torch.Tensor, stream=None):
+    """dsa_decode_step holding the scores of at most score_budget_bytes // (stride * 4)
+    queries at a time; bitwise the same results."""
+    st = load().dsa_decode_step_bounded(C.byref(args), int(score_budget_bytes), _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "dsa_decode_step_bounded")
 
 
 def dsa_get_error(ws: torch.Tensor, stream=None) -> int:

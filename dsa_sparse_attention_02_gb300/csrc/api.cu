@@ -271,24 +271,34 @@ dsa_status_t dsa_sparse_mla_attend(const dsa_geom_t* geom, dsa_dtype_t kv_dtype,
                     reinterpret_cast<cudaStream_t>(stream));
 }
 
-size_t dsa_decode_step_workspace_size(const dsa_step_args_t* a) {
-  if (!a) return kHeaderBytes;
+}  // extern "C"
+
+namespace {
+
+// Workspace of the step when at most `rows` queries' scores are held at a time
+// (rows >= T: all at once). Layout: header | query-range geometry (chunked only) |
+// scores [rows, stride] | idx [T, k] (unless idx_out) | attention / top-k scratch.
+size_t step_workspace_bytes(const dsa_step_args_t* a, int64_t rows) {
   const dsa_geom_t* g = &a->geom;
   size_t bytes = kHeaderBytes;
+  const int64_t r = rows < g->T ? rows : g->T;
   if (!a->reuse_idx) {
-    bytes += align_up((size_t)g->T * step_score_stride(g) * sizeof(float), 256);
+    if (r < g->T) bytes += align_up((size_t)(2 * g->B + 1) * sizeof(int32_t), 256);
+    bytes += align_up((size_t)r * step_score_stride(g) * sizeof(float), 256);
     if (!a->idx_out) bytes += align_up((size_t)g->T * (a->topk > 0 ? a->topk : 1) * sizeof(int32_t), 256);
   }
   size_t scratch = attend_scratch_bytes(g, a->H > 0 ? a->H : 1, a->topk > 0 ? a->topk : 1);
   if (!a->reuse_idx && a->topk > 0) {
-    const size_t tk = topk_workspace_bytes(g->T, g->max_seq_len, a->topk);
+    const size_t tk = topk_workspace_bytes((int)r, g->max_seq_len, a->topk);
     if (tk > scratch) scratch = tk;
   }
   return bytes + align_up(scratch, 256);
 }
 
-dsa_status_t dsa_decode_step(const dsa_step_args_t* a, void* ws, size_t ws_bytes, void* stream) {
-  if (!a) return DSA_ERR_INVALID_ARG;
+// The step with the queries' scores computed and reduced to their selection `rows`
+// queries at a time (the selection of each query does not depend on the others', so
+// the result is the same for every rows >= 1).
+dsa_status_t run_step(const dsa_step_args_t* a, int64_t rows, void* ws, size_t ws_bytes, void* stream) {
   const dsa_geom_t* g = &a->geom;
   const int64_t stride = step_score_stride(g);
   dsa_status_t s;
@@ -302,7 +312,7 @@ dsa_status_t dsa_decode_step(const dsa_step_args_t* a, void* ws, size_t ws_bytes
   s = check_attend(g, a->kv_dtype, a->H, a->q, a->kv_cache, a->reuse_idx ? a->reuse_idx : reinterpret_cast<const int*>(ws),
                    a->topk, a->sm_scale, a->out);
   if (s != DSA_OK) return s;
-  if (!ws || ws_bytes < dsa_decode_step_workspace_size(a) || (reinterpret_cast<uintptr_t>(ws) & 255u))
+  if (!ws || ws_bytes < step_workspace_bytes(a, rows) || (reinterpret_cast<uintptr_t>(ws) & 255u))
     return DSA_ERR_WORKSPACE;
   if (g->T == 0) return DSA_OK;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -311,24 +321,95 @@ dsa_status_t dsa_decode_step(const dsa_step_args_t* a, void* ws, size_t ws_bytes
   p += kHeaderBytes;
   const int32_t* idx = a->reuse_idx;
   if (!idx) {
+    const bool chunked = rows < g->T;
+    int32_t* range_geom = nullptr;
+    if (chunked) {
+      range_geom = reinterpret_cast<int32_t*>(p);
+      p += align_up((size_t)(2 * g->B + 1) * sizeof(int32_t), 256);
+    }
+    const int64_t r = chunked ? rows : g->T;
     float* scores = reinterpret_cast<float*>(p);
-    p += align_up((size_t)g->T * stride * sizeof(float), 256);
+    p += align_up((size_t)r * stride * sizeof(float), 256);
     int32_t* idx_buf = a->idx_out;
     if (!idx_buf) {
       idx_buf = reinterpret_cast<int32_t*>(p);
       p += align_up((size_t)g->T * a->topk * sizeof(int32_t), 256);
     }
-    s = run_indexer(g, a->qk_dtype, a->Hi, a->q_idx, a->q_scale, a->w, a->idx_k_cache, a->idx_k_scale, scores, stride,
-                    err, st);
-    if (s != DSA_OK) return s;
-    // The top-k and attention kernels follow this call's own kernels, so they may
-    // launch early (programmatic dependent launch) and wait for their inputs inside.
-    s = from_cuda(topk_launch(to_dev(g), scores, stride, a->topk, idx_buf, p, err, true, st));
-    if (s != DSA_OK) return s;
+    if (!chunked) {
+      s = run_indexer(g, a->qk_dtype, a->Hi, a->q_idx, a->q_scale, a->w, a->idx_k_cache, a->idx_k_scale, scores,
+                      stride, err, st);
+      if (s != DSA_OK) return s;
+      // The top-k and attention kernels follow this call's own kernels, so they may
+      // launch early (programmatic dependent launch) and wait for their inputs inside.
+      s = from_cuda(topk_launch(to_dev(g), scores, stride, a->topk, idx_buf, p, err, true, st));
+      if (s != DSA_OK) return s;
+    } else {
+      // Bounded scoring: queries [t0, t0 + rows) at a time, each range described by
+      // its own geometry (same requests, block table and positions), scored into the
+      // same rows of `scores` and reduced to its selection before the next range.
+      const size_t qrow = (size_t)a->Hi * 128 * (a->qk_dtype == DSA_E4M3 ? 1 : 2);
+      for (int64_t t0 = 0; t0 < g->T; t0 += rows) {
+        const int t1 = (int)(t0 + rows < g->T ? t0 + rows : g->T);
+        s = from_cuda(query_range_launch(g->cu_q, g->seq_lens, g->B, (int)t0, t1, range_geom,
+                                         range_geom + g->B + 1, st));
+        if (s != DSA_OK) return s;
+        dsa_geom_t sub = *g;
+        sub.T = t1 - (int)t0;
+        sub.cu_q = range_geom;
+        sub.seq_lens = range_geom + g->B + 1;
+        s = run_indexer(&sub, a->qk_dtype, a->Hi, reinterpret_cast<const uint8_t*>(a->q_idx) + (size_t)t0 * qrow,
+                        a->q_scale ? a->q_scale + (size_t)t0 * a->Hi : nullptr, a->w + (size_t)t0 * a->Hi,
+                        a->idx_k_cache, a->idx_k_scale, scores, stride, err, st);
+        if (s != DSA_OK) return s;
+        s = from_cuda(topk_launch(to_dev(&sub), scores, stride, a->topk, idx_buf + (size_t)t0 * a->topk, p, err, true,
+                                  st));
+        if (s != DSA_OK) return s;
+      }
+    }
     idx = idx_buf;
   }
   return run_attend(g, a->kv_dtype, a->H, a->q, a->kv_cache, idx, a->topk, a->sm_scale, a->out, a->lse, p, err,
                     a->reuse_idx == nullptr, st);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t dsa_decode_step_workspace_size(const dsa_step_args_t* a) {
+  if (!a) return kHeaderBytes;
+  return step_workspace_bytes(a, a->geom.T);
+}
+
+dsa_status_t dsa_decode_step(const dsa_step_args_t* a, void* ws, size_t ws_bytes, void* stream) {
+  if (!a) return DSA_ERR_INVALID_ARG;
+  return run_step(a, a->geom.T, ws, ws_bytes, stream);
+}
+
+// Queries whose scores fit the budget at once; 0 if not even one does.
+static int64_t bounded_rows(const dsa_step_args_t* a, size_t score_budget_bytes) {
+  const size_t row = (size_t)step_score_stride(&a->geom) * sizeof(float);
+  return row > 0 ? (int64_t)(score_budget_bytes / row) : 0;
+}
+
+size_t dsa_decode_step_bounded_workspace_size(const dsa_step_args_t* a, size_t score_budget_bytes) {
+  if (!a) return kHeaderBytes;
+  const int64_t rows = bounded_rows(a, score_budget_bytes);
+  return step_workspace_bytes(a, rows < 1 ? 1 : rows);
+}
+
+dsa_status_t dsa_decode_step_bounded(const dsa_step_args_t* a, size_t score_budget_bytes, void* ws, size_t ws_bytes,
+                                     void* stream) {
+  if (!a) return DSA_ERR_INVALID_ARG;
+  const int64_t rows = bounded_rows(a, score_budget_bytes);
+  if (rows < 1 && !a->reuse_idx) {
+    char buf[160];
+    snprintf(buf, sizeof(buf), "score budget %zu bytes is below one query's score row (%zu bytes)",
+             score_budget_bytes, (size_t)step_score_stride(&a->geom) * sizeof(float));
+    set_last_error("dsa_decode_step_bounded", buf);
+    return DSA_ERR_INVALID_ARG;
+  }
+  return run_step(a, rows < 1 ? 1 : rows, ws, ws_bytes, stream);
 }
 
 size_t dsa_cache_append_workspace_size(const dsa_geom_t*) { return kHeaderBytes; }

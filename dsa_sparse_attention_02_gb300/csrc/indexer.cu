@@ -430,6 +430,30 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, Ind
   }
 }
 
+// The geometry of queries [t0, t1) alone (bounded scoring, lmdeploy "glm5.3-flash
+// support", Capacity improvement: bounded KPool scoring): request b keeps the part
+// of its queries inside the range, and its length becomes the last such query's
+// position + 1, so every kept query keeps its position (L - n + j) and the keys it
+// can see; a request with no query in the range gets none and length 0.
+__global__ void query_range_kernel(const int* __restrict__ cu_q, const int* __restrict__ seq_lens, int B, int t0,
+                                   int t1, int* __restrict__ cu_out, int* __restrict__ len_out) {
+  for (int b = threadIdx.x; b <= B; b += blockDim.x) {
+    const int q0 = cu_q[b];
+    cu_out[b] = min(max(q0, t0), t1) - t0;
+    if (b < B) {
+      const int q1 = cu_q[b + 1];
+      const int n = min(q1, t1) - max(q0, t0);
+      len_out[b] = n > 0 ? seq_lens[b] - (q1 - min(q1, t1)) : 0;
+    }
+  }
+}
+
+cudaError_t query_range_launch(const int* cu_q, const int* seq_lens, int B, int t0, int t1, int* cu_out,
+                               int* len_out, cudaStream_t st) {
+  query_range_kernel<<<1, 1024, 0, st>>>(cu_q, seq_lens, B, t0, t1, cu_out, len_out);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ host side
 template <bool kFp8, int kHp, int kQG>
 static cudaError_t launch_indexer_t(const CUtensorMap& mk, const CUtensorMap& mq, const IndexerArgs& A,

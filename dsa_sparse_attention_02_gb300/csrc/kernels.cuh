@@ -71,6 +71,11 @@ struct AppendArgs {
 };
 cudaError_t cache_append_launch(const AppendArgs& A, cudaStream_t st);
 
+// ---- query ranges (indexer.cu): cu_out [B+1] and len_out [B] describe queries
+// [t0, t1) of the geometry alone, with their positions unchanged.
+cudaError_t query_range_launch(const int* cu_q, const int* seq_lens, int B, int t0, int t1, int* cu_out,
+                               int* len_out, cudaStream_t st);
+
 // ---- indexer preparation (indexer_prep.cu)
 struct PrepArgs {
   GeomDev g;

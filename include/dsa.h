@@ -272,6 +272,22 @@ dsa_status_t dsa_decode_step(const dsa_step_args_t* args, void* ws, size_t ws_by
                              void* stream);
 size_t dsa_decode_step_workspace_size(const dsa_step_args_t* args);
 
+/*
+ * dsa_decode_step_bounded -- dsa_decode_step with the indexer's score workspace
+ *   bounded (lmdeploy "glm5.3-flash support", Capacity improvement: bounded KPool
+ *   scoring: a configurable score budget, top-k selected per query chunk right after
+ *   that chunk is scored, indices identical). The fp32 scores of at most
+ *   floor(score_budget_bytes / (stride * 4)) queries exist at a time, stride being
+ *   max_seq_len rounded up to 64; each such range of queries is scored and reduced to
+ *   its selection before the next. Results (idx_out, out, lse) are bitwise those of
+ *   dsa_decode_step. A budget below one query's score row returns
+ *   DSA_ERR_INVALID_ARG (dsa_last_error gives the row size). With reuse_idx the
+ *   budget is not used. Graph-capturable like dsa_decode_step.
+ */
+dsa_status_t dsa_decode_step_bounded(const dsa_step_args_t* args, size_t score_budget_bytes, void* ws,
+                                     size_t ws_bytes, void* stream);
+size_t dsa_decode_step_bounded_workspace_size(const dsa_step_args_t* args, size_t score_budget_bytes);
+
 /* Synchronizes `stream`, reads the device error word of `ws` (DSA_OK if none)
  * and clears it. Returns DSA_ERR_CUDA if the stream itself reports an error. */
 dsa_status_t dsa_get_error(void* ws, void* stream);

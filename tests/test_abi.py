@@ -133,3 +133,19 @@ def test_workspace_sizes_are_consistent(lib):
     assert base >= 256 + 64 * 8192 * 4 + 64 * 2048 * 4
     a.reuse_idx = 16
     assert lib.dsa_decode_step_workspace_size(C.byref(a)) < base
+
+
+def test_bounded_step_budget_floor_and_workspace_sizes(lib):
+    a = _lib.dsa_step_args_t()
+    a.geom = _geom(T=64, B=64, max_seq_len=8192, bt_stride=128)
+    a.topk = 2048
+    a.H = 16
+    a.Hi = 64
+    row = 8192 * 4
+    # below one query's score row: rejected before anything is enqueued
+    assert lib.dsa_decode_step_bounded(C.byref(a), row - 1, 256, 1 << 30, None) == _lib.DSA_ERR_INVALID_ARG
+    full = lib.dsa_decode_step_workspace_size(C.byref(a))
+    assert lib.dsa_decode_step_bounded_workspace_size(C.byref(a), 64 * row) == full   # all rows fit: no ranges
+    one = lib.dsa_decode_step_bounded_workspace_size(C.byref(a), row)
+    assert one < full - 62 * row                               # 63 fewer score rows, plus the range geometry
+    assert lib.dsa_decode_step_bounded_workspace_size(C.byref(a), 8 * row) > one
