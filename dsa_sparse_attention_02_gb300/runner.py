@@ -21,6 +21,28 @@ def _dev(a: np.ndarray, device, view=None) -> torch.Tensor:
     return t.view(view) if view is not None else t
 
 
+class _Arena:
+    """Several tensors back to back in one device buffer (each 256-byte aligned), so that
+    a step's per-call inputs, or its outputs, move between host and device in one copy."""
+
+    def __init__(self):
+        self.parts = []
+        self.nbytes = 0
+
+    def add(self, nbytes: int, dtype, shape):
+        self.parts.append((self.nbytes, int(nbytes), dtype, tuple(shape)))
+        self.nbytes = (self.nbytes + int(nbytes) + 255) // 256 * 256
+        return len(self.parts) - 1
+
+    def build(self, device):
+        self.buf = torch.empty(max(self.nbytes, 256), dtype=torch.uint8, device=device)
+        return [self.buf[o:o + n].view(dt).view(sh) for o, n, dt, sh in self.parts]
+
+
+def _bytes_of(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a).reshape(-1).view(np.uint8))
+
+
 @dataclass
 class DeviceLayer:
     q: torch.Tensor          # [T, H, 576] bf16
@@ -31,39 +53,63 @@ class DeviceLayer:
 
 
 class DeviceWorkload:
+    """The workload on the device. The per-call inputs (geometry, indexer q / scales /
+    weights, each layer's MLA q) are views into one buffer, `inputs`, and the layers'
+    outputs into another, `outputs`; the caches are resident tensors of their own."""
+
     def __init__(self, wl: Workload, device="cuda"):
         self.wl = wl
         self.device = torch.device(device)
         d = self.device
-        self.seq_lens = _dev(wl.seq_lens.astype(np.int32), d)
-        self.cu_q = _dev(wl.cu_q.astype(np.int32), d)
-        self.block_table = _dev(wl.block_table.astype(np.int32), d)
+        fp8 = wl.qk_dtype == "e4m3"
+        self.qk_dtype = _lib.DSA_E4M3 if fp8 else _lib.DSA_BF16
+        T = wl.T
+        ins = _Arena()
+        src = []
+
+        def put(a, dtype, shape):
+            src.append(_bytes_of(a))
+            return ins.add(src[-1].numel(), dtype, shape)
+
+        i_seq = put(wl.seq_lens.astype(np.int32), torch.int32, wl.seq_lens.shape)
+        i_cu = put(wl.cu_q.astype(np.int32), torch.int32, wl.cu_q.shape)
+        i_bt = put(wl.block_table.astype(np.int32), torch.int32, wl.block_table.shape)
+        i_qi = put(wl.q_idx, torch.float8_e4m3fn if fp8 else torch.bfloat16, wl.q_idx.shape)
+        i_qs = put(wl.q_scale, torch.float32, wl.q_scale.shape) if fp8 else None
+        i_w = put(wl.w, torch.float32, wl.w.shape)
+        i_q = [put(L.q, torch.bfloat16, L.q.shape) for L in wl.layers]
+        views = ins.build(d)
+        for v, b in zip(views, src):
+            v.view(-1).view(torch.uint8).copy_(b)
+        self.inputs = ins.buf
+        self.seq_lens, self.cu_q, self.block_table = views[i_seq], views[i_cu], views[i_bt]
         self.geom = _lib.Geometry(self.seq_lens, self.cu_q, self.block_table, wl.num_pages,
                                   wl.max_seq_len, wl.T)
-        if wl.qk_dtype == "e4m3":
-            self.qk_dtype = _lib.DSA_E4M3
-            self.q_idx = _dev(wl.q_idx, d, torch.float8_e4m3fn)
-            self.q_scale = _dev(wl.q_scale, d)
+        self.q_idx = views[i_qi]
+        self.q_scale = views[i_qs] if fp8 else None
+        self.w = views[i_w]
+        if fp8:
             self.idx_k = _dev(wl.idx_k, d, torch.float8_e4m3fn)
             self.idx_k_scale = _dev(wl.idx_k_scale, d)
         else:
-            self.qk_dtype = _lib.DSA_BF16
-            self.q_idx = _dev(wl.q_idx.view(np.int16), d, torch.bfloat16)
-            self.q_scale = None
             self.idx_k = _dev(wl.idx_k.view(np.int16), d, torch.bfloat16)
             self.idx_k_scale = None
-        self.w = _dev(wl.w, d)
-        self.layers = []
+        outs = _Arena()
+        o_idx = []
         for L in wl.layers:
-            q = _dev(L.q.view(np.int16), d, torch.bfloat16)
+            H = L.q.shape[1]
+            o_idx.append((outs.add(T * H * 512 * 2, torch.bfloat16, (T, H, 512)),
+                          outs.add(T * H * 4, torch.float32, (T, H))))
+        oviews = outs.build(d)
+        self.outputs = outs.buf
+        self.layers = []
+        for li, L in enumerate(wl.layers):
+            q = views[i_q[li]]
             if L.kv_dtype == "bf16":
                 kv, kd = _dev(L.kv.view(np.int16), d, torch.bfloat16), _lib.DSA_BF16
             else:
                 kv, kd = _dev(L.kv, d), (_lib.DSA_E4M3 if L.kv_dtype == "e4m3" else _lib.DSA_I8)
-            T, H = q.shape[0], q.shape[1]
-            self.layers.append(DeviceLayer(q, kv, kd,
-                                           torch.empty(T, H, 512, dtype=torch.bfloat16, device=d),
-                                           torch.empty(T, H, dtype=torch.float32, device=d)))
+            self.layers.append(DeviceLayer(q, kv, kd, oviews[o_idx[li][0]], oviews[o_idx[li][1]]))
         self.idx = torch.empty(wl.T, wl.topk, dtype=torch.int32, device=d)
         self.args = [self._args(i) for i in range(len(self.layers))]
         need = max(_lib.dsa_decode_step_workspace_size(a) for a in self.args)
