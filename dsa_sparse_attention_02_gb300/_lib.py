@@ -25,7 +25,7 @@ EXPORTED = (
     "dsa_decode_step", "dsa_decode_step_workspace_size",
     "dsa_decode_step_bounded", "dsa_decode_step_bounded_workspace_size",
     "dsa_cache_append", "dsa_cache_append_workspace_size",
-    "dsa_indexer_prepare", "dsa_indexer_prepare_workspace_size",
+    "dsa_indexer_prepare", "dsa_indexer_prepare_workspace_size", "dsa_stage_copy",
     "dsa_get_error", "dsa_clear_error", "dsa_status_string", "dsa_last_error", "dsa_abi_version",
 )
 
@@ -89,6 +89,7 @@ def load(path: str = LIB_PATH):
         "dsa_cache_append_workspace_size": (SZ, [G]),
         "dsa_indexer_prepare": (C.c_int, [G, I32, I32, P, P, P, P, P, P, F, P, P, P, P, P, SZ, P]),
         "dsa_indexer_prepare_workspace_size": (SZ, [G]),
+        "dsa_stage_copy": (C.c_int, [P, P, SZ, P]),
         "dsa_get_error": (C.c_int, [P, P]),
         "dsa_clear_error": (C.c_int, [P, P]),
         "dsa_status_string": (C.c_char_p, [C.c_int]),
@@ -247,6 +248,12 @@ def dsa_decode_step_workspace_size(args: dsa_step_args_t) -> int:
 def dsa_decode_step(args: dsa_step_args_t, ws: torch.Tensor, stream=None):
     st = load().dsa_decode_step(C.byref(args), _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "dsa_decode_step")
+
+
+def dsa_stage_copy(dst, src, nbytes: int, stream=None):
+    """Copies nbytes from src to dst (device tensors or pinned host tensors) with the SMs."""
+    st = load().dsa_stage_copy(_ptr(dst), _ptr(src), int(nbytes), _stream(stream))
+    _check(st, "dsa_stage_copy")
 
 
 def dsa_decode_step_bounded_workspace_size(args: dsa_step_args_t, score_budget_bytes: int) -> int:

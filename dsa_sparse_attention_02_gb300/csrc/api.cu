@@ -442,6 +442,48 @@ dsa_status_t dsa_cache_append(const dsa_geom_t* geom, dsa_dtype_t kv_dtype, cons
   return from_cuda(cache_append_launch(A, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+}  // extern "C"
+
+namespace {
+
+// Device-visible address of the range [p, p + bytes): device or managed memory, or
+// page-locked host memory the device maps; both ends must resolve to one contiguous
+// mapping. Anything else (pageable host memory, unknown pointers) is refused.
+bool device_range(const void* p, size_t bytes, const void** out) {
+  cudaPointerAttributes a0, a1;
+  const void* last = reinterpret_cast<const uint8_t*>(p) + (bytes - 1);
+  if (cudaPointerGetAttributes(&a0, p) != cudaSuccess || cudaPointerGetAttributes(&a1, last) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  auto visible = [](const cudaPointerAttributes& a) {
+    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged ||
+           (a.type == cudaMemoryTypeHost && a.devicePointer != nullptr);
+  };
+  if (!visible(a0) || !visible(a1) || a0.type != a1.type || a0.device != a1.device) return false;
+  const uint8_t* d0 = reinterpret_cast<const uint8_t*>(a0.devicePointer ? a0.devicePointer : p);
+  const uint8_t* d1 = reinterpret_cast<const uint8_t*>(a1.devicePointer ? a1.devicePointer : last);
+  if (d1 != d0 + (bytes - 1)) return false;
+  *out = d0;
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+dsa_status_t dsa_stage_copy(void* dst, const void* src, size_t bytes, void* stream) {
+  if (bytes == 0) return DSA_OK;
+  if (!dst || !src || !aligned16(dst) || !aligned16(src)) return DSA_ERR_INVALID_ARG;
+  const void *d = nullptr, *s = nullptr;
+  if (!device_range(dst, bytes, &d) || !device_range(src, bytes, &s)) {
+    set_last_error("dsa_stage_copy", "both ranges must be device memory or page-locked host memory the device maps");
+    return DSA_ERR_INVALID_ARG;
+  }
+  if (!aligned16(d) || !aligned16(s)) return DSA_ERR_INVALID_ARG;
+  return from_cuda(stage_copy_launch(const_cast<void*>(d), s, bytes, num_sms(), reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t dsa_indexer_prepare_workspace_size(const dsa_geom_t*) { return kHeaderBytes; }
 
 dsa_status_t dsa_indexer_prepare(const dsa_geom_t* geom, int32_t Hi, int32_t rope_dim, const void* q_in,

@@ -76,6 +76,10 @@ cudaError_t cache_append_launch(const AppendArgs& A, cudaStream_t st);
 cudaError_t query_range_launch(const int* cu_q, const int* seq_lens, int B, int t0, int t1, int* cu_out,
                                int* len_out, cudaStream_t st);
 
+// ---- staging copy (stage_copy.cu): `bytes` from src to dst by the SMs; both are
+// device-visible addresses (device memory, or mapped page-locked host memory).
+cudaError_t stage_copy_launch(void* dst, const void* src, size_t bytes, int num_sms, cudaStream_t st);
+
 // ---- indexer preparation (indexer_prep.cu)
 struct PrepArgs {
   GeomDev g;

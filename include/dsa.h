@@ -235,6 +235,22 @@ dsa_status_t dsa_indexer_prepare(const dsa_geom_t* geom, int32_t Hi, int32_t rop
                                  void* stream);
 size_t dsa_indexer_prepare_workspace_size(const dsa_geom_t* geom);
 
+/*
+ * dsa_stage_copy -- copies `bytes` from src to dst with the GPU's SMs, as a kernel in
+ *   `stream`: for moving a step's packed inputs from page-locked host memory to the
+ *   device and its outputs back. On a part whose host memory is reached over a
+ *   coherent chip-to-chip link this beats a copy-engine transfer of the same size.
+ *   Not part of the DSA method (the pages have no counterpart); the step's own
+ *   entry points take device memory as before.
+ *   Each range must lie in device (or managed) memory, or in page-locked host memory
+ *   the device maps (cudaHostAlloc, cudaHostRegister), and be 16-byte aligned; both
+ *   ends of each range are resolved with cudaPointerGetAttributes and must map
+ *   contiguously, otherwise DSA_ERR_INVALID_ARG before anything is enqueued
+ *   (pageable host memory is refused). The ranges must not overlap. bytes == 0 is a
+ *   no-op.
+ */
+dsa_status_t dsa_stage_copy(void* dst, const void* src, size_t bytes, void* stream);
+
 /* Arguments of the fused step. */
 typedef struct {
   dsa_geom_t geom;
