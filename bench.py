@@ -336,31 +336,59 @@ def main():
 
 
 def measure_e2e(dw, graph, flush, stream, n):
-    """Same metric with per-step host inputs: the step's inputs (geometry, indexer q,
-    scales and weights, MLA q; packed in one pinned host buffer laid out like the
-    device's input buffer) copied host->device, the step, and its outputs (O, LSE)
-    copied device->host, all inside the timed events, one copy each way, both by
-    dsa_stage_copy (the SMs read and write the page-locked host memory)."""
+    """Same metric with per-step host inputs, all inside the timed events: the step's
+    inputs copied host->device from page-locked memory (geometry, indexer q, scales
+    and weights in one copy; the MLA query, which only the attention reads, in a second
+    copy on a side stream that overlaps the indexer and top-k), the step
+    (dsa_decode_step_wait_q: its attention waits for the MLA query's copy), and O and
+    LSE copied device->host. The copies are dsa_stage_copy; the whole is one CUDA graph
+    per step."""
     host_in = dw.inputs.detach().cpu().pin_memory()
     host_out = torch.empty(dw.outputs.shape, dtype=dw.outputs.dtype, pin_memory=True)
     h2d = host_in.numel() * host_in.element_size()
     d2h = host_out.numel() * host_out.element_size()
+    off = dw.inputs_mla_q_offset
+    side = torch.cuda.Stream()
+    fork, q_ready = torch.cuda.Event(), torch.cuda.Event()
+
+    def enqueue():
+        cur = torch.cuda.current_stream()
+        fork.record(cur)
+        side.wait_event(fork)
+        with torch.cuda.stream(side):
+            _lib.dsa_stage_copy(dw.inputs[off:], host_in[off:], h2d - off)
+            q_ready.record(side)
+        _lib.dsa_stage_copy(dw.inputs, host_in, off)
+        for i, a in enumerate(dw.args):
+            if i == 0:
+                _lib.dsa_decode_step_wait_q(a, q_ready, dw.ws)
+            else:
+                _lib.dsa_decode_step(a, dw.ws)
+        _lib.dsa_stage_copy(host_out, dw.outputs, d2h)
+
+    warm = torch.cuda.Stream()
+    warm.wait_stream(stream)
+    with torch.cuda.stream(warm):
+        enqueue()
+    stream.wait_stream(warm)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        enqueue()
     ms = []
     for i in range(n):
         flush.fill_(i & 0xFF)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        _lib.dsa_stage_copy(dw.inputs, host_in, h2d)
-        graph.replay()
-        _lib.dsa_stage_copy(host_out, dw.outputs, d2h)
+        g.replay()
         e1.record(stream)
         e1.synchronize()
         ms.append(e0.elapsed_time(e1))
     avg = sum(ms) / len(ms)
     return {"value": dw.wl.T / (avg / 1000.0), "unit": "queries/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": avg,
-            "copies": "dsa_stage_copy (an SM copy kernel) of the packed inputs host->device and of O and LSE "
-                      "device->host, one each per step, from and to page-locked host memory"}
+            "copies": ("dsa_stage_copy (an SM copy kernel) from and to page-locked host memory: the indexer's "
+                       "inputs and the MLA query (overlapping the indexer and top-k) in, O and LSE out")}
 
 
 def measure_components(dw, flush, stream, n):

@@ -23,7 +23,7 @@ EXPORTED = (
     "dsa_topk", "dsa_topk_workspace_size",
     "dsa_sparse_mla_attend", "dsa_sparse_mla_attend_workspace_size", "dsa_sparse_mla_attend_static",
     "dsa_decode_step", "dsa_decode_step_workspace_size",
-    "dsa_decode_step_bounded", "dsa_decode_step_bounded_workspace_size",
+    "dsa_decode_step_bounded", "dsa_decode_step_bounded_workspace_size", "dsa_decode_step_wait_q",
     "dsa_cache_append", "dsa_cache_append_workspace_size",
     "dsa_indexer_prepare", "dsa_indexer_prepare_workspace_size", "dsa_stage_copy",
     "dsa_get_error", "dsa_clear_error", "dsa_status_string", "dsa_last_error", "dsa_abi_version",
@@ -84,6 +84,7 @@ def load(path: str = LIB_PATH):
         "dsa_decode_step": (C.c_int, [S, P, SZ, P]),
         "dsa_decode_step_workspace_size": (SZ, [S]),
         "dsa_decode_step_bounded": (C.c_int, [S, SZ, P, SZ, P]),
+        "dsa_decode_step_wait_q": (C.c_int, [S, P, P, SZ, P]),
         "dsa_decode_step_bounded_workspace_size": (SZ, [S, SZ]),
         "dsa_cache_append": (C.c_int, [G, C.c_int, P, P, C.c_int, P, P, P, P, SZ, P]),
         "dsa_cache_append_workspace_size": (SZ, [G]),
@@ -254,6 +255,13 @@ def dsa_stage_copy(dst, src, nbytes: int, stream=None):
     """Copies nbytes from src to dst (device tensors or pinned host tensors) with the SMs."""
     st = load().dsa_stage_copy(_ptr(dst), _ptr(src), int(nbytes), _stream(stream))
     _check(st, "dsa_stage_copy")
+
+
+def dsa_decode_step_wait_q(args: dsa_step_args_t, q_ready: torch.cuda.Event, ws: torch.Tensor, stream=None):
+    """dsa_decode_step whose attention waits on q_ready (the MLA query's copy)."""
+    ev = None if q_ready is None else C.c_void_p(q_ready.cuda_event)
+    st = load().dsa_decode_step_wait_q(C.byref(args), ev, _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "dsa_decode_step_wait_q")
 
 
 def dsa_decode_step_bounded_workspace_size(args: dsa_step_args_t, score_budget_bytes: int) -> int:

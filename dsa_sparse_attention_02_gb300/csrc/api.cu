@@ -298,7 +298,8 @@ size_t step_workspace_bytes(const dsa_step_args_t* a, int64_t rows) {
 // The step with the queries' scores computed and reduced to their selection `rows`
 // queries at a time (the selection of each query does not depend on the others', so
 // the result is the same for every rows >= 1).
-dsa_status_t run_step(const dsa_step_args_t* a, int64_t rows, void* ws, size_t ws_bytes, void* stream) {
+dsa_status_t run_step(const dsa_step_args_t* a, int64_t rows, void* ws, size_t ws_bytes, void* stream,
+                      cudaEvent_t q_ready = nullptr) {
   const dsa_geom_t* g = &a->geom;
   const int64_t stride = step_score_stride(g);
   dsa_status_t s;
@@ -368,8 +369,15 @@ dsa_status_t run_step(const dsa_step_args_t* a, int64_t rows, void* ws, size_t w
     }
     idx = idx_buf;
   }
+  // The MLA query may still be arriving (its copy recorded q_ready): the attention
+  // waits for it, the indexer and top-k above did not. Its launch then waits on the
+  // event as a whole instead of overlapping the top-k's tail.
+  if (q_ready) {
+    s = from_cuda(cudaStreamWaitEvent(st, q_ready, 0));
+    if (s != DSA_OK) return s;
+  }
   return run_attend(g, a->kv_dtype, a->H, a->q, a->kv_cache, idx, a->topk, a->sm_scale, a->out, a->lse, p, err,
-                    a->reuse_idx == nullptr, st);
+                    a->reuse_idx == nullptr && q_ready == nullptr, st);
 }
 
 }  // namespace
@@ -384,6 +392,11 @@ size_t dsa_decode_step_workspace_size(const dsa_step_args_t* a) {
 dsa_status_t dsa_decode_step(const dsa_step_args_t* a, void* ws, size_t ws_bytes, void* stream) {
   if (!a) return DSA_ERR_INVALID_ARG;
   return run_step(a, a->geom.T, ws, ws_bytes, stream);
+}
+
+dsa_status_t dsa_decode_step_wait_q(const dsa_step_args_t* a, void* q_ready, void* ws, size_t ws_bytes, void* stream) {
+  if (!a) return DSA_ERR_INVALID_ARG;
+  return run_step(a, a->geom.T, ws, ws_bytes, stream, reinterpret_cast<cudaEvent_t>(q_ready));
 }
 
 // Queries whose scores fit the budget at once; 0 if not even one does.

@@ -680,10 +680,17 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         z[h] = (z[h] == neg_inf) ? 0.f : fast_exp2(z[h] - m[h]);   // z now holds p <= 256
         l[h] += z[h];
       }
+      // o_full completes once per chunk's PV, and a parity wait is only unambiguous
+      // while the barrier is at most one phase ahead of the phase waited for. So the
+      // softmax observes every phase in order: here PV(i-1) (it observed PV(i-2) at
+      // chunk i-1, and PV(i) cannot complete before P(i) is written), and at a segment
+      // end PV(i). Waiting only at segment ends let a wait for PV(i) return on
+      // PV(i-2)'s completion while PV(i-1) was still in flight, and the epilogue then
+      // read O without the last chunks' contributions.
+      if (i > 0 && !mbar_wait(smem_u32(&o_full), (i - 1) & 1, &abort_flag, A.err)) break;
       if (any_raise && !cp.first) {
-        // O in TMEM holds this segment's earlier chunks; once PV(i-1) has completed,
+        // O in TMEM holds this segment's earlier chunks; PV(i-1) has completed (above):
         // scale the raised heads' columns by alpha (PV(i) waits for this chunk's P).
-        if (!mbar_wait(smem_u32(&o_full), (i - 1) & 1, &abort_flag, A.err)) break;
         tc_fence_after();
 #pragma unroll
         for (int mb = 0; mb < 2; ++mb) {

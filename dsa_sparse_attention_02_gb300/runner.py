@@ -82,6 +82,8 @@ class DeviceWorkload:
         for v, b in zip(views, src):
             v.view(-1).view(torch.uint8).copy_(b)
         self.inputs = ins.buf
+        # byte offset of the first MLA query: what the indexer and top-k read lies before it
+        self.inputs_mla_q_offset = ins.parts[i_q[0]][0]
         self.seq_lens, self.cu_q, self.block_table = views[i_seq], views[i_cu], views[i_bt]
         self.geom = _lib.Geometry(self.seq_lens, self.cu_q, self.block_table, wl.num_pages,
                                   wl.max_seq_len, wl.T)

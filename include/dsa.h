@@ -289,6 +289,17 @@ dsa_status_t dsa_decode_step(const dsa_step_args_t* args, void* ws, size_t ws_by
 size_t dsa_decode_step_workspace_size(const dsa_step_args_t* args);
 
 /*
+ * dsa_decode_step_wait_q -- dsa_decode_step for a caller whose MLA query (args->q)
+ *   may still be on its way to the device when the call is enqueued: the indexer
+ *   and top-k are enqueued as usual, and the sparse-MLA attention waits on the CUDA
+ *   event q_ready (cudaEvent_t, recorded after q's copy, e.g. on another stream)
+ *   before it starts; NULL behaves as dsa_decode_step. Same results. (Not a step of
+ *   the method: it lets the copy of the largest per-step input overlap the indexer.)
+ */
+dsa_status_t dsa_decode_step_wait_q(const dsa_step_args_t* args, void* q_ready, void* ws, size_t ws_bytes,
+                                    void* stream);
+
+/*
  * dsa_decode_step_bounded -- dsa_decode_step with the indexer's score workspace
  *   bounded (lmdeploy "glm5.3-flash support", Capacity improvement: bounded KPool
  *   scoring: a configurable score budget, top-k selected per query chunk right after
