@@ -147,3 +147,18 @@ def test_attend_split_merge_is_deterministic_and_needs_no_initial_workspace():
     out = ref[0].view(torch.bfloat16).float().cpu().numpy()
     lse = ref[1].view(torch.float32).cpu().numpy()
     _check(wl, 0, idx.cpu().numpy(), out, lse, ts=list(range(0, wl.T, 11)))
+
+
+@pytest.mark.parametrize("heads,k,ctx", [(128, 512, [900, 3000]), (16, 16384, [20000])],
+                         ids=["128-heads", "k-16384"])
+def test_attend_maximum_sizes(heads, k, ctx):
+    # the API's limits: H = 128 (eight head groups of 16 on the grid's y axis) and
+    # k = 16384 (128 key chunks per query, spread over the clusters and merged)
+    rng = np.random.default_rng(heads + k)
+    wl = inputs.make_workload("attn", ctx, [1] * len(ctx), topk=k, hi=4, qk_dtype="bf16",
+                              kv_dtypes=("bf16",), heads=heads, seed=36)
+    dw = runner.DeviceWorkload(wl, DEV)
+    idx = _random_idx(rng, wl, k, pad_frac=0.01)
+    out, lse = _attend(wl, dw, 0, idx, k)
+    worst = _check(wl, 0, idx, out, lse)
+    print(f"H={heads} k={k}: max |O err| {worst:.3g}")
