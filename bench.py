@@ -215,6 +215,26 @@ def run_reference(args, rank, world):
 
 # ----------------------------------------------------------------------------- our arm
 
+def replica_seed(rank):
+    """Seed of rank `rank`'s replica of the decode workload: every rank draws its own
+    requests (data-parallel over requests; no rank reads another's data)."""
+    return inputs.CONFIG_SEEDS["decode"] + 1000 * rank
+
+
+def aggregate_over_ranks(units, ms, dist=None, device="cpu"):
+    """Whole-job throughput of a data-parallel run: the units that all ranks processed
+    divided by the slowest rank's time. `units` and `ms` are this rank's; returns
+    (units per second over all ranks, the maximum of `ms` over ranks)."""
+    if dist is None:
+        return units / (ms / 1000.0), ms
+    t_ms = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    t_units = torch.tensor([float(units)], dtype=torch.float64, device=device)
+    dist.all_reduce(t_ms, op=dist.ReduceOp.MAX)
+    dist.all_reduce(t_units, op=dist.ReduceOp.SUM)
+    ms_max = float(t_ms.item())
+    return float(t_units.item()) / (ms_max / 1000.0), ms_max
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
@@ -232,7 +252,7 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    wl = inputs.make_config("decode", seed=inputs.CONFIG_SEEDS["decode"] + 1000 * rank)
+    wl = inputs.make_config("decode", seed=replica_seed(rank))
     dw = runner.DeviceWorkload(wl, dev)
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
@@ -277,15 +297,14 @@ def main():
     total_ms = float(sum(step_ms))
     if dw.check_error() != 0:
         raise SystemExit("device error during the timed steps")
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    value, total_ms = aggregate_over_ranks(wl.T * args.steps, total_ms, dist, dev)
     ms_per_step = total_ms / args.steps
-    value = wl.T * world * args.steps / (total_ms / 1000.0)
 
     # ---- end to end through the public API with host buffers
+    if dist:
+        dist.barrier()
     e2e = measure_e2e(dw, graph, flush, stream, max(20, min(args.steps, 200)))
+    e2e["value"], e2e["ms_per_step"] = aggregate_over_ranks(wl.T, e2e["ms_per_step"], dist, dev)
     # ---- per-kernel breakdown for the roofline of the dominant kernel
     comp = measure_components(dw, flush, stream, max(20, min(args.steps, 200)))
     # ---- next row beyond the step: the cache update (timed alone; not part of `value`)
