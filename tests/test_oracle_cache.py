@@ -4,6 +4,7 @@ torch's e4m3 cast over a dense sweep, hand-worked encodings and a hand-worked re
 that no other row changes."""
 import json
 import os
+from fractions import Fraction
 
 import numpy as np
 import pytest
@@ -37,6 +38,25 @@ def test_encoder_hand_cases():
         cases = json.load(f)["cases"]
     for c in cases:
         assert oc.encode_e4m3(np.array([c["value"]]))[0] == int(c["code"], 16), c
+
+
+def test_group_quotient_is_rounded_to_fp32_before_the_code():
+    """A hand-worked group where the fp32 quotient sits exactly on an e4m3 midpoint
+    (ties to the even code) while the exact quotient lies just above it
+    (tests/golden/e4m3_fp32_quotient.json holds the derivation)."""
+    with open(os.path.join(GOLDEN, "e4m3_fp32_quotient.json")) as f:
+        g = json.load(f)
+    vals = np.array([int(b, 16) for b in g["values_f32_bits"]], dtype=np.uint32).view(np.float32)
+    x = np.zeros(g["group"], dtype=np.float32)
+    x[: vals.shape[0]] = vals
+    codes, scale = oc.quantize_groups(x, g["group"])
+    assert int(np.asarray(scale, dtype=np.float32).reshape(-1).view(np.uint32)[0]) == int(g["expected_scale_f32_bits"], 16)
+    assert codes[: vals.shape[0]].tolist() == [int(c, 16) for c in g["expected_codes"]]
+    assert np.all(codes[vals.shape[0]:] == 0)
+    # the premise: rounding the exact quotient would pick the other code
+    exact = Fraction(float(vals[1])) / Fraction(float(np.float32(vals[0]) / np.float32(448.0)))
+    lo, hi = Fraction(1), Fraction(9, 8)
+    assert (lo + hi) / 2 < exact < hi and int(g["code_if_rounded_exactly"], 16) == 0x39
 
 
 def test_encoder_round_trip_is_nearest():

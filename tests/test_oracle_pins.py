@@ -313,6 +313,52 @@ def test_indexshare_layer_reuses_full_layer_selection():
         np.testing.assert_array_equal(res["out"][1][t][0], alone[t][0])
         assert np.array_equal(reused["idx"][t], res["idx"][t])
         np.testing.assert_array_equal(reused["out"][0][t][0], res["out"][0][t][0])
+    # a given selection that is not the indexer's: every layer attends over exactly it,
+    # and no score is computed (the shared layer skips the indexer)
+    _, pos = oracle.query_positions(wl.seq_lens, wl.n_q)
+    other = {t: np.array([s if s <= pos[t] else -1 for s in range(0, 2 * 32, 2)], dtype=np.int32)
+             for t in range(wl.T)}
+    assert any(set(other[t]) != set(res["idx"][t]) for t in range(wl.T))
+    given = oracle.dsa_step(wl, reuse_idx=other)
+    assert given["scores"] == {}
+    for li, layer in enumerate(wl.layers):
+        ref = oracle.sparse_mla(layer.q, layer.kv, layer.kv_dtype, other, wl.seq_lens, wl.n_q,
+                                wl.block_table, wl.sm_scale)
+        for t in range(wl.T):
+            assert np.array_equal(given["idx"][t], other[t])
+            np.testing.assert_array_equal(given["out"][li][t][0], ref[t][0])
+
+
+def test_split_merge_identity_and_empty_selection():
+    """Attention over a set S equals the log-sum-exp merge of attention over any two
+    disjoint parts of S: LSE = log(e^LSE1 + e^LSE2), O = e^(LSE1-LSE) O1 + e^(LSE2-LSE) O2
+    (the split-KV combine's identity). An all-padding selection is the empty sum:
+    LSE = log 0 = -inf and, as the merge requires, contributes nothing (O = 0)."""
+    wl = synth.make_workload("pin", [400, 230], [2, 1], topk=64, hi=4, qk_dtype="bf16",
+                             kv_dtypes=("bf16", "e4m3"), seed=28)
+    res = oracle.dsa_step(wl)
+    rng = np.random.default_rng(8)
+    for layer in wl.layers:
+        full = oracle.sparse_mla(layer.q, layer.kv, layer.kv_dtype, res["idx"], wl.seq_lens, wl.n_q,
+                                 wl.block_table, wl.sm_scale)
+        for t in range(wl.T):
+            sel = res["idx"][t]
+            part = rng.random(sel.shape[0]) < 0.3
+            a = {t: np.where(part, sel, -1)}
+            b = {t: np.where(part, -1, sel)}
+            empty = {t: np.full(sel.shape[0], -1, dtype=np.int32)}
+            (o1, l1), (o2, l2), (o0, l0) = (
+                oracle.sparse_mla(layer.q, layer.kv, layer.kv_dtype, x, wl.seq_lens, wl.n_q,
+                                  wl.block_table, wl.sm_scale, ts=[t])[t] for x in (a, b, empty))
+            lse = np.logaddexp(l1, l2)
+            o = np.exp(l1 - lse)[:, None] * o1 + np.exp(l2 - lse)[:, None] * o2
+            np.testing.assert_allclose(lse, full[t][1], rtol=1e-13)
+            np.testing.assert_allclose(o, full[t][0], rtol=1e-11, atol=1e-13)
+            assert np.all(l0 == -np.inf) and np.all(o0 == 0.0)
+            lse0 = np.logaddexp(full[t][1], l0)
+            np.testing.assert_array_equal(lse0, full[t][1])
+            np.testing.assert_array_equal(np.exp(full[t][1] - lse0)[:, None] * full[t][0]
+                                          + np.exp(l0 - lse0)[:, None] * o0, full[t][0])
 
 
 def test_fp8_latent_dequant_is_exact_product():

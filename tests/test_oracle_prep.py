@@ -102,6 +102,59 @@ def test_layer_norm_special_cases():
     assert np.isclose(y.var(), var / (var + 1e-6), rtol=1e-12)
 
 
+def test_prepared_key_closed_form_layernorm_then_rope():
+    """Key = +a on its first 64 values and -a on the rest: mean 0, biased variance a^2,
+    so LayerNorm gives x_hat = +-a / sqrt(a^2 + eps), then gamma * x_hat + beta; RoPE
+    (rope_dim 64) then turns pair i (elements i and i + 32, both from the +a half) by
+    the angle of position p, and the other 64 values pass through."""
+    a, eps, p = 1.5, 1e-6, 5
+    k = np.concatenate([np.full(64, a), np.full(64, -a)]).astype(np.float32)
+    k_bits = (k.view(np.uint32) >> 16).astype(np.uint16)[None, :]       # exact in bf16
+    gamma = 1.0 + np.arange(128) / 128.0
+    beta = np.arange(128) / 256.0
+    cos, sin = _tables(16, 64)
+    got = prep.prepared_k(k_bits, np.array([p]), cos, sin, 64, gamma, beta, eps)[0]
+    xh = np.concatenate([np.full(64, a), np.full(64, -a)]) / np.sqrt(a * a + eps)
+    n = xh * gamma + beta
+    exp = n.copy()
+    for i in range(32):
+        c, s = cos[p, i], sin[p, i]
+        exp[i] = n[i] * c - n[i + 32] * s
+        exp[i + 32] = n[i + 32] * c + n[i] * s
+    np.testing.assert_allclose(got, exp, rtol=1e-13, atol=1e-15)
+
+
+def test_rope_uses_the_table_row_of_each_tokens_position():
+    """Tables that hold a quarter turn at one position and the identity elsewhere: only
+    the token at that position is turned (y_i = -x_(i+r), y_(i+r) = x_i), for queries
+    and keys alike."""
+    rng = np.random.default_rng(12)
+    r, L, p_turn = 32, 12, 7
+    cos, sin = np.ones((L, r)), np.zeros((L, r))
+    cos[p_turn], sin[p_turn] = 0.0, 1.0
+    pos = np.array([p_turn - 1, p_turn, p_turn + 1])
+    q = rng.standard_normal((3, 2, 128)).astype(np.float32)
+    q_bits = (q.view(np.uint32) >> 16).astype(np.uint16)
+    qd = (q_bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    got = prep.prepared_q(q_bits, pos, cos, sin, 2 * r)
+    turned = qd.copy()
+    turned[..., :r], turned[..., r:2 * r] = -qd[..., r:2 * r], qd[..., :r]
+    np.testing.assert_array_equal(got[0], qd[0])
+    np.testing.assert_array_equal(got[1], turned[1])
+    np.testing.assert_array_equal(got[2], qd[2])
+    # keys: the same rows, applied after the LayerNorm (pinned to torch above)
+    kv = rng.standard_normal((3, 128)).astype(np.float32)
+    k_bits = (kv.view(np.uint32) >> 16).astype(np.uint16)
+    kd = (k_bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    kn = prep.layer_norm(kd, np.ones(128), np.zeros(128), 1e-6)
+    gk = prep.prepared_k(k_bits, pos, cos, sin, 2 * r, np.ones(128), np.zeros(128), 1e-6)
+    kt = kn.copy()
+    kt[:, :r], kt[:, r:2 * r] = -kn[:, r:2 * r], kn[:, :r]
+    np.testing.assert_array_equal(gk[0], kn[0])
+    np.testing.assert_array_equal(gk[1], kt[1])
+    np.testing.assert_array_equal(gk[2], kn[2])
+
+
 def _geometry():
     seq = np.array([70, 200, 129], dtype=np.int32)
     nq = np.array([2, 1, 3], dtype=np.int32)
