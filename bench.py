@@ -185,12 +185,14 @@ def cpu_baseline(wl, budget_s=12.0):
                       f"decode workload, repeated for >= {budget_s:.0f} s; BLAS threads = host cores"}
 
 
-def run_reference(args, rank, world):
+def run_reference(args, rank, world, budget=90.0):
+    """The reference arm: the float64 oracle on this host's cores, rank 0 only, each
+    step a sample of the decode workload's queries sized so that the whole run takes
+    about `budget` seconds."""
     if rank != 0:
         return
     wl = inputs.make_config("decode")
-    per_q = oracle_step_time(wl, 2, 1.0)                       # calibration
-    budget = 90.0                                              # whole run
+    per_q = oracle_step_time(wl, 2, min(1.0, budget / 10))     # calibration
     nq = int(max(1, min(wl.T, budget / max(1, args.steps + args.warmup) / per_q)))
     for _ in range(args.warmup):
         oracle_step_time(wl, nq, 0.0)
