@@ -149,3 +149,82 @@ def test_bounded_step_budget_floor_and_workspace_sizes(lib):
     one = lib.dsa_decode_step_bounded_workspace_size(C.byref(a), row)
     assert one < full - 62 * row                               # 63 fewer score rows, plus the range geometry
     assert lib.dsa_decode_step_bounded_workspace_size(C.byref(a), 8 * row) > one
+
+
+# ----------------------------------------------------------------------------- header vs binding
+
+_SCALAR = {"int32_t": C.c_int32, "int64_t": C.c_int64, "size_t": C.c_size_t, "float": C.c_float,
+           "dsa_dtype_t": C.c_int, "dsa_status_t": C.c_int, "int": C.c_int}
+
+
+def _header_text():
+    return re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+
+
+def _ctype_of(decl):
+    """ctypes type of one C declaration's type part ('const float*', 'int32_t', ...)."""
+    decl = decl.replace("const", "").strip()
+    if "*" in decl:
+        return "pointer"
+    return _SCALAR[decl.split()[0]]
+
+
+def _prototypes():
+    protos = {}
+    for ret, name, params in re.findall(r"([A-Za-z_][\w\s\*]*?)\b(dsa_\w+)\s*\(([^)]*)\)\s*;", _header_text()):
+        params = params.strip()
+        plist = [] if params in ("", "void") else [p.strip() for p in params.split(",")]
+        types = []
+        for p in plist:
+            m = re.match(r"(.*?)(\w+)$", p)                 # drop the parameter name
+            types.append(_ctype_of(m.group(1) if m and m.group(1).strip() else p))
+        protos[name] = (ret.strip(), types)
+    return protos
+
+
+def _is_pointer_type(t):
+    return t in (C.c_void_p, C.c_char_p) or (isinstance(t, type) and issubclass(t, C._Pointer))
+
+
+def test_binding_signatures_match_the_header(lib):
+    protos = _prototypes()
+    assert sorted(protos) == sorted(_lib.EXPORTED)
+    for name, (ret, params) in protos.items():
+        fn = getattr(lib, name)
+        assert fn.argtypes is not None and len(fn.argtypes) == len(params), (name, params, fn.argtypes)
+        for i, (want, got) in enumerate(zip(params, fn.argtypes)):
+            if want == "pointer":
+                assert _is_pointer_type(got), (name, i, got)
+            else:
+                assert got is want, (name, i, want, got)
+        want_ret = "pointer" if "*" in ret else _SCALAR[ret.replace("const", "").strip()]
+        if want_ret == "pointer":
+            assert fn.restype is C.c_char_p, name
+        else:
+            assert fn.restype is want_ret, (name, ret, fn.restype)
+
+
+def _header_struct(name):
+    m = re.search(r"typedef struct\s*\{([^{}]*)\}\s*" + name + r"\s*;", _header_text())
+    fields = []
+    for decl in m.group(1).split(";"):
+        decl = " ".join(decl.split())
+        if not decl:
+            continue
+        fm = re.match(r"(.*?)(\w+)$", decl)
+        fields.append((fm.group(2), fm.group(1).strip()))
+    return fields
+
+
+@pytest.mark.parametrize("name", ["dsa_geom_t", "dsa_step_args_t"])
+def test_binding_structs_match_the_header(name):
+    fields = _header_struct(name)
+    ct = getattr(_lib, name)
+    assert [f for f, _ in fields] == [f for f, _ in ct._fields_]
+    for (fname, ctype), (_, got) in zip(fields, ct._fields_):
+        if ctype in ("dsa_geom_t",):
+            assert got is _lib.dsa_geom_t, fname
+        elif "*" in ctype:
+            assert got is C.c_void_p, fname
+        else:
+            assert got is _SCALAR[ctype.replace("const", "").strip()], (fname, ctype, got)
