@@ -45,6 +45,8 @@ WORKLOAD = ("decode: batch 64, context ~U[2048,8192], 1 query token, index_topk 
 PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+E4M3_PER_BF16 = 2.0          # nominal dense e4m3 : bf16 tensor rate on this part (4.5 : 2.25 PFLOP/s)
 
 
 def parse():
@@ -81,6 +83,14 @@ def load_peaks():
         return float(p["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def load_bf16_tflops():
+    try:
+        with open(PEAKS_PATH) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def kernel_source_hash():
@@ -314,6 +324,7 @@ def main():
     int8_attend = measure_int8_attend(dw, flush, stream, max(20, min(args.steps, 100)))
     fp8_attend = measure_int8_attend(dw, flush, stream, max(20, min(args.steps, 100)), kv_dtype=_lib.DSA_E4M3)
     prep = measure_indexer_prep(dw, flush, stream, max(20, min(args.steps, 100)))
+    idx_prefill = measure_indexer_prefill(flush, stream, max(10, min(args.steps, 30)), dev)
     bounded = measure_bounded_step(dw, flush, stream, max(20, min(args.steps, 100)))
 
     idx_b, lat_b, selected = algorithmic_bytes(wl)
@@ -344,6 +355,7 @@ def main():
         "next_rows": {"cache_append": append, "int8_latent_attend": int8_attend, "indexer_prep": prep,
                       "bounded_scoring": bounded},
         "e4m3_latent_attend": fp8_attend,
+        "indexer_prefill": idx_prefill,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks.summary(),
@@ -410,6 +422,48 @@ def measure_e2e(dw, graph, flush, stream, n):
             "d2h_bytes_per_step": d2h, "ms_per_step": avg,
             "copies": ("dsa_stage_copy (an SM copy kernel) from and to page-locked host memory: the indexer's "
                        "inputs and the MLA query (overlapping the indexer and top-k) in, O and LSE out")}
+
+
+def measure_indexer_prefill(flush, stream, n, device):
+    """The lightning indexer alone on the prefill workload (2048 queries at positions
+    14336..16383 of one 16384-token request, 64 e4m3 heads x 128): a contraction, so
+    it is read against the e4m3 tensor rate, taken as the measured bf16 rate times
+    the nominal e4m3/bf16 ratio. Algorithmic work: 2 x 128 x heads flops per causal
+    (query, key) pair."""
+    wl = inputs.make_config("prefill")
+    dw = runner.DeviceWorkload(wl, device)
+    g = dw.geom
+    stride = int(-(-wl.max_seq_len // 64) * 64)
+    scores = torch.empty(wl.T, stride, dtype=torch.float32, device=device)
+    ws = _lib.workspace(_lib.dsa_indexer_scores_workspace_size(g), device)
+
+    def launch():
+        _lib.dsa_indexer_scores(g, dw.qk_dtype, dw.q_idx, dw.q_scale, dw.w, dw.idx_k, dw.idx_k_scale,
+                                scores, ws)
+
+    for _ in range(3):
+        launch()
+    torch.cuda.synchronize()
+    if _lib.dsa_get_error(ws) != 0:
+        raise SystemExit("device error in the prefill indexer")
+    total = 0.0
+    for i in range(n):
+        flush.fill_(i & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        launch()
+        e1.record(stream)
+        e1.synchronize()
+        total += e0.elapsed_time(e1)
+    ms = total / n
+    _, pos = _positions(wl)
+    flops = 2.0 * 128 * int(dw.w.shape[1]) * float((pos.astype(np.int64) + 1).sum())
+    bf16, kind = load_bf16_tflops()
+    peak = bf16 * E4M3_PER_BF16
+    achieved = flops / (ms / 1000.0) / 1e12
+    return {"ms": ms, "queries": wl.T, "context": int(wl.max_seq_len), "algorithmic_tflop": flops / 1e12,
+            "achieved_tflops": achieved, "peak_tflops": peak, "frac": achieved / peak,
+            "peak_kind": f"{kind} bf16 x {E4M3_PER_BF16:g} (nominal e4m3/bf16 ratio)", "bound": "tensor"}
 
 
 def measure_components(dw, flush, stream, n):
