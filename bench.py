@@ -93,21 +93,31 @@ def load_bf16_tflops():
         return FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def kernel_source_hash():
-    h = hashlib.sha256()
+# The sources that decide what a kernel does and how it is launched: its own file,
+# the shared device headers and the host entry points that configure the launch.
+KERNEL_SOURCES = {"sparse_mla_kernel": ["sparse_mla.cu"], "indexer_kernel": ["indexer.cu"],
+                  "topk_kernel": ["topk.cu"]}
+SHARED_SOURCES = ["api.cu", "common.cuh", "kernels.cuh", "ptx.cuh"]
+
+
+def kernel_source_hash(kernel=None):
+    """Hash of every CUDA source (kernel None) or of one kernel's sources."""
     csrc = os.path.join(ROOT, "dsa_sparse_attention_02_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    files = sorted(os.listdir(csrc)) if kernel is None else sorted(KERNEL_SOURCES[kernel] + SHARED_SOURCES)
+    h = hashlib.sha256()
+    for f in files:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
 def load_traffic(kernel):
-    """DRAM bytes per launch from the committed ncu summary, if taken on the current source."""
+    """DRAM bytes per launch from the committed ncu summary, if taken on the kernel's
+    current sources."""
     try:
         with open(TRAFFIC_PATH) as f:
             t = json.load(f)
-        if t.get("source_hash") != kernel_source_hash():
+        if t["kernels"][kernel].get("source_hash") != kernel_source_hash(kernel):
             return None
         return t["kernels"][kernel]["dram_bytes_per_launch"]
     except Exception:
