@@ -113,7 +113,20 @@ def status_string(status: int) -> str:
 
 
 def _ptr(t):
+    """Address of a tensor of any device (None -> NULL): only for dsa_stage_copy, whose
+    C side resolves and checks both ends itself."""
     return None if t is None else t.data_ptr()
+
+
+def _dptr(t):
+    """Address of a CUDA tensor (None -> NULL). Anything else is refused here, so that a
+    host address never reaches a kernel."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"expected a CUDA tensor, got {type(t).__name__}"
+                        + (f" on {t.device}" if isinstance(t, torch.Tensor) else ""))
+    return t.data_ptr()
 
 
 def _stream(stream=None):
@@ -141,7 +154,7 @@ class Geometry:
         self.max_seq_len = int(max_seq_len)
         self.c = dsa_geom_t(self.B, self.T, self.max_seq_len, self.num_pages, 64,
                             int(block_table.shape[1]) if block_table.dim() == 2 else 0,
-                            _ptr(seq_lens), _ptr(cu_q), _ptr(block_table))
+                            _dptr(seq_lens), _dptr(cu_q), _dptr(block_table))
 
     @property
     def ref(self):
@@ -160,9 +173,9 @@ def dsa_indexer_scores_workspace_size(geom: Geometry) -> int:
 def dsa_indexer_scores(geom: Geometry, qk_dtype: int, q_idx, q_scale, w, idx_k_cache, idx_k_scale,
                        scores: torch.Tensor, ws: torch.Tensor, stream=None):
     Hi = int(w.shape[1])
-    st = load().dsa_indexer_scores(geom.ref, qk_dtype, Hi, _ptr(q_idx), _ptr(q_scale), _ptr(w),
-                                   _ptr(idx_k_cache), _ptr(idx_k_scale), _ptr(scores),
-                                   int(scores.stride(0)), _ptr(ws), ws.numel(), _stream(stream))
+    st = load().dsa_indexer_scores(geom.ref, qk_dtype, Hi, _dptr(q_idx), _dptr(q_scale), _dptr(w),
+                                   _dptr(idx_k_cache), _dptr(idx_k_scale), _dptr(scores),
+                                   int(scores.stride(0)), _dptr(ws), ws.numel(), _stream(stream))
     _check(st, "dsa_indexer_scores")
 
 
@@ -172,8 +185,8 @@ def dsa_topk_workspace_size(geom: Geometry, k: int) -> int:
 
 def dsa_topk(geom: Geometry, scores: torch.Tensor, k: int, idx: torch.Tensor, ws: torch.Tensor,
              stream=None):
-    st = load().dsa_topk(geom.ref, _ptr(scores), int(scores.stride(0)), int(k), _ptr(idx),
-                         _ptr(ws), ws.numel(), _stream(stream))
+    st = load().dsa_topk(geom.ref, _dptr(scores), int(scores.stride(0)), int(k), _dptr(idx),
+                         _dptr(ws), ws.numel(), _stream(stream))
     _check(st, "dsa_topk")
 
 
@@ -184,9 +197,9 @@ def dsa_sparse_mla_attend_workspace_size(geom: Geometry, H: int, k: int) -> int:
 def dsa_sparse_mla_attend(geom: Geometry, kv_dtype: int, q, kv_cache, idx, k: int, sm_scale: float,
                           out, lse, ws, stream=None):
     H = int(q.shape[1])
-    st = load().dsa_sparse_mla_attend(geom.ref, kv_dtype, H, _ptr(q), _ptr(kv_cache), _ptr(idx),
-                                      int(k), float(sm_scale), _ptr(out), _ptr(lse),
-                                      _ptr(ws), ws.numel(), _stream(stream))
+    st = load().dsa_sparse_mla_attend(geom.ref, kv_dtype, H, _dptr(q), _dptr(kv_cache), _dptr(idx),
+                                      int(k), float(sm_scale), _dptr(out), _dptr(lse),
+                                      _dptr(ws), ws.numel(), _stream(stream))
     _check(st, "dsa_sparse_mla_attend")
 
 
@@ -195,9 +208,9 @@ def dsa_sparse_mla_attend_static(geom: Geometry, kv_dtype: int, q, kv_cache, idx
     """dsa_sparse_mla_attend without a workspace, for callers that cannot allocate device
     memory at call time; its partials use the library's static per-GPU buffer."""
     H = int(q.shape[1])
-    st = load().dsa_sparse_mla_attend_static(geom.ref, kv_dtype, H, _ptr(q), _ptr(kv_cache), _ptr(idx),
-                                             int(k), float(sm_scale), _ptr(out), _ptr(lse),
-                                             _ptr(err_word), _stream(stream))
+    st = load().dsa_sparse_mla_attend_static(geom.ref, kv_dtype, H, _dptr(q), _dptr(kv_cache), _dptr(idx),
+                                             int(k), float(sm_scale), _dptr(out), _dptr(lse),
+                                             _dptr(err_word), _stream(stream))
     _check(st, "dsa_sparse_mla_attend_static")
 
 
@@ -208,8 +221,8 @@ def dsa_cache_append_workspace_size(geom: Geometry) -> int:
 def dsa_cache_append(geom: Geometry, kv_dtype: int, kv_new, kv_cache, qk_dtype: int = DSA_E4M3, k_new=None,
                      idx_k_cache=None, idx_k_scale=None, ws=None, stream=None):
     """Writes the geom.T new tokens (flattened like queries) into the paged caches."""
-    st = load().dsa_cache_append(geom.ref, kv_dtype, _ptr(kv_new), _ptr(kv_cache), qk_dtype, _ptr(k_new),
-                                 _ptr(idx_k_cache), _ptr(idx_k_scale), _ptr(ws), ws.numel() if ws is not None else 0,
+    st = load().dsa_cache_append(geom.ref, kv_dtype, _dptr(kv_new), _dptr(kv_cache), qk_dtype, _dptr(k_new),
+                                 _dptr(idx_k_cache), _dptr(idx_k_scale), _dptr(ws), ws.numel() if ws is not None else 0,
                                  _stream(stream))
     _check(st, "dsa_cache_append")
 
@@ -223,9 +236,9 @@ def dsa_indexer_prepare(geom: Geometry, Hi: int, rope_dim: int, q_in, k_in, rope
                         stream=None):
     """RoPE + e4m3 of the indexer queries into q_out / q_scale; LayerNorm + RoPE + e4m3
     of the new tokens' keys (k_in, or None) into the paged index cache."""
-    st = load().dsa_indexer_prepare(geom.ref, int(Hi), int(rope_dim), _ptr(q_in), _ptr(k_in), _ptr(rope_cos),
-                                    _ptr(rope_sin), _ptr(ln_gamma), _ptr(ln_beta), float(ln_eps), _ptr(q_out),
-                                    _ptr(q_scale), _ptr(idx_k_cache), _ptr(idx_k_scale), _ptr(ws),
+    st = load().dsa_indexer_prepare(geom.ref, int(Hi), int(rope_dim), _dptr(q_in), _dptr(k_in), _dptr(rope_cos),
+                                    _dptr(rope_sin), _dptr(ln_gamma), _dptr(ln_beta), float(ln_eps), _dptr(q_out),
+                                    _dptr(q_scale), _dptr(idx_k_cache), _dptr(idx_k_scale), _dptr(ws),
                                     ws.numel() if ws is not None else 0, _stream(stream))
     _check(st, "dsa_indexer_prepare")
 
@@ -236,10 +249,10 @@ def make_step_args(geom: Geometry, topk: int, *, qk_dtype=DSA_E4M3, q_idx=None, 
                    lse=None) -> dsa_step_args_t:
     Hi = int(w.shape[1]) if w is not None else 0
     H = int(q.shape[1]) if q is not None else 0
-    return dsa_step_args_t(geom.c, int(topk), int(qk_dtype), Hi, _ptr(q_idx), _ptr(q_scale),
-                           _ptr(w), _ptr(idx_k_cache), _ptr(idx_k_scale), _ptr(reuse_idx),
-                           _ptr(idx_out), int(kv_dtype), H, _ptr(q), _ptr(kv_cache),
-                           float(sm_scale), _ptr(out), _ptr(lse))
+    return dsa_step_args_t(geom.c, int(topk), int(qk_dtype), Hi, _dptr(q_idx), _dptr(q_scale),
+                           _dptr(w), _dptr(idx_k_cache), _dptr(idx_k_scale), _dptr(reuse_idx),
+                           _dptr(idx_out), int(kv_dtype), H, _dptr(q), _dptr(kv_cache),
+                           float(sm_scale), _dptr(out), _dptr(lse))
 
 
 def dsa_decode_step_workspace_size(args: dsa_step_args_t) -> int:
@@ -247,7 +260,7 @@ def dsa_decode_step_workspace_size(args: dsa_step_args_t) -> int:
 
 
 def dsa_decode_step(args: dsa_step_args_t, ws: torch.Tensor, stream=None):
-    st = load().dsa_decode_step(C.byref(args), _ptr(ws), ws.numel(), _stream(stream))
+    st = load().dsa_decode_step(C.byref(args), _dptr(ws), ws.numel(), _stream(stream))
     _check(st, "dsa_decode_step")
 
 
@@ -260,7 +273,7 @@ def dsa_stage_copy(dst, src, nbytes: int, stream=None):
 def dsa_decode_step_wait_q(args: dsa_step_args_t, q_ready: torch.cuda.Event, ws: torch.Tensor, stream=None):
     """dsa_decode_step whose attention waits on q_ready (the MLA query's copy)."""
     ev = None if q_ready is None else C.c_void_p(q_ready.cuda_event)
-    st = load().dsa_decode_step_wait_q(C.byref(args), ev, _ptr(ws), ws.numel(), _stream(stream))
+    st = load().dsa_decode_step_wait_q(C.byref(args), ev, _dptr(ws), ws.numel(), _stream(stream))
     _check(st, "dsa_decode_step_wait_q")
 
 
@@ -271,16 +284,16 @@ def dsa_decode_step_bounded_workspace_size(args: dsa_step_args_t, score_budget_b
 def dsa_decode_step_bounded(args: dsa_step_args_t, score_budget_bytes: int, ws: torch.Tensor, stream=None):
     """dsa_decode_step holding the scores of at most score_budget_bytes // (stride * 4)
     queries at a time; bitwise the same results."""
-    st = load().dsa_decode_step_bounded(C.byref(args), int(score_budget_bytes), _ptr(ws), ws.numel(), _stream(stream))
+    st = load().dsa_decode_step_bounded(C.byref(args), int(score_budget_bytes), _dptr(ws), ws.numel(), _stream(stream))
     _check(st, "dsa_decode_step_bounded")
 
 
 def dsa_get_error(ws: torch.Tensor, stream=None) -> int:
-    return int(load().dsa_get_error(_ptr(ws), _stream(stream)))
+    return int(load().dsa_get_error(_dptr(ws), _stream(stream)))
 
 
 def dsa_clear_error(ws: torch.Tensor, stream=None):
-    _check(load().dsa_clear_error(_ptr(ws), _stream(stream)), "dsa_clear_error")
+    _check(load().dsa_clear_error(_dptr(ws), _stream(stream)), "dsa_clear_error")
 
 
 def dsa_abi_version() -> int:

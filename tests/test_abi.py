@@ -228,3 +228,22 @@ def test_binding_structs_match_the_header(name):
             assert got is C.c_void_p, fname
         else:
             assert got is _SCALAR[ctype.replace("const", "").strip()], (fname, ctype, got)
+
+
+def test_binding_refuses_host_tensors_for_device_arguments(lib):
+    """Host tensors are refused by the binding before any call reaches the library,
+    so a host address never reaches a kernel (dsa_stage_copy alone takes host memory,
+    and checks it on the C side)."""
+    import torch
+    seq = torch.tensor([64], dtype=torch.int32)
+    cu = torch.tensor([0, 1], dtype=torch.int32)
+    bt = torch.zeros(1, 1, dtype=torch.int32)
+    with pytest.raises(TypeError, match="CUDA tensor"):
+        _lib.Geometry(seq, cu, bt, num_pages=1, max_seq_len=64, T=1)
+    with pytest.raises(TypeError, match="CUDA tensor"):
+        _lib.dsa_decode_step(_lib.dsa_step_args_t(), torch.zeros(256, dtype=torch.uint8))
+    with pytest.raises(TypeError, match="CUDA tensor"):
+        _lib.dsa_get_error(torch.zeros(256, dtype=torch.uint8))
+    with pytest.raises(TypeError, match="CUDA tensor"):
+        _lib._dptr(bytearray(16))
+    assert _lib._dptr(None) is None
