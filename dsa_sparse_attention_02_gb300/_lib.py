@@ -26,7 +26,7 @@ EXPORTED = (
     "dsa_decode_step_bounded", "dsa_decode_step_bounded_workspace_size", "dsa_decode_step_wait_q",
     "dsa_cache_append", "dsa_cache_append_workspace_size",
     "dsa_indexer_prepare", "dsa_indexer_prepare_workspace_size", "dsa_stage_copy",
-    "dsa_get_error", "dsa_clear_error", "dsa_status_string", "dsa_last_error", "dsa_abi_version",
+    "dsa_get_error", "dsa_clear_error", "dsa_wait_probe", "dsa_status_string", "dsa_last_error", "dsa_abi_version",
 )
 
 
@@ -93,6 +93,7 @@ def load(path: str = LIB_PATH):
         "dsa_stage_copy": (C.c_int, [P, P, SZ, P]),
         "dsa_get_error": (C.c_int, [P, P]),
         "dsa_clear_error": (C.c_int, [P, P]),
+        "dsa_wait_probe": (C.c_int, [P, SZ, C.c_uint32, P]),
         "dsa_status_string": (C.c_char_p, [C.c_int]),
         "dsa_last_error": (C.c_char_p, []),
         "dsa_abi_version": (I32, []),
@@ -294,6 +295,12 @@ def dsa_get_error(ws: torch.Tensor, stream=None) -> int:
 
 def dsa_clear_error(ws: torch.Tensor, stream=None):
     _check(load().dsa_clear_error(_dptr(ws), _stream(stream)), "dsa_clear_error")
+
+
+def dsa_wait_probe(ws: torch.Tensor, limit_us: int, stream=None):
+    """Enqueues a wait that nothing completes, bounded by limit_us; the kernel records
+    DSA_ERR_TIMEOUT in ws's error word (read it with dsa_get_error)."""
+    _check(load().dsa_wait_probe(_dptr(ws), ws.numel(), int(limit_us), _stream(stream)), "dsa_wait_probe")
 
 
 def dsa_abi_version() -> int:

@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libdsa.so")
-SOURCES = ["api.cu", "indexer.cu", "topk.cu", "sparse_mla.cu", "noalloc.cu", "cache_append.cu", "indexer_prep.cu", "stage_copy.cu"]
+SOURCES = ["api.cu", "indexer.cu", "topk.cu", "sparse_mla.cu", "noalloc.cu", "cache_append.cu", "indexer_prep.cu", "stage_copy.cu", "wait_probe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 

@@ -321,6 +321,20 @@ dsa_status_t dsa_get_error(void* ws, void* stream);
 /* Enqueues a clear of the error word of `ws` on `stream`. */
 dsa_status_t dsa_clear_error(void* ws, void* stream);
 
+/*
+ * dsa_wait_probe -- runs the failure path of the kernels' bounded waits on purpose.
+ *   Every pipeline wait (an mbarrier phase completed by a copy, an MMA or another
+ *   warp) gives up after a time limit and records DSA_ERR_TIMEOUT in the workspace's
+ *   error word instead of hanging. This call enqueues one block whose thread waits
+ *   on an mbarrier phase that nothing completes, for at most limit_us microseconds
+ *   (1 .. 1,000,000), then records DSA_ERR_TIMEOUT in `ws`'s error word and exits.
+ *   Read it with dsa_get_error; the context stays usable.
+ *   ws: device, 256-byte aligned, ws_bytes >= 256. Returns DSA_ERR_INVALID_ARG for a
+ *   limit out of range, DSA_ERR_WORKSPACE for a missing or misaligned workspace,
+ *   DSA_ERR_CUDA if the launch fails.
+ */
+dsa_status_t dsa_wait_probe(void* ws, size_t ws_bytes, uint32_t limit_us, void* stream);
+
 const char* dsa_status_string(dsa_status_t status);
 /* Text describing the last failure seen by an entry point on the calling host
  * thread (the failing call and its CUDA error), or "" if none. Owned by the

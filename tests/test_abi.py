@@ -153,7 +153,7 @@ def test_bounded_step_budget_floor_and_workspace_sizes(lib):
 
 # ----------------------------------------------------------------------------- header vs binding
 
-_SCALAR = {"int32_t": C.c_int32, "int64_t": C.c_int64, "size_t": C.c_size_t, "float": C.c_float,
+_SCALAR = {"int32_t": C.c_int32, "uint32_t": C.c_uint32, "int64_t": C.c_int64, "size_t": C.c_size_t, "float": C.c_float,
            "dsa_dtype_t": C.c_int, "dsa_status_t": C.c_int, "int": C.c_int}
 
 
@@ -247,3 +247,11 @@ def test_binding_refuses_host_tensors_for_device_arguments(lib):
     with pytest.raises(TypeError, match="CUDA tensor"):
         _lib._dptr(bytearray(16))
     assert _lib._dptr(None) is None
+
+
+def test_wait_probe_validates_before_launch(lib):
+    assert lib.dsa_wait_probe(256, 256, 0, None) == _lib.DSA_ERR_INVALID_ARG
+    assert lib.dsa_wait_probe(256, 256, 1000001, None) == _lib.DSA_ERR_INVALID_ARG
+    assert lib.dsa_wait_probe(None, 256, 1000, None) == _lib.DSA_ERR_WORKSPACE
+    assert lib.dsa_wait_probe(260, 256, 1000, None) == _lib.DSA_ERR_WORKSPACE      # misaligned
+    assert lib.dsa_wait_probe(256, 128, 1000, None) == _lib.DSA_ERR_WORKSPACE      # too small
