@@ -31,8 +31,9 @@
  *     pos = seq_lens[b] - n_b + j with n_b = cu_q[b+1]-cu_q[b]; seq_lens counts
  *     the cached tokens including the query tokens' own keys. Keys 0..pos are
  *     visible to it.
- *   - Workspace: every entry point takes `ws`/`ws_bytes`, device memory of at
- *     least the size its *_workspace_size() function returns, 256-byte aligned.
+ *   - Workspace: every compute entry point takes `ws`/`ws_bytes`, device memory
+ *     of at least the size its *_workspace_size() function returns (256 bytes for
+ *     dsa_wait_probe; dsa_stage_copy takes none), 256-byte aligned.
  *     Its first 256 bytes hold the device error word; zero them once before
  *     first use (dsa_clear_error). Calls on the same workspace must be ordered
  *     on one stream.
