@@ -205,9 +205,10 @@ def dsa_sparse_mla_attend(geom: Geometry, kv_dtype: int, q, kv_cache, idx, k: in
 
 
 def dsa_sparse_mla_attend_static(geom: Geometry, kv_dtype: int, q, kv_cache, idx, k: int,
-                                 sm_scale: float, out, lse, err_word=None, stream=None):
+                                 sm_scale: float, out, lse, err_word, stream=None):
     """dsa_sparse_mla_attend without a workspace, for callers that cannot allocate device
-    memory at call time; its partials use the library's static per-GPU buffer."""
+    memory at call time; its partials use the library's static per-GPU buffer. err_word
+    is a device int32 (zeroed by the caller) that receives device-side errors."""
     H = int(q.shape[1])
     st = load().dsa_sparse_mla_attend_static(geom.ref, kv_dtype, H, _dptr(q), _dptr(kv_cache), _dptr(idx),
                                              int(k), float(sm_scale), _dptr(out), _dptr(lse),

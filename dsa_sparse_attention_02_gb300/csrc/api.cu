@@ -70,7 +70,6 @@ namespace {
 
 constexpr size_t kHeaderBytes = 256;
 constexpr int kMaxTopk = 16384;
-constexpr int kTopkCap = 16384;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -87,6 +86,10 @@ int num_sms() {
   return n;
 }
 
+}  // namespace
+
+namespace dsa {
+
 dsa_status_t check_geom(const dsa_geom_t* g) {
   if (!g) return DSA_ERR_INVALID_ARG;
   if (g->B < 0 || g->T < 0 || g->max_seq_len < 1 || g->num_pages < 1) return DSA_ERR_INVALID_ARG;
@@ -97,6 +100,24 @@ dsa_status_t check_geom(const dsa_geom_t* g) {
   if (g->B > 0 && (!g->seq_lens || !g->cu_q || !g->block_table)) return DSA_ERR_INVALID_ARG;
   return DSA_OK;
 }
+
+dsa_status_t check_attend(const dsa_geom_t* g, dsa_dtype_t dt, int H, const void* q, const void* kv, const int* idx,
+                          int k, float sm_scale, const void* out) {
+  dsa_status_t s = check_geom(g);
+  if (s != DSA_OK) return s;
+  if (dt != DSA_BF16 && dt != DSA_E4M3 && dt != DSA_I8) return DSA_ERR_INVALID_ARG;
+  if (H < 1 || H > 128 || (H > 16 && H % 16 != 0)) return DSA_ERR_INVALID_ARG;
+  if (k < 1 || k > kMaxTopk) return DSA_ERR_INVALID_ARG;
+  if (!std::isfinite(sm_scale)) return DSA_ERR_INVALID_ARG;
+  if (g->T == 0) return DSA_OK;
+  if (!q || !kv || !idx || !out) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv)) return DSA_ERR_INVALID_ARG;
+  return DSA_OK;
+}
+
+}  // namespace dsa
+
+namespace {
 
 GeomDev to_dev(const dsa_geom_t* g) {
   GeomDev d;
@@ -117,8 +138,7 @@ dsa_status_t check_indexer(const dsa_geom_t* g, dsa_dtype_t dt, int Hi, const vo
   dsa_status_t s = check_geom(g);
   if (s != DSA_OK) return s;
   if (dt != DSA_BF16 && dt != DSA_E4M3) return DSA_ERR_INVALID_ARG;
-  if (Hi < 4 || Hi > 64 || Hi % 4 != 0) return DSA_ERR_INVALID_ARG;
-  if (g->B > indexer_max_requests()) return DSA_ERR_UNSUPPORTED;
+  if (Hi < 1 || Hi > 64) return DSA_ERR_INVALID_ARG;
   if (stride < g->max_seq_len) return DSA_ERR_INVALID_ARG;
   if (g->T == 0) return DSA_OK;
   if (!q_idx || !w || !kc || !scores) return DSA_ERR_INVALID_ARG;
@@ -129,9 +149,13 @@ dsa_status_t check_indexer(const dsa_geom_t* g, dsa_dtype_t dt, int Hi, const vo
   return DSA_OK;
 }
 
+// Scores of keys [key_begin, key_end) (multiples of 128; key_end past every length for
+// all keys) into column s - key_begin of `scores`. The kernel holds the metadata of up
+// to indexer_max_requests() requests; more are scored in groups of that many, one
+// launch each (query rows stay absolute: each group's cu_q entries index them).
 dsa_status_t run_indexer(const dsa_geom_t* g, dsa_dtype_t dt, int Hi, const void* q_idx, const float* q_scale,
                          const float* w, const void* kc, const float* ks, float* scores, int64_t stride, int* err,
-                         cudaStream_t st) {
+                         cudaStream_t st, int key_begin = 0, int key_end = INT32_MAX) {
   const bool fp8 = dt == DSA_E4M3;
   CUtensorMap mk, mq;
   const CUtensorMapDataType tdt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -140,10 +164,22 @@ dsa_status_t run_indexer(const dsa_geom_t* g, dsa_dtype_t dt, int Hi, const void
   if (!encode_tensor_map_2d(&mk, tdt, kc, 128, (uint64_t)g->num_pages * 64, row_bytes, box_cols, 64)) return DSA_ERR_CUDA;
   if (!encode_tensor_map_2d(&mq, tdt, q_idx, 128, (uint64_t)g->T * Hi, row_bytes, box_cols, (uint32_t)Hi)) return DSA_ERR_CUDA;
   IndexerArgs A;
-  A.g = to_dev(g); A.Hi = Hi; A.q_scale = q_scale; A.w = w; A.k_scale = ks; A.scores = scores; A.stride = stride;
+  A.Hi = Hi; A.q_scale = q_scale; A.w = w; A.k_scale = ks; A.scores = scores; A.stride = stride;
+  A.key_begin = key_begin; A.key_end = key_end;
   A.err = err;
   const bool multi = g->T > g->B;   // some request has more than one query token
-  return from_cuda(indexer_launch(fp8, Hi, multi, mk, mq, A, num_sms(), st));
+  const int group = indexer_max_requests();
+  for (int b0 = 0; b0 < g->B; b0 += group) {
+    dsa_geom_t sub = *g;
+    sub.B = g->B - b0 < group ? g->B - b0 : group;
+    sub.seq_lens = g->seq_lens + b0;
+    sub.cu_q = g->cu_q + b0;
+    sub.block_table = g->block_table + (int64_t)b0 * g->bt_stride;
+    A.g = to_dev(&sub);
+    const dsa_status_t s = from_cuda(indexer_launch(fp8, Hi, multi, mk, mq, A, num_sms(), st));
+    if (s != DSA_OK) return s;
+  }
+  return DSA_OK;
 }
 
 // ---------------------------------------------------------------- top-k
@@ -152,9 +188,9 @@ dsa_status_t check_topk(const dsa_geom_t* g, const float* scores, int64_t stride
   if (s != DSA_OK) return s;
   if (k < 1 || k > kMaxTopk) return DSA_ERR_INVALID_ARG;
   if (stride < g->max_seq_len) return DSA_ERR_INVALID_ARG;
-  if (g->max_seq_len > kTopkCap) {
-    const int64_t nch = (g->max_seq_len + kTopkCap - 1) / kTopkCap;
-    if (nch * k > kTopkCap) return DSA_ERR_UNSUPPORTED;
+  if (topk_merge_levels(g->max_seq_len, k) < 0) {
+    set_last_error("dsa_topk", "rows longer than 16384 positions need index_topk <= 8192");
+    return DSA_ERR_UNSUPPORTED;
   }
   if (g->T == 0) return DSA_OK;
   if (!scores || !idx) return DSA_ERR_INVALID_ARG;
@@ -162,20 +198,6 @@ dsa_status_t check_topk(const dsa_geom_t* g, const float* scores, int64_t stride
 }
 
 // ---------------------------------------------------------------- attention
-dsa_status_t check_attend(const dsa_geom_t* g, dsa_dtype_t dt, int H, const void* q, const void* kv, const int* idx,
-                          int k, float sm_scale, const void* out) {
-  dsa_status_t s = check_geom(g);
-  if (s != DSA_OK) return s;
-  if (dt != DSA_BF16 && dt != DSA_E4M3 && dt != DSA_I8) return DSA_ERR_INVALID_ARG;
-  if (H < 1 || H > 128 || (H > 16 && H % 16 != 0)) return DSA_ERR_INVALID_ARG;
-  if (k < 1 || k > kMaxTopk) return DSA_ERR_INVALID_ARG;
-  if (!std::isfinite(sm_scale)) return DSA_ERR_INVALID_ARG;
-  if (g->T == 0) return DSA_OK;
-  if (!q || !kv || !idx || !out) return DSA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(kv)) return DSA_ERR_INVALID_ARG;
-  return DSA_OK;
-}
-
 size_t attend_scratch_bytes(const dsa_geom_t* g, int H, int k) {
   const int64_t C = (k + 127) / 128;
   const int grid = mla_grid((int64_t)g->T * C, num_sms());
@@ -275,16 +297,29 @@ dsa_status_t dsa_sparse_mla_attend(const dsa_geom_t* geom, dsa_dtype_t kv_dtype,
 
 namespace {
 
-// Workspace of the step when at most `rows` queries' scores are held at a time
-// (rows >= T: all at once). Layout: header | query-range geometry (chunked only) |
-// scores [rows, stride] | idx [T, k] (unless idx_out) | attention / top-k scratch.
-size_t step_workspace_bytes(const dsa_step_args_t* a, int64_t rows) {
+// How the step holds its scores: `rows` queries at a time (rows >= T: all at once),
+// each over keys in spans of `span` positions (0: whole rows). A span is a multiple
+// of the top-k chunk length, so every chunk of a row is scored within one span.
+struct ScorePlan {
+  int64_t rows;
+  int64_t span;
+};
+
+ScorePlan whole_rows(const dsa_step_args_t* a) { return ScorePlan{a->geom.T, 0}; }
+
+// Width of the score buffer's rows.
+int64_t plan_width(const dsa_geom_t* g, const ScorePlan& p) { return p.span > 0 ? p.span : step_score_stride(g); }
+
+// Workspace of the step under a score plan. Layout: header | query-range geometry
+// (ranges only) | scores [rows, width] | idx [T, k] (unless idx_out) | attention /
+// top-k scratch.
+size_t step_workspace_bytes(const dsa_step_args_t* a, const ScorePlan& p) {
   const dsa_geom_t* g = &a->geom;
   size_t bytes = kHeaderBytes;
-  const int64_t r = rows < g->T ? rows : g->T;
+  const int64_t r = p.rows < g->T ? p.rows : g->T;
   if (!a->reuse_idx) {
     if (r < g->T) bytes += align_up((size_t)(2 * g->B + 1) * sizeof(int32_t), 256);
-    bytes += align_up((size_t)r * step_score_stride(g) * sizeof(float), 256);
+    bytes += align_up((size_t)r * plan_width(g, p) * sizeof(float), 256);
     if (!a->idx_out) bytes += align_up((size_t)g->T * (a->topk > 0 ? a->topk : 1) * sizeof(int32_t), 256);
   }
   size_t scratch = attend_scratch_bytes(g, a->H > 0 ? a->H : 1, a->topk > 0 ? a->topk : 1);
@@ -295,62 +330,89 @@ size_t step_workspace_bytes(const dsa_step_args_t* a, int64_t rows) {
   return bytes + align_up(scratch, 256);
 }
 
-// The step with the queries' scores computed and reduced to their selection `rows`
-// queries at a time (the selection of each query does not depend on the others', so
-// the result is the same for every rows >= 1).
-dsa_status_t run_step(const dsa_step_args_t* a, int64_t rows, void* ws, size_t ws_bytes, void* stream,
+// Scores and selects one range of queries (geometry `sub`, whose rows are the step's
+// rows t0.. onward) into idx_out: the whole rows at once, or span by span, each
+// span's chunks reduced to candidate lists before the next span is scored.
+dsa_status_t select_range(const dsa_step_args_t* a, const dsa_geom_t* sub, int64_t t0, const ScorePlan& p,
+                          float* scores, int32_t* idx_out, void* scratch, int* err, cudaStream_t st) {
+  const dsa_geom_t* g = &a->geom;
+  const size_t qrow = (size_t)a->Hi * 128 * (a->qk_dtype == DSA_E4M3 ? 1 : 2);
+  const uint8_t* q_idx = reinterpret_cast<const uint8_t*>(a->q_idx) + (size_t)t0 * qrow;
+  const float* q_scale = a->q_scale ? a->q_scale + (size_t)t0 * a->Hi : nullptr;
+  const float* w = a->w + (size_t)t0 * a->Hi;
+  dsa_status_t s;
+  if (p.span == 0) {
+    const int64_t stride = step_score_stride(g);
+    s = run_indexer(sub, a->qk_dtype, a->Hi, q_idx, q_scale, w, a->idx_k_cache, a->idx_k_scale, scores, stride, err, st);
+    if (s != DSA_OK) return s;
+    // The top-k kernels follow this call's own kernels, so they may launch early
+    // (programmatic dependent launch) and wait for their inputs inside.
+    return from_cuda(topk_launch(to_dev(sub), scores, stride, a->topk, idx_out, scratch, err, true, st));
+  }
+  const int chunk = topk_chunk_len();
+  const int nch = (g->max_seq_len + chunk - 1) / chunk;
+  const int per_span = (int)(p.span / chunk);
+  for (int c0 = 0; c0 < nch; c0 += per_span) {
+    const int nl = nch - c0 < per_span ? nch - c0 : per_span;
+    const int64_t k0 = (int64_t)c0 * chunk;
+    s = run_indexer(sub, a->qk_dtype, a->Hi, q_idx, q_scale, w, a->idx_k_cache, a->idx_k_scale, scores, p.span, err,
+                    st, (int)k0, (int)(k0 + p.span < INT32_MAX ? k0 + p.span : INT32_MAX));
+    if (s != DSA_OK) return s;
+    s = from_cuda(topk_chunks_launch(to_dev(sub), scores, p.span, a->topk, c0, nl, scratch, err, true, st));
+    if (s != DSA_OK) return s;
+  }
+  return from_cuda(topk_merge_launch(to_dev(sub), a->topk, idx_out, scratch, err, true, st));
+}
+
+// The step with the queries' scores held as the plan says (the selection of each
+// query does not depend on the others', and a span's chunk lists are those the whole
+// row gives, so the result is the same for every plan).
+dsa_status_t run_step(const dsa_step_args_t* a, const ScorePlan& p, void* ws, size_t ws_bytes, void* stream,
                       cudaEvent_t q_ready = nullptr) {
   const dsa_geom_t* g = &a->geom;
-  const int64_t stride = step_score_stride(g);
   dsa_status_t s;
   if (!a->reuse_idx) {
     s = check_indexer(g, a->qk_dtype, a->Hi, a->q_idx, a->q_scale, a->w, a->idx_k_cache, a->idx_k_scale,
-                      reinterpret_cast<const float*>(ws), stride);
+                      reinterpret_cast<const float*>(ws), step_score_stride(g));
     if (s != DSA_OK) return s;
-    s = check_topk(g, reinterpret_cast<const float*>(ws), stride, a->topk, reinterpret_cast<const int*>(ws));
+    s = check_topk(g, reinterpret_cast<const float*>(ws), step_score_stride(g), a->topk, reinterpret_cast<const int*>(ws));
     if (s != DSA_OK) return s;
   }
   s = check_attend(g, a->kv_dtype, a->H, a->q, a->kv_cache, a->reuse_idx ? a->reuse_idx : reinterpret_cast<const int*>(ws),
                    a->topk, a->sm_scale, a->out);
   if (s != DSA_OK) return s;
-  if (!ws || ws_bytes < step_workspace_bytes(a, rows) || (reinterpret_cast<uintptr_t>(ws) & 255u))
+  if (!ws || ws_bytes < step_workspace_bytes(a, p) || (reinterpret_cast<uintptr_t>(ws) & 255u))
     return DSA_ERR_WORKSPACE;
   if (g->T == 0) return DSA_OK;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  uint8_t* p = reinterpret_cast<uint8_t*>(ws);
+  uint8_t* ptr = reinterpret_cast<uint8_t*>(ws);
   int* err = reinterpret_cast<int*>(ws);
-  p += kHeaderBytes;
+  ptr += kHeaderBytes;
   const int32_t* idx = a->reuse_idx;
   if (!idx) {
-    const bool chunked = rows < g->T;
+    const bool ranges = p.rows < g->T;
     int32_t* range_geom = nullptr;
-    if (chunked) {
-      range_geom = reinterpret_cast<int32_t*>(p);
-      p += align_up((size_t)(2 * g->B + 1) * sizeof(int32_t), 256);
+    if (ranges) {
+      range_geom = reinterpret_cast<int32_t*>(ptr);
+      ptr += align_up((size_t)(2 * g->B + 1) * sizeof(int32_t), 256);
     }
-    const int64_t r = chunked ? rows : g->T;
-    float* scores = reinterpret_cast<float*>(p);
-    p += align_up((size_t)r * stride * sizeof(float), 256);
+    const int64_t r = ranges ? p.rows : g->T;
+    float* scores = reinterpret_cast<float*>(ptr);
+    ptr += align_up((size_t)r * plan_width(g, p) * sizeof(float), 256);
     int32_t* idx_buf = a->idx_out;
     if (!idx_buf) {
-      idx_buf = reinterpret_cast<int32_t*>(p);
-      p += align_up((size_t)g->T * a->topk * sizeof(int32_t), 256);
+      idx_buf = reinterpret_cast<int32_t*>(ptr);
+      ptr += align_up((size_t)g->T * a->topk * sizeof(int32_t), 256);
     }
-    if (!chunked) {
-      s = run_indexer(g, a->qk_dtype, a->Hi, a->q_idx, a->q_scale, a->w, a->idx_k_cache, a->idx_k_scale, scores,
-                      stride, err, st);
-      if (s != DSA_OK) return s;
-      // The top-k and attention kernels follow this call's own kernels, so they may
-      // launch early (programmatic dependent launch) and wait for their inputs inside.
-      s = from_cuda(topk_launch(to_dev(g), scores, stride, a->topk, idx_buf, p, err, true, st));
+    if (!ranges) {
+      s = select_range(a, g, 0, p, scores, idx_buf, ptr, err, st);
       if (s != DSA_OK) return s;
     } else {
       // Bounded scoring: queries [t0, t0 + rows) at a time, each range described by
       // its own geometry (same requests, block table and positions), scored into the
       // same rows of `scores` and reduced to its selection before the next range.
-      const size_t qrow = (size_t)a->Hi * 128 * (a->qk_dtype == DSA_E4M3 ? 1 : 2);
-      for (int64_t t0 = 0; t0 < g->T; t0 += rows) {
-        const int t1 = (int)(t0 + rows < g->T ? t0 + rows : g->T);
+      for (int64_t t0 = 0; t0 < g->T; t0 += p.rows) {
+        const int t1 = (int)(t0 + p.rows < g->T ? t0 + p.rows : g->T);
         s = from_cuda(query_range_launch(g->cu_q, g->seq_lens, g->B, (int)t0, t1, range_geom,
                                          range_geom + g->B + 1, st));
         if (s != DSA_OK) return s;
@@ -358,12 +420,7 @@ dsa_status_t run_step(const dsa_step_args_t* a, int64_t rows, void* ws, size_t w
         sub.T = t1 - (int)t0;
         sub.cu_q = range_geom;
         sub.seq_lens = range_geom + g->B + 1;
-        s = run_indexer(&sub, a->qk_dtype, a->Hi, reinterpret_cast<const uint8_t*>(a->q_idx) + (size_t)t0 * qrow,
-                        a->q_scale ? a->q_scale + (size_t)t0 * a->Hi : nullptr, a->w + (size_t)t0 * a->Hi,
-                        a->idx_k_cache, a->idx_k_scale, scores, stride, err, st);
-        if (s != DSA_OK) return s;
-        s = from_cuda(topk_launch(to_dev(&sub), scores, stride, a->topk, idx_buf + (size_t)t0 * a->topk, p, err, true,
-                                  st));
+        s = select_range(a, &sub, t0, p, scores, idx_buf + (size_t)t0 * a->topk, ptr, err, st);
         if (s != DSA_OK) return s;
       }
     }
@@ -376,7 +433,7 @@ dsa_status_t run_step(const dsa_step_args_t* a, int64_t rows, void* ws, size_t w
     s = from_cuda(cudaStreamWaitEvent(st, q_ready, 0));
     if (s != DSA_OK) return s;
   }
-  return run_attend(g, a->kv_dtype, a->H, a->q, a->kv_cache, idx, a->topk, a->sm_scale, a->out, a->lse, p, err,
+  return run_attend(g, a->kv_dtype, a->H, a->q, a->kv_cache, idx, a->topk, a->sm_scale, a->out, a->lse, ptr, err,
                     a->reuse_idx == nullptr && q_ready == nullptr, st);
 }
 
@@ -386,43 +443,49 @@ extern "C" {
 
 size_t dsa_decode_step_workspace_size(const dsa_step_args_t* a) {
   if (!a) return kHeaderBytes;
-  return step_workspace_bytes(a, a->geom.T);
+  return step_workspace_bytes(a, whole_rows(a));
 }
 
 dsa_status_t dsa_decode_step(const dsa_step_args_t* a, void* ws, size_t ws_bytes, void* stream) {
   if (!a) return DSA_ERR_INVALID_ARG;
-  return run_step(a, a->geom.T, ws, ws_bytes, stream);
+  return run_step(a, whole_rows(a), ws, ws_bytes, stream);
 }
 
 dsa_status_t dsa_decode_step_wait_q(const dsa_step_args_t* a, void* q_ready, void* ws, size_t ws_bytes, void* stream) {
   if (!a) return DSA_ERR_INVALID_ARG;
-  return run_step(a, a->geom.T, ws, ws_bytes, stream, reinterpret_cast<cudaEvent_t>(q_ready));
+  return run_step(a, whole_rows(a), ws, ws_bytes, stream, reinterpret_cast<cudaEvent_t>(q_ready));
 }
 
-// Queries whose scores fit the budget at once; 0 if not even one does.
-static int64_t bounded_rows(const dsa_step_args_t* a, size_t score_budget_bytes) {
+// The score plan a budget allows: as many whole rows as fit; below one row, one query
+// at a time over spans of whole top-k chunks. rows == 0: not even one chunk fits.
+static ScorePlan bounded_plan(const dsa_step_args_t* a, size_t score_budget_bytes) {
   const size_t row = (size_t)step_score_stride(&a->geom) * sizeof(float);
-  return row > 0 ? (int64_t)(score_budget_bytes / row) : 0;
+  if (score_budget_bytes >= row) return ScorePlan{(int64_t)(score_budget_bytes / row), 0};
+  const size_t chunk = (size_t)topk_chunk_len();
+  const int64_t span = (int64_t)(score_budget_bytes / (chunk * sizeof(float)) * chunk);
+  return span > 0 ? ScorePlan{1, span} : ScorePlan{0, 0};
 }
 
 size_t dsa_decode_step_bounded_workspace_size(const dsa_step_args_t* a, size_t score_budget_bytes) {
   if (!a) return kHeaderBytes;
-  const int64_t rows = bounded_rows(a, score_budget_bytes);
-  return step_workspace_bytes(a, rows < 1 ? 1 : rows);
+  const ScorePlan p = bounded_plan(a, score_budget_bytes);
+  return step_workspace_bytes(a, p.rows < 1 ? ScorePlan{1, 0} : p);
 }
 
 dsa_status_t dsa_decode_step_bounded(const dsa_step_args_t* a, size_t score_budget_bytes, void* ws, size_t ws_bytes,
                                      void* stream) {
   if (!a) return DSA_ERR_INVALID_ARG;
-  const int64_t rows = bounded_rows(a, score_budget_bytes);
-  if (rows < 1 && !a->reuse_idx) {
-    char buf[160];
-    snprintf(buf, sizeof(buf), "score budget %zu bytes is below one query's score row (%zu bytes)",
-             score_budget_bytes, (size_t)step_score_stride(&a->geom) * sizeof(float));
+  const ScorePlan p = bounded_plan(a, score_budget_bytes);
+  if (p.rows < 1 && !a->reuse_idx) {
+    char buf[192];
+    snprintf(buf, sizeof(buf),
+             "score budget %zu bytes holds neither one query's score row (%zu bytes) nor one top-k chunk (%zu bytes)",
+             score_budget_bytes, (size_t)step_score_stride(&a->geom) * sizeof(float),
+             (size_t)topk_chunk_len() * sizeof(float));
     set_last_error("dsa_decode_step_bounded", buf);
     return DSA_ERR_INVALID_ARG;
   }
-  return run_step(a, rows < 1 ? 1 : rows, ws, ws_bytes, stream);
+  return run_step(a, p.rows < 1 ? ScorePlan{1, 0} : p, ws, ws_bytes, stream);
 }
 
 size_t dsa_cache_append_workspace_size(const dsa_geom_t*) { return kHeaderBytes; }

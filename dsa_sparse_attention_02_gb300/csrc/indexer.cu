@@ -89,7 +89,8 @@ struct UnitInfo {
 
 template <int kQG>
 // prefix, cuq and lens are shared-memory copies of the unit prefix, cu_q and seq_lens.
-__device__ __forceinline__ UnitInfo decode_unit(const int* prefix, const int* cuq, const int* lens, int B, int u) {
+__device__ __forceinline__ UnitInfo decode_unit(const int* prefix, const int* cuq, const int* lens, int B, int tile0,
+                                                int u) {
   int lo = 0, hi = B - 1;
   while (lo < hi) {  // last b with prefix[b] <= u
     const int mid = (lo + hi + 1) >> 1;
@@ -101,8 +102,9 @@ __device__ __forceinline__ UnitInfo decode_unit(const int* prefix, const int* cu
   const int nq = q1 - q0;
   const int ngroups = (nq + kQG - 1) / kQG;
   const int local = u - prefix[lo];
-  ui.tile = local / ngroups;
-  const int grp = local - ui.tile * ngroups;
+  const int lt = local / ngroups;
+  const int grp = local - lt * ngroups;
+  ui.tile = tile0 + lt;
   ui.q_start = q0 + grp * kQG;
   ui.q_count = min(kQG, nq - grp * kQG);
   ui.len = lens[lo];
@@ -160,7 +162,7 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, Ind
         const int nq = q1 - q0;
         const bool ok = nq >= 0 && nq <= len && len <= g.max_seq_len && q1 <= g.T;
         if (!ok) record_error(A.err, kDevBadIndex);
-        else units = ((nq + kQG - 1) / kQG) * ((len + 127) / 128);
+        else units = ((nq + kQG - 1) / kQG) * max(0, (min(len, A.key_end) + 127) / 128 - A.key_begin / 128);
       }
       int incl = units;
 #pragma unroll
@@ -216,7 +218,7 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, Ind
       UnitInfo ui{};
       int pg0 = -1, pg1 = -1;
       if (u < u_end) {
-        ui = decode_unit<kQG>(prefix, cuq_s, lens_s, B, u);
+        ui = decode_unit<kQG>(prefix, cuq_s, lens_s, B, A.key_begin / 128, u);
         const int s0 = ui.tile * 128;
         const int* bt = g.block_table + (int64_t)ui.b * g.bt_stride;
         if (s0 < ui.len) pg0 = __ldg(bt + (s0 >> 6));
@@ -265,13 +267,30 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, Ind
             if (ok) {
               uint8_t* sl = q_slots + qs * C::kQSlotBytes;
               const uint32_t bar = smem_u32(&q_full[qs]);
-              mbar_arrive_expect_tx(bar, q_count * Hi * (128 * C::kAtoms + 4 + (kFp8 ? 4 : 0)));
+              // w and q_scale rows of Hi floats are bulk-copied when Hi * 4 is a multiple
+              // of 16 bytes; otherwise they go as 4-byte copies whose completion the barrier
+              // also tracks (that arrival is registered before the expect_tx arrival, so the
+              // phase cannot complete without them).
+              const bool vec = (Hi & 3) == 0;
+              if (!vec) {
+                for (int j = 0; j < q_count; ++j) {
+                  const int64_t t = q_start + j;
+                  for (int h = 0; h < Hi; ++h) {
+                    cp_async_4(smem_u32(sl + C::kWOff + (j * kHp + h) * 4), A.w + t * Hi + h, 4u);
+                    if (kFp8) cp_async_4(smem_u32(sl + C::kQsOff + (j * kHp + h) * 4), A.q_scale + t * Hi + h, 4u);
+                  }
+                }
+                cp_async_arrive(bar);
+              }
+              mbar_arrive_expect_tx(bar, q_count * Hi * (128 * C::kAtoms + (vec ? 4 + (kFp8 ? 4 : 0) : 0)));
               for (int j = 0; j < q_count; ++j) {
                 const int t = q_start + j;
                 for (int a = 0; a < C::kAtoms; ++a)
                   tma_load_2d(smem_u32(sl + a * (C::kN * 128) + j * kHp * 128), &map_q, bar, a * (kFp8 ? 128 : 64), t * Hi);
-                bulk_load(smem_u32(sl + C::kWOff + j * kHp * 4), A.w + (int64_t)t * Hi, Hi * 4, bar);
-                if (kFp8) bulk_load(smem_u32(sl + C::kQsOff + j * kHp * 4), A.q_scale + (int64_t)t * Hi, Hi * 4, bar);
+                if (vec) {
+                  bulk_load(smem_u32(sl + C::kWOff + j * kHp * 4), A.w + (int64_t)t * Hi, Hi * 4, bar);
+                  if (kFp8) bulk_load(smem_u32(sl + C::kQsOff + j * kHp * 4), A.q_scale + (int64_t)t * Hi, Hi * 4, bar);
+                }
               }
               ++qcount;
             }
@@ -386,7 +405,7 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, Ind
       if (!mbar_wait(smem_u32(&tfull_bar[acc]), (i / C::kAccs) & 1, &abort_flag, A.err)) break;
       tc_fence_after();
       const int sidx = d.tile * 128 + key;
-      const bool in_ctx = sidx < d.len;
+      const bool in_ctx = sidx < d.len && sidx < A.key_end;
 #pragma unroll 1
       for (int j = half; j < kQG; j += C::kEW) {
         if (j >= d.q_count) break;
@@ -413,7 +432,7 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, Ind
           const int t = d.q_start + j;
           const int pos = d.pos0 + j;
           const float out = (sidx <= pos && page >= 0) ? sum * ks : neg_inf;
-          A.scores[(int64_t)t * A.stride + sidx] = out;
+          A.scores[(int64_t)t * A.stride + (sidx - A.key_begin)] = out;
         }
       }
       tc_fence_before();

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include "common.cuh"
+#include "dsa.h"
 
 namespace dsa {
 
@@ -15,21 +16,35 @@ struct IndexerArgs {
   const float* q_scale;   // [T, Hi] or null (bf16)
   const float* w;         // [T, Hi]
   const float* k_scale;   // [P*64] or null (bf16)
-  float* scores;
+  float* scores;        // column s - key_begin of row t holds I[t, s]
   int64_t stride;
+  int key_begin;        // keys [key_begin, key_end) are scored; key_begin a multiple of 128
+  int key_end;          // a multiple of 128, or past every request's length
   int* err;
 };
 cudaError_t indexer_launch(bool fp8, int Hi, bool multi_query, const CUtensorMap& mk, const CUtensorMap& mq,
                            const IndexerArgs& A, int grid, cudaStream_t st);
-int indexer_max_requests();
+int indexer_max_requests();   // requests per launch (a call with more loops over groups)
 
 // ---- radix top-k (topk.cu)
+// Rows longer than topk_chunk_len() are cut into chunks of that length whose top-k
+// lists are merged topk_fan_in(k) at a time over topk_merge_levels() levels (-1: k
+// too large for rows that long).
+int topk_chunk_len();
+int topk_fan_in(int k);
+int topk_merge_levels(int max_seq_len, int k);
 size_t topk_workspace_bytes(int T, int max_seq_len, int k);
 // pdl: the launch may overlap the tail of the kernel just before it on the stream
 // (programmatic dependent launch); set only when that kernel is one of this library's
 // and the geometry was complete before it started.
 cudaError_t topk_launch(const GeomDev& g, const float* scores, int64_t stride, int k, int* idx,
                         void* scratch, int* err, bool pdl, cudaStream_t st);
+// The two halves of topk_launch for rows scored a key span at a time: the chunk pass
+// over chunks c0 .. c0+nl-1 of every row (scores: row t's key c0 * chunk_len at
+// scores + t * stride), writing their lists into scratch; then the merge levels.
+cudaError_t topk_chunks_launch(const GeomDev& g, const float* scores, int64_t stride, int k, int c0, int nl,
+                               void* scratch, int* err, bool pdl, cudaStream_t st);
+cudaError_t topk_merge_launch(const GeomDev& g, int k, int* idx, void* scratch, int* err, bool pdl, cudaStream_t st);
 
 // ---- sparse MLA + combine (sparse_mla.cu)
 struct MlaArgs {
@@ -102,6 +117,10 @@ struct PrepArgs {
 cudaError_t indexer_prep_launch(const PrepArgs& A, cudaStream_t st);
 
 // ---- host helpers defined in api.cu
+// Host-side argument checks shared by every entry point that takes these arguments.
+dsa_status_t check_geom(const dsa_geom_t* g);
+dsa_status_t check_attend(const dsa_geom_t* g, dsa_dtype_t dt, int H, const void* q, const void* kv, const int* idx,
+                          int k, float sm_scale, const void* out);
 bool encode_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t cols,
                           uint64_t rows, uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows);
 void set_last_error(const char* what, const char* detail);

@@ -45,8 +45,6 @@ cudaError_t scratch_address(void** out) {
   return cudaSuccess;
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 }  // namespace
 
 using namespace dsa;
@@ -55,17 +53,14 @@ extern "C" dsa_status_t dsa_sparse_mla_attend_static(const dsa_geom_t* geom, dsa
                                                      const void* q, const void* kv_cache, const int32_t* idx,
                                                      int32_t k, float sm_scale, void* out, float* lse,
                                                      int32_t* err_word, void* stream) {
-  if (!geom || geom->B < 0 || geom->T < 0 || geom->max_seq_len < 1 || geom->num_pages < 1) return DSA_ERR_INVALID_ARG;
-  if (geom->page_size != 64) return DSA_ERR_UNSUPPORTED;
-  if (geom->T > 0 && geom->B < 1) return DSA_ERR_INVALID_ARG;
-  if (geom->bt_stride < (geom->max_seq_len + 63) / 64) return DSA_ERR_INVALID_ARG;
-  if (kv_dtype != DSA_BF16 && kv_dtype != DSA_E4M3 && kv_dtype != DSA_I8) return DSA_ERR_INVALID_ARG;
-  if (H < 1 || H > 128 || (H > 16 && H % 16 != 0)) return DSA_ERR_INVALID_ARG;
-  if (k < 1 || k > 16384) return DSA_ERR_INVALID_ARG;
-  if (!std::isfinite(sm_scale)) return DSA_ERR_INVALID_ARG;
+  // the same argument rules as dsa_sparse_mla_attend
+  const dsa_status_t s = check_attend(geom, kv_dtype, H, q, kv_cache, idx, k, sm_scale, out);
+  if (s != DSA_OK) return s;
+  // A bounded wait that gives up stops the kernel before it writes its partial rows,
+  // and the merge then reads rows an earlier call left in the shared buffer: the
+  // error word is what reports that, so it is required here.
+  if (!err_word || (reinterpret_cast<uintptr_t>(err_word) & 3u)) return DSA_ERR_INVALID_ARG;
   if (geom->T == 0) return DSA_OK;
-  if (!geom->seq_lens || !geom->cu_q || !geom->block_table) return DSA_ERR_INVALID_ARG;
-  if (!q || !kv_cache || !idx || !out || !aligned16(q) || !aligned16(kv_cache)) return DSA_ERR_INVALID_ARG;
 
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)

@@ -14,12 +14,14 @@
 // `rem` equal ones by position (ties to the lower position). Output positions come
 // from one block-wide exclusive scan of every thread's (above, equal) counts, in
 // position order since each thread holds a contiguous run, so indices leave in
-// ascending order.
+// ascending order. A segment with no more valid entries than k keeps all of them.
 //
-// Rows longer than one CTA's capacity are split into chunks whose exact top-k
-// (with their keys) become candidates; a second pass over the concatenated
-// candidates, which are in ascending original position, gives the row's top-k.
-// Any element of the row's top-k is in its chunk's top-k, so this is exact.
+// Rows longer than one CTA's capacity are cut into chunks of 16384 positions whose
+// exact top-k (with their keys) become candidate lists. Lists are then merged in
+// groups of floor(16384 / k), level after level, until one list remains: a group's
+// lists are concatenated in chunk order, so its candidates stay in ascending
+// position and ties still go to the lower position. Any element of the row's top-k
+// is in the top-k of every group that contains it, so every level is exact.
 #include <cstdint>
 #include "kernels.cuh"
 
@@ -35,19 +37,27 @@ __device__ __forceinline__ uint32_t orderable_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Modes of one launch:
+//   kDirect: score rows (<= 16384 long) -> final idx
+//   kChunks: chunks c0 .. c0+nl-1 of every row -> candidate lists (key, position)
+//   kMerge:  groups of `fan` candidate lists -> lists (n_out > 1) or final idx (n_out == 1)
+enum : int { kDirect = 0, kChunks = 1, kMerge = 2 };
+
 struct TopkLaunch {
   GeomDev g;
   int k;
-  int mode;                // 0: scores -> final idx; 1: scores chunk -> candidates; 2: candidates -> final idx
-  const float* scores;     // modes 0, 1
+  int mode;
+  const float* scores;           // kDirect, kChunks (key c0*chunk of each row for kChunks)
   int64_t score_stride;
-  int chunk;               // mode 1: chunk length; mode 2: unused
-  int nchunks;             // mode 1: chunks per row; mode 2: candidate chunks per row (row len = nchunks*k)
-  const uint32_t* cand_key_in;   // mode 2
-  const int* cand_idx_in;        // mode 2
-  uint32_t* cand_key_out;        // mode 1
-  int* cand_idx_out;             // mode 1
-  int* idx_out;                  // modes 0, 2: [T, k]
+  int chunk;                     // kChunks: chunk length
+  int c0, nl;                    // kChunks: first chunk of the launch, chunks per row in it
+  int nchunks;                   // kChunks: chunks per row (layout of the candidate lists)
+  int n_in, fan, n_out;          // kMerge: lists per row in, lists merged per group, lists per row out
+  const uint32_t* cand_key_in;   // kMerge
+  const int* cand_idx_in;        // kMerge
+  uint32_t* cand_key_out;        // kChunks, kMerge with n_out > 1
+  int* cand_idx_out;
+  int* idx_out;                  // kDirect, kMerge with n_out == 1: [T, k]
   int* err;
 };
 
@@ -57,10 +67,11 @@ struct TopkShared {
   int sel_bin, sel_above, sel_cnt;
   int ncand;     // candidates appended so far
   int total;     // block total of the last scan
+  int count;     // results of the segment: min(k, valid entries)
 };
 
-// Exclusive scan over the block of one int per thread (block total in *total).
-__device__ __forceinline__ int topk_block_scan(int v, TopkShared& S, int* total) {
+// Exclusive scan over the block of one int per thread (block total in S.total).
+__device__ __forceinline__ int topk_block_scan(int v, TopkShared& S) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int incl = v;
 #pragma unroll
@@ -82,20 +93,20 @@ __device__ __forceinline__ int topk_block_scan(int v, TopkShared& S, int* total)
     if (lane == 31) S.total = iw;
   }
   __syncthreads();
-  if (total) *total = S.total;
   return S.wsum[warp] + incl - v;
 }
 
 // From the histogram S.hist[0..nb), highest bin first, find the bin holding the
 // rem-th largest counted key: sel_bin, sel_above (count above it), sel_cnt. Thread t
-// owns bins nb-1-2t and nb-2-2t.
+// owns bins nb-1-2t and nb-2-2t. If fewer than rem keys are counted, sel_cnt stays
+// -1 and S.total holds their number.
 __device__ __forceinline__ void topk_find_bin(TopkShared& S, int nb, int rem) {
   const int tid = threadIdx.x;
   const int hi_bin = nb - 1 - 2 * tid;
   const int c0 = hi_bin >= 0 ? S.hist[hi_bin] : 0;
   const int c1 = hi_bin - 1 >= 0 ? S.hist[hi_bin - 1] : 0;
   const int own = c0 + c1;
-  const int excl = topk_block_scan(own, S, nullptr);
+  const int excl = topk_block_scan(own, S);
   if (own > 0 && excl < rem && rem <= excl + own) {
     if (excl + c0 >= rem) { S.sel_bin = hi_bin; S.sel_above = excl; S.sel_cnt = c0; }
     else { S.sel_bin = hi_bin - 1; S.sel_above = excl + c0; S.sel_cnt = c1; }
@@ -103,9 +114,21 @@ __device__ __forceinline__ void topk_find_bin(TopkShared& S, int nb, int rem) {
   __syncthreads();
 }
 
-// The selection proper over a segment whose n (> k) entries are spread as runs of
-// CNT per thread. cand: shared array of at least min(n, capacity) keys.
-template <int CNT>
+// Appends key to the shared candidate list (warp-aggregated: one atomic per warp).
+__device__ __forceinline__ void topk_append(bool take, uint32_t key, TopkShared& S, uint32_t* cand) {
+  const int lane = threadIdx.x & 31;
+  const unsigned m = __ballot_sync(0xffffffffu, take);
+  if (m == 0u) return;
+  int base = 0;
+  if (lane == __ffs(m) - 1) base = atomicAdd(&S.ncand, __popc(m));
+  base = __shfl_sync(0xffffffffu, base, __ffs(m) - 1);
+  if (take) cand[base + __popc(m & ((1u << lane) - 1u))] = key;
+}
+
+// The selection proper over a segment of n (> k) entries spread as runs of CNT per
+// thread; entries whose valid bit is clear take no part. cand: shared array of at
+// least min(n, capacity) keys. Writes min(k, valid entries) results then -1 padding.
+template <int CNT, int MODE>
 __device__ __forceinline__ void topk_select(const TopkLaunch& L, int n, int64_t in_base, int64_t out_base,
                                             int idx_offset, TopkShared& S, uint32_t* cand, int* out_s,
                                             uint32_t* key_s) {
@@ -114,7 +137,7 @@ __device__ __forceinline__ void topk_select(const TopkLaunch& L, int n, int64_t 
   const int e0 = tid * CNT;
   uint32_t key[CNT];
   uint32_t valid = 0;
-  if (L.mode != 2 && e0 + CNT <= n && ((reinterpret_cast<uintptr_t>(L.scores + in_base) & 15) == 0)) {
+  if (MODE != kMerge && e0 + CNT <= n && ((reinterpret_cast<uintptr_t>(L.scores + in_base) & 15) == 0)) {
     const float4* src = reinterpret_cast<const float4*>(L.scores + in_base + e0);
 #pragma unroll
     for (int q = 0; q < CNT / 4; ++q) {
@@ -122,14 +145,14 @@ __device__ __forceinline__ void topk_select(const TopkLaunch& L, int n, int64_t 
       key[4 * q] = orderable_key(v.x); key[4 * q + 1] = orderable_key(v.y);
       key[4 * q + 2] = orderable_key(v.z); key[4 * q + 3] = orderable_key(v.w);
     }
-    valid = (CNT == 32) ? 0xffffffffu : ((1u << CNT) - 1u);
+    valid = (1u << CNT) - 1u;
   } else {
 #pragma unroll
     for (int i = 0; i < CNT; ++i) {
       const int e = e0 + i;
       key[i] = 0u;
       if (e < n) {
-        if (L.mode == 2) {
+        if (MODE == kMerge) {
           key[i] = L.cand_key_in[in_base + e];
           if (L.cand_idx_in[in_base + e] >= 0) valid |= 1u << i;
         } else {
@@ -149,44 +172,54 @@ __device__ __forceinline__ void topk_select(const TopkLaunch& L, int n, int64_t 
     if ((valid >> i) & 1u) atomicAdd(&S.hist[key[i] >> 21], 1);
   __syncthreads();
   topk_find_bin(S, 2048, k);
-  int rem = k - S.sel_above;
-  uint32_t prefix = (uint32_t)S.sel_bin << 21, pmask = 0xFFE00000u;
-  if (S.sel_cnt != rem) {
-    // ---- the keys of the threshold bin become a short candidate list; the lower
-    // 21 bits are resolved over that list only (bits 10-20, then 0-9)
-    const int ncand0 = S.sel_cnt;
-    __syncthreads();   // every thread has read sel_* before they are reset
-    if (tid == 0) S.ncand = 0;
-    for (int j = tid; j < 2048; j += kTopkThreads) S.hist[j] = 0;
-    __syncthreads();
-#pragma unroll
-    for (int i = 0; i < CNT; ++i) {
-      if (((valid >> i) & 1u) && (key[i] & pmask) == prefix) {
-        const int at = atomicAdd(&S.ncand, 1);
-        cand[at] = key[i];
-        atomicAdd(&S.hist[(key[i] >> 10) & 2047u], 1);
-      }
-    }
-    if (tid == 0) { S.sel_bin = 0; S.sel_above = 0; S.sel_cnt = -1; }
-    __syncthreads();
-    topk_find_bin(S, 2048, rem);
-    rem -= S.sel_above;
-    prefix |= (uint32_t)S.sel_bin << 10;
-    pmask |= 0x001FFC00u;
+  int rem;
+  uint32_t prefix, pmask;
+  if (S.sel_cnt < 0) {
+    // no more valid entries than k: every one of them is taken
+    rem = S.total;
+    prefix = 0u;
+    pmask = 0u;
+    if (tid == 0) S.count = rem;
+  } else {
+    if (tid == 0) S.count = k;
+    rem = k - S.sel_above;
+    prefix = (uint32_t)S.sel_bin << 21;
+    pmask = 0xFFE00000u;
     if (S.sel_cnt != rem) {
+      // ---- the keys of the threshold bin become a short candidate list; the lower
+      // 21 bits are resolved over that list only (bits 10-20, then 0-9)
+      const int ncand0 = S.sel_cnt;
+      __syncthreads();   // every thread has read sel_* before they are reset
+      if (tid == 0) S.ncand = 0;
+      for (int j = tid; j < 2048; j += kTopkThreads) S.hist[j] = 0;
       __syncthreads();
-      for (int j = tid; j < 1024; j += kTopkThreads) S.hist[j] = 0;
+#pragma unroll
+      for (int i = 0; i < CNT; ++i) {
+        const bool in_bin = ((valid >> i) & 1u) && (key[i] & pmask) == prefix;
+        topk_append(in_bin, key[i], S, cand);
+        if (in_bin) atomicAdd(&S.hist[(key[i] >> 10) & 2047u], 1);
+      }
       if (tid == 0) { S.sel_bin = 0; S.sel_above = 0; S.sel_cnt = -1; }
       __syncthreads();
-      for (int c = tid; c < ncand0; c += kTopkThreads) {
-        const uint32_t kc = cand[c];
-        if ((kc & pmask) == prefix) atomicAdd(&S.hist[kc & 1023u], 1);
-      }
-      __syncthreads();
-      topk_find_bin(S, 1024, rem);
+      topk_find_bin(S, 2048, rem);
       rem -= S.sel_above;
-      prefix |= (uint32_t)S.sel_bin;
-      pmask = 0xFFFFFFFFu;
+      prefix |= (uint32_t)S.sel_bin << 10;
+      pmask |= 0x001FFC00u;
+      if (S.sel_cnt != rem) {
+        __syncthreads();
+        for (int j = tid; j < 1024; j += kTopkThreads) S.hist[j] = 0;
+        if (tid == 0) { S.sel_bin = 0; S.sel_above = 0; S.sel_cnt = -1; }
+        __syncthreads();
+        for (int c = tid; c < ncand0; c += kTopkThreads) {
+          const uint32_t kc = cand[c];
+          if ((kc & pmask) == prefix) atomicAdd(&S.hist[kc & 1023u], 1);
+        }
+        __syncthreads();
+        topk_find_bin(S, 1024, rem);
+        rem -= S.sel_above;
+        prefix |= (uint32_t)S.sel_bin;
+        pmask = 0xFFFFFFFFu;
+      }
     }
   }
 
@@ -200,7 +233,7 @@ __device__ __forceinline__ void topk_select(const TopkLaunch& L, int n, int64_t 
     if (((valid >> i) & 1u) && m > prefix) gt_bits |= 1u << i;
     if (((valid >> i) & 1u) && m == prefix) eq_bits |= 1u << i;
   }
-  const int excl = topk_block_scan((__popc(gt_bits) << 16) | __popc(eq_bits), S, nullptr);
+  const int excl = topk_block_scan((__popc(gt_bits) << 16) | __popc(eq_bits), S);
   int rg = excl >> 16, re = excl & 0xffff;
   if (gt_bits | eq_bits) {
 #pragma unroll
@@ -209,32 +242,46 @@ __device__ __forceinline__ void topk_select(const TopkLaunch& L, int n, int64_t 
       if (is_gt || (is_eq && re < rem)) {
         const int pos = rg + min(re, rem);
         const int e = e0 + i;
-        if (L.mode == 1) { out_s[pos] = idx_offset + e; key_s[pos] = key[i]; }
-        else if (L.mode == 0) out_s[pos] = e;
-        else out_s[pos] = L.cand_idx_in[in_base + e];
+        out_s[pos] = (MODE == kMerge) ? L.cand_idx_in[in_base + e] : idx_offset + e;
+        if (MODE != kDirect) key_s[pos] = key[i];
       }
       if (is_gt) ++rg;
       if (is_eq) ++re;
     }
   }
   __syncthreads();
-  if (L.mode == 1) {
-    for (int j = tid; j < k; j += kTopkThreads) {
-      L.cand_idx_out[out_base + j] = out_s[j];
-      L.cand_key_out[out_base + j] = key_s[j];
+  const bool lists = MODE == kChunks || (MODE == kMerge && L.n_out > 1);
+  const int count = S.count;
+  for (int j = tid; j < k; j += kTopkThreads) {
+    const bool v = j < count;
+    if (lists) {
+      L.cand_idx_out[out_base + j] = v ? out_s[j] : -1;
+      L.cand_key_out[out_base + j] = v ? key_s[j] : 0u;
+    } else {
+      L.idx_out[out_base + j] = v ? out_s[j] : -1;
     }
-  } else {
-    for (int j = tid; j < k; j += kTopkThreads) L.idx_out[out_base + j] = out_s[j];
   }
 }
 
+// Runs of 4, 8 or 16 entries per thread, whichever spreads the segment over the most threads.
+template <int MODE>
+__device__ __forceinline__ void topk_select_runs(const TopkLaunch& L, int n, int64_t in_base, int64_t out_base,
+                                                 int idx_offset, TopkShared& S, uint32_t* cand, int* out_s,
+                                                 uint32_t* key_s) {
+  if (n <= 4 * kTopkThreads) topk_select<4, MODE>(L, n, in_base, out_base, idx_offset, S, cand, out_s, key_s);
+  else if (n <= 8 * kTopkThreads) topk_select<8, MODE>(L, n, in_base, out_base, idx_offset, S, cand, out_s, key_s);
+  else topk_select<16, MODE>(L, n, in_base, out_base, idx_offset, S, cand, out_s, key_s);
+}
+
+template <int MODE>
 __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkLaunch L) {
   __shared__ TopkShared S;
-  __shared__ int row_len_s;
+  __shared__ int row_len_s, pos_s;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int t, c = 0;
-  if (L.mode == 1) { t = blockIdx.x / L.nchunks; c = blockIdx.x % L.nchunks; }
+  int t, c = 0, grp = 0;
+  if (MODE == kChunks) { t = blockIdx.x / L.nl; c = L.c0 + blockIdx.x % L.nl; }
+  else if (MODE == kMerge) { t = blockIdx.x / L.n_out; grp = blockIdx.x % L.n_out; }
   else t = blockIdx.x;
 
   // Row length from the geometry (an input of the call, not of the preceding
@@ -242,18 +289,14 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkLaunch 
   if (warp == 0) {
     const QueryInfo qi = query_info_warp(L.g, t);
     if (lane == 0) {
-      int n;
-      if (L.mode == 2) {
-        // A row with no more valid keys than k keeps all of them: its candidates are
-        // exactly positions 0..pos, so it takes the short path below with n = pos+1.
-        const int valid = qi.ok ? qi.pos + 1 : 0;
-        n = valid <= L.k ? valid : L.nchunks * L.k;
-      } else {
-        if (!qi.ok) { record_error(L.err, kDevBadIndex); n = 0; }
-        else n = qi.pos + 1;
-        if (L.mode == 1) n = max(0, min(L.chunk, n - c * L.chunk));
-      }
+      int n, pos = -1;
+      if (!qi.ok && MODE != kMerge) record_error(L.err, kDevBadIndex);
+      if (qi.ok) pos = qi.pos;
+      if (MODE == kMerge) n = min(L.fan, L.n_in - grp * L.fan) * L.k;
+      else if (MODE == kChunks) n = max(0, min(L.chunk, pos + 1 - c * L.chunk));
+      else n = pos + 1;
       row_len_s = n;
+      pos_s = pos;
     }
   }
   griddep_launch_dependents();
@@ -263,77 +306,93 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkLaunch 
   const int k = L.k;
 
   // Where the row's entries and outputs live.
-  const int64_t in_base = (L.mode == 0) ? (int64_t)t * L.score_stride
-                        : (L.mode == 1) ? (int64_t)t * L.score_stride + (int64_t)c * L.chunk
-                                        : (int64_t)t * L.nchunks * k;
-  const int64_t out_base = (L.mode == 1) ? ((int64_t)t * L.nchunks + c) * k : (int64_t)t * k;
-  const int idx_offset = (L.mode == 1) ? c * L.chunk : 0;
+  const int64_t in_base = (MODE == kDirect) ? (int64_t)t * L.score_stride
+                        : (MODE == kChunks) ? (int64_t)t * L.score_stride + (int64_t)(c - L.c0) * L.chunk
+                                              : ((int64_t)t * L.n_in + (int64_t)grp * L.fan) * k;
+  const int64_t out_base = (MODE == kChunks) ? ((int64_t)t * L.nchunks + c) * k
+                         : (MODE == kMerge && L.n_out > 1) ? ((int64_t)t * L.n_out + grp) * k
+                                                             : (int64_t)t * k;
+  const int idx_offset = (MODE == kChunks) ? c * L.chunk : 0;
 
+  if (MODE == kMerge && L.n_out == 1 && pos_s + 1 <= k) {
+    // every valid key is kept: positions 0..pos in order (no candidate is read)
+    for (int i = tid; i < k; i += kTopkThreads) L.idx_out[out_base + i] = i <= pos_s ? i : -1;
+    return;
+  }
   if (n <= k) {
-    // Everything valid is taken; positions are already ascending.
+    // Everything valid is taken; positions are already ascending (a single merged
+    // list is copied as it is: its valid entries come first).
     for (int i = tid; i < k; i += kTopkThreads) {
-      if (L.mode == 1) {
+      if (MODE == kChunks) {
         const bool v = i < n;
         L.cand_key_out[out_base + i] = v ? orderable_key(L.scores[in_base + i]) : 0u;
         L.cand_idx_out[out_base + i] = v ? idx_offset + i : -1;
-      } else if (L.mode == 0) {
+      } else if (MODE == kDirect) {
         L.idx_out[out_base + i] = i < n ? i : -1;
-      } else {  // mode 2: the first chunk's candidates are positions 0..n-1 in order
-        L.idx_out[out_base + i] = i < n ? L.cand_idx_in[in_base + i] : -1;
+      } else if (L.n_out > 1) {
+        L.cand_key_out[out_base + i] = L.cand_key_in[in_base + i];
+        L.cand_idx_out[out_base + i] = L.cand_idx_in[in_base + i];
+      } else {
+        L.idx_out[out_base + i] = L.cand_idx_in[in_base + i];
       }
     }
     return;
   }
-  // Dynamic shared memory: [k] staged output indices, [k] keys (mode 1), then the
+  // Dynamic shared memory: [k] staged output positions, [k] their keys, then the
   // candidate list of the threshold bin (at most n <= capacity keys).
   extern __shared__ int dyn_s[];
   int* out_s = dyn_s;
   uint32_t* key_s = reinterpret_cast<uint32_t*>(out_s + k);
-  uint32_t* cand = key_s + (L.mode == 1 ? k : 0);
-  // runs of 4, 8 or 16 entries per thread, whichever spreads the row over the most threads
-  if (n <= 4 * kTopkThreads) topk_select<4>(L, n, in_base, out_base, idx_offset, S, cand, out_s, key_s);
-  else if (n <= 8 * kTopkThreads) topk_select<8>(L, n, in_base, out_base, idx_offset, S, cand, out_s, key_s);
-  else topk_select<16>(L, n, in_base, out_base, idx_offset, S, cand, out_s, key_s);
+  uint32_t* cand = key_s + k;
+  topk_select_runs<MODE>(L, n, in_base, out_base, idx_offset, S, cand, out_s, key_s);
 }
 
-// Host-side launch sequence (called from the API layer). Returns a cudaError_t.
-struct TopkPlan {
-  int levels;      // 1: direct; 2: chunks + merge
-  int chunk;
-  int nchunks;
-};
+// ------------------------------------------------------------------ host side
+int topk_chunk_len() { return kTopkCapacity; }
 
-TopkPlan topk_plan(int max_seq_len, int k) {
-  TopkPlan p;
-  if (max_seq_len <= kTopkCapacity) { p.levels = 1; p.chunk = 0; p.nchunks = 1; return p; }
-  p.levels = 2;
-  p.chunk = kTopkCapacity;
-  p.nchunks = (max_seq_len + kTopkCapacity - 1) / kTopkCapacity;
-  return p;
+// Lists merged per group: as many whole lists of k as one CTA holds.
+int topk_fan_in(int k) { return kTopkCapacity / k; }
+
+// Merge levels after the chunk pass for rows of up to max_seq_len (0: no chunking).
+int topk_merge_levels(int max_seq_len, int k) {
+  if (max_seq_len <= kTopkCapacity) return 0;
+  const int fan = topk_fan_in(k);
+  if (fan < 2) return -1;
+  int lists = (max_seq_len + kTopkCapacity - 1) / kTopkCapacity, levels = 0;
+  while (lists > 1) { lists = (lists + fan - 1) / fan; ++levels; }
+  return levels;
+}
+
+// Candidate storage: the chunk pass's lists (buffer A), and the lists of the first
+// merge level when a second level follows (buffer B); later levels alternate.
+static size_t topk_list_bytes(int64_t T, int64_t lists, int k) {
+  return (size_t)(T * lists * k) * (sizeof(uint32_t) + sizeof(int));
 }
 
 size_t topk_workspace_bytes(int T, int max_seq_len, int k) {
-  const TopkPlan p = topk_plan(max_seq_len, k);
-  if (p.levels == 1) return 0;
-  return (size_t)T * p.nchunks * k * (sizeof(uint32_t) + sizeof(int));
+  const int levels = topk_merge_levels(max_seq_len, k);
+  if (levels <= 0) return 0;
+  const int64_t nch = (max_seq_len + kTopkCapacity - 1) / kTopkCapacity;
+  size_t bytes = (topk_list_bytes(T, nch, k) + 255) / 256 * 256;
+  if (levels >= 2) bytes += topk_list_bytes(T, (nch + topk_fan_in(k) - 1) / topk_fan_in(k), k);
+  return bytes;
 }
 
-// Dynamic shared memory of one launch: the staged outputs (indices, and keys in mode
-// 1) and the candidate keys of the threshold bin (at most one row segment's entries).
-static size_t topk_smem_bytes(const TopkLaunch& L, int seg_len) {
-  return (size_t)L.k * (L.mode == 1 ? 8 : 4) + (size_t)seg_len * 4;
-}
+// Dynamic shared memory of one launch: the staged outputs (positions and keys) and
+// the candidate keys of the threshold bin (at most one row segment's entries).
+static size_t topk_smem_bytes(int k, int seg_len) { return (size_t)k * 8 + (size_t)seg_len * 4; }
 
 static cudaError_t launch_topk_kernel(const TopkLaunch& L, int grid, int seg_len, bool pdl, cudaStream_t st) {
-  const size_t smem = topk_smem_bytes(L, seg_len);
+  const size_t smem = topk_smem_bytes(L.k, seg_len < kTopkCapacity ? seg_len : kTopkCapacity);
+  auto kern = L.mode == kDirect ? topk_kernel<kDirect> : L.mode == kChunks ? topk_kernel<kChunks> : topk_kernel<kMerge>;
   // the 48 KB default covers static and dynamic shared memory together
   if (smem + sizeof(TopkShared) + 64 > 48 * 1024) {
-    const cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
   // The attention kernel that follows needs the whole shared-memory carveout; an SM
   // left in the same configuration takes its CTAs without reconfiguring.
-  cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                                        (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute at[1];
@@ -345,25 +404,58 @@ static cudaError_t launch_topk_kernel(const TopkLaunch& L, int grid, int seg_len
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = at; cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, topk_kernel, L);
+  return cudaLaunchKernelEx(&cfg, kern, L);
+}
+
+cudaError_t topk_chunks_launch(const GeomDev& g, const float* scores, int64_t stride, int k, int c0, int nl,
+                               void* scratch, int* err, bool pdl, cudaStream_t st) {
+  const int nch = (g.max_seq_len + kTopkCapacity - 1) / kTopkCapacity;
+  TopkLaunch L{};
+  L.g = g; L.k = k; L.mode = kChunks; L.scores = scores; L.score_stride = stride; L.err = err;
+  L.chunk = kTopkCapacity; L.c0 = c0; L.nl = nl; L.nchunks = nch;
+  L.cand_key_out = reinterpret_cast<uint32_t*>(scratch);
+  L.cand_idx_out = reinterpret_cast<int*>(L.cand_key_out + (size_t)g.T * nch * k);
+  return launch_topk_kernel(L, g.T * nl, kTopkCapacity, pdl, st);
+}
+
+cudaError_t topk_merge_launch(const GeomDev& g, int k, int* idx, void* scratch, int* err, bool pdl, cudaStream_t st) {
+  const int nch = (g.max_seq_len + kTopkCapacity - 1) / kTopkCapacity;
+  const int fan = topk_fan_in(k);
+  uint8_t* buf[2] = {reinterpret_cast<uint8_t*>(scratch),
+                     reinterpret_cast<uint8_t*>(scratch) + (topk_list_bytes(g.T, nch, k) + 255) / 256 * 256};
+  int lists = nch, src = 0;
+  while (true) {
+    const int out = (lists + fan - 1) / fan;
+    TopkLaunch L{};
+    L.g = g; L.k = k; L.mode = kMerge; L.err = err;
+    L.n_in = lists; L.fan = fan; L.n_out = out;
+    L.cand_key_in = reinterpret_cast<const uint32_t*>(buf[src]);
+    L.cand_idx_in = reinterpret_cast<const int*>(L.cand_key_in + (size_t)g.T * lists * k);
+    if (out > 1) {
+      L.cand_key_out = reinterpret_cast<uint32_t*>(buf[src ^ 1]);
+      L.cand_idx_out = reinterpret_cast<int*>(L.cand_key_out + (size_t)g.T * out * k);
+    } else {
+      L.idx_out = idx;
+    }
+    const cudaError_t e = launch_topk_kernel(L, g.T * out, (lists < fan ? lists : fan) * k, pdl, st);
+    if (e != cudaSuccess || out == 1) return e;
+    pdl = true;   // each level follows the one just launched
+    lists = out;
+    src ^= 1;
+  }
 }
 
 cudaError_t topk_launch(const GeomDev& g, const float* scores, int64_t stride, int k, int* idx,
                         void* scratch, int* err, bool pdl, cudaStream_t st) {
-  const TopkPlan p = topk_plan(g.max_seq_len, k);
-  TopkLaunch L{};
-  L.g = g; L.k = k; L.scores = scores; L.score_stride = stride; L.idx_out = idx; L.err = err;
-  if (p.levels == 1) {
-    L.mode = 0;
+  if (g.max_seq_len <= kTopkCapacity) {
+    TopkLaunch L{};
+    L.g = g; L.k = k; L.mode = kDirect; L.scores = scores; L.score_stride = stride; L.idx_out = idx; L.err = err;
     return launch_topk_kernel(L, g.T, g.max_seq_len, pdl, st);
   }
-  uint32_t* ck = reinterpret_cast<uint32_t*>(scratch);
-  int* ci = reinterpret_cast<int*>(ck + (size_t)g.T * p.nchunks * k);
-  L.mode = 1; L.chunk = p.chunk; L.nchunks = p.nchunks; L.cand_key_out = ck; L.cand_idx_out = ci;
-  cudaError_t e = launch_topk_kernel(L, g.T * p.nchunks, p.chunk, pdl, st);
+  const int nch = (g.max_seq_len + kTopkCapacity - 1) / kTopkCapacity;
+  cudaError_t e = topk_chunks_launch(g, scores, stride, k, 0, nch, scratch, err, pdl, st);
   if (e != cudaSuccess) return e;
-  L.mode = 2; L.cand_key_in = ck; L.cand_idx_in = ci;
-  return launch_topk_kernel(L, g.T, p.nchunks * k, true, st);   // follows the chunk pass just launched
+  return topk_merge_launch(g, k, idx, scratch, err, true, st);   // follows the chunk pass just launched
 }
 
 }  // namespace dsa

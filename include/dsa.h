@@ -72,10 +72,11 @@ typedef enum { DSA_BF16 = 0, DSA_E4M3 = 1, DSA_I8 = 2 } dsa_dtype_t;
 
 /* Request geometry shared by every entry point. */
 typedef struct {
-  int32_t B;                  /* requests, >= 0                                      */
+  int32_t B;                  /* requests, >= 0 (no upper bound)                     */
   int32_t T;                  /* flattened query tokens = cu_q[B], >= 0              */
-  int32_t max_seq_len;        /* host upper bound on every seq_lens[b], >= 1         */
-  int32_t num_pages;          /* physical pages in each paged cache, >= 1            */
+  int32_t max_seq_len;        /* host upper bound on every seq_lens[b], >= 1; sizes the
+                                 grids and the top-k levels                          */
+  int32_t num_pages;          /* physical pages in each paged cache, 1 .. 2^31/64    */
   int32_t page_size;          /* must be 64                                          */
   int32_t bt_stride;          /* int32 elements between block-table rows,
                                  >= ceil(max_seq_len/64)                             */
@@ -91,8 +92,10 @@ typedef struct {
  *     (one scale per token); the scores use q = code*q_scale, k = code*k_scale.
  *   qk_dtype DSA_BF16: q_idx [T, Hi, 128] bf16, idx_k_cache [num_pages, 64, 128]
  *     bf16; q_scale and idx_k_scale must be NULL.
- *   w [T, Hi] fp32 head weights. Hi is a multiple of 4, 4 <= Hi <= 64.
- *   At most 1024 requests per call (B > 1024 returns DSA_ERR_UNSUPPORTED).
+ *   w [T, Hi] fp32 head weights. 1 <= Hi <= 64; the kernel pads the heads to 16 or 64
+ *     with zero weights (when Hi is a multiple of 4 the w and q_scale rows move as
+ *     16-byte bulk copies, otherwise 4 bytes at a time). Any B: requests are scored in
+ *     launches of up to 1024 each.
  *   scores [T, score_stride] fp32 (device, written): for query t and s <= pos(t),
  *     scores[t*score_stride + s] = I[t,s]; entries pos(t) < s < seq_len are set to
  *     -inf; entries s >= seq_len are not written. score_stride >= max_seq_len.
@@ -111,7 +114,11 @@ size_t dsa_indexer_scores_workspace_size(const dsa_geom_t* geom);
  *   idx [T, k] int32 (device, written): the min(k, pos(t)+1) positions with the
  *     largest scores, ties broken toward the lower position, in ascending order,
  *     followed by -1 up to k. -0.0 and +0.0 compare equal. Scores must not be NaN.
- *   1 <= k <= 16384.
+ *   1 <= k <= 16384. Rows of up to 16384 positions are selected in one pass; longer
+ *     rows are cut into 16384-position chunks whose top-k lists (keys and positions, in
+ *     the workspace) are merged floor(16384/k) at a time, level after level, so any
+ *     max_seq_len works when k <= 8192; k > 8192 with max_seq_len > 16384 returns
+ *     DSA_ERR_UNSUPPORTED.
  */
 dsa_status_t dsa_topk(const dsa_geom_t* geom, const float* scores, int64_t score_stride,
                       int32_t k, int32_t* idx, void* ws, size_t ws_bytes, void* stream);
@@ -152,8 +159,10 @@ size_t dsa_sparse_mla_attend_workspace_size(const dsa_geom_t* geom, int32_t H, i
  *   holds until the process exits. (The pages have no counterpart to this entry
  *   point.)
  *   Arguments, layouts and results are those of dsa_sparse_mla_attend, except:
- *   err_word: optional device int32 (NULL allowed) that receives device-side data
- *     errors (DSA_ERR_BAD_INDEX, DSA_ERR_TIMEOUT); the caller zeroes it.
+ *   err_word: device int32, 4-byte aligned, not NULL: it receives device-side data
+ *     errors (DSA_ERR_BAD_INDEX, DSA_ERR_TIMEOUT); the caller zeroes it. (A bounded
+ *     wait that gives up leaves the call's partial rows unwritten, and the merge would
+ *     read an earlier call's; the error word is what reports it.)
  *   The call needs (T + G) * H * 2056 bytes of the buffer (G = min(SM count,
  *   T * ceil(k/128))); a larger call returns DSA_ERR_WORKSPACE and
  *   dsa_last_error() says how much was needed.
@@ -304,13 +313,18 @@ dsa_status_t dsa_decode_step_wait_q(const dsa_step_args_t* args, void* q_ready, 
  * dsa_decode_step_bounded -- dsa_decode_step with the indexer's score workspace
  *   bounded (lmdeploy "glm5.3-flash support", Capacity improvement: bounded KPool
  *   scoring: a configurable score budget, top-k selected per query chunk right after
- *   that chunk is scored, indices identical). The fp32 scores of at most
- *   floor(score_budget_bytes / (stride * 4)) queries exist at a time, stride being
- *   max_seq_len rounded up to 64; each such range of queries is scored and reduced to
- *   its selection before the next. Results (idx_out, out, lse) are bitwise those of
- *   dsa_decode_step. A budget below one query's score row returns
- *   DSA_ERR_INVALID_ARG (dsa_last_error gives the row size). With reuse_idx the
- *   budget is not used. Graph-capturable like dsa_decode_step.
+ *   that chunk is scored, indices identical). With R = (max_seq_len rounded up to 64)
+ *   * 4 bytes, one query's score row:
+ *   - budget >= R: the fp32 scores of floor(budget / R) queries exist at a time; each
+ *     such range of queries is scored and reduced to its selection before the next.
+ *   - 65536 <= budget < R: one query at a time, its keys in spans of
+ *     floor(budget / 65536) * 16384 positions; each span is scored and reduced to the
+ *     top-k lists of its 16384-position chunks before the next span, and the lists are
+ *     merged at the end (as dsa_topk does for long rows), so the scores of at most
+ *     one span exist at a time whatever the context length.
+ *   - budget < min(R, 65536): DSA_ERR_INVALID_ARG (dsa_last_error gives the sizes).
+ *   Results (idx_out, out, lse) are bitwise those of dsa_decode_step. With reuse_idx
+ *   the budget is not used. Graph-capturable like dsa_decode_step.
  */
 dsa_status_t dsa_decode_step_bounded(const dsa_step_args_t* args, size_t score_budget_bytes, void* ws,
                                      size_t ws_bytes, void* stream);

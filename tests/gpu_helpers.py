@@ -52,3 +52,41 @@ def assert_close(got, ref, atol, rtol, what):
     assert not bad.any(), (f"{what}: {int(bad.sum())} of {bad.size} outside tolerance; "
                            f"max err {np.nanmax(err):.3g}")
     return float(np.nanmax(err)) if err.size else 0.0
+
+
+TOL = {"bf16": 2e-2, "e4m3": 5e-2, "int8": 5e-2}
+
+
+def verify_step(wl, dw, ts, idx=None):
+    """The step's selection (dw.idx, or `idx`) against the oracle's index sets, and every
+    layer's output and LSE against the oracle's attention over that same selection."""
+    idx = dw.idx.cpu().numpy() if idx is None else idx
+    ref_scores = oracle.indexer_scores(wl.q_idx, wl.q_scale, wl.w, wl.idx_k, wl.idx_k_scale,
+                                       wl.qk_dtype, wl.seq_lens, wl.n_q, wl.block_table, ts)
+    for t in ts:
+        ok, msg = index_set_parity(idx[t], ref_scores[t], wl.topk)
+        assert ok, (t, msg)
+    sel = {t: idx[t] for t in ts}
+    for li, (lay, dl) in enumerate(zip(wl.layers, dw.layers)):
+        ref = oracle.sparse_mla(lay.q, lay.kv, lay.kv_dtype, sel, wl.seq_lens, wl.n_q,
+                                wl.block_table, wl.sm_scale, ts)
+        out = dl.out.float().cpu().numpy()
+        lse = dl.lse.cpu().numpy()
+        tol = TOL[lay.kv_dtype]
+        for t in ts:
+            assert_close(out[t], ref[t][0], tol, tol, f"layer {li} out t={t}")
+            assert_close(lse[t], ref[t][1], tol, tol, f"layer {li} lse t={t}")
+    return ref_scores
+
+
+def gpu_scores(wl, dw, fill=None):
+    """The indexer's fp32 scores of every query through the standalone entry point."""
+    stride = int(-(-wl.max_seq_len // 64) * 64)
+    scores = torch.empty((wl.T, stride), dtype=torch.float32, device=DEV)
+    if fill is not None:
+        scores.fill_(fill)
+    ws = _lib.workspace(_lib.dsa_indexer_scores_workspace_size(dw.geom), DEV)
+    _lib.dsa_indexer_scores(dw.geom, dw.qk_dtype, dw.q_idx, dw.q_scale, dw.w, dw.idx_k, dw.idx_k_scale,
+                            scores, ws)
+    assert _lib.dsa_get_error(ws) == 0
+    return scores

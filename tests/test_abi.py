@@ -62,15 +62,18 @@ def test_host_validation(lib):
     assert _topk(lib, _geom(), scores=None) == _lib.DSA_ERR_INVALID_ARG
     assert _topk(lib, _geom(), ws=None) == _lib.DSA_ERR_WORKSPACE
     assert _topk(lib, _geom(), ws=260) == _lib.DSA_ERR_WORKSPACE          # misaligned
-    assert _topk(lib, _geom(max_seq_len=200000, bt_stride=4000), k=4096) == _lib.DSA_ERR_UNSUPPORTED
+    # rows longer than one top-k pass need k <= 8192 (merges of at least two lists);
+    # any length works below that (checked with zero queries: nothing is launched)
+    assert _topk(lib, _geom(max_seq_len=200000, bt_stride=4000), k=8193) == _lib.DSA_ERR_UNSUPPORTED
+    for L in (16385, 200000, 1 << 20, 1 << 28):
+        assert _topk(lib, _geom(T=0, max_seq_len=L, bt_stride=(L + 63) // 64), k=8192) == _lib.DSA_OK
     # zero work: OK without touching the device
     assert _topk(lib, _geom(T=0)) == _lib.DSA_OK
     g = _geom()
-    # indexer: Hi out of range or not a multiple of 4, bf16 with a scale pointer, misaligned cache
-    assert lib.dsa_indexer_scores(C.byref(g), _lib.DSA_E4M3, 6, 16, 16, 16, 16, 16, 16, 128, 256,
-                                  4096, None) == _lib.DSA_ERR_INVALID_ARG
-    assert lib.dsa_indexer_scores(C.byref(g), _lib.DSA_E4M3, 65, 16, 16, 16, 16, 16, 16, 128, 256,
-                                  4096, None) == _lib.DSA_ERR_INVALID_ARG
+    # indexer: Hi out of range, bf16 with a scale pointer, misaligned cache
+    for hi in (0, -1, 65, 128):
+        assert lib.dsa_indexer_scores(C.byref(g), _lib.DSA_E4M3, hi, 16, 16, 16, 16, 16, 16, 128, 256,
+                                      4096, None) == _lib.DSA_ERR_INVALID_ARG, hi
     assert lib.dsa_indexer_scores(C.byref(g), _lib.DSA_BF16, 4, 16, 16, 16, 16, None, 16, 128, 256,
                                   4096, None) == _lib.DSA_ERR_INVALID_ARG
     assert lib.dsa_indexer_scores(C.byref(g), _lib.DSA_E4M3, 4, 16, 16, 16, 24, 16, 16, 128, 256,
@@ -255,3 +258,66 @@ def test_wait_probe_validates_before_launch(lib):
     assert lib.dsa_wait_probe(None, 256, 1000, None) == _lib.DSA_ERR_WORKSPACE
     assert lib.dsa_wait_probe(260, 256, 1000, None) == _lib.DSA_ERR_WORKSPACE      # misaligned
     assert lib.dsa_wait_probe(256, 128, 1000, None) == _lib.DSA_ERR_WORKSPACE      # too small
+
+
+def test_indexer_accepts_any_head_count_up_to_64(lib):
+    # zero queries: the arguments are checked, nothing is launched
+    g = _geom(T=0)
+    for hi in (1, 2, 3, 5, 17, 63, 64):
+        assert lib.dsa_indexer_scores(C.byref(g), _lib.DSA_E4M3, hi, 16, 16, 16, 16, 16, 16, 128, 256,
+                                      4096, None) == _lib.DSA_OK, hi
+        assert lib.dsa_indexer_scores(C.byref(g), _lib.DSA_BF16, hi, 16, None, 16, 16, None, 16, 128, 256,
+                                      4096, None) == _lib.DSA_OK, hi
+    # more requests than one launch holds are accepted too
+    gb = _geom(T=0, B=5000)
+    assert lib.dsa_indexer_scores(C.byref(gb), _lib.DSA_E4M3, 64, 16, 16, 16, 16, 16, 16, 128, 256,
+                                  4096, None) == _lib.DSA_OK
+
+
+_ATTEND_BAD = [
+    dict(H=24), dict(H=0), dict(H=129), dict(kv=7), dict(k=0), dict(k=16385), dict(scale=float("inf")),
+    dict(scale=float("nan")), dict(q=None), dict(kvp=None), dict(idx=None), dict(out=None), dict(q=24),
+    dict(kvp=40), dict(geom=dict(page_size=32)), dict(geom=dict(bt_stride=1)),
+    dict(geom=dict(num_pages=(1 << 25) + 1)), dict(geom=dict(max_seq_len=0)), dict(geom=dict(B=0)),
+]
+
+
+@pytest.mark.parametrize("bad", _ATTEND_BAD, ids=[str(b) for b in _ATTEND_BAD])
+def test_static_entry_point_refuses_what_the_workspace_entry_point_refuses(lib, bad):
+    a = dict(H=16, kv=_lib.DSA_BF16, k=64, scale=0.1, q=16, kvp=16, idx=16, out=16, geom={})
+    a.update(bad)
+    g = _geom(**a["geom"])
+    ws = lib.dsa_sparse_mla_attend(C.byref(g), a["kv"], a["H"], a["q"], a["kvp"], a["idx"], a["k"], a["scale"],
+                                   a["out"], None, 256, 1 << 30, None)
+    st = lib.dsa_sparse_mla_attend_static(C.byref(g), a["kv"], a["H"], a["q"], a["kvp"], a["idx"], a["k"],
+                                          a["scale"], a["out"], None, 64, None)
+    assert ws in (_lib.DSA_ERR_INVALID_ARG, _lib.DSA_ERR_UNSUPPORTED), ws
+    assert st == ws
+
+
+def test_static_entry_point_requires_an_error_word(lib):
+    g = _geom()
+    for err in (None, 66):        # missing, or not 4-byte aligned
+        assert lib.dsa_sparse_mla_attend_static(C.byref(g), _lib.DSA_BF16, 16, 16, 16, 16, 64, 0.1, 16, None,
+                                                err, None) == _lib.DSA_ERR_INVALID_ARG
+    g0 = _geom(T=0)
+    assert lib.dsa_sparse_mla_attend_static(C.byref(g0), _lib.DSA_BF16, 16, None, None, None, 64, 0.1, None,
+                                            None, 64, None) == _lib.DSA_OK
+
+
+def test_bounded_step_key_spans_below_one_row(lib):
+    L = 262144
+    a = _lib.dsa_step_args_t()
+    a.geom = _geom(T=2, B=1, max_seq_len=L, bt_stride=L // 64)
+    a.topk = 2048
+    a.H = 16
+    a.Hi = 64
+    row = L * 4
+    full = lib.dsa_decode_step_workspace_size(C.byref(a))
+    one_row = lib.dsa_decode_step_bounded_workspace_size(C.byref(a), row)
+    span = lib.dsa_decode_step_bounded_workspace_size(C.byref(a), 65536)       # one 16384-key span
+    assert span < one_row < full
+    assert one_row - span >= row - 65536
+    # a budget that holds neither a row nor one top-k chunk is refused before launch
+    assert lib.dsa_decode_step_bounded(C.byref(a), 65535, 256, 1 << 30, None) == _lib.DSA_ERR_INVALID_ARG
+    assert b"top-k chunk" in lib.dsa_last_error()

@@ -1,15 +1,17 @@
 """dsa_decode_step_bounded (bounded scoring: the indexer's scores of at most a budget's
 worth of queries exist at a time, each range reduced to its selection before the next)
-against dsa_decode_step on the same inputs: the selection, the output and the LSE are
-bitwise equal for every budget, from one query's score row up to all but one; the
-bounded step is graph-capturable; a budget below one row is rejected before launch.
-dsa_decode_step itself is checked against the oracle in test_gpu_step.py."""
+against the oracle and against dsa_decode_step on the same inputs: index sets and
+attention match the oracle, and the selection, the output and the LSE are bitwise
+those of the unbounded step for every budget, from one query's score row up to all but
+one; the bounded step is graph-capturable; a budget below one row is rejected before
+launch. Contexts of 262144 tokens, with budgets below one row, are in
+test_gpu_long_context.py."""
 import numpy as np
 import pytest
 import torch
 
 from dsa_sparse_attention_02_gb300 import _lib, inputs, runner
-from gpu_helpers import DEV
+from gpu_helpers import DEV, verify_step
 
 pytestmark = pytest.mark.gpu
 
@@ -56,6 +58,10 @@ def test_bounded_step_equals_unbounded_bitwise(name, kw):
         got = _snapshot(dw)
         for r, g in zip(ref, got):
             assert torch.equal(r, g), (name, rows)
+        if rows == 3:
+            # and against the oracle directly (index sets, attention over the selection)
+            ts = list(range(T)) if T <= 32 else list(np.linspace(0, T - 1, 12).astype(int))
+            verify_step(wl, dw, ts)
     # the bounded workspace is smaller than the unbounded one once it holds fewer rows
     a0 = dw.args[0]
     row_bytes = (-(-wl.max_seq_len // 64) * 64) * 4

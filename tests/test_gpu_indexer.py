@@ -77,3 +77,39 @@ def test_topk_of_gpu_scores_exact_and_index_sets_match_oracle(name, kw):
         assert np.array_equal(got[t], oracle.topk_row(sc[t, : p + 1].astype(np.float64), k)), t
         ok, msg = index_set_parity(got[t], ref[t], k)
         assert ok, (t, msg)
+
+
+@pytest.mark.parametrize("hi", [1, 3, 5, 63])
+@pytest.mark.parametrize("qk", ["e4m3", "bf16"])
+def test_indexer_any_head_count(hi, qk):
+    """Head counts that are not a multiple of 4 (w and q_scale rows off 16-byte copies)
+    and below the MMA's 16: padded with zero weights in the kernel."""
+    wl = inputs.make_workload(f"hi{hi}", [700, 3000, 129], [1, 3, 2], topk=256, hi=hi, qk_dtype=qk, seed=20 + hi)
+    dw = runner.DeviceWorkload(wl, DEV)
+    sc = _scores(wl, dw).cpu().numpy()
+    req, pos = oracle.query_positions(wl.seq_lens, wl.n_q)
+    ref = oracle.indexer_scores(wl.q_idx, wl.q_scale, wl.w, wl.idx_k, wl.idx_k_scale, wl.qk_dtype,
+                                wl.seq_lens, wl.n_q, wl.block_table)
+    for t in range(wl.T):
+        p, L = int(pos[t]), int(wl.seq_lens[req[t]])
+        r = ref[t]
+        err = np.abs(sc[t, : p + 1].astype(np.float64) - r).max() / max(np.abs(r).max(), 1e-30)
+        assert err <= 1e-4, (hi, qk, t, err)
+        assert np.all(np.isneginf(sc[t, p + 1: L]))
+
+
+def test_indexer_more_requests_than_one_launch_holds():
+    """1100 requests (the kernel holds 1024 per launch): scored in two launches."""
+    rng = np.random.default_rng(4)
+    lens = rng.integers(70, 400, size=1100)
+    wl = inputs.make_workload("many", lens, [1] * 1100, topk=64, hi=16, qk_dtype="e4m3", seed=5)
+    dw = runner.DeviceWorkload(wl, DEV)
+    sc = _scores(wl, dw).cpu().numpy()
+    _, pos = oracle.query_positions(wl.seq_lens, wl.n_q)
+    ts = [0, 1, 511, 1023, 1024, 1025, 1099]
+    ref = oracle.indexer_scores(wl.q_idx, wl.q_scale, wl.w, wl.idx_k, wl.idx_k_scale, wl.qk_dtype,
+                                wl.seq_lens, wl.n_q, wl.block_table, ts)
+    for t in ts:
+        p = int(pos[t])
+        err = np.abs(sc[t, : p + 1].astype(np.float64) - ref[t]).max() / np.abs(ref[t]).max()
+        assert err <= 1e-4, (t, err)

@@ -7,30 +7,11 @@ import torch
 
 import oracle
 from dsa_sparse_attention_02_gb300 import _lib, inputs, runner
-from gpu_helpers import DEV, assert_close, index_set_parity
+from gpu_helpers import DEV, verify_step
 
 pytestmark = pytest.mark.gpu
 
-TOL = {"bf16": 2e-2, "e4m3": 5e-2, "int8": 5e-2}
-
-
-def _verify(wl, dw, ts):
-    idx = dw.idx.cpu().numpy()
-    ref_scores = oracle.indexer_scores(wl.q_idx, wl.q_scale, wl.w, wl.idx_k, wl.idx_k_scale,
-                                       wl.qk_dtype, wl.seq_lens, wl.n_q, wl.block_table, ts)
-    for t in ts:
-        ok, msg = index_set_parity(idx[t], ref_scores[t], wl.topk)
-        assert ok, (t, msg)
-    sel = {t: idx[t] for t in ts}
-    for li, (lay, dl) in enumerate(zip(wl.layers, dw.layers)):
-        ref = oracle.sparse_mla(lay.q, lay.kv, lay.kv_dtype, sel, wl.seq_lens, wl.n_q,
-                                wl.block_table, wl.sm_scale, ts)
-        out = dl.out.float().cpu().numpy()
-        lse = dl.lse.cpu().numpy()
-        tol = TOL[lay.kv_dtype]
-        for t in ts:
-            assert_close(out[t], ref[t][0], tol, tol, f"layer {li} out t={t}")
-            assert_close(lse[t], ref[t][1], tol, tol, f"layer {li} lse t={t}")
+_verify = verify_step
 
 
 SMALL = [

@@ -88,3 +88,20 @@ def test_rows_longer_than_context_are_read_only_up_to_position():
         pos = L - nq + j
         exp = oracle.topk_row(sc[j, : pos + 1].astype(np.float64), k)
         assert np.array_equal(got[j], exp)
+
+
+def test_long_rows_multi_level_merges():
+    """Rows cut into many 16384-position chunks whose lists merge over two or three
+    levels: 262144 and 300000 positions at k = 2048 (16 and 19 chunks, fan-in 8), and
+    k = 4096 and 8192 (fan-in 4 and 2), next to short rows of the same call whose later
+    chunks hold no valid entry (their merge groups carry fewer valid entries than k)."""
+    rng = np.random.default_rng(7)
+    rows = list(inputs.tied_scores(rng, 2, 262144, k=2048))
+    rows += [rng.standard_normal(300000).astype(np.float32), rng.standard_normal(16484).astype(np.float32),
+             rng.standard_normal(1000).astype(np.float32), rng.standard_normal(20000).astype(np.float32),
+             rng.integers(0, 3, size=140000).astype(np.float32)]
+    lengths = [len(r) for r in rows]
+    _run(rows, lengths, 2048)
+    _run(rows, lengths, 4096)
+    _run(rows[2:5], lengths[2:5], 8192)
+    _run(rows[:1], lengths[:1], 1)

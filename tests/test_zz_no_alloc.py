@@ -8,8 +8,9 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from dsa_sparse_attention_02_gb300 import _lib, inputs, runner
-from gpu_helpers import DEV
+from gpu_helpers import DEV, assert_close
 
 pytestmark = pytest.mark.gpu
 
@@ -26,7 +27,17 @@ def _selection(wl, k, seed):
     return torch.from_numpy(idx).to(DEV)
 
 
-def test_static_scratch_matches_workspace_entry_point_twice():
+def _static(dw, idx, k, err):
+    L = dw.layers[0]
+    out = torch.full_like(L.out, float("nan"))
+    lse = torch.full_like(L.lse, float("nan"))
+    _lib.dsa_sparse_mla_attend_static(dw.geom, L.kv_dtype, L.q, L.kv, idx, k, dw.wl.sm_scale, out, lse, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    return out, lse
+
+
+def test_static_scratch_matches_workspace_entry_point_and_oracle_twice():
     wl = inputs.make_config("decode", batch=12)
     dw = runner.DeviceWorkload(wl, DEV)
     L = dw.layers[0]
@@ -36,17 +47,24 @@ def test_static_scratch_matches_workspace_entry_point_twice():
     _lib.dsa_sparse_mla_attend(dw.geom, L.kv_dtype, L.q, L.kv, idx, wl.topk, wl.sm_scale, ref_out, ref_lse, ws)
     torch.cuda.synchronize()
     assert _lib.dsa_get_error(ws) == 0
+    sel = idx.cpu().numpy()
+    oref = oracle.sparse_mla(wl.layers[0].q, wl.layers[0].kv, "bf16", {t: sel[t] for t in range(wl.T)},
+                             wl.seq_lens, wl.n_q, wl.block_table, wl.sm_scale)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    # A call with another selection, index_topk and batch first leaves different partial
+    # rows in the shared buffer: nothing of it may leak into the calls checked below.
+    other = inputs.make_config("decode", batch=7, seed=77)
+    dwo = runner.DeviceWorkload(other, DEV)
+    _static(dwo, _selection(other, 1536, 9), 1536, err)
     for _ in range(2):                     # the buffer keeps the previous call's contents
-        out = torch.full_like(L.out, float("nan"))
-        lse = torch.full_like(L.lse, float("nan"))
-        _lib.dsa_sparse_mla_attend_static(dw.geom, L.kv_dtype, L.q, L.kv, idx, wl.topk, wl.sm_scale, out, lse, err)
-        torch.cuda.synchronize()
-        assert int(err.item()) == 0
+        out, lse = _static(dw, idx, wl.topk, err)
         o, r = out.float().cpu().numpy(), ref_out.float().cpu().numpy()
         assert np.all(np.abs(o - r) <= TOL + TOL * np.abs(r))
         l, rl = lse.cpu().numpy(), ref_lse.cpu().numpy()
         assert np.all(np.abs(l - rl) <= TOL + TOL * np.abs(rl))
+        for t in range(wl.T):
+            assert_close(o[t], oref[t][0], TOL, TOL, f"static out t={t}")
+            assert_close(l[t], oref[t][1], TOL, TOL, f"static lse t={t}")
 
 
 def test_static_scratch_rejects_calls_beyond_its_size():
@@ -54,8 +72,9 @@ def test_static_scratch_rejects_calls_beyond_its_size():
     dw = runner.DeviceWorkload(wl, DEV)
     L = dw.layers[0]
     idx = torch.full((wl.T, wl.topk), -1, dtype=torch.int32, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
     with pytest.raises(_lib.DsaError) as e:
         _lib.dsa_sparse_mla_attend_static(dw.geom, L.kv_dtype, L.q, L.kv, idx, wl.topk, wl.sm_scale,
-                                          L.out, L.lse)
+                                          L.out, L.lse, err)
     assert e.value.status == _lib.DSA_ERR_WORKSPACE
     assert "static scratch" in str(e.value)
