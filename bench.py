@@ -56,6 +56,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-configuration step lines")
     return ap.parse_args()
 
 
@@ -197,10 +198,52 @@ def oracle_step_time(wl, nq, reps_min_s):
             return el / n
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True,
+                             timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith(("model name", "cpu part")):
+                    return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return None
+
+
+def oracle_one_thread(name, budget_s=4.0):
+    """Oracle queries/s of configuration `name` with every BLAS pool held to one thread (a
+    fresh interpreter, since the pools size themselves when numpy loads)."""
+    code = ("import sys, time; sys.path.insert(0, %r)\n"
+            "import oracle\n"
+            "from dsa_sparse_attention_02_gb300 import inputs\n"
+            "wl = inputs.make_config(%r)\n"
+            "ts = list(range(wl.T)); n = 0; t0 = time.perf_counter()\n"
+            "while time.perf_counter() - t0 < %f:\n"
+            "    oracle.dsa_step(wl, ts=ts); n += len(ts)\n"
+            "print(n / (time.perf_counter() - t0))\n") % (ROOT, name, budget_s)
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               BLIS_NUM_THREADS="1", VECLIB_MAXIMUM_THREADS="1")
+    try:
+        out = subprocess.run([sys.executable, "-c", code], stdout=subprocess.PIPE, stderr=subprocess.PIPE,
+                             text=True, env=env, timeout=300)
+        return float(out.stdout.strip().splitlines()[-1])
+    except Exception:
+        return None
+
+
 def cpu_baseline(wl, budget_s=12.0):
     import oracle  # noqa: F401  (the oracle is the baseline)
     sec_per_q = oracle_step_time(wl, wl.T, budget_s)
     return {"value": 1.0 / sec_per_q, "unit": "queries/s", "cores": os.cpu_count(), "kind": "oracle",
+            "cpu_model": cpu_model(),
             "sample": f"float64 numpy oracle (indexer, top-k, attention) over all {wl.T} queries of the "
                       f"decode workload, repeated for >= {budget_s:.0f} s; BLAS threads = host cores"}
 
@@ -336,6 +379,8 @@ def main():
     prep = measure_indexer_prep(dw, flush, stream, max(20, min(args.steps, 100)))
     idx_prefill = measure_indexer_prefill(flush, stream, max(10, min(args.steps, 30)), dev)
     bounded = measure_bounded_step(dw, flush, stream, max(20, min(args.steps, 100)))
+    configs = {} if args.no_configs else {
+        c: measure_config(c, flush, stream, max(10, min(args.steps, 30)), dev) for c in ("tiny", "mtp", "prefill", "longctx")}
 
     idx_b, lat_b, selected = algorithmic_bytes(wl)
     peak, peak_kind = load_peaks()
@@ -365,6 +410,7 @@ def main():
         "next_rows": {"cache_append": append, "int8_latent_attend": int8_attend, "indexer_prep": prep,
                       "bounded_scoring": bounded},
         "e4m3_latent_attend": fp8_attend,
+        "configs": configs,
         "indexer_prefill": idx_prefill,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
@@ -372,6 +418,7 @@ def main():
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl)
+        line["cpu_baseline"]["tiny_one_thread_queries_per_s"] = oracle_one_thread("tiny")
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:
@@ -538,7 +585,7 @@ def measure_cache_append(dw, flush, stream, n):
     cu = torch.tensor([0, m], dtype=torch.int32, device=dev)
     bt = torch.from_numpy(rng.permutation(P).astype(np.int32).reshape(1, P)).to(dev)
     g2 = _lib.Geometry(seq, cu, bt, num_pages=P, max_seq_len=L, T=m)
-    kv2 = torch.zeros(P, 64, 656, dtype=torch.uint8, device=dev)
+    kv2 = torch.zeros(P, 64 * 656, dtype=torch.uint8, device=dev)
     ik2 = torch.zeros(P, 64, 128, dtype=torch.uint8, device=dev)
     is2 = torch.zeros(P, 64, dtype=torch.float32, device=dev)
     cases["prefill_2048_tokens_e4m3_latent"] = (g2, _lib.DSA_E4M3, bits((m, 576)), kv2, bits((m, 128)),
@@ -654,6 +701,88 @@ def measure_bounded_step(dw, flush, stream, n, rows=16):
             "score_workspace_bytes": budget, "unbounded_score_workspace_bytes": wl.T * row_bytes}
 
 
+CONFIG_LINES = {
+    "tiny": "batch 2, contexts 200 and 256, 1 query, index_topk 64, 4 bf16 indexer heads, bf16 latent",
+    "mtp": ("FP8-latent MTP verify: batch 32, context ~U[4096,16384], 4 causal queries per request, "
+            "index_topk 2048, 64 e4m3 indexer heads, e4m3 latent records, two layers (IndexShare)"),
+    "prefill": ("chunked prefill: 1 request, 16384 cached tokens, 2048 queries at positions 14336..16383, "
+                "index_topk 2048, 64 e4m3 indexer heads, bf16 latent"),
+    "longctx": ("long-context decode: batch 8, context 131072, 1 query, index_topk 2048, 64 e4m3 indexer "
+                "heads (1% of key rows duplicated: exact score ties), bf16 latent"),
+}
+
+
+def latent_row_bytes(kv_dtype):
+    return 576 * 2 if kv_dtype == "bf16" else 656
+
+
+def measure_config(name, flush, stream, n, device, oracle_budget_s=3.0):
+    """One whole step (every layer, through dsa_decode_step, captured in a CUDA graph) of
+    configuration `name`, timed like the headline step; its algorithmic bytes (index keys,
+    and the selected latent rows per query, and their union per request) and, for the
+    prefill, flops; the oracle's time per query on a sample of the same workload."""
+    import oracle
+    wl = inputs.make_config(name)
+    dw = runner.DeviceWorkload(wl, device)
+    for _ in range(3):
+        dw.step()
+    torch.cuda.synchronize()
+    if dw.check_error() != 0:
+        raise SystemExit(f"device error in the {name} step")
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        dw.step()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        dw.step()
+    ms = []
+    for i in range(n):
+        flush.fill_(i & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        e1.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    step_ms = statistics.median(ms)
+    req, pos = _positions(wl)
+    idx = dw.idx.cpu().numpy()
+    idx_key_bytes = int(wl.seq_lens.astype(np.int64).sum()) * (128 + 4 if wl.qk_dtype == "e4m3" else 256)
+    per_token_rows = int((idx >= 0).sum())
+    union_rows = sum(len(np.unique(idx[req == b][idx[req == b] >= 0])) for b in range(wl.B))
+    lat_tok = sum(per_token_rows * latent_row_bytes(L.kv_dtype) for L in wl.layers)
+    lat_union = sum(union_rows * latent_row_bytes(L.kv_dtype) for L in wl.layers)
+    peak, kind = load_peaks()
+    out = {"workload": CONFIG_LINES[name], "queries": wl.T, "layers": len(wl.layers), "ms": step_ms,
+           "queries_per_s": wl.T / (step_ms / 1000.0),
+           "index_key_bytes": idx_key_bytes, "selected_latent_bytes_per_token": lat_tok,
+           "selected_latent_bytes_union_per_request": lat_union,
+           "algorithmic_bytes": idx_key_bytes + lat_tok,
+           "achieved_gbs": (idx_key_bytes + lat_tok) / (step_ms / 1000.0) / 1e9,
+           "frac_of_peak": (idx_key_bytes + lat_tok) / (step_ms / 1000.0) / 1e9 / peak,
+           "achieved_gbs_union_bytes": (idx_key_bytes + lat_union) / (step_ms / 1000.0) / 1e9,
+           "peak_gbs": peak, "peak_kind": kind}
+    if name == "prefill":
+        idx_flops = 2.0 * 128 * wl.Hi * float((pos.astype(np.int64) + 1).sum())
+        att_flops = 2.0 * (576 + 512) * wl.heads * float(np.minimum(pos + 1, wl.topk).sum()) * len(wl.layers)
+        bf16, bkind = load_bf16_tflops()
+        out.update({"indexer_tflop": idx_flops / 1e12, "attention_tflop": att_flops / 1e12,
+                    "achieved_tflops": (idx_flops + att_flops) / (step_ms / 1000.0) / 1e12,
+                    "tensor_peak_tflops_e4m3": bf16 * E4M3_PER_BF16, "tensor_peak_kind": bkind,
+                    "bound": "tensor (indexer) + L2 gather (attention)"})
+    # the oracle on a bounded sample of the same workload
+    nq = 1 if name in ("longctx", "prefill") else min(wl.T, 4)
+    sec = oracle_step_time(wl, nq, oracle_budget_s)
+    out["oracle"] = {"queries_per_s": 1.0 / sec, "sample_queries": nq, "cores": os.cpu_count(),
+                     "sample": f"the first {nq} queries of the workload, repeated for >= {oracle_budget_s:.0f} s"}
+    del dw
+    torch.cuda.empty_cache()
+    return out
+
+
 def measure_int8_attend(dw, flush, stream, n, kv_dtype=None):
     """Device time of dsa_sparse_mla_attend over an int8 (next row f4) or, with
     kv_dtype=DSA_E4M3, an e4m3 latent record cache: the decode workload's bf16 latent
@@ -670,7 +799,7 @@ def measure_int8_attend(dw, flush, stream, n, kv_dtype=None):
     cu = torch.tensor([0, rows], dtype=torch.int32, device=dev)
     bt = torch.arange(P, dtype=torch.int32, device=dev).view(1, P)
     g_all = _lib.Geometry(seq, cu, bt, num_pages=P, max_seq_len=rows, T=rows)
-    kv8 = torch.empty(P, 64, 656, dtype=torch.uint8, device=dev)
+    kv8 = torch.empty(P, 64 * 656, dtype=torch.uint8, device=dev)
     ws = _lib.workspace(max(256, _lib.dsa_sparse_mla_attend_workspace_size(dw.geom, lay.q.shape[1], wl.topk)), dev)
     _lib.dsa_cache_append(g_all, kv_dtype, lay.kv.view(rows, 576), kv8, _lib.DSA_E4M3, None, None, None, ws)
     dw.step()

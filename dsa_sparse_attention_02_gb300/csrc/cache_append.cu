@@ -13,8 +13,9 @@
 //   * e4m3 latent record (656 B): lane l quantizes latent values 16l..16l+15; the
 //     eight lanes of a 128-value group reduce its amax, scale = amax / 448 (1 for an
 //     all-zero group), code = e4m3(x / scale) with the quotient in fp32 and the
-//     conversion rounding to nearest even and saturating at +-448; the four scales
-//     follow the codes, then the 64 RoPE values as given (bf16);
+//     conversion rounding to nearest even and saturating at +-448; the 512 codes, the
+//     four scales and the 64 RoPE values as given (bf16) go to the token's slot of
+//     its page's code, scale and RoPE planes;
 //   * index key: e4m3 with one such scale per token over its 128 values (the scale to
 //     the [P, 64] tensor), or the bf16 key as given.
 // Every row other than the new tokens' is left as it was. Page ids out of range
@@ -92,7 +93,7 @@ __global__ void __launch_bounds__(32 * kAppendWarps) cache_append_kernel(const A
     dst[32 + lane] = d1;
     if (lane < 8) dst[64 + lane] = d2;
   } else {
-    uint8_t* rec = A.kv_cache + row * kFp8Record;
+    uint8_t* const kv = A.kv_cache;
     float v[16];
     {
       float a[8], b[8];
@@ -118,9 +119,9 @@ __global__ void __launch_bounds__(32 * kAppendWarps) cache_append_kernel(const A
     codes.y = pack4(4);
     codes.z = pack4(8);
     codes.w = pack4(12);
-    *reinterpret_cast<uint4*>(rec + 16 * lane) = codes;
-    if ((lane & 7) == 0) *reinterpret_cast<float*>(rec + kDimLatent + 4 * (lane >> 3)) = scale;
-    if (lane < 8) *reinterpret_cast<uint4*>(rec + kDimLatent + 16 + 16 * lane) = d2;
+    *reinterpret_cast<uint4*>(kv + rec_codes_at(row) + 16 * lane) = codes;
+    if ((lane & 7) == 0) *reinterpret_cast<float*>(kv + rec_scales_at(row) + 4 * (lane >> 3)) = scale;
+    if (lane < 8) *reinterpret_cast<uint4*>(kv + rec_rope_at(row) + 16 * lane) = d2;
   }
   // ---- index key
   if (A.k_new) {

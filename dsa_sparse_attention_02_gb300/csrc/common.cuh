@@ -11,7 +11,13 @@ constexpr int kDimIdx = 128;      // indexer head dim
 constexpr int kDimLatent = 512;   // latent (value) width
 constexpr int kDimRope = 64;
 constexpr int kDimQK = 576;       // 512 latent + 64 RoPE
-constexpr int kFp8Record = 656;   // e4m3 latent record bytes per token
+constexpr int kFp8Record = 656;   // latent record bytes per token (e4m3 or int8 codes)
+// A page of latent records holds its 64 tokens' fields as three planes: codes
+// [64][512], fp32 scales [64][4], bf16 RoPE [64][64]; every token's codes start on a
+// 512-byte boundary and its RoPE values on a 128-byte one.
+constexpr int kRecPageBytes = kPage * kFp8Record;                   // 41984
+constexpr int kRecScalesAt = kPage * kDimLatent;                    // 32768
+constexpr int kRecRopeAt = kRecScalesAt + kPage * 16;               // 33792
 
 struct GeomDev {
   int B, T, max_seq_len, num_pages, bt_stride;
@@ -73,6 +79,17 @@ __device__ __forceinline__ QueryInfo query_info_warp(const GeomDev& g, int t) {
   qi.pos = qi.len - (q1 - q0) + (t - q0);
   qi.ok = (t >= q0) && (t < q1) && (qi.len <= g.max_seq_len) && (qi.pos >= 0) && (qi.pos < qi.len);
   return qi;
+}
+
+// Byte offsets of physical row r's fields in a latent record cache.
+__host__ __device__ __forceinline__ int64_t rec_codes_at(int64_t r) {
+  return (r >> 6) * kRecPageBytes + (r & 63) * kDimLatent;
+}
+__host__ __device__ __forceinline__ int64_t rec_scales_at(int64_t r) {
+  return (r >> 6) * kRecPageBytes + kRecScalesAt + (r & 63) * 16;
+}
+__host__ __device__ __forceinline__ int64_t rec_rope_at(int64_t r) {
+  return (r >> 6) * kRecPageBytes + kRecRopeAt + (r & 63) * (kDimRope * 2);
 }
 
 // Physical row (page*64 + s%64) of request b's logical token s, or -1 if the page id

@@ -66,8 +66,9 @@ struct MlaArgs {
 int mla_grid(int64_t n_chunks, int num_sms);
 size_t mla_partial_bytes(int T, int H, int grid);
 // map_q: [T*H, 576] bf16 query rows, 64 x min(H,16) box, 128-byte swizzle.
-// Latent cache formats: bf16 rows of 576, or 656-byte records of 512 codes (e4m3 or
-// int8), four fp32 scales per 128 codes, 64 bf16 RoPE values.
+// Latent cache formats: bf16 rows of 576, or pages of 656-byte records (512 codes, e4m3
+// or int8; four fp32 scales, one per 128 codes; 64 bf16 RoPE values) stored per page as
+// code, scale and RoPE planes (common.cuh).
 enum KvFormat : int { kKvBf16 = 0, kKvE4m3 = 1, kKvInt8 = 2 };
 cudaError_t mla_launch(int kv_format, const CUtensorMap& map_q, MlaArgs A, int grid, bool pdl, cudaStream_t st);
 bool encode_mla_q_map(CUtensorMap* map_q, const void* q, int T, int H);

@@ -51,17 +51,29 @@ namespace dsa {
 
 constexpr int kMlaHeads = 16;                       // heads per CTA (MMA N)
 constexpr int kMlaKeys = 128;                       // keys per chunk (MMA M)
+constexpr int kMlaKeysC = kMlaKeys;
 constexpr int kAtomBytes = kMlaKeys * 128;          // 16 KB: 128 rows x 64 bf16
 constexpr int kPairBytes = 2 * kAtomBytes;          // 32 KB
-constexpr int kPairSlots = 5;                       // two and a half chunks of the CTA's two pairs
+// bf16 cache: five pair slots (two and a half chunks of the CTA's two pairs) that the
+// rows are gathered into. Record caches (e4m3 / int8 codes): three bf16 pair slots that
+// the codes are converted into, fed by two code stages of one chunk each (the CTA's
+// 256 codes and two scales of each of the chunk's 128 rows), so that the code bytes in
+// flight do not wait on the bf16 slots.
+template <int kKv> constexpr int kPairSlotsOf = kKv == kKvBf16 ? 5 : 3;
+constexpr int kCodeStages = 2;
+constexpr int kCodeRowBytes = 256;                          // the CTA's half of a row's codes
+constexpr int kCodeBytes = kMlaKeysC * kCodeRowBytes;       // 32 KB
+constexpr int kCodeStageBytes = kCodeBytes + kMlaKeysC * 8;   // + two fp32 scales per row
 constexpr int kRopeSlots = 2;                       // halves of one RoPE atom (chunk parity)
 constexpr int kQAtomBytes = kMlaHeads * 128;        // 2 KB
 constexpr int kQAtoms = 6;                          // the CTA's 4 latent atoms + 2 RoPE atoms
 constexpr int kQBufBytes = kQAtoms * kQAtomBytes;   // 12 KB
 constexpr int kPBufBytes = 2 * kQAtomBytes;         // P^T: 16 heads x 128 keys bf16 = 4 KB
 constexpr int kXBufBytes = kMlaKeys * kMlaHeads * 4;  // partial scores from the other CTA: 8 KB
-constexpr int kMlaSmemBytes = 1024 + kPairSlots * kPairBytes + kAtomBytes + kQBufBytes +
-                              2 * kPBufBytes + 2 * kXBufBytes;
+template <int kKv>
+constexpr int kMlaSmemBytesOf = 1024 + kPairSlotsOf<kKv> * kPairBytes + (kKv == kKvBf16 ? 0 : kCodeStages * kCodeStageBytes) +
+                                kAtomBytes + kQBufBytes + 2 * kPBufBytes + 2 * kXBufBytes;
+constexpr int kMlaSmemBytes = kMlaSmemBytesOf<kKvBf16>;
 // Twelve warps, 168 registers each (three per SM sub-partition):
 //   warps 0-3   softmax (one per TMEM lane quarter)
 //   warps 4-7   producers (one per sub-partition, so that copy issue runs on all four)
@@ -110,6 +122,22 @@ __device__ __forceinline__ void codes4_to_f32(uint32_t w, float (&f)[4]) {
     const float2 a = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xFFFFu), __NV_E4M3)));
     const float2 b = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3)));
     f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+  }
+}
+
+// Sixteen latent codes (byte i of word j of c = code 4j+i) times sc, rounded to bf16
+// and packed in pairs: pk[k] = (bf16(code[2k] * sc), bf16(code[2k+1] * sc)), the
+// exact code times sc rounded once to fp32, then to bf16. (An integer construction of
+// the e4m3 values measured 40% slower than the hardware conversion on this part.)
+template <int kKv>
+__device__ __forceinline__ void dequant16(const uint4 c, float sc, uint32_t (&pk)[8]) {
+  const uint32_t w4[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float f[4];
+    codes4_to_f32<kKv>(w4[j], f);
+    pk[2 * j] = pack_bf16x2(f[0] * sc, f[1] * sc);
+    pk[2 * j + 1] = pack_bf16x2(f[2] * sc, f[3] * sc);
   }
 }
 
@@ -184,16 +212,19 @@ __device__ __forceinline__ int64_t selected_row(const MlaArgs& A, const QueryInf
 template <int kKv>
 __global__ void __launch_bounds__(kMlaThreads, 1)
     sparse_mla_kernel(const __grid_constant__ CUtensorMap map_q, const MlaArgs A) {
+  constexpr bool kRecord = kKv != kKvBf16;   // 656-byte records: codes, scales, RoPE
+  constexpr int kPairSlots = kPairSlotsOf<kKv>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* pair_buf = smem;                                         // 4 x 32 KB
-  uint8_t* rope_buf = pair_buf + kPairSlots * kPairBytes;           // 16 KB
+  uint8_t* pair_buf = smem;                                         // kPairSlots x 32 KB
+  uint8_t* code_buf = pair_buf + kPairSlots * kPairBytes;           // record caches: kCodeStages x 33 KB
+  uint8_t* rope_buf = code_buf + (kRecord ? kCodeStages * kCodeStageBytes : 0);   // 16 KB
   uint8_t* q_buf = rope_buf + kAtomBytes;                           // 12 KB
   uint8_t* p_buf = q_buf + kQBufBytes;                              // 2 x 4 KB
   float4* x_buf = reinterpret_cast<float4*>(p_buf + 2 * kPBufBytes);  // 2 x [4 head quads][128 keys]
 
   __shared__ uint64_t pair_full[kPairSlots], pair_empty[kPairSlots], rope_full[kRopeSlots], rope_empty[kRopeSlots];
-  __shared__ __align__(16) float scale_stage[kKv != kKvBf16 ? kPairSlots : 1][kMlaKeys];   // record caches
+  __shared__ uint64_t code_full[kCodeStages], code_empty[kCodeStages];   // record caches
   __shared__ uint64_t q_full, q_empty;
   __shared__ uint64_t s_full[2], s_empty[2], p_full[2], p_empty[2], o_full, o_free, grp_bar;
   __shared__ uint64_t x_full[2], x_free[2];   // partial-score exchange with the other CTA
@@ -250,7 +281,16 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
 
   if (tid == 0) {
     abort_flag = 0;
-    for (int j = 0; j < kPairSlots; ++j) { mbar_init(smem_u32(&pair_full[j]), 64); mbar_init(smem_u32(&pair_empty[j]), 1); }
+    // bf16: a pair slot is filled by the cp.async copies of 64 producer threads (noinc
+    // arrivals); records: by the conversions of all 128 producer threads
+    for (int j = 0; j < kPairSlots; ++j) {
+      mbar_init(smem_u32(&pair_full[j]), kRecord ? slot_producers : 64);
+      mbar_init(smem_u32(&pair_empty[j]), 1);
+    }
+    for (int j = 0; j < kCodeStages; ++j) {
+      mbar_init(smem_u32(&code_full[j]), slot_producers);    // noinc arrivals of every producer thread
+      mbar_init(smem_u32(&code_empty[j]), slot_producers);   // every producer thread has read its codes
+    }
     for (int j = 0; j < kRopeSlots; ++j) { mbar_init(smem_u32(&rope_full[j]), slot_producers); mbar_init(smem_u32(&rope_empty[j]), 1); }
     mbar_init(smem_u32(&q_full), 1);
     mbar_init(smem_u32(&q_empty), 1);
@@ -290,85 +330,26 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
   // waits for that kernel (griddepcontrol.wait) before its first index load, and
   // every other role depends on the resolver's row table.
 
-  if (warp >= kProdWarp0 && warp < kProdWarp0 + kProdWarps) {
-    // ================================================================ producers
+  if (warp >= kProdWarp0 && warp < kProdWarp0 + kProdWarps && !kRecord) {
+    // ================================================================ producers (bf16 cache)
     // Two groups of two warps: group jl (warps 4-5: jl = 0; warps 6-7: jl = 1) fills
     // latent pair jl of every chunk, so that both pairs of a chunk are requested at
     // once; warp wg of a group copies rows [64*wg, 64*wg+64) of the pair. Every
-    // producer warp also copies the RoPE columns of rows [32*pw, 32*pw+32). bf16:
-    // 16-byte cp.async (zero-fill for padding), slot completion through
-    // cp.async.mbarrier.arrive.noinc. e4m3 / int8 records: the codes and scales are
-    // staged by cp.async, and dequantized to bf16 in the slot one chunk later, so that
-    // the next chunk's loads are in flight during the conversion; each thread then
-    // arrives.
+    // producer warp also copies the RoPE columns of rows [32*pw, 32*pw+32). 16-byte
+    // cp.async (zero-fill for padding), slot completion through
+    // cp.async.mbarrier.arrive.noinc.
     const int pw = warp - kProdWarp0;
     const int jl = pw >> 1, wg = pw & 1;
     const int j = 2 * rank + jl;                 // pair of the row: latent columns 128j..128j+127
     int seg = 0;
-    constexpr bool kRecord = kKv != kKvBf16;   // 656-byte record: codes, scales, RoPE
-    // Record caches: dequantizes the codes staged in the second atom of pair slot fps
-    // (this warp's 64 rows; lane part p = lane % 8 holds codes 16p..16p+15 of a row) to
-    // bf16 in the slot's swizzled layout, then marks the warp's share of the slot full.
-    // The bf16 row's second atom overwrites the staging of the same row, so all eight
-    // lanes of a row read before any writes. newer: the copies of one newer chunk may
-    // still be in flight.
-    int pend_ps = -1;
-    auto finish_record = [&](int fps, bool newer) {
-      if (newer) cp_async_wait<1>();
-      else cp_async_wait<0>();
-      __syncwarp();                               // the scale of a row is staged by its part-0 lane
-      uint8_t* fslot = pair_buf + fps * kPairBytes;
-      const uint8_t* stg = fslot + kAtomBytes;
-      const int part = lane & 7, sub = lane >> 3;
-      const int col_byte = (part >> 2) * 128 + (part & 3) * 32;   // pair columns 16p.. -> atom p/4
-#pragma unroll 1
-      for (int g = 0; g < 4; ++g) {
-        uint4 c[4];
-        float sc[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int r = 64 * wg + 16 * g + 4 * q + sub;
-          c[q] = *reinterpret_cast<const uint4*>(stg + r * 128 + 16 * part);
-          sc[q] = scale_stage[fps][r];
-        }
-        __syncwarp();
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int r = 64 * wg + 16 * g + 4 * q + sub;
-          const uint32_t w4[4] = {c[q].x, c[q].y, c[q].z, c[q].w};
-          uint32_t pk[8];
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            float f[4];
-            codes4_to_f32<kKv>(w4[h], f);
-            pk[2 * h] = pack_bf16x2(f[0] * sc[q], f[1] * sc[q]);
-            pk[2 * h + 1] = pack_bf16x2(f[2] * sc[q], f[3] * sc[q]);
-          }
-          *reinterpret_cast<uint4*>(fslot + sw128_offset(r, col_byte, kAtomBytes)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          *reinterpret_cast<uint4*>(fslot + sw128_offset(r, col_byte + 16, kAtomBytes)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-        }
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(smem_u32(&pair_full[fps]));
-    };
-    // Warp-uniform bounded wait. A staged chunk is never held across a wait that is not
-    // already satisfied: every such wait may depend, through the MMA's order, on the
-    // staged chunk being converted (five pair slots cannot hold two pending chunks per
-    // group), so the chunk is converted first.
+    // warp-uniform bounded wait
     auto slot_acquire = [&](uint32_t bar, uint32_t parity) -> bool {
-      if (kRecord && pend_ps >= 0) {
-        const int ready = __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_test_wait(bar, parity) : 0, 0);
-        if (!ready) {
-          finish_record(pend_ps, false);
-          pend_ps = -1;
-        }
-      }
       int ok = 1;
       if (lane == 0) ok = mbar_wait(bar, parity, &abort_flag, A.err) ? 1 : 0;
       return __shfl_sync(0xffffffffu, ok, 0) != 0;
     };
-    const size_t row_bytes = kRecord ? (size_t)kFp8Record : (size_t)(kDimQK * 2);
-    const size_t rope_off = (kRecord ? (size_t)(kDimLatent + 16) : (size_t)(kDimLatent * 2)) + 64 * rank;
+    const size_t row_bytes = (size_t)(kDimQK * 2);
+    const size_t rope_off = (size_t)(kDimLatent * 2) + 64 * rank;
     ChunkPos cp = chunk_pos(0);
     for (int i = 0; i < n_mine; chunk_next(cp, ++i)) {
       if (cp.first) {
@@ -401,51 +382,132 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       const int gidx = 2 * i + jl, ps = gidx % kPairSlots;
       if (!slot_acquire(smem_u32(&pair_empty[ps]), ((gidx / kPairSlots) & 1) ^ 1)) break;
       uint8_t* slot = pair_buf + ps * kPairBytes;
-      if (!kRecord) {
-        // 16 lanes per row (256 B of the pair), 2 rows per instruction: lane half h
-        // takes rows r0 .. r0+31, r0 = 64*wg + 32*h, whose indices it reads up front
-        const int r0 = 64 * wg + 32 * (lane >> 4);
-        const int cb = (lane & 15) * 16;
-        int rr[32];
+      // 16 lanes per row (256 B of the pair), 2 rows per instruction: lane half h
+      // takes rows r0 .. r0+31, r0 = 64*wg + 32*h, whose indices it reads up front
+      const int r0 = 64 * wg + 32 * (lane >> 4);
+      const int cb = (lane & 15) * 16;
+      int rr[32];
 #pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int4 v = *reinterpret_cast<const int4*>(rows + r0 + 4 * q);
+        rr[4 * q] = v.x; rr[4 * q + 1] = v.y; rr[4 * q + 2] = v.z; rr[4 * q + 3] = v.w;
+      }
+      const uint32_t dst0 = smem_u32(slot);
+      const uint8_t* src0 = kv + j * 256 + cb;
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) {
+        const int row = rr[jj];
+        cp_async_16(dst0 + sw128_offset(r0 + jj, cb, kAtomBytes), src0 + (int64_t)(row >= 0 ? row : 0) * row_bytes,
+                    row >= 0 ? 16u : 0u);
+      }
+      cp_async_arrive_noinc(smem_u32(&pair_full[ps]));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&rows_empty[rb]));
+    }
+  } else if (warp >= kProdWarp0 && warp < kProdWarp0 + kProdWarps) {
+    // ================================================================ producers (record caches)
+    // Warp pw owns rows [32*pw, 32*pw+32) of every chunk. For chunk i it copies those
+    // rows' RoPE columns of this CTA into the RoPE atom, and their 256 codes and two
+    // scales (latent groups 2*rank, 2*rank+1) into code stage i % 2 (16-byte and
+    // 8-byte cp.async, zero-fill for padding, noinc arrivals on code_full); then it
+    // converts chunk i-1's codes of the same rows, code * scale rounded to bf16, into
+    // that chunk's two bf16 pair slots (in the swizzled K-major layout the MMA reads)
+    // and marks its share of each slot full. The copies of chunk i are therefore in
+    // flight while chunk i-1 is converted, and code bytes never wait on a pair slot.
+    // Every wait a warp makes before converting chunk i-1 depends only on chunks
+    // before it (the query buffer of a new segment, which the MMA frees after the
+    // previous chunk's scores, is taken after the conversion).
+    const int pw = warp - kProdWarp0;
+    auto slot_acquire = [&](uint32_t bar, uint32_t parity) -> bool {
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(bar, parity, &abort_flag, A.err) ? 1 : 0;
+      return __shfl_sync(0xffffffffu, ok, 0) != 0;
+    };
+    const uint8_t* kv = A.kv;
+    // Chunk ic's rows of this warp, code stage ic % 2 -> bf16 pair slots of the chunk.
+    auto convert = [&](int ic) -> bool {
+      const int cs = ic % kCodeStages;
+      if (!slot_acquire(smem_u32(&code_full[cs]), (ic / kCodeStages) & 1)) return false;
+      mbar_try_wait(smem_u32(&code_full[cs]), (ic / kCodeStages) & 1);   // acquire in every lane
+      const uint8_t* stg = code_buf + cs * kCodeStageBytes;
+      const float* scl = reinterpret_cast<const float*>(stg + kCodeBytes);   // [128 rows][2]
+      const int part = lane & 7, sub = lane >> 3;
+      const int col_byte = (part >> 2) * 128 + (part & 3) * 32;   // pair columns 16p.. -> atom p/4
+#pragma unroll 1
+      for (int jl = 0; jl < 2; ++jl) {
+        const int gidx = 2 * ic + jl, ps = gidx % kPairSlots;
+        if (!slot_acquire(smem_u32(&pair_empty[ps]), ((gidx / kPairSlots) & 1) ^ 1)) return false;
+        uint8_t* slot = pair_buf + ps * kPairBytes;
+#pragma unroll 2
         for (int q = 0; q < 8; ++q) {
-          const int4 v = *reinterpret_cast<const int4*>(rows + r0 + 4 * q);
-          rr[4 * q] = v.x; rr[4 * q + 1] = v.y; rr[4 * q + 2] = v.z; rr[4 * q + 3] = v.w;
+          const int r = 32 * pw + 4 * q + sub;
+          const uint4 c = *reinterpret_cast<const uint4*>(stg + r * kCodeRowBytes + 128 * jl + 16 * part);
+          const float sc = scl[2 * r + jl];
+          uint32_t pk[8];
+          dequant16<kKv>(c, sc, pk);
+          *reinterpret_cast<uint4*>(slot + sw128_offset(r, col_byte, kAtomBytes)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(slot + sw128_offset(r, col_byte + 16, kAtomBytes)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
         }
-        const uint32_t dst0 = smem_u32(slot);
-        const uint8_t* src0 = kv + j * 256 + cb;
+        fence_proxy_async_smem();   // the MMA reads the slot through the async proxy
+        mbar_arrive(smem_u32(&pair_full[ps]));
+      }
+      mbar_arrive(smem_u32(&code_empty[cs]));
+      return true;
+    };
+    int seg = 0;
+    bool ok = true;
+    ChunkPos cp = chunk_pos(0);
+    for (int i = 0; i < n_mine && ok; chunk_next(cp, ++i)) {
+      const int rb = i % kRowBufs, rs = i % kRopeSlots, cs = i % kCodeStages;
+      if (!slot_acquire(smem_u32(&rows_full[rb]), (i / kRowBufs) & 1)) break;
+      mbar_try_wait(smem_u32(&rows_full[rb]), (i / kRowBufs) & 1);   // acquire in every lane (phase is complete)
+      const int* rows = rows_s[rb];
+      if (!slot_acquire(smem_u32(&rope_empty[rs]), ((i / kRopeSlots) & 1) ^ 1)) break;
+      {
+        const uint32_t dst0 = smem_u32(rope_buf);
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          const int row = rr[jj];
-          cp_async_16(dst0 + sw128_offset(r0 + jj, cb, kAtomBytes), src0 + (int64_t)(row >= 0 ? row : 0) * row_bytes,
-                      row >= 0 ? 16u : 0u);
+        for (int q = 0; q < 4; ++q) {
+          const int ri = 32 * pw + 8 * q + (lane >> 2);
+          const int row = rows[ri];
+          const int cb = (lane & 3) * 16;
+          cp_async_16(dst0 + sw128_offset(ri, 64 * rs + cb, 0),
+                      kv + rec_rope_at(row >= 0 ? row : 0) + 64 * rank + cb, row >= 0 ? 16u : 0u);
         }
-        cp_async_arrive_noinc(smem_u32(&pair_full[ps]));
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&rows_empty[rb]));
-      } else {
-        // Record cache: the pair's 128 codes of each of this warp's 64 rows land by
-        // cp.async in the slot's second atom (row r at 16 KB + 128 r: exactly one atom),
-        // its scale in scale_stage[ps]; the codes are dequantized into the slot one
-        // iteration later, after the next chunk's copies are on their way.
-        const uint32_t stage = smem_u32(slot + kAtomBytes);
-        const int part = lane & 7, sub = lane >> 3;
+        cp_async_arrive_noinc(smem_u32(&rope_full[rs]));
+      }
+      if (!slot_acquire(smem_u32(&code_empty[cs]), ((i / kCodeStages) & 1) ^ 1)) break;
+      {
+        uint8_t* stg = code_buf + cs * kCodeStageBytes;
+        const uint32_t dst_codes = smem_u32(stg), dst_scales = smem_u32(stg + kCodeBytes);
+        const int part = lane & 15;
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const int r = 64 * wg + 4 * q + sub;
+        for (int q = 0; q < 16; ++q) {   // 16 lanes per row (256 B), 2 rows per instruction
+          const int r = 32 * pw + 2 * q + (lane >> 4);
           const int row = rows[r];
-          const uint8_t* rec = kv + (int64_t)(row >= 0 ? row : 0) * kFp8Record;
-          cp_async_16(stage + r * 128 + 16 * part, rec + 128 * j + 16 * part, row >= 0 ? 16u : 0u);
-          if (part == 0) cp_async_4(smem_u32(&scale_stage[ps][r]), rec + kDimLatent + 4 * j, row >= 0 ? 4u : 0u);
+          cp_async_16(dst_codes + r * kCodeRowBytes + 16 * part,
+                      kv + rec_codes_at(row >= 0 ? row : 0) + kCodeRowBytes * rank + 16 * part, row >= 0 ? 16u : 0u);
         }
-        cp_async_commit();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&rows_empty[rb]));   // the staged chunk needs no row ids
-        if (pend_ps >= 0) finish_record(pend_ps, true);
-        pend_ps = ps;
+        {
+          const int r = 32 * pw + lane;
+          const int row = rows[r];
+          cp_async_8(dst_scales + 8 * r, kv + rec_scales_at(row >= 0 ? row : 0) + 8 * rank, row >= 0 ? 8u : 0u);
+        }
+        cp_async_arrive_noinc(smem_u32(&code_full[cs]));
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&rows_empty[rb]));   // the copies need no row ids any more
+      if (i > 0 && !convert(i - 1)) { ok = false; break; }
+      if (cp.first) {
+        // a new segment's query: the MMA frees the buffer after the previous segment's
+        // last scores, which needed the conversion just done
+        if (pw == 0 && seg > 0) {
+          if (!slot_acquire(smem_u32(&q_empty), (seg & 1) ^ 1)) break;
+          if (lane == 0) load_q(cp.t);
+        }
+        ++seg;
       }
     }
-    if (kRecord && pend_ps >= 0) finish_record(pend_ps, false);   // no waits inside: safe after an abort too
+    if (ok && n_mine > 0 && !abort_flag) convert(n_mine - 1);
   } else if (warp == kResolverWarp) {
     // ================================================================ row resolver
     ChunkPos cp = chunk_pos(0);
@@ -857,7 +919,8 @@ cudaError_t mla_launch(int kv_format, const CUtensorMap& map_q, MlaArgs A, int g
   const int hgroups = (A.H + kMlaHeads - 1) / kMlaHeads;
   auto kern = kv_format == kKvE4m3 ? sparse_mla_kernel<kKvE4m3>
             : kv_format == kKvInt8 ? sparse_mla_kernel<kKvInt8> : sparse_mla_kernel<kKvBf16>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMlaSmemBytes);
+  const int smem = kv_format == kKvBf16 ? kMlaSmemBytesOf<kKvBf16> : kMlaSmemBytesOf<kKvE4m3>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
@@ -867,7 +930,7 @@ cudaError_t mla_launch(int kv_format, const CUtensorMap& map_q, MlaArgs A, int g
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(2 * grid, hgroups, 1);
   cfg.blockDim = dim3(kMlaThreads, 1, 1);
-  cfg.dynamicSmemBytes = kMlaSmemBytes;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = at; cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, kern, map_q, A);

@@ -28,8 +28,10 @@ Storage formats (one token per row, pages of 64 tokens):
   index key cache   [P, 64, 128] e4m3 bytes + [P, 64] fp32 per-token scale,
                     or [P, 64, 128] bf16 bits (no scale) for the tiny case
   latent KV, bf16   [P, 64, 576] bf16 bits (512 latent + 64 RoPE)
-  latent KV, e4m3   [P, 64, 656] bytes: 512 e4m3 latent bytes, 4 fp32 scales
-                    (one per 128 latent elements), 64 bf16 RoPE values
+  latent KV, e4m3   [P, 64 * 656] bytes, 656 per token as three planes per page:
+                    codes [64][512] e4m3, scales [64][4] fp32 (one per 128 latent
+                    elements), RoPE [64][64] bf16; int8 latent the same with
+                    two's-complement codes
 """
 from __future__ import annotations
 
@@ -45,6 +47,7 @@ D_LATENT = 512
 D_ROPE = 64
 D_QK = D_LATENT + D_ROPE
 FP8_RECORD = D_LATENT + 4 * 4 + 2 * D_ROPE  # 656 bytes per token
+REC_PAGE_BYTES = PAGE * FP8_RECORD           # a page of latent records: codes | scales | RoPE planes
 E4M3_MAX = 448.0
 
 CONFIG_NAMES = ("tiny", "decode", "mtp", "prefill", "longctx")
@@ -55,7 +58,7 @@ CONFIG_SEEDS = {"tiny": 1, "decode": 2, "mtp": 3, "prefill": 4, "longctx": 5}
 class Layer:
     """One attention layer's MLA inputs."""
     q: np.ndarray            # [T, H, 576] uint16 (bf16 bits)
-    kv: np.ndarray           # [P, 64, 576] uint16 (bf16) or [P, 64, 656] uint8 (e4m3 record)
+    kv: np.ndarray           # [P, 64, 576] uint16 (bf16) or [P, 64 * 656] uint8 (record pages)
     kv_dtype: str            # "bf16", "e4m3" or "int8"
 
 
@@ -156,17 +159,24 @@ def make_kv_bf16(rng, num_pages: int) -> np.ndarray:
     return to_bf16_bits(_normal(rng, (num_pages, PAGE, D_QK), 0.5))
 
 
+def record_pages(codes: np.ndarray, scales: np.ndarray, rope_bits: np.ndarray) -> np.ndarray:
+    """Latent record pages [P, 64 * 656] from codes [P, 64, 512] (bytes), scales
+    [P, 64, 4] (fp32) and RoPE [P, 64, 64] (bf16 bits): per page the 64 tokens' codes,
+    then their scales, then their RoPE values (a storage layout, no arithmetic)."""
+    P = codes.shape[0]
+    rec = np.empty((P, REC_PAGE_BYTES), dtype=np.uint8)
+    rec[:, :PAGE * D_LATENT] = codes.reshape(P, -1)
+    rec[:, PAGE * D_LATENT:PAGE * (D_LATENT + 16)] = np.ascontiguousarray(scales, dtype="<f4").view(np.uint8).reshape(P, -1)
+    rec[:, PAGE * (D_LATENT + 16):] = np.ascontiguousarray(rope_bits, dtype="<u2").view(np.uint8).reshape(P, -1)
+    return rec
+
+
 def make_kv_e4m3(rng, num_pages: int) -> np.ndarray:
     """Latent KV rows ~ N(0, 0.5^2) as 656-byte records: the 512 latent values in
     e4m3 with one fp32 scale (amax/448) per 128 of them, then the 64 RoPE values in bf16."""
     x = _normal(rng, (num_pages, PAGE, D_QK), 0.5)
     codes, scales = quantize_rows_e4m3(x[..., :D_LATENT], 128)
-    rope = to_bf16_bits(x[..., D_LATENT:])
-    rec = np.empty((num_pages, PAGE, FP8_RECORD), dtype=np.uint8)
-    rec[..., :D_LATENT] = codes
-    rec[..., D_LATENT:D_LATENT + 16] = np.ascontiguousarray(scales, dtype="<f4").view(np.uint8)
-    rec[..., D_LATENT + 16:] = np.ascontiguousarray(rope, dtype="<u2").view(np.uint8)
-    return rec
+    return record_pages(codes, scales, to_bf16_bits(x[..., D_LATENT:]))
 
 
 def make_kv_int8(rng, num_pages: int) -> np.ndarray:
@@ -177,12 +187,7 @@ def make_kv_int8(rng, num_pages: int) -> np.ndarray:
     amax = np.abs(g).max(axis=-1)
     scales = np.where(amax > 0, amax / np.float32(127.0), np.float32(1.0)).astype(np.float32)
     codes = np.clip(np.rint(g / scales[..., None]), -127, 127).astype(np.int8).view(np.uint8)
-    rope = to_bf16_bits(x[..., D_LATENT:])
-    rec = np.empty((num_pages, PAGE, FP8_RECORD), dtype=np.uint8)
-    rec[..., :D_LATENT] = codes.reshape(num_pages, PAGE, D_LATENT)
-    rec[..., D_LATENT:D_LATENT + 16] = np.ascontiguousarray(scales, dtype="<f4").view(np.uint8).reshape(num_pages, PAGE, 16)
-    rec[..., D_LATENT + 16:] = np.ascontiguousarray(rope, dtype="<u2").view(np.uint8)
-    return rec
+    return record_pages(codes.reshape(num_pages, PAGE, D_LATENT), scales, to_bf16_bits(x[..., D_LATENT:]))
 
 
 def make_workload(name: str, seq_lens, n_q, topk: int, hi: int, qk_dtype: str,

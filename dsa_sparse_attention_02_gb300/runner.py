@@ -46,7 +46,7 @@ def _bytes_of(a: np.ndarray) -> torch.Tensor:
 @dataclass
 class DeviceLayer:
     q: torch.Tensor          # [T, H, 576] bf16
-    kv: torch.Tensor         # [P, 64, 576] bf16 or [P, 64, 656] uint8
+    kv: torch.Tensor         # [P, 64, 576] bf16 or [P, 64 * 656] uint8 record pages
     kv_dtype: int
     out: torch.Tensor        # [T, H, 512] bf16
     lse: torch.Tensor        # [T, H] fp32

@@ -128,10 +128,13 @@ size_t dsa_topk_workspace_size(const dsa_geom_t* geom, int32_t k);
  * dsa_sparse_mla_attend -- step 3 (absorbed MLA over the selected latent rows).
  *   q [T, H, 576] bf16 (device): the absorbed query (W_UK already folded in).
  *   kv_dtype DSA_BF16: kv_cache [num_pages, 64, 576] bf16.
- *   kv_dtype DSA_E4M3: kv_cache [num_pages, 64, 656] bytes per token: 512 e4m3
+ *   kv_dtype DSA_E4M3: kv_cache [num_pages, 41984] bytes, 656 per token: 512 e4m3
  *     latent codes, 4 little-endian fp32 scales (latent element 128c+e is
- *     code*scale[c]), 64 bf16 RoPE values.
- *   kv_dtype DSA_I8: the same 656-byte record with two's-complement int8 codes
+ *     code*scale[c]), 64 bf16 RoPE values. Each page holds its 64 tokens' fields as
+ *     three planes: codes [64][512] at byte 0, scales [64][4] at byte 32768, RoPE
+ *     [64][64] at byte 33792 (token s of the page: codes at 512*s, scales at
+ *     32768 + 16*s, RoPE at 33792 + 128*s).
+ *   kv_dtype DSA_I8: the same record pages with two's-complement int8 codes
  *     (the int8 latent cache of mlx-lm "GLM-5.2 (glm_moe_dsa) inference": only
  *     the compressed latent is quantized; dequantized on read).
  *   idx [T, k] int32 (device): logical positions of the request's tokens; -1 is
@@ -189,11 +192,12 @@ dsa_status_t dsa_sparse_mla_attend_static(const dsa_geom_t* geom, dsa_dtype_t kv
  *     read for that position. geom->T is the number of new tokens.
  *   kv_new [T, 576] bf16 (device): latent (512) then RoPE (64) of each token.
  *   kv_dtype DSA_BF16: kv_cache [num_pages, 64, 576] bf16 receives kv_new as is.
- *   kv_dtype DSA_E4M3: kv_cache [num_pages, 64, 656] bytes receives, per token,
- *     for each group c of 128 latent values scale_c = amax_c / 448 (fp32; 1 for
- *     an all-zero group) and code = e4m3(x / scale_c) (quotient in fp32, round
- *     to nearest even, saturating at +-448): 512 codes, the 4 scales as
- *     little-endian fp32, then the 64 RoPE values as bf16.
+ *   kv_dtype DSA_E4M3: kv_cache [num_pages, 41984] bytes (the record pages of
+ *     dsa_sparse_mla_attend) receives, per token, for each group c of 128 latent
+ *     values scale_c = amax_c / 448 (fp32; 1 for an all-zero group) and
+ *     code = e4m3(x / scale_c) (quotient in fp32, round to nearest even, saturating
+ *     at +-448): its 512 codes, 4 scales (little-endian fp32) and 64 RoPE values
+ *     (bf16) at its slot of the page's three planes.
  *   kv_dtype DSA_I8: the same record with scale_c = amax_c / 127 and int8 codes
  *     round-to-nearest-even(x / scale_c) clamped to +-127.
  *   k_new [T, 128] bf16 (device) or NULL to leave the index cache alone.

@@ -19,8 +19,9 @@ print no layout or rounding, so this follows the layouts the attention reads:
   * e4m3 latent record (656 bytes): for each group c of 128 latent values,
     scale_c = amax_c / 448 in fp32 (1 for an all-zero group) and
     code = e4m3(x / scale_c), the quotient taken in fp32 and rounded to the nearest
-    e4m3 value, ties to the even code, saturating at +-448; then the four scales
-    (little-endian fp32), then the 64 RoPE values in bf16;
+    e4m3 value, ties to the even code, saturating at +-448; the 512 codes, the four
+    scales (little-endian fp32) and the 64 RoPE values (bf16) go to the token's slot
+    of its page's three planes (codes [64][512], scales [64][4], RoPE [64][64]);
   * index keys: e4m3 with one such scale per token over its 128 values (or bf16 as
     given); the scale goes to the [P, 64] scale tensor.
 The fp32 steps are taken in fp32 on purpose: they decide integer codes, and the
@@ -30,6 +31,7 @@ from __future__ import annotations
 
 import numpy as np
 
+from .dsa import record_planes
 from .fp8 import E4M3_TABLE
 
 E4M3_MAX = 448.0
@@ -124,25 +126,29 @@ def cache_append(kv_cache, kv_dtype, kv_new_bits, idx_k_cache, idx_k_scale, qk_d
                  seq_lens, n_q, block_table):
     """Return updated copies of the caches after appending the new tokens.
 
-    kv_cache: [P, 64, 576] uint16 (bf16 bits) or [P, 64, 656] uint8 (e4m3 / int8 records).
+    kv_cache: [P, 64, 576] uint16 (bf16 bits) or [P, 64 * 656] uint8 (e4m3 / int8 record pages).
     kv_new_bits: [T, 576] uint16 bf16 bits.
     idx_k_cache: [P, 64, 128] uint8 (e4m3) or uint16 (bf16 bits), or None;
     idx_k_scale: [P, 64] float32 or None; k_new_bits: [T, 128] uint16 or None.
     """
     rows = token_rows(seq_lens, n_q, block_table)
     kv = np.array(kv_cache, copy=True)
-    flat = kv.reshape(-1, kv.shape[-1])
     x = bf16_bits_to_f32(kv_new_bits)
+    if kv_dtype == "bf16":
+        flat = kv.reshape(-1, kv.shape[-1])
+    else:
+        code_plane, scale_plane, rope_plane = record_planes(kv)
     for t, r in enumerate(rows):
         if kv_dtype == "bf16":
             flat[r] = np.asarray(kv_new_bits[t], dtype=np.uint16)
         else:
             quant = quantize_groups if kv_dtype == "e4m3" else quantize_groups_int8
             codes, scales = quant(x[t, :512], 128)
-            flat[r, :512] = codes
-            flat[r, 512:528] = np.ascontiguousarray(scales, dtype="<f4").view(np.uint8)
-            flat[r, 528:656] = np.ascontiguousarray(np.asarray(kv_new_bits[t, 512:], dtype=np.uint16),
-                                                    dtype="<u2").view(np.uint8)
+            page, slot = r // PAGE, r % PAGE
+            code_plane[page, slot] = codes
+            scale_plane[page, slot] = np.ascontiguousarray(scales, dtype="<f4").view(np.uint8)
+            rope_plane[page, slot] = np.ascontiguousarray(np.asarray(kv_new_bits[t, 512:], dtype=np.uint16),
+                                                          dtype="<u2").view(np.uint8)
     out_k = out_s = None
     if idx_k_cache is not None:
         out_k = np.array(idx_k_cache, copy=True)

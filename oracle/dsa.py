@@ -42,6 +42,13 @@ from .fp8 import decode_bf16, decode_e4m3, decode_f32le, decode_int8
 
 PAGE = 64
 D_LATENT = 512
+# Latent record pages (e4m3 or int8 latent): 656 bytes per token, laid out per page
+# of 64 tokens as three planes, codes [64][512] | fp32 scales [64][4] | bf16 RoPE
+# [64][64], so that every token's codes, scales and RoPE values start on their own
+# 512-, 16- and 128-byte boundaries.
+REC_PAGE_BYTES = PAGE * 656
+REC_SCALES_AT = PAGE * D_LATENT
+REC_ROPE_AT = REC_SCALES_AT + PAGE * 16
 
 
 # ----------------------------------------------------------------------------- geometry
@@ -79,22 +86,36 @@ def decode_index_keys(idx_k, idx_k_scale, qk_dtype, rows):
     return decode_e4m3(flat) * np.asarray(idx_k_scale, dtype=np.float64).reshape(-1)[rows][:, None]
 
 
+def record_planes(kv):
+    """A latent record cache [P, 64*656] bytes -> its per-token fields as views:
+    codes [P, 64, 512], scale bytes [P, 64, 16], RoPE bytes [P, 64, 128]."""
+    pages = np.asarray(kv).reshape(-1, REC_PAGE_BYTES)
+    P = pages.shape[0]
+    return (pages[:, :REC_SCALES_AT].reshape(P, PAGE, D_LATENT),
+            pages[:, REC_SCALES_AT:REC_ROPE_AT].reshape(P, PAGE, 16),
+            pages[:, REC_ROPE_AT:].reshape(P, PAGE, 128))
+
+
 def decode_kv_rows(kv, kv_dtype, rows):
     """Selected rows of the paged latent cache -> float64 [len(rows), 576].
 
     bf16: the 576 stored values. e4m3 or int8 (656-byte record): element 128c+e of
     the latent is code[128c+e] * scale[c] for c = 0..3, followed by the 64 bf16 RoPE
-    values. The int8 latent cache is mlx-lm "GLM-5.2 (glm_moe_dsa) inference",
-    int8 MLA latent KV (only the compressed latent is quantized, dequantized on read);
-    its code layout is the e4m3 record's with two's-complement int8 codes.
+    values; each page stores its tokens' codes, scales and RoPE values as three planes
+    (record_planes). The int8 latent cache is mlx-lm "GLM-5.2 (glm_moe_dsa)
+    inference", int8 MLA latent KV (only the compressed latent is quantized,
+    dequantized on read); its layout is the e4m3 record's with two's-complement codes.
     """
-    flat = kv.reshape(-1, kv.shape[-1])[rows]
+    rows = np.asarray(rows, dtype=np.int64)
     if kv_dtype == "bf16":
-        return decode_bf16(flat)
-    lat = decode_e4m3(flat[:, :D_LATENT]) if kv_dtype == "e4m3" else decode_int8(flat[:, :D_LATENT])
-    scales = decode_f32le(flat[:, D_LATENT:D_LATENT + 16])           # [n, 4]
+        return decode_bf16(kv.reshape(-1, kv.shape[-1])[rows])
+    codes, scale_bytes, rope_bytes = record_planes(kv)
+    page, slot = rows // PAGE, rows % PAGE
+    c = codes[page, slot]                                             # [n, 512]
+    lat = decode_e4m3(c) if kv_dtype == "e4m3" else decode_int8(c)
+    scales = decode_f32le(scale_bytes[page, slot])                    # [n, 4]
     lat = lat * np.repeat(scales, 128, axis=1)
-    rope = decode_bf16(np.ascontiguousarray(flat[:, D_LATENT + 16:]).view("<u2").astype(np.uint16))
+    rope = decode_bf16(np.ascontiguousarray(rope_bytes[page, slot]).view("<u2").astype(np.uint16))
     return np.concatenate([lat, rope], axis=1)
 
 

@@ -162,3 +162,62 @@ def test_attend_maximum_sizes(heads, k, ctx):
     out, lse = _attend(wl, dw, 0, idx, k)
     worst = _check(wl, 0, idx, out, lse)
     print(f"H={heads} k={k}: max |O err| {worst:.3g}")
+
+
+@pytest.mark.parametrize("kv_dtype", ["e4m3", "int8"])
+def test_record_dequantization_bit_exact(kv_dtype):
+    """Every code value times scales from 2^-110 to 1000, read back through the
+    attention with one selected row per query (softmax weight exactly 1, so the output
+    is the dequantized latent row itself): bit for bit bf16(fp32(code * scale)), the
+    rounding the kernel documents, and within bf16 rounding of the oracle's exact
+    value. A row holding a NaN code scores NaN, so its whole output row is NaN (as the
+    oracle's)."""
+    rng = np.random.default_rng(40)
+    P, T, H, k = 4, 64, 16, 8
+    n_rows = P * 64
+    codes = np.empty((n_rows, 512), dtype=np.uint8)
+    for r in range(n_rows):
+        codes[r] = (np.arange(512) + 37 * r) % 256          # every byte value in every row
+    if kv_dtype == "e4m3":   # every 7th row without NaN codes; the others hold both NaN codes
+        codes[5:n_rows:7] = np.where(codes[5:n_rows:7] % 128 == 127, 0x7E, codes[5:n_rows:7])
+    # scales below 2^7 take the kernel's integer path, larger ones the conversion path;
+    # 2^-110 makes the subnormal codes' intermediate fp32 values subnormal too
+    scale_set = np.array([1.0, 0.125, 3.7, 200.0, 1e-3, 2.0 ** -110, 0.0078125, 1000.0], dtype=np.float32)
+    scales = scale_set[rng.integers(0, len(scale_set), size=(n_rows, 4))].astype(np.float32)
+    rope = inputs.to_bf16_bits(rng.standard_normal((n_rows, 64)).astype(np.float32))
+    kv = inputs.record_pages(codes.reshape(P, 64, 512), scales.reshape(P, 64, 4), rope.reshape(P, 64, 64))
+    # T one-query requests over the same pages (identity block table: position = row)
+    bt = np.arange(P, dtype=np.int32)[None].repeat(T, axis=0)
+    sel_rows = rng.permutation(n_rows)[:T]
+    sel_rows[:2] = [5, 6]                                    # a row without NaN codes and one with them
+    q = inputs.to_bf16_bits(rng.standard_normal((T, H, 576)).astype(np.float32))
+    seq_t = torch.full((T,), n_rows, dtype=torch.int32, device=DEV)
+    cu_t = torch.arange(T + 1, dtype=torch.int32, device=DEV)
+    bt_t = torch.from_numpy(bt).to(DEV)
+    g = _lib.Geometry(seq_t, cu_t, bt_t, num_pages=P, max_seq_len=n_rows, T=T)
+    idx = np.full((T, k), -1, dtype=np.int32)
+    idx[:, 3] = sel_rows
+    kv_t = torch.from_numpy(kv).to(DEV)
+    q_t = torch.from_numpy(q.view(np.int16)).to(DEV).view(torch.bfloat16)
+    out = torch.empty(T, H, 512, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(T, H, dtype=torch.float32, device=DEV)
+    ws = _lib.workspace(_lib.dsa_sparse_mla_attend_workspace_size(g, H, k), DEV)
+    kvd = _lib.DSA_E4M3 if kv_dtype == "e4m3" else _lib.DSA_I8
+    _lib.dsa_sparse_mla_attend(g, kvd, q_t, kv_t, torch.from_numpy(idx).to(DEV), k, 0.1, out, lse, ws)
+    assert _lib.dsa_get_error(ws) == 0
+    got = out.float().cpu().numpy()
+    table = oracle.fp8.E4M3_TABLE if kv_dtype == "e4m3" else np.arange(256, dtype=np.uint8).view(np.int8).astype(np.float64)
+    for t in range(T):
+        r = int(sel_rows[t])
+        vals = table[codes[r]].astype(np.float32) * np.repeat(scales[r], 128)    # fp32 product, one rounding
+        exp = torch.from_numpy(vals).to(torch.bfloat16).float().numpy()
+        exact = oracle.decode_kv_rows(kv, kv_dtype, np.array([r]))[0, :512]
+        ref = oracle.sparse_mla(q, kv, kv_dtype, {t: idx[t]}, seq_t.cpu().numpy(), np.ones(T, dtype=np.int32),
+                                bt, 0.1, ts=[t])[t][0]
+        if np.isnan(exp).any():
+            assert np.isnan(got[t]).all() and np.isnan(ref).all(), (t, r)
+            continue
+        for h in range(H):
+            assert np.array_equal(got[t, h], exp), (t, h, r)
+            assert np.all(np.abs(got[t, h] - exact) <= 2.0 ** -8 * np.abs(exact)), (t, h)
+            assert np.all(np.abs(got[t, h] - ref[h]) <= 2.0 ** -8 * np.abs(ref[h]) + 1e-12), (t, h)

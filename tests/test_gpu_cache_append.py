@@ -54,7 +54,7 @@ def _case(rng, kv_dtype, qk_dtype):
     kx[1, :4] = [448.0, 1.0625 * 4, -1.1875 * 4, -0.0]
     kbits = _bits(kx)
     kv = (rng.integers(0, 2 ** 16, size=(P, 64, 576), dtype=np.uint16) if kv_dtype == "bf16"
-          else rng.integers(0, 256, size=(P, 64, 656), dtype=np.uint8))
+          else rng.integers(0, 256, size=(P, 64 * 656), dtype=np.uint8))
     if qk_dtype == "bf16":
         ik = rng.integers(0, 2 ** 16, size=(P, 64, 128), dtype=np.uint16)
         isc = None
@@ -138,7 +138,7 @@ def test_append_prefill_chunk_e4m3():
     bt = rng.permutation(P)[: L // 64].reshape(1, -1).astype(np.int32)
     bits = _bits((rng.standard_normal((n, 576)) * 0.5).astype(np.float32))
     kbits = _bits(rng.standard_normal((n, 128)).astype(np.float32))
-    kv = np.zeros((P, 64, 656), dtype=np.uint8)
+    kv = np.zeros((P, 64 * 656), dtype=np.uint8)
     ik = np.zeros((P, 64, 128), dtype=np.uint8)
     isc = np.zeros((P, 64), dtype=np.float32)
     g = _geometry(seq, nq, bt, P)

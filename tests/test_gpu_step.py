@@ -151,7 +151,12 @@ def test_causality_on_gpu():
     wl2.idx_k = wl.idx_k.copy()
     wl2.idx_k.reshape(-1, 128)[rows] = np.uint8(0x48)
     kv = wl.layers[0].kv.copy()
-    kv.reshape(-1, kv.shape[-1])[rows] = np.uint8(0x48)
+    pages = kv.reshape(-1, 64 * 656)                 # e4m3 record pages: codes | scales | RoPE planes
+    for r in rows:
+        pg, sl = divmod(int(r), 64)
+        pages[pg, 512 * sl:512 * (sl + 1)] = np.uint8(0x48)
+        pages[pg, 32768 + 16 * sl:32768 + 16 * (sl + 1)] = np.uint8(0x48)
+        pages[pg, 33792 + 128 * sl:33792 + 128 * (sl + 1)] = np.uint8(0x48)
     wl2.layers = [inputs.Layer(q=wl.layers[0].q, kv=kv, kv_dtype=wl.layers[0].kv_dtype), wl.layers[1]]
     dw2 = runner.DeviceWorkload(wl2, DEV)
     dw2.step()

@@ -31,7 +31,7 @@ def test_small_variants_of_large_configs():
     assert wl.q_idx.dtype == np.uint8 and wl.q_scale.shape == (4, 64)
     wl = synth.make_config("mtp", batch=2, ctx_scale=0.25)
     _check_geometry(wl)
-    assert wl.T == 8 and len(wl.layers) == 2 and wl.layers[0].kv.shape[-1] == 656
+    assert wl.T == 8 and len(wl.layers) == 2 and wl.layers[0].kv.shape[-1] == 64 * 656
     wl = synth.make_config("longctx", batch=1, ctx_scale=1 / 64)
     _check_geometry(wl)
     assert wl.seq_lens.tolist() == [2048]

@@ -17,6 +17,15 @@ from oracle.fp8 import E4M3_TABLE, decode_bf16, decode_e4m3, decode_f32le
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 
+def _record(kv, r):
+    """Bytes of physical row r in a latent record cache, read at the layout's offsets:
+    per 64-token page, codes [64][512] at 0, scales [64][4] fp32 at 32768, RoPE
+    [64][64] bf16 at 33792."""
+    page, s = divmod(int(r), 64)
+    pg = kv.reshape(-1, 64 * 656)[page]
+    return pg[s * 512:(s + 1) * 512], pg[32768 + s * 16:32768 + (s + 1) * 16], pg[33792 + s * 128:33792 + (s + 1) * 128]
+
+
 def torch_e4m3(v):
     t = torch.tensor(np.asarray(v, dtype=np.float32)).clamp(-448.0, 448.0)
     return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
@@ -85,20 +94,24 @@ def test_hand_worked_e4m3_record():
     bits = (x.view(np.uint32) >> 16).astype(np.uint16)          # exact in bf16
     assert np.array_equal(decode_bf16(bits), x.astype(np.float64))
     seq, nq, bt = _one_token_geometry(pos=70)   # logical page 1 -> physical page bt[0][1] = 0, slot 6
-    kv = np.zeros((3, 64, 656), dtype=np.uint8)
+    kv = np.zeros((3, 64 * 656), dtype=np.uint8)
     out, _, _ = oc.cache_append(kv, "e4m3", bits[None], None, None, "e4m3", None, seq, nq, bt)
-    row = out.reshape(-1, 656)[0 * 64 + 70 % 64]
+    codes, sc_bytes, rope_bytes = _record(out, 0 * 64 + 70 % 64)
     for k, code in g["expected_codes"].items():
-        assert row[int(k)] == int(code, 16), (k, hex(row[int(k)]))
-    scales = decode_f32le(row[512:528])
+        assert codes[int(k)] == int(code, 16), (k, hex(codes[int(k)]))
+    scales = decode_f32le(sc_bytes)
     for c, s in enumerate(g["expected_scales_exact"]):
         if s is None:
             assert scales[c] == float(np.float32(3.0) / np.float32(448.0))
         else:
             assert scales[c] == s
-    assert np.array_equal(decode_bf16(row[528:].view(np.uint16)), x[512:].astype(np.float64))
-    # every other row is untouched
-    rest = np.delete(out.reshape(-1, 656), 6, axis=0)
+    assert np.array_equal(decode_bf16(rope_bytes.view(np.uint16)), x[512:].astype(np.float64))
+    # every other byte is untouched
+    rest = out.copy()
+    page = rest.reshape(-1, 64 * 656)[0]
+    page[6 * 512:7 * 512] = 0
+    page[32768 + 6 * 16:32768 + 7 * 16] = 0
+    page[33792 + 6 * 128:33792 + 7 * 128] = 0
     assert not rest.any()
 
 
@@ -117,7 +130,7 @@ def _random_append_case(rng, kv_dtype, qk_dtype):
     if kv_dtype == "bf16":
         kv = rng.integers(0, 2 ** 16, size=(P, 64, 576), dtype=np.uint16)
     else:
-        kv = rng.integers(0, 256, size=(P, 64, 656), dtype=np.uint8)
+        kv = rng.integers(0, 256, size=(P, 64 * 656), dtype=np.uint8)
     if qk_dtype == "bf16":
         ik = rng.integers(0, 2 ** 16, size=(P, 64, 128), dtype=np.uint16)
         isc = None
@@ -136,19 +149,26 @@ def test_append_rows_round_trip_and_untouched_rows(kv_dtype, qk_dtype):
     req, pos = oracle.query_positions(seq, nq)
     rows = np.array([bt[b][p // 64] * 64 + p % 64 for b, p in zip(req, pos)])
     assert np.array_equal(rows, oc.token_rows(seq, nq, bt))
-    width = out.shape[-1]
     touched = np.zeros(out.shape[0] * 64, dtype=bool)
     touched[rows] = True
-    assert np.array_equal(out.reshape(-1, width)[~touched], kv.reshape(-1, width)[~touched])
+    if kv_dtype == "bf16":
+        assert np.array_equal(out.reshape(-1, 576)[~touched], kv.reshape(-1, 576)[~touched])
+    else:
+        # every byte outside the new tokens' codes, scales and RoPE values is unchanged
+        mask = np.ones(out.size, dtype=bool)
+        for r in rows:
+            for field in _record(np.arange(out.size).reshape(out.shape), r):
+                mask[field] = False
+        assert np.array_equal(out.reshape(-1)[mask], kv.reshape(-1)[mask])
     assert np.array_equal(ok_.reshape(-1, 128)[~touched], ik.reshape(-1, 128)[~touched])
     x = decode_bf16(bits)
     for t, r in enumerate(rows):
-        rec = out.reshape(-1, width)[r]
         if kv_dtype == "bf16":
-            assert np.array_equal(rec, bits[t])
+            assert np.array_equal(out.reshape(-1, 576)[r], bits[t])
         else:
-            scales = decode_f32le(rec[512:528])
-            deq = decode_e4m3(rec[:512]) * np.repeat(scales, 128)
+            codes, sc_bytes, rope_bytes = _record(out, r)
+            scales = decode_f32le(sc_bytes)
+            deq = decode_e4m3(codes) * np.repeat(scales, 128)
             amax = np.abs(x[t, :512]).reshape(4, 128).max(axis=1)
             # scale = amax/448 in fp32; round trip within half an e4m3 step (2^-4 relative,
             # 2^-10 * scale absolute in the subnormal range)
@@ -156,7 +176,7 @@ def test_append_rows_round_trip_and_untouched_rows(kv_dtype, qk_dtype):
             assert np.all(scales[amax == 0] == 1.0)
             bound = np.abs(x[t, :512]) * 2.0 ** -4 + np.repeat(scales, 128) * 2.0 ** -10
             assert np.all(np.abs(deq - x[t, :512]) <= bound * (1 + 1e-6))
-            assert np.array_equal(rec[528:].view(np.uint16), bits[t, 512:])
+            assert np.array_equal(rope_bytes.view(np.uint16), bits[t, 512:])
         krow = ok_.reshape(-1, 128)[r]
         if qk_dtype == "bf16":
             assert np.array_equal(krow, kbits[t])
@@ -194,10 +214,10 @@ def test_int8_append_round_trip_within_half_a_step():
     rows = oc.token_rows(seq, nq, bt)
     x = decode_bf16(bits)
     for t, r in enumerate(rows):
-        rec = out.reshape(-1, 656)[r]
-        scales = decode_f32le(rec[512:528])
+        codes, sc_bytes, rope_bytes = _record(out, r)
+        scales = decode_f32le(sc_bytes)
         amax = np.abs(x[t, :512]).reshape(4, 128).max(axis=1)
         assert np.all(scales[amax > 0] == amax[amax > 0].astype(np.float32) / np.float32(127))
-        deq = rec[:512].view(np.int8).astype(np.float64) * np.repeat(scales, 128)
+        deq = codes.view(np.int8).astype(np.float64) * np.repeat(scales, 128)
         assert np.all(np.abs(deq - x[t, :512]) <= np.repeat(scales, 128) * (0.5 + 1e-6))
-        assert np.array_equal(rec[528:].view(np.uint16), bits[t, 512:])
+        assert np.array_equal(rope_bytes.view(np.uint16), bits[t, 512:])

@@ -59,8 +59,8 @@ MUTANTS = [
      [(".reshape(-1)[rows][:, None]", ".reshape(-1)[np.asarray(rows) - np.asarray(rows) % 64][:, None]")]),
     ("latent-scales-interleaved", "dsa", "decode_kv_rows",
      [("np.repeat(scales, 128, axis=1)", "np.tile(scales, (1, 128))")]),
-    ("rope-read-over-the-scales", "dsa", "decode_kv_rows",
-     [("flat[:, D_LATENT + 16:]", "flat[:, D_LATENT:D_LATENT + 128]")]),
+    ("rope-of-the-next-slot", "dsa", "decode_kv_rows",
+     [("rope_bytes[page, slot]", "rope_bytes[page, (slot + 1) % PAGE]")]),
     ("int8-latent-decoded-as-e4m3", "dsa", "decode_kv_rows",
      [('if kv_dtype == "e4m3" else', 'if kv_dtype in ("e4m3", "int8") else')]),
     # indexer
@@ -120,7 +120,14 @@ MUTANTS = [
      [("amax / np.float32(I8_MAX)", "amax / np.float32(E4M3_MAX)")]),
     ("append-position-off-by-one", "cache", "token_rows",
      [("pos = int(L) - int(n) + j", "pos = int(L) - int(n) + j + 1")]),
-    ("append-rope-over-the-scales", "cache", "cache_append", [("flat[r, 528:656]", "flat[r, 512:640]")]),
+    ("append-rope-over-the-scales", "cache", "cache_append",
+     [("rope_plane[page, slot] = np.ascontiguousarray", "scale_plane[page, slot, :] = 0\n"
+       "            rope_plane[page, slot] = np.ascontiguousarray")]),
+    ("record-rope-plane-offset", "dsa", "record_planes",
+     [("pages[:, REC_ROPE_AT:].reshape", "pages[:, REC_ROPE_AT - 128:-128].reshape")]),
+    ("record-scale-plane-not-per-token", "dsa", "record_planes",
+     [("pages[:, REC_SCALES_AT:REC_ROPE_AT].reshape(P, PAGE, 16)",
+       "pages[:, REC_SCALES_AT:REC_ROPE_AT].reshape(P, 16, PAGE).transpose(0, 2, 1)")]),
     ("append-key-scale-not-written", "cache", "cache_append", [("out_s[r] = scale[0]", "pass")]),
     ("append-e4m3-scale-per-row", "cache", "cache_append",
      [("codes, scales = quant(x[t, :512], 128)", "codes, scales = quant(x[t, :512], 512)\n"

@@ -50,13 +50,19 @@ def test_bf16_decode_matches_torch():
 
 def test_fp8_record_decode_by_hand():
     g = _golden("fp8_record.json")
-    rec = np.zeros((1, 64, 656), dtype=np.uint8)
-    rec[0, 0, :512] = g["latent_code"]
-    rec[0, 0, 512:528] = np.array(g["scales"], dtype="<f4").view(np.uint8)
-    rec[0, 0, 528:] = np.full(64, g["rope_bf16_bits"], dtype="<u2").view(np.uint8)
-    row = oracle.decode_kv_rows(rec, "e4m3", np.array([0]))[0]
+    # two pages of records; the record sits at page 1, slot 5 (physical row 69), at the
+    # byte offsets the golden gives: codes, scales and RoPE each in their own plane
+    rec = np.zeros((2, 64 * 656), dtype=np.uint8)
+    off = g["offsets_in_page_for_slot_5"]
+    rec[1, off["codes"]:off["codes"] + 512] = g["latent_code"]
+    rec[1, off["scales"]:off["scales"] + 16] = np.array(g["scales"], dtype="<f4").view(np.uint8)
+    rec[1, off["rope"]:off["rope"] + 128] = np.full(64, g["rope_bf16_bits"], dtype="<u2").view(np.uint8)
+    row = oracle.decode_kv_rows(rec, "e4m3", np.array([69]))[0]
     exp = np.concatenate([np.full(128, s) for s in g["scales"]] + [np.full(64, g["rope_value"])])
     assert np.array_equal(row, exp)
+    # every other row of the two pages decodes to zeros (nothing of it was written)
+    others = oracle.decode_kv_rows(rec, "e4m3", np.array([r for r in range(128) if r != 69]))
+    assert not others.any()
 
 
 # ----------------------------------------------------------------------------- geometry
@@ -367,9 +373,9 @@ def test_fp8_latent_dequant_is_exact_product():
     rec = wl.layers[0].kv
     rows = np.arange(64)
     dec = oracle.decode_kv_rows(rec, "e4m3", rows)
-    flat = rec.reshape(-1, 656)[rows]
-    scales = flat[:, 512:528].copy().view("<f4").astype(np.float64)
-    codes = torch.from_numpy(flat[:, :512].copy()).view(torch.float8_e4m3fn)
+    page = rec.reshape(-1, 64 * 656)[0]                       # rows 0..63 are page 0's slots
+    scales = page[32768:33792].reshape(64, 16).copy().view("<f4").astype(np.float64)
+    codes = torch.from_numpy(page[:32768].reshape(64, 512).copy()).view(torch.float8_e4m3fn)
     ref = codes.to(torch.float64).numpy() * np.repeat(scales, 128, axis=1)
     np.testing.assert_array_equal(dec[:, :512], ref)
     # the quantized latent stays within half an e4m3 step (2^-4 relative) of amax-scaled data
@@ -386,10 +392,10 @@ def test_int8_latent_record_decodes_like_the_bf16_rows_it_stands_for():
     codes = rng.integers(-127, 128, size=(P, 64, 512)).astype(np.int8)
     rope = rng.standard_normal((P, 64, 64)).astype(np.float32)
     rope_bits = (rope.view(np.uint32) >> 16).astype(np.uint16)
-    rec = np.empty((P, 64, 656), dtype=np.uint8)
-    rec[..., :512] = codes.view(np.uint8)
-    rec[..., 512:528] = np.ascontiguousarray(scales, dtype="<f4").view(np.uint8).reshape(P, 64, 16)
-    rec[..., 528:] = np.ascontiguousarray(rope_bits, dtype="<u2").view(np.uint8)
+    rec = np.empty((P, 64 * 656), dtype=np.uint8)              # per page: codes | scales | RoPE planes
+    rec[:, :32768] = codes.view(np.uint8).reshape(P, -1)
+    rec[:, 32768:33792] = np.ascontiguousarray(scales, dtype="<f4").view(np.uint8).reshape(P, -1)
+    rec[:, 33792:] = np.ascontiguousarray(rope_bits, dtype="<u2").view(np.uint8).reshape(P, -1)
     lat = codes.astype(np.float32) * np.repeat(scales, 128, axis=-1)          # exact in bf16 (8-bit codes x 2^k)
     full = np.concatenate([lat, decode_bf16(rope_bits).astype(np.float32)], axis=-1)
     kv_bf16 = (full.view(np.uint32) >> 16).astype(np.uint16)
