@@ -55,15 +55,20 @@ constexpr int kMlaKeysC = kMlaKeys;
 constexpr int kAtomBytes = kMlaKeys * 128;          // 16 KB: 128 rows x 64 bf16
 constexpr int kPairBytes = 2 * kAtomBytes;          // 32 KB
 // bf16 cache: five pair slots (two and a half chunks of the CTA's two pairs) that the
-// rows are gathered into. Record caches (e4m3 / int8 codes): three bf16 pair slots that
-// the codes are converted into, fed by two code stages of one chunk each (the CTA's
-// 256 codes and two scales of each of the chunk's 128 rows), so that the code bytes in
-// flight do not wait on the bf16 slots.
-template <int kKv> constexpr int kPairSlotsOf = kKv == kKvBf16 ? 5 : 3;
-constexpr int kCodeStages = 2;
-constexpr int kCodeRowBytes = 256;                          // the CTA's half of a row's codes
-constexpr int kCodeBytes = kMlaKeysC * kCodeRowBytes;       // 32 KB
-constexpr int kCodeStageBytes = kCodeBytes + kMlaKeysC * 8;   // + two fp32 scales per row
+// rows are gathered into. Record caches (e4m3 / int8 codes): four bf16 pair slots (two
+// chunks) that the codes are converted into, so that a chunk's conversion waits only on
+// the attention of the chunk two before it, fed by three code stages of one pair each
+// (the pair's 128 codes and one scale of each of the chunk's 128 rows), so that the
+// code bytes in flight do not wait on the bf16 slots. To fit, record caches keep one P
+// buffer and one partial-score exchange buffer (the softmax writes P(i) only after
+// PV(i-1) has completed, so a second P buffer would never be used).
+template <int kKv> constexpr int kPairSlotsOf = kKv == kKvBf16 ? 5 : 4;
+template <int kKv> constexpr int kPBufsOf = kKv == kKvBf16 ? 2 : 1;
+template <int kKv> constexpr int kXBufsOf = kKv == kKvBf16 ? 2 : 1;
+constexpr int kCodeStages = 3;
+constexpr int kCodeRowBytes = 128;                          // one pair's codes of a row
+constexpr int kCodeBytes = kMlaKeysC * kCodeRowBytes;       // 16 KB
+constexpr int kCodeStageBytes = kCodeBytes + kMlaKeysC * 4;   // + the pair's fp32 scale per row
 constexpr int kRopeSlots = 2;                       // halves of one RoPE atom (chunk parity)
 constexpr int kQAtomBytes = kMlaHeads * 128;        // 2 KB
 constexpr int kQAtoms = 6;                          // the CTA's 4 latent atoms + 2 RoPE atoms
@@ -72,7 +77,7 @@ constexpr int kPBufBytes = 2 * kQAtomBytes;         // P^T: 16 heads x 128 keys 
 constexpr int kXBufBytes = kMlaKeys * kMlaHeads * 4;  // partial scores from the other CTA: 8 KB
 template <int kKv>
 constexpr int kMlaSmemBytesOf = 1024 + kPairSlotsOf<kKv> * kPairBytes + (kKv == kKvBf16 ? 0 : kCodeStages * kCodeStageBytes) +
-                                kAtomBytes + kQBufBytes + 2 * kPBufBytes + 2 * kXBufBytes;
+                                kAtomBytes + kQBufBytes + kPBufsOf<kKv> * kPBufBytes + kXBufsOf<kKv> * kXBufBytes;
 constexpr int kMlaSmemBytes = kMlaSmemBytesOf<kKvBf16>;
 // Twelve warps, 168 registers each (three per SM sub-partition):
 //   warps 0-3   softmax (one per TMEM lane quarter)
@@ -216,15 +221,17 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
   constexpr int kPairSlots = kPairSlotsOf<kKv>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // Swizzled operand tiles first (each 1024-byte aligned), then the record caches' code
+  // stages, which cp.async and plain loads address at 16-byte granularity.
   uint8_t* pair_buf = smem;                                         // kPairSlots x 32 KB
-  uint8_t* code_buf = pair_buf + kPairSlots * kPairBytes;           // record caches: kCodeStages x 33 KB
-  uint8_t* rope_buf = code_buf + (kRecord ? kCodeStages * kCodeStageBytes : 0);   // 16 KB
+  uint8_t* rope_buf = pair_buf + kPairSlots * kPairBytes;           // 16 KB
   uint8_t* q_buf = rope_buf + kAtomBytes;                           // 12 KB
   uint8_t* p_buf = q_buf + kQBufBytes;                              // 2 x 4 KB
-  float4* x_buf = reinterpret_cast<float4*>(p_buf + 2 * kPBufBytes);  // 2 x [4 head quads][128 keys]
+  constexpr int kPBufs = kPBufsOf<kKv>, kXBufs = kXBufsOf<kKv>;
+  float4* x_buf = reinterpret_cast<float4*>(p_buf + kPBufs * kPBufBytes);  // kXBufs x [4 head quads][128 keys]
+  uint8_t* code_buf = reinterpret_cast<uint8_t*>(x_buf) + kXBufs * kXBufBytes;   // record caches: kCodeStages x 16.5 KB
 
   __shared__ uint64_t pair_full[kPairSlots], pair_empty[kPairSlots], rope_full[kRopeSlots], rope_empty[kRopeSlots];
-  __shared__ uint64_t code_full[kCodeStages], code_empty[kCodeStages];   // record caches
   __shared__ uint64_t q_full, q_empty;
   __shared__ uint64_t s_full[2], s_empty[2], p_full[2], p_empty[2], o_full, o_free, grp_bar;
   __shared__ uint64_t x_full[2], x_free[2];   // partial-score exchange with the other CTA
@@ -286,10 +293,6 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     for (int j = 0; j < kPairSlots; ++j) {
       mbar_init(smem_u32(&pair_full[j]), kRecord ? slot_producers : 64);
       mbar_init(smem_u32(&pair_empty[j]), 1);
-    }
-    for (int j = 0; j < kCodeStages; ++j) {
-      mbar_init(smem_u32(&code_full[j]), slot_producers);    // noinc arrivals of every producer thread
-      mbar_init(smem_u32(&code_empty[j]), slot_producers);   // every producer thread has read its codes
     }
     for (int j = 0; j < kRopeSlots; ++j) { mbar_init(smem_u32(&rope_full[j]), slot_producers); mbar_init(smem_u32(&rope_empty[j]), 1); }
     mbar_init(smem_u32(&q_full), 1);
@@ -406,17 +409,19 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     }
   } else if (warp >= kProdWarp0 && warp < kProdWarp0 + kProdWarps) {
     // ================================================================ producers (record caches)
-    // Warp pw owns rows [32*pw, 32*pw+32) of every chunk. For chunk i it copies those
-    // rows' RoPE columns of this CTA into the RoPE atom, and their 256 codes and two
-    // scales (latent groups 2*rank, 2*rank+1) into code stage i % 2 (16-byte and
-    // 8-byte cp.async, zero-fill for padding, noinc arrivals on code_full); then it
-    // converts chunk i-1's codes of the same rows, code * scale rounded to bf16, into
-    // that chunk's two bf16 pair slots (in the swizzled K-major layout the MMA reads)
-    // and marks its share of each slot full. The copies of chunk i are therefore in
-    // flight while chunk i-1 is converted, and code bytes never wait on a pair slot.
-    // Every wait a warp makes before converting chunk i-1 depends only on chunks
-    // before it (the query buffer of a new segment, which the MMA frees after the
-    // previous chunk's scores, is taken after the conversion).
+    // Pair g = 2i + jl is latent pair jl of chunk i (this CTA's latent group 2*rank+jl).
+    // Warp pw owns rows [32*pw, 32*pw+32) of every chunk. Step g: the warp copies its
+    // rows' 128 codes and one scale of pair g into code stage g % 3 (16-byte and 4-byte
+    // cp.async, zero-fill for padding, one commit group per step), and, with a new
+    // chunk, its rows' RoPE columns into the RoPE atom; then it converts pair g - 2 of
+    // the same rows, code * scale rounded to bf16, into pair slot (g - 2) % 4 (the
+    // swizzled K-major layout the MMA reads) and marks its share of the slot full. Two
+    // pairs are thus in flight while one is converted, and a pair's slot is the one
+    // pair g - 6 used, freed by the attention of the chunk two before: the conversion
+    // never waits on the chunk just before it. Every wait before converting pair g - 2
+    // depends only on pairs before it (the query buffer of a new segment, which the MMA
+    // frees after the previous chunk's scores, is taken after that chunk's conversion).
+    constexpr int kLag = 2;
     const int pw = warp - kProdWarp0;
     auto slot_acquire = [&](uint32_t bar, uint32_t parity) -> bool {
       int ok = 1;
@@ -424,90 +429,111 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       return __shfl_sync(0xffffffffu, ok, 0) != 0;
     };
     const uint8_t* kv = A.kv;
-    // Chunk ic's rows of this warp, code stage ic % 2 -> bf16 pair slots of the chunk.
-    auto convert = [&](int ic) -> bool {
-      const int cs = ic % kCodeStages;
-      if (!slot_acquire(smem_u32(&code_full[cs]), (ic / kCodeStages) & 1)) return false;
-      mbar_try_wait(smem_u32(&code_full[cs]), (ic / kCodeStages) & 1);   // acquire in every lane
+    // A warp's rows of a code stage are copied and read by that warp alone, so the
+    // stages need no barrier: cp.async groups (one per step) say when a pair's copies
+    // have landed, and the warp's own order says when a stage may be reused.
+    auto convert = [&](int gc, int pending) -> bool {
+      const int cs = gc % kCodeStages, ps = gc % kPairSlots;
+      if (pending >= 2) cp_async_wait<2>();
+      else if (pending == 1) cp_async_wait<1>();
+      else cp_async_wait<0>();
+      __syncwarp();   // the row's scale was copied by another lane of the warp
+      if (!slot_acquire(smem_u32(&pair_empty[ps]), ((gc / kPairSlots) & 1) ^ 1)) return false;
       const uint8_t* stg = code_buf + cs * kCodeStageBytes;
-      const float* scl = reinterpret_cast<const float*>(stg + kCodeBytes);   // [128 rows][2]
-      const int part = lane & 7, sub = lane >> 3;
-      const int col_byte = (part >> 2) * 128 + (part & 3) * 32;   // pair columns 16p.. -> atom p/4
+      const float* scl = reinterpret_cast<const float*>(stg + kCodeBytes);   // [128 rows]
+      uint8_t* slot = pair_buf + ps * kPairBytes;
+      // A quarter warp converts rows r0 (even) and r0+1 together: lanes 0-3 of it take
+      // pieces p = 4a + (0..3) of row r0 and lanes 4-7 pieces 4(1-a) + (0..3) of row
+      // r0+1. With the stage and the slot both swizzled by row, the eight lanes then
+      // touch eight different 16-byte bank groups on every load and store.
+      const int rsel = (lane >> 2) & 1, p4 = lane & 3;
 #pragma unroll 1
-      for (int jl = 0; jl < 2; ++jl) {
-        const int gidx = 2 * ic + jl, ps = gidx % kPairSlots;
-        if (!slot_acquire(smem_u32(&pair_empty[ps]), ((gidx / kPairSlots) & 1) ^ 1)) return false;
-        uint8_t* slot = pair_buf + ps * kPairBytes;
-#pragma unroll 2
-        for (int q = 0; q < 8; ++q) {
-          const int r = 32 * pw + 4 * q + sub;
-          const uint4 c = *reinterpret_cast<const uint4*>(stg + r * kCodeRowBytes + 128 * jl + 16 * part);
-          const float sc = scl[2 * r + jl];
+      for (int q = 0; q < 4; ++q) {
+        const int r = 32 * pw + 8 * q + 2 * (lane >> 3) + rsel;
+        const float sc = scl[r];
+#pragma unroll
+        for (int a = 0; a < 2; ++a) {
+          const int piece = 4 * (a ^ rsel) + p4;   // codes 16*piece .. 16*piece+15 of the pair
+          const uint4 c = *reinterpret_cast<const uint4*>(stg + r * kCodeRowBytes + ((piece ^ (r & 7)) << 4));
           uint32_t pk[8];
           dequant16<kKv>(c, sc, pk);
-          *reinterpret_cast<uint4*>(slot + sw128_offset(r, col_byte, kAtomBytes)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          *reinterpret_cast<uint4*>(slot + sw128_offset(r, col_byte + 16, kAtomBytes)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          *reinterpret_cast<uint4*>(slot + sw128_offset(r, 32 * piece, kAtomBytes)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(slot + sw128_offset(r, 32 * piece + 16, kAtomBytes)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
         }
-        fence_proxy_async_smem();   // the MMA reads the slot through the async proxy
-        mbar_arrive(smem_u32(&pair_full[ps]));
       }
-      mbar_arrive(smem_u32(&code_empty[cs]));
+      fence_proxy_async_smem();   // the MMA reads the slot through the async proxy
+      mbar_arrive(smem_u32(&pair_full[ps]));
       return true;
     };
-    int seg = 0;
+    int seg = 1;   // segments whose query has been loaded (the first at the kernel's start)
     bool ok = true;
+    const int n_pairs = 2 * n_mine;
     ChunkPos cp = chunk_pos(0);
-    for (int i = 0; i < n_mine && ok; chunk_next(cp, ++i)) {
-      const int rb = i % kRowBufs, rs = i % kRopeSlots, cs = i % kCodeStages;
-      if (!slot_acquire(smem_u32(&rows_full[rb]), (i / kRowBufs) & 1)) break;
-      mbar_try_wait(smem_u32(&rows_full[rb]), (i / kRowBufs) & 1);   // acquire in every lane (phase is complete)
-      const int* rows = rows_s[rb];
-      if (!slot_acquire(smem_u32(&rope_empty[rs]), ((i / kRopeSlots) & 1) ^ 1)) break;
-      {
-        const uint32_t dst0 = smem_u32(rope_buf);
+    for (int g = 0; g < n_pairs + kLag && ok; ++g) {
+      if (g < n_pairs) {
+        const int i = g >> 1, jl = g & 1, rb = i % kRowBufs, cs = g % kCodeStages;
+        if (!slot_acquire(smem_u32(&rows_full[rb]), (i / kRowBufs) & 1)) break;
+        mbar_try_wait(smem_u32(&rows_full[rb]), (i / kRowBufs) & 1);   // acquire in every lane (phase is complete)
+        const int* rows = rows_s[rb];
+        if (jl == 0) {
+          const int rs = i % kRopeSlots;
+          if (!slot_acquire(smem_u32(&rope_empty[rs]), ((i / kRopeSlots) & 1) ^ 1)) break;
+          const uint32_t dst0 = smem_u32(rope_buf);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int ri = 32 * pw + 8 * q + (lane >> 2);
-          const int row = rows[ri];
-          const int cb = (lane & 3) * 16;
-          cp_async_16(dst0 + sw128_offset(ri, 64 * rs + cb, 0),
-                      kv + rec_rope_at(row >= 0 ? row : 0) + 64 * rank + cb, row >= 0 ? 16u : 0u);
+          for (int q = 0; q < 4; ++q) {
+            const int ri = 32 * pw + 8 * q + (lane >> 2);
+            const int row = rows[ri];
+            const int cb = (lane & 3) * 16;
+            cp_async_16(dst0 + sw128_offset(ri, 64 * rs + cb, 0),
+                        kv + rec_rope_at(row >= 0 ? row : 0) + 64 * rank + cb, row >= 0 ? 16u : 0u);
+          }
+          cp_async_arrive_noinc(smem_u32(&rope_full[rs]));
         }
-        cp_async_arrive_noinc(smem_u32(&rope_full[rs]));
-      }
-      if (!slot_acquire(smem_u32(&code_empty[cs]), ((i / kCodeStages) & 1) ^ 1)) break;
-      {
-        uint8_t* stg = code_buf + cs * kCodeStageBytes;
-        const uint32_t dst_codes = smem_u32(stg), dst_scales = smem_u32(stg + kCodeBytes);
-        const int part = lane & 15;
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {   // 16 lanes per row (256 B), 2 rows per instruction
-          const int r = 32 * pw + 2 * q + (lane >> 4);
-          const int row = rows[r];
-          cp_async_16(dst_codes + r * kCodeRowBytes + 16 * part,
-                      kv + rec_codes_at(row >= 0 ? row : 0) + kCodeRowBytes * rank + 16 * part, row >= 0 ? 16u : 0u);
-        }
+        __syncwarp();   // every lane has read this stage's previous pair (converted two steps ago)
         {
+          uint8_t* stg = code_buf + cs * kCodeStageBytes;
+          const uint32_t dst_codes = smem_u32(stg), dst_scales = smem_u32(stg + kCodeBytes);
+          const int part = lane & 7;
+          const int64_t col = 256 * rank + 128 * jl + 16 * part;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {   // 8 lanes per row (128 B), 4 rows per instruction; piece swizzled by row
+            const int r = 32 * pw + 4 * q + (lane >> 3);
+            const int row = rows[r];
+            cp_async_16(dst_codes + r * kCodeRowBytes + ((part ^ (r & 7)) << 4), kv + rec_codes_at(row >= 0 ? row : 0) + col,
+                        row >= 0 ? 16u : 0u);
+          }
           const int r = 32 * pw + lane;
           const int row = rows[r];
-          cp_async_8(dst_scales + 8 * r, kv + rec_scales_at(row >= 0 ? row : 0) + 8 * rank, row >= 0 ? 8u : 0u);
+          cp_async_4(dst_scales + 4 * r, kv + rec_scales_at(row >= 0 ? row : 0) + 4 * (2 * rank + jl),
+                     row >= 0 ? 4u : 0u);
+          cp_async_commit();
         }
-        cp_async_arrive_noinc(smem_u32(&code_full[cs]));
+        if (jl == 1) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&rows_empty[rb]));   // the copies need no row ids any more
+        }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&rows_empty[rb]));   // the copies need no row ids any more
-      if (i > 0 && !convert(i - 1)) { ok = false; break; }
-      if (cp.first) {
-        // a new segment's query: the MMA frees the buffer after the previous segment's
-        // last scores, which needed the conversion just done
-        if (pw == 0 && seg > 0) {
-          if (!slot_acquire(smem_u32(&q_empty), (seg & 1) ^ 1)) break;
-          if (lane == 0) load_q(cp.t);
+      if (g >= kLag) {
+        const int gc = g - kLag;
+        // groups committed after pair gc's: pairs gc+1 .. min(g, n_pairs-1)
+        if (!convert(gc, (g < n_pairs ? g : n_pairs - 1) - gc)) { ok = false; break; }
+        if (gc & 1) {
+          // chunk gc/2 is converted; a new segment's query follows once the MMA has
+          // freed the buffer after the previous segment's last scores
+          const int ic = gc >> 1;
+          if (ic + 1 < n_mine) {
+            chunk_next(cp, ic + 1);
+            if (cp.first) {
+              if (pw == 0) {
+                if (!slot_acquire(smem_u32(&q_empty), (seg & 1) ^ 1)) break;
+                if (lane == 0) load_q(cp.t);
+              }
+              ++seg;
+            }
+          }
         }
-        ++seg;
       }
     }
-    if (ok && n_mine > 0 && !abort_flag) convert(n_mine - 1);
   } else if (warp == kResolverWarp) {
     // ================================================================ row resolver
     ChunkPos cp = chunk_pos(0);
@@ -550,10 +576,10 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         bool progress = false;
         if (pv_i < s_i) {
           const ChunkPos& cp = pv_cp;
-          const int sb = pv_i & 1;
+          const int sb = pv_i % kPBufs;
           // a new segment's first PV overwrites O: the previous segment's O must have been read
           const bool o_ok = !cp.first || pv_seg < 0 || mbar_test_wait(smem_u32(&o_free), pv_seg & 1);
-          if (o_ok && mbar_test_wait(smem_u32(&p_full[sb]), (pv_i >> 1) & 1)) {
+          if (o_ok && mbar_test_wait(smem_u32(&p_full[sb]), (pv_i / kPBufs) & 1)) {
             if (cp.first) ++pv_seg;
             tc_fence_after();
             const uint64_t bd0 = desc_add(dk_p, sb * kPBufBytes);
@@ -649,8 +675,10 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     const uint32_t xfree_remote = mapa_shared(smem_u32(&x_free[0]), peer);
     ChunkPos cp = chunk_pos(0);
     for (int i = 0; i < n_mine; chunk_next(cp, ++i)) {
-      const int sb = i & 1;
+      const int sb = i & 1;                          // S buffer in TMEM
       const uint32_t ph2 = (i >> 1) & 1;
+      const int xb = i % kXBufs, pbi = i % kPBufs;   // exchange and P buffers
+      const uint32_t xph = (i / kXBufs) & 1, pph = (i / kPBufs) & 1;
       if (cp.first) {
 #pragma unroll
         for (int h = 0; h < kMlaHeads; ++h) { m[h] = neg_inf; l[h] = 0.f; }
@@ -671,20 +699,20 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       if (lane == 0) mbar_arrive(smem_u32(&s_empty[sb]));
       // ---- exchange the partial scores with the other CTA (buffer sb, layout [quad][key]):
       // st.async into its buffer, counted on its x_full; it signals x_free once read.
-      if (!mbar_wait(smem_u32(&x_free[sb]), ph2 ^ 1, &abort_flag, A.err)) break;   // it has read buffer sb
+      if (!mbar_wait(smem_u32(&x_free[xb]), xph ^ 1, &abort_flag, A.err)) break;   // it has read buffer xb
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4)
-        st_async_v4(x_remote + (uint32_t)(sb * kXBufBytes + q4 * kMlaKeys * 16), z[4 * q4], z[4 * q4 + 1],
-                    z[4 * q4 + 2], z[4 * q4 + 3], xfull_remote + sb * 8);
-      if (tid == 0) mbar_arrive_expect_tx(smem_u32(&x_full[sb]), kXBufBytes);
-      if (!mbar_wait<true>(smem_u32(&x_full[sb]), ph2, &abort_flag, A.err)) break;
+        st_async_v4(x_remote + (uint32_t)(xb * kXBufBytes + q4 * kMlaKeys * 16), z[4 * q4], z[4 * q4 + 1],
+                    z[4 * q4 + 2], z[4 * q4 + 3], xfull_remote + xb * 8);
+      if (tid == 0) mbar_arrive_expect_tx(smem_u32(&x_full[xb]), kXBufBytes);
+      if (!mbar_wait<true>(smem_u32(&x_full[xb]), xph, &abort_flag, A.err)) break;
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
-        const float4 v = x_buf[sb * (kXBufBytes / 16) + q4 * kMlaKeys + tid];
+        const float4 v = x_buf[xb * (kXBufBytes / 16) + q4 * kMlaKeys + tid];
         z[4 * q4] += v.x; z[4 * q4 + 1] += v.y; z[4 * q4 + 2] += v.z; z[4 * q4 + 3] += v.w;
       }
       __syncwarp();   // the warp's reads of the buffer are done (their sums are in registers)
-      if (lane == 0) mbar_arrive_remote_signal(xfree_remote + sb * 8);
+      if (lane == 0) mbar_arrive_remote_signal(xfree_remote + xb * 8);
 #pragma unroll
       for (int h = 0; h < kMlaHeads; ++h) z[h] = valid ? z[h] * A.scale_log2 : neg_inf;
       // The reference max of a head moves only where this chunk exceeds it by more
@@ -766,15 +794,15 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         tmem_st_wait();
       }
       // P^T (K-major: row = head, 128 keys = 2 atoms) for the second MMA
-      if (!mbar_wait(smem_u32(&p_empty[sb]), ph2 ^ 1, &abort_flag, A.err)) break;
-      uint8_t* pb = p_buf + sb * kPBufBytes;
+      if (!mbar_wait(smem_u32(&p_empty[pbi]), pph ^ 1, &abort_flag, A.err)) break;
+      uint8_t* pb = p_buf + pbi * kPBufBytes;
 #pragma unroll
       for (int h = 0; h < kMlaHeads; ++h)
         *reinterpret_cast<__nv_bfloat16*>(pb + sw128_offset(h, tid * 2, kQAtomBytes)) = __float2bfloat16_rn(z[h]);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&p_full[sb]));
+      if (lane == 0) mbar_arrive(smem_u32(&p_full[pbi]));
 
       if (cp.last) {
         // total sum per head over the 128 key lanes
