@@ -137,12 +137,15 @@ __device__ __forceinline__ void codes4_to_f32(uint32_t w, float (&f)[4]) {
 template <int kKv>
 __device__ __forceinline__ void dequant16(const uint4 c, float sc, uint32_t (&pk)[8]) {
   const uint32_t w4[4] = {c.x, c.y, c.z, c.w};
+  const float2 s2 = make_float2(sc, sc);
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     float f[4];
     codes4_to_f32<kKv>(w4[j], f);
-    pk[2 * j] = pack_bf16x2(f[0] * sc, f[1] * sc);
-    pk[2 * j + 1] = pack_bf16x2(f[2] * sc, f[3] * sc);
+    // two products per packed fp32x2 multiply (each rounded as a single multiply)
+    const float2 lo = __fmul2_rn(make_float2(f[0], f[1]), s2), hi = __fmul2_rn(make_float2(f[2], f[3]), s2);
+    pk[2 * j] = pack_bf16x2(lo.x, lo.y);
+    pk[2 * j + 1] = pack_bf16x2(hi.x, hi.y);
   }
 }
 
@@ -475,20 +478,6 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         if (!slot_acquire(smem_u32(&rows_full[rb]), (i / kRowBufs) & 1)) break;
         mbar_try_wait(smem_u32(&rows_full[rb]), (i / kRowBufs) & 1);   // acquire in every lane (phase is complete)
         const int* rows = rows_s[rb];
-        if (jl == 0) {
-          const int rs = i % kRopeSlots;
-          if (!slot_acquire(smem_u32(&rope_empty[rs]), ((i / kRopeSlots) & 1) ^ 1)) break;
-          const uint32_t dst0 = smem_u32(rope_buf);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int ri = 32 * pw + 8 * q + (lane >> 2);
-            const int row = rows[ri];
-            const int cb = (lane & 3) * 16;
-            cp_async_16(dst0 + sw128_offset(ri, 64 * rs + cb, 0),
-                        kv + rec_rope_at(row >= 0 ? row : 0) + 64 * rank + cb, row >= 0 ? 16u : 0u);
-          }
-          cp_async_arrive_noinc(smem_u32(&rope_full[rs]));
-        }
         __syncwarp();   // every lane has read this stage's previous pair (converted two steps ago)
         {
           uint8_t* stg = code_buf + cs * kCodeStageBytes;
@@ -507,6 +496,22 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
           cp_async_4(dst_scales + 4 * r, kv + rec_scales_at(row >= 0 ? row : 0) + 4 * (2 * rank + jl),
                      row >= 0 ? 4u : 0u);
           cp_async_commit();
+        }
+        // the RoPE copies after the codes: their slot frees only once the chunk two
+        // before has been scored, which the codes need not wait for
+        if (jl == 0) {
+          const int rs = i % kRopeSlots;
+          if (!slot_acquire(smem_u32(&rope_empty[rs]), ((i / kRopeSlots) & 1) ^ 1)) break;
+          const uint32_t dst0 = smem_u32(rope_buf);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int ri = 32 * pw + 8 * q + (lane >> 2);
+            const int row = rows[ri];
+            const int cb = (lane & 3) * 16;
+            cp_async_16(dst0 + sw128_offset(ri, 64 * rs + cb, 0),
+                        kv + rec_rope_at(row >= 0 ? row : 0) + 64 * rank + cb, row >= 0 ? 16u : 0u);
+          }
+          cp_async_arrive_noinc(smem_u32(&rope_full[rs]));
         }
         if (jl == 1) {
           __syncwarp();
