@@ -57,6 +57,9 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-configuration step lines")
+    ap.add_argument("--only-config", choices=list(inputs.CONFIG_NAMES), default=None,
+                    help="run just --warmup + --steps steps of one configuration (no graph, no flush; for "
+                         "profiler launch lists) and print its step time")
     return ap.parse_args()
 
 
@@ -312,6 +315,9 @@ def main():
         raise SystemExit("--warmup must be >= 3")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if args.only_config:
+        run_one_config(args.only_config, args.warmup, args.steps, dev)
+        return
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -423,6 +429,25 @@ def main():
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def run_one_config(name, warmup, steps, device):
+    """Eager steps of one configuration, for profilers: warmup + steps calls of the whole
+    step (every layer), then a device-error check and one JSON line with the mean time."""
+    wl = inputs.make_config(name)
+    dw = runner.DeviceWorkload(wl, device)
+    for _ in range(warmup):
+        dw.step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        dw.step()
+    e1.record()
+    torch.cuda.synchronize()
+    if dw.check_error() != 0:
+        raise SystemExit(f"device error in the {name} steps")
+    print(json.dumps({"config": name, "steps": steps, "ms_per_step_eager": e0.elapsed_time(e1) / max(1, steps)}))
 
 
 def measure_e2e(dw, graph, flush, stream, n):

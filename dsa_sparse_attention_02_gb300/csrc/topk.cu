@@ -64,10 +64,15 @@ struct TopkLaunch {
 struct TopkShared {
   int hist[2048];
   int wsum[32];
+  uint32_t wand[32], wor[32];   // per warp: AND and OR of its valid keys
+  int wcnt[32];                 // per warp: valid keys
   int sel_bin, sel_above, sel_cnt;
   int ncand;     // candidates appended so far
   int total;     // block total of the last scan
   int count;     // results of the segment: min(k, valid entries)
+  uint32_t common;   // bits every valid key has (their top ncommon bits are shared)
+  int ncommon;
+  int nvalid;
 };
 
 // Exclusive scan over the block of one int per thread (block total in S.total).
@@ -163,63 +168,100 @@ __device__ __forceinline__ void topk_select(const TopkLaunch& L, int n, int64_t 
     }
   }
 
-  // ---- pass over the top 11 bits (21-31) of every valid key
+  // ---- the leading bits every valid key shares, and the number of valid keys: the
+  // radix digits start below the shared bits (scores in a narrow range, such as the
+  // top candidates a merge level sees, would otherwise crowd a few bins of the first
+  // digit), and a segment with no more valid keys than k keeps them all
+  const int lane = tid & 31, warp = tid >> 5;
+  {
+    uint32_t a = 0xFFFFFFFFu, o = 0u;
+#pragma unroll
+    for (int i = 0; i < CNT; ++i)
+      if ((valid >> i) & 1u) { a &= key[i]; o |= key[i]; }
+    a = __reduce_and_sync(0xffffffffu, a);
+    o = __reduce_or_sync(0xffffffffu, o);
+    const int c = (int)__reduce_add_sync(0xffffffffu, (uint32_t)__popc(valid));
+    if (lane == 0) { S.wand[warp] = a; S.wor[warp] = o; S.wcnt[warp] = c; }
+  }
   for (int j = tid; j < 2048; j += kTopkThreads) S.hist[j] = 0;
   if (tid == 0) { S.sel_bin = 0; S.sel_above = 0; S.sel_cnt = -1; }
   __syncthreads();
-#pragma unroll
-  for (int i = 0; i < CNT; ++i)
-    if ((valid >> i) & 1u) atomicAdd(&S.hist[key[i] >> 21], 1);
+  if (warp == 0) {
+    const uint32_t a = __reduce_and_sync(0xffffffffu, S.wand[lane]);
+    const uint32_t o = __reduce_or_sync(0xffffffffu, S.wor[lane]);
+    const int c = (int)__reduce_add_sync(0xffffffffu, (uint32_t)S.wcnt[lane]);
+    if (lane == 0) { S.common = a; S.ncommon = (a == o) ? 32 : __clz(a ^ o); S.nvalid = c; }
+  }
   __syncthreads();
-  topk_find_bin(S, 2048, k);
-  int rem;
+  int rem, consumed;
   uint32_t prefix, pmask;
-  if (S.sel_cnt < 0) {
+  bool done;
+  if (S.nvalid <= k) {
     // no more valid entries than k: every one of them is taken
-    rem = S.total;
+    rem = S.nvalid;
     prefix = 0u;
     pmask = 0u;
+    done = true;
     if (tid == 0) S.count = rem;
   } else {
     if (tid == 0) S.count = k;
-    rem = k - S.sel_above;
-    prefix = (uint32_t)S.sel_bin << 21;
-    pmask = 0xFFE00000u;
-    if (S.sel_cnt != rem) {
-      // ---- the keys of the threshold bin become a short candidate list; the lower
-      // 21 bits are resolved over that list only (bits 10-20, then 0-9)
-      const int ncand0 = S.sel_cnt;
+    rem = k;
+    consumed = S.ncommon;
+    pmask = consumed == 0 ? 0u : (0xFFFFFFFFu << (32 - consumed));
+    prefix = S.common & pmask;
+    done = consumed == 32;   // every valid key equal: the first k by position
+    // Resolves the next digit (up to 11 bits below those consumed) from the histogram
+    // S.hist; false once the threshold key is known.
+    auto next_digit = [&](int w, int sh) -> bool {
+      topk_find_bin(S, 1 << w, rem);
+      rem -= S.sel_above;
+      prefix |= (uint32_t)S.sel_bin << sh;
+      pmask |= ((1u << w) - 1u) << sh;
+      consumed += w;
+      return !(S.sel_cnt == rem || consumed == 32);
+    };
+    int ncand0 = 0;
+    if (!done) {
+      // ---- first digit over every valid key (they all match the shared prefix)
+      const int w = min(11, 32 - consumed), sh = 32 - consumed - w;
+#pragma unroll
+      for (int i = 0; i < CNT; ++i)
+        if ((valid >> i) & 1u) atomicAdd(&S.hist[(key[i] >> sh) & ((1u << w) - 1u)], 1);
+      __syncthreads();
+      done = !next_digit(w, sh);
+      ncand0 = S.sel_cnt;
+    }
+    if (!done) {
+      // ---- the keys of the threshold bin become a short candidate list; the next
+      // digit's histogram is taken as they are appended
+      const int w = min(11, 32 - consumed), sh = 32 - consumed - w;
       __syncthreads();   // every thread has read sel_* before they are reset
-      if (tid == 0) S.ncand = 0;
+      if (tid == 0) { S.ncand = 0; S.sel_bin = 0; S.sel_above = 0; S.sel_cnt = -1; }
       for (int j = tid; j < 2048; j += kTopkThreads) S.hist[j] = 0;
       __syncthreads();
 #pragma unroll
       for (int i = 0; i < CNT; ++i) {
         const bool in_bin = ((valid >> i) & 1u) && (key[i] & pmask) == prefix;
         topk_append(in_bin, key[i], S, cand);
-        if (in_bin) atomicAdd(&S.hist[(key[i] >> 10) & 2047u], 1);
+        if (in_bin) atomicAdd(&S.hist[(key[i] >> sh) & ((1u << w) - 1u)], 1);
       }
-      if (tid == 0) { S.sel_bin = 0; S.sel_above = 0; S.sel_cnt = -1; }
       __syncthreads();
-      topk_find_bin(S, 2048, rem);
-      rem -= S.sel_above;
-      prefix |= (uint32_t)S.sel_bin << 10;
-      pmask |= 0x001FFC00u;
-      if (S.sel_cnt != rem) {
-        __syncthreads();
-        for (int j = tid; j < 1024; j += kTopkThreads) S.hist[j] = 0;
-        if (tid == 0) { S.sel_bin = 0; S.sel_above = 0; S.sel_cnt = -1; }
-        __syncthreads();
-        for (int c = tid; c < ncand0; c += kTopkThreads) {
-          const uint32_t kc = cand[c];
-          if ((kc & pmask) == prefix) atomicAdd(&S.hist[kc & 1023u], 1);
-        }
-        __syncthreads();
-        topk_find_bin(S, 1024, rem);
-        rem -= S.sel_above;
-        prefix |= (uint32_t)S.sel_bin;
-        pmask = 0xFFFFFFFFu;
+      done = !next_digit(w, sh);
+    }
+    if (!done) {
+      // ---- the remaining (at most 10) bits over the candidate list
+      const int w = 32 - consumed, sh = 0;
+      __syncthreads();
+      if (tid == 0) { S.sel_bin = 0; S.sel_above = 0; S.sel_cnt = -1; }
+      for (int j = tid; j < 2048; j += kTopkThreads) S.hist[j] = 0;
+      __syncthreads();
+      for (int c = tid; c < ncand0; c += kTopkThreads) {
+        const uint32_t kc = cand[c];
+        if ((kc & pmask) == prefix) atomicAdd(&S.hist[kc & ((1u << w) - 1u)], 1);
       }
+      __syncthreads();
+      next_digit(w, sh);
+      pmask = 0xFFFFFFFFu;
     }
   }
 
