@@ -136,13 +136,33 @@ __device__ __forceinline__ void topk_append(bool take, uint32_t key, TopkShared&
 template <int CNT, int MODE>
 __device__ __forceinline__ void topk_select(const TopkLaunch& L, int n, int64_t in_base, int64_t out_base,
                                             int idx_offset, TopkShared& S, uint32_t* cand, int* out_s,
-                                            uint32_t* key_s) {
+                                            uint32_t* key_s, int* pos_s) {
   const int tid = threadIdx.x;
   const int k = L.k;
   const int e0 = tid * CNT;
   uint32_t key[CNT];
   uint32_t valid = 0;
-  if (MODE != kMerge && e0 + CNT <= n && ((reinterpret_cast<uintptr_t>(L.scores + in_base) & 15) == 0)) {
+  // candidate keys and positions with 16-byte accesses where all three addresses allow
+  // them (k a multiple of 4 makes them aligned; other k take the scalar loop)
+  const bool vec_merge = MODE == kMerge && e0 + CNT <= n &&
+                         ((reinterpret_cast<uintptr_t>(L.cand_key_in + in_base + e0) |
+                           reinterpret_cast<uintptr_t>(L.cand_idx_in + in_base + e0) |
+                           reinterpret_cast<uintptr_t>(pos_s + e0)) & 15) == 0;
+  if (vec_merge) {
+    // the positions go to this thread's slots of pos_s (read back only by this thread
+    // when it places its results)
+    const uint4* ks = reinterpret_cast<const uint4*>(L.cand_key_in + in_base + e0);
+    const int4* is = reinterpret_cast<const int4*>(L.cand_idx_in + in_base + e0);
+#pragma unroll
+    for (int q = 0; q < CNT / 4; ++q) {
+      const uint4 kv = ks[q];
+      const int4 iv = is[q];
+      key[4 * q] = kv.x; key[4 * q + 1] = kv.y; key[4 * q + 2] = kv.z; key[4 * q + 3] = kv.w;
+      *reinterpret_cast<int4*>(pos_s + e0 + 4 * q) = iv;
+      valid |= (iv.x >= 0 ? 1u : 0u) << (4 * q) | (iv.y >= 0 ? 1u : 0u) << (4 * q + 1) |
+               (iv.z >= 0 ? 1u : 0u) << (4 * q + 2) | (iv.w >= 0 ? 1u : 0u) << (4 * q + 3);
+    }
+  } else if (MODE != kMerge && e0 + CNT <= n && ((reinterpret_cast<uintptr_t>(L.scores + in_base) & 15) == 0)) {
     const float4* src = reinterpret_cast<const float4*>(L.scores + in_base + e0);
 #pragma unroll
     for (int q = 0; q < CNT / 4; ++q) {
@@ -159,7 +179,9 @@ __device__ __forceinline__ void topk_select(const TopkLaunch& L, int n, int64_t 
       if (e < n) {
         if (MODE == kMerge) {
           key[i] = L.cand_key_in[in_base + e];
-          if (L.cand_idx_in[in_base + e] >= 0) valid |= 1u << i;
+          const int ci = L.cand_idx_in[in_base + e];
+          pos_s[e] = ci;
+          if (ci >= 0) valid |= 1u << i;
         } else {
           key[i] = orderable_key(L.scores[in_base + e]);
           valid |= 1u << i;
@@ -284,7 +306,7 @@ __device__ __forceinline__ void topk_select(const TopkLaunch& L, int n, int64_t 
       if (is_gt || (is_eq && re < rem)) {
         const int pos = rg + min(re, rem);
         const int e = e0 + i;
-        out_s[pos] = (MODE == kMerge) ? L.cand_idx_in[in_base + e] : idx_offset + e;
+        out_s[pos] = (MODE == kMerge) ? pos_s[e] : idx_offset + e;
         if (MODE != kDirect) key_s[pos] = key[i];
       }
       if (is_gt) ++rg;
@@ -309,16 +331,16 @@ __device__ __forceinline__ void topk_select(const TopkLaunch& L, int n, int64_t 
 template <int MODE>
 __device__ __forceinline__ void topk_select_runs(const TopkLaunch& L, int n, int64_t in_base, int64_t out_base,
                                                  int idx_offset, TopkShared& S, uint32_t* cand, int* out_s,
-                                                 uint32_t* key_s) {
-  if (n <= 4 * kTopkThreads) topk_select<4, MODE>(L, n, in_base, out_base, idx_offset, S, cand, out_s, key_s);
-  else if (n <= 8 * kTopkThreads) topk_select<8, MODE>(L, n, in_base, out_base, idx_offset, S, cand, out_s, key_s);
-  else topk_select<16, MODE>(L, n, in_base, out_base, idx_offset, S, cand, out_s, key_s);
+                                                 uint32_t* key_s, int* pos_s) {
+  if (n <= 4 * kTopkThreads) topk_select<4, MODE>(L, n, in_base, out_base, idx_offset, S, cand, out_s, key_s, pos_s);
+  else if (n <= 8 * kTopkThreads) topk_select<8, MODE>(L, n, in_base, out_base, idx_offset, S, cand, out_s, key_s, pos_s);
+  else topk_select<16, MODE>(L, n, in_base, out_base, idx_offset, S, cand, out_s, key_s, pos_s);
 }
 
 template <int MODE>
 __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkLaunch L) {
   __shared__ TopkShared S;
-  __shared__ int row_len_s, pos_s;
+  __shared__ int row_len_s, row_pos_s;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int t, c = 0, grp = 0;
@@ -338,7 +360,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkLaunch 
       else if (MODE == kChunks) n = max(0, min(L.chunk, pos + 1 - c * L.chunk));
       else n = pos + 1;
       row_len_s = n;
-      pos_s = pos;
+      row_pos_s = pos;
     }
   }
   griddep_launch_dependents();
@@ -356,9 +378,9 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkLaunch 
                                                              : (int64_t)t * k;
   const int idx_offset = (MODE == kChunks) ? c * L.chunk : 0;
 
-  if (MODE == kMerge && L.n_out == 1 && pos_s + 1 <= k) {
+  if (MODE == kMerge && L.n_out == 1 && row_pos_s + 1 <= k) {
     // every valid key is kept: positions 0..pos in order (no candidate is read)
-    for (int i = tid; i < k; i += kTopkThreads) L.idx_out[out_base + i] = i <= pos_s ? i : -1;
+    for (int i = tid; i < k; i += kTopkThreads) L.idx_out[out_base + i] = i <= row_pos_s ? i : -1;
     return;
   }
   if (n <= k) {
@@ -380,13 +402,15 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkLaunch 
     }
     return;
   }
-  // Dynamic shared memory: [k] staged output positions, [k] their keys, then the
-  // candidate list of the threshold bin (at most n <= capacity keys).
+  // Dynamic shared memory: [k] staged output positions, [k] their keys, the candidate
+  // list of the threshold bin (at most n <= capacity keys), and for merges the input
+  // candidates' positions (n).
   extern __shared__ int dyn_s[];
   int* out_s = dyn_s;
   uint32_t* key_s = reinterpret_cast<uint32_t*>(out_s + k);
   uint32_t* cand = key_s + k;
-  topk_select_runs<MODE>(L, n, in_base, out_base, idx_offset, S, cand, out_s, key_s);
+  int* pos_s = reinterpret_cast<int*>(cand + n);
+  topk_select_runs<MODE>(L, n, in_base, out_base, idx_offset, S, cand, out_s, key_s, pos_s);
 }
 
 // ------------------------------------------------------------------ host side
@@ -422,10 +446,12 @@ size_t topk_workspace_bytes(int T, int max_seq_len, int k) {
 
 // Dynamic shared memory of one launch: the staged outputs (positions and keys) and
 // the candidate keys of the threshold bin (at most one row segment's entries).
-static size_t topk_smem_bytes(int k, int seg_len) { return (size_t)k * 8 + (size_t)seg_len * 4; }
+static size_t topk_smem_bytes(int k, int seg_len, bool merge) {
+  return (size_t)k * 8 + (size_t)seg_len * (merge ? 8 : 4);
+}
 
 static cudaError_t launch_topk_kernel(const TopkLaunch& L, int grid, int seg_len, bool pdl, cudaStream_t st) {
-  const size_t smem = topk_smem_bytes(L.k, seg_len < kTopkCapacity ? seg_len : kTopkCapacity);
+  const size_t smem = topk_smem_bytes(L.k, seg_len < kTopkCapacity ? seg_len : kTopkCapacity, L.mode == kMerge);
   auto kern = L.mode == kDirect ? topk_kernel<kDirect> : L.mode == kChunks ? topk_kernel<kChunks> : topk_kernel<kMerge>;
   // the 48 KB default covers static and dynamic shared memory together
   if (smem + sizeof(TopkShared) + 64 > 48 * 1024) {
