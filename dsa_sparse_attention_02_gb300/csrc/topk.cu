@@ -6,15 +6,18 @@
 // registers as runs of 4, 8 or 16 consecutive entries per thread (the smallest run
 // that covers the segment, so that the row spreads over as many threads as it can;
 // read as 16-byte loads where the row is aligned). Scores map to 32-bit keys whose
-// unsigned order is the float order (-0 folded onto +0). A histogram of the top 11
-// key bits locates the bin holding the k-th largest key; unless that bin is taken
-// whole, its keys are copied to a shared-memory candidate list, and the next 11 and
-// then 10 bits are resolved over that short list only. An element is then taken if
-// its masked key is above the prefix so found, or equal to it and among the first
-// `rem` equal ones by position (ties to the lower position). Output positions come
-// from one block-wide exclusive scan of every thread's (above, equal) counts, in
-// position order since each thread holds a contiguous run, so indices leave in
-// ascending order. A segment with no more valid entries than k keeps all of them.
+// unsigned order is the float order (-0 folded onto +0). Radix digits of up to 11
+// bits, starting below the leading bits that every valid key shares, are resolved
+// one after the other: a shared-memory histogram of the digit over the keys that
+// match the prefix found so far (read from the registers each time) locates the bin
+// holding the rem-th largest of them. Every warp finds that bin itself from the
+// histogram, so a digit costs two block barriers. An element is then taken if its
+// masked key is above the prefix so found, or equal to it and among the first `rem`
+// equal ones by position (ties to the lower position). Output positions come from
+// one block-wide exclusive scan of every thread's (above, equal) counts, in position
+// order since each thread holds a contiguous run, so indices leave in ascending
+// order; each thread writes its results straight to the output. A segment with no
+// more valid entries than k keeps all of them.
 //
 // Rows longer than one CTA's capacity are cut into chunks of 16384 positions whose
 // exact top-k (with their keys) become candidate lists. Lists are then merged in
@@ -62,81 +65,73 @@ struct TopkLaunch {
 };
 
 struct TopkShared {
-  int hist[2048];
-  int wsum[32];
+  int hist[2][2048];            // digit histograms (alternating between digits)
+  int wsum[32];                 // per warp: its histogram bins' total
+  int wscan[32];                // per warp: its placement counts
   uint32_t wand[32], wor[32];   // per warp: AND and OR of its valid keys
   int wcnt[32];                 // per warp: valid keys
-  int sel_bin, sel_above, sel_cnt;
-  int ncand;     // candidates appended so far
-  int total;     // block total of the last scan
-  int count;     // results of the segment: min(k, valid entries)
-  uint32_t common;   // bits every valid key has (their top ncommon bits are shared)
-  int ncommon;
-  int nvalid;
 };
+constexpr int kTopkWarps = kTopkThreads / 32;
+static_assert(kTopkWarps == 32 && 64 * kTopkWarps == 2048, "two bins per thread");
 
-// Exclusive scan over the block of one int per thread (block total in S.total).
-__device__ __forceinline__ int topk_block_scan(int v, TopkShared& S) {
+struct TopkBin { int bin, above, cnt; };
+
+// The bin of histogram h[0..nb) that holds the rem-th largest counted key, with the
+// count of keys in the bins above it and in it. Warp w sums bins nb-1-64w down to
+// nb-64-64w (two per lane); after a barrier every warp scans the 32 warp totals,
+// picks the warp range that holds the rem-th key and scans that range's bins, so that
+// all threads return the same bin with no further barrier. The histogram must be
+// complete on entry (the first barrier). zero: an array of 2048 ints that every warp
+// has finished reading (before the first barrier), cleared for a later digit; or null.
+__device__ __forceinline__ TopkBin topk_find_bin(TopkShared& S, const int* h, int nb, int rem, int* zero) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();   // every count is in h
+  if (zero) { zero[threadIdx.x] = 0; zero[threadIdx.x + kTopkThreads] = 0; }
+  {
+    const int hi = nb - 1 - 64 * warp - 2 * lane;
+    const int own = (hi >= 0 ? h[hi] : 0) + (hi >= 1 ? h[hi - 1] : 0);
+    const int tot = (int)__reduce_add_sync(0xffffffffu, (uint32_t)own);
+    if (lane == 0) S.wsum[warp] = tot;
+  }
+  __syncthreads();
+  const int v = S.wsum[lane];
   int incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int u = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += u;
   }
-  if (lane == 31) S.wsum[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    const int w = S.wsum[lane];
-    int iw = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int u = __shfl_up_sync(0xffffffffu, iw, o);
-      if (lane >= o) iw += u;
-    }
-    S.wsum[lane] = iw - w;
-    if (lane == 31) S.total = iw;
-  }
-  __syncthreads();
-  return S.wsum[warp] + incl - v;
-}
-
-// From the histogram S.hist[0..nb), highest bin first, find the bin holding the
-// rem-th largest counted key: sel_bin, sel_above (count above it), sel_cnt. Thread t
-// owns bins nb-1-2t and nb-2-2t. If fewer than rem keys are counted, sel_cnt stays
-// -1 and S.total holds their number.
-__device__ __forceinline__ void topk_find_bin(TopkShared& S, int nb, int rem) {
-  const int tid = threadIdx.x;
-  const int hi_bin = nb - 1 - 2 * tid;
-  const int c0 = hi_bin >= 0 ? S.hist[hi_bin] : 0;
-  const int c1 = hi_bin - 1 >= 0 ? S.hist[hi_bin - 1] : 0;
+  TopkBin r{0, 0, -1};
+  const unsigned mw = __ballot_sync(0xffffffffu, v > 0 && incl - v < rem && rem <= incl);
+  if (mw == 0u) return r;   // fewer than rem keys counted (not reached by the callers)
+  const int W = __ffs(mw) - 1;
+  const int above_w = __shfl_sync(0xffffffffu, incl - v, W);
+  const int hi = nb - 1 - 64 * W - 2 * lane;
+  const int c0 = hi >= 0 ? h[hi] : 0, c1 = hi >= 1 ? h[hi - 1] : 0;
   const int own = c0 + c1;
-  const int excl = topk_block_scan(own, S);
-  if (own > 0 && excl < rem && rem <= excl + own) {
-    if (excl + c0 >= rem) { S.sel_bin = hi_bin; S.sel_above = excl; S.sel_cnt = c0; }
-    else { S.sel_bin = hi_bin - 1; S.sel_above = excl + c0; S.sel_cnt = c1; }
+  int in2 = own;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, in2, o);
+    if (lane >= o) in2 += u;
   }
-  __syncthreads();
-}
-
-// Appends key to the shared candidate list (warp-aggregated: one atomic per warp).
-__device__ __forceinline__ void topk_append(bool take, uint32_t key, TopkShared& S, uint32_t* cand) {
-  const int lane = threadIdx.x & 31;
-  const unsigned m = __ballot_sync(0xffffffffu, take);
-  if (m == 0u) return;
-  int base = 0;
-  if (lane == __ffs(m) - 1) base = atomicAdd(&S.ncand, __popc(m));
-  base = __shfl_sync(0xffffffffu, base, __ffs(m) - 1);
-  if (take) cand[base + __popc(m & ((1u << lane) - 1u))] = key;
+  const int ex2 = above_w + in2 - own;
+  const unsigned ml = __ballot_sync(0xffffffffu, own > 0 && ex2 < rem && rem <= ex2 + own);
+  const int L = __ffs(ml) - 1;   // the range's counts add up to above_w + v >= rem
+  const int bin = __shfl_sync(0xffffffffu, hi, L), ex = __shfl_sync(0xffffffffu, ex2, L);
+  const int a0 = __shfl_sync(0xffffffffu, c0, L), a1 = __shfl_sync(0xffffffffu, c1, L);
+  if (ex + a0 >= rem) { r.bin = bin; r.above = ex; r.cnt = a0; }
+  else { r.bin = bin - 1; r.above = ex + a0; r.cnt = a1; }
+  return r;
 }
 
 // The selection proper over a segment of n (> k) entries spread as runs of CNT per
-// thread; entries whose valid bit is clear take no part. cand: shared array of at
-// least min(n, capacity) keys. Writes min(k, valid entries) results then -1 padding.
+// thread; entries whose valid bit is clear take no part. pos_s (merges): shared array
+// of n ints for the input candidates' positions. Writes min(k, valid entries) results
+// then -1 padding.
 template <int CNT, int MODE>
 __device__ __forceinline__ void topk_select(const TopkLaunch& L, int n, int64_t in_base, int64_t out_base,
-                                            int idx_offset, TopkShared& S, uint32_t* cand, int* out_s,
-                                            uint32_t* key_s, int* pos_s) {
+                                            int idx_offset, TopkShared& S, int* pos_s) {
   const int tid = threadIdx.x;
   const int k = L.k;
   const int e0 = tid * CNT;
@@ -193,7 +188,8 @@ __device__ __forceinline__ void topk_select(const TopkLaunch& L, int n, int64_t 
   // ---- the leading bits every valid key shares, and the number of valid keys: the
   // radix digits start below the shared bits (scores in a narrow range, such as the
   // top candidates a merge level sees, would otherwise crowd a few bins of the first
-  // digit), and a segment with no more valid keys than k keeps them all
+  // digit), and a segment with no more valid keys than k keeps them all. Every warp
+  // reduces the per-warp values itself after one barrier.
   const int lane = tid & 31, warp = tid >> 5;
   {
     uint32_t a = 0xFFFFFFFFu, o = 0u;
@@ -205,85 +201,38 @@ __device__ __forceinline__ void topk_select(const TopkLaunch& L, int n, int64_t 
     const int c = (int)__reduce_add_sync(0xffffffffu, (uint32_t)__popc(valid));
     if (lane == 0) { S.wand[warp] = a; S.wor[warp] = o; S.wcnt[warp] = c; }
   }
-  for (int j = tid; j < 2048; j += kTopkThreads) S.hist[j] = 0;
-  if (tid == 0) { S.sel_bin = 0; S.sel_above = 0; S.sel_cnt = -1; }
+  for (int j = tid; j < 2 * 2048; j += kTopkThreads) (&S.hist[0][0])[j] = 0;
   __syncthreads();
-  if (warp == 0) {
-    const uint32_t a = __reduce_and_sync(0xffffffffu, S.wand[lane]);
-    const uint32_t o = __reduce_or_sync(0xffffffffu, S.wor[lane]);
-    const int c = (int)__reduce_add_sync(0xffffffffu, (uint32_t)S.wcnt[lane]);
-    if (lane == 0) { S.common = a; S.ncommon = (a == o) ? 32 : __clz(a ^ o); S.nvalid = c; }
-  }
-  __syncthreads();
-  int rem, consumed;
-  uint32_t prefix, pmask;
-  bool done;
-  if (S.nvalid <= k) {
-    // no more valid entries than k: every one of them is taken
-    rem = S.nvalid;
-    prefix = 0u;
-    pmask = 0u;
-    done = true;
-    if (tid == 0) S.count = rem;
+  const uint32_t common = __reduce_and_sync(0xffffffffu, S.wand[lane]);
+  const uint32_t any = __reduce_or_sync(0xffffffffu, S.wor[lane]);
+  const int nvalid = (int)__reduce_add_sync(0xffffffffu, (uint32_t)S.wcnt[lane]);
+
+  int rem, count;
+  uint32_t prefix = 0u, pmask = 0u;
+  if (nvalid <= k) {
+    // no more valid entries than k: every one of them is taken (prefix and mask 0)
+    rem = count = nvalid;
   } else {
-    if (tid == 0) S.count = k;
-    rem = k;
-    consumed = S.ncommon;
+    rem = count = k;
+    int consumed = (common == any) ? 32 : __clz(common ^ any);
     pmask = consumed == 0 ? 0u : (0xFFFFFFFFu << (32 - consumed));
-    prefix = S.common & pmask;
-    done = consumed == 32;   // every valid key equal: the first k by position
-    // Resolves the next digit (up to 11 bits below those consumed) from the histogram
-    // S.hist; false once the threshold key is known.
-    auto next_digit = [&](int w, int sh) -> bool {
-      topk_find_bin(S, 1 << w, rem);
-      rem -= S.sel_above;
-      prefix |= (uint32_t)S.sel_bin << sh;
-      pmask |= ((1u << w) - 1u) << sh;
-      consumed += w;
-      return !(S.sel_cnt == rem || consumed == 32);
-    };
-    int ncand0 = 0;
-    if (!done) {
-      // ---- first digit over every valid key (they all match the shared prefix)
+    prefix = common & pmask;
+    bool done = consumed == 32;   // every valid key equal: the first k by position
+    // at most three digits (11 + 11 + 10 bits); the third reuses the first histogram,
+    // cleared while the second digit is resolved
+    for (int d = 0; d < 3 && !done; ++d) {
       const int w = min(11, 32 - consumed), sh = 32 - consumed - w;
+      const uint32_t dmask = (1u << w) - 1u;
+      int* h = S.hist[d & 1];
 #pragma unroll
       for (int i = 0; i < CNT; ++i)
-        if ((valid >> i) & 1u) atomicAdd(&S.hist[(key[i] >> sh) & ((1u << w) - 1u)], 1);
-      __syncthreads();
-      done = !next_digit(w, sh);
-      ncand0 = S.sel_cnt;
-    }
-    if (!done) {
-      // ---- the keys of the threshold bin become a short candidate list; the next
-      // digit's histogram is taken as they are appended
-      const int w = min(11, 32 - consumed), sh = 32 - consumed - w;
-      __syncthreads();   // every thread has read sel_* before they are reset
-      if (tid == 0) { S.ncand = 0; S.sel_bin = 0; S.sel_above = 0; S.sel_cnt = -1; }
-      for (int j = tid; j < 2048; j += kTopkThreads) S.hist[j] = 0;
-      __syncthreads();
-#pragma unroll
-      for (int i = 0; i < CNT; ++i) {
-        const bool in_bin = ((valid >> i) & 1u) && (key[i] & pmask) == prefix;
-        topk_append(in_bin, key[i], S, cand);
-        if (in_bin) atomicAdd(&S.hist[(key[i] >> sh) & ((1u << w) - 1u)], 1);
-      }
-      __syncthreads();
-      done = !next_digit(w, sh);
-    }
-    if (!done) {
-      // ---- the remaining (at most 10) bits over the candidate list
-      const int w = 32 - consumed, sh = 0;
-      __syncthreads();
-      if (tid == 0) { S.sel_bin = 0; S.sel_above = 0; S.sel_cnt = -1; }
-      for (int j = tid; j < 2048; j += kTopkThreads) S.hist[j] = 0;
-      __syncthreads();
-      for (int c = tid; c < ncand0; c += kTopkThreads) {
-        const uint32_t kc = cand[c];
-        if ((kc & pmask) == prefix) atomicAdd(&S.hist[kc & ((1u << w) - 1u)], 1);
-      }
-      __syncthreads();
-      next_digit(w, sh);
-      pmask = 0xFFFFFFFFu;
+        if (((valid >> i) & 1u) && (key[i] & pmask) == prefix) atomicAdd(&h[(key[i] >> sh) & dmask], 1);
+      const TopkBin b = topk_find_bin(S, h, 1 << w, rem, (d == 1 && consumed + w < 32) ? S.hist[0] : nullptr);
+      rem -= b.above;
+      prefix |= (uint32_t)b.bin << sh;
+      pmask |= dmask << sh;
+      consumed += w;
+      done = b.cnt == rem || consumed == 32;
     }
   }
 
@@ -297,44 +246,52 @@ __device__ __forceinline__ void topk_select(const TopkLaunch& L, int n, int64_t 
     if (((valid >> i) & 1u) && m > prefix) gt_bits |= 1u << i;
     if (((valid >> i) & 1u) && m == prefix) eq_bits |= 1u << i;
   }
-  const int excl = topk_block_scan((__popc(gt_bits) << 16) | __popc(eq_bits), S);
+  const int packed = (__popc(gt_bits) << 16) | __popc(eq_bits);
+  int incl = packed;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (lane == 31) S.wscan[warp] = incl;
+  __syncthreads();
+  int wv = S.wscan[lane], wincl = wv;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, wincl, o);
+    if (lane >= o) wincl += u;
+  }
+  const int excl = __shfl_sync(0xffffffffu, wincl - wv, warp) + incl - packed;
   int rg = excl >> 16, re = excl & 0xffff;
+  const bool lists = MODE == kChunks || (MODE == kMerge && L.n_out > 1);
   if (gt_bits | eq_bits) {
 #pragma unroll
     for (int i = 0; i < CNT; ++i) {
       const bool is_gt = (gt_bits >> i) & 1u, is_eq = (eq_bits >> i) & 1u;
       if (is_gt || (is_eq && re < rem)) {
-        const int pos = rg + min(re, rem);
+        const int64_t o = out_base + rg + min(re, rem);
         const int e = e0 + i;
-        out_s[pos] = (MODE == kMerge) ? pos_s[e] : idx_offset + e;
-        if (MODE != kDirect) key_s[pos] = key[i];
+        const int v = (MODE == kMerge) ? pos_s[e] : idx_offset + e;
+        if (lists) { L.cand_idx_out[o] = v; L.cand_key_out[o] = key[i]; }
+        else L.idx_out[o] = v;
       }
       if (is_gt) ++rg;
       if (is_eq) ++re;
     }
   }
-  __syncthreads();
-  const bool lists = MODE == kChunks || (MODE == kMerge && L.n_out > 1);
-  const int count = S.count;
-  for (int j = tid; j < k; j += kTopkThreads) {
-    const bool v = j < count;
-    if (lists) {
-      L.cand_idx_out[out_base + j] = v ? out_s[j] : -1;
-      L.cand_key_out[out_base + j] = v ? key_s[j] : 0u;
-    } else {
-      L.idx_out[out_base + j] = v ? out_s[j] : -1;
-    }
+  for (int j = count + tid; j < k; j += kTopkThreads) {
+    if (lists) { L.cand_idx_out[out_base + j] = -1; L.cand_key_out[out_base + j] = 0u; }
+    else L.idx_out[out_base + j] = -1;
   }
 }
 
 // Runs of 4, 8 or 16 entries per thread, whichever spreads the segment over the most threads.
 template <int MODE>
 __device__ __forceinline__ void topk_select_runs(const TopkLaunch& L, int n, int64_t in_base, int64_t out_base,
-                                                 int idx_offset, TopkShared& S, uint32_t* cand, int* out_s,
-                                                 uint32_t* key_s, int* pos_s) {
-  if (n <= 4 * kTopkThreads) topk_select<4, MODE>(L, n, in_base, out_base, idx_offset, S, cand, out_s, key_s, pos_s);
-  else if (n <= 8 * kTopkThreads) topk_select<8, MODE>(L, n, in_base, out_base, idx_offset, S, cand, out_s, key_s, pos_s);
-  else topk_select<16, MODE>(L, n, in_base, out_base, idx_offset, S, cand, out_s, key_s, pos_s);
+                                                 int idx_offset, TopkShared& S, int* pos_s) {
+  if (n <= 4 * kTopkThreads) topk_select<4, MODE>(L, n, in_base, out_base, idx_offset, S, pos_s);
+  else if (n <= 8 * kTopkThreads) topk_select<8, MODE>(L, n, in_base, out_base, idx_offset, S, pos_s);
+  else topk_select<16, MODE>(L, n, in_base, out_base, idx_offset, S, pos_s);
 }
 
 template <int MODE>
@@ -402,15 +359,9 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkLaunch 
     }
     return;
   }
-  // Dynamic shared memory: [k] staged output positions, [k] their keys, the candidate
-  // list of the threshold bin (at most n <= capacity keys), and for merges the input
-  // candidates' positions (n).
-  extern __shared__ int dyn_s[];
-  int* out_s = dyn_s;
-  uint32_t* key_s = reinterpret_cast<uint32_t*>(out_s + k);
-  uint32_t* cand = key_s + k;
-  int* pos_s = reinterpret_cast<int*>(cand + n);
-  topk_select_runs<MODE>(L, n, in_base, out_base, idx_offset, S, cand, out_s, key_s, pos_s);
+  // Dynamic shared memory (merges only): the input candidates' positions (n).
+  extern __shared__ int4 dyn_s[];
+  topk_select_runs<MODE>(L, n, in_base, out_base, idx_offset, S, reinterpret_cast<int*>(dyn_s));
 }
 
 // ------------------------------------------------------------------ host side
@@ -444,14 +395,14 @@ size_t topk_workspace_bytes(int T, int max_seq_len, int k) {
   return bytes;
 }
 
-// Dynamic shared memory of one launch: the staged outputs (positions and keys) and
-// the candidate keys of the threshold bin (at most one row segment's entries).
-static size_t topk_smem_bytes(int k, int seg_len, bool merge) {
-  return (size_t)k * 8 + (size_t)seg_len * (merge ? 8 : 4);
+// Dynamic shared memory of one launch: for merges, the positions of one segment's
+// input candidates.
+static size_t topk_smem_bytes(int seg_len, bool merge) {
+  return merge ? (size_t)seg_len * 4 : 0;
 }
 
 static cudaError_t launch_topk_kernel(const TopkLaunch& L, int grid, int seg_len, bool pdl, cudaStream_t st) {
-  const size_t smem = topk_smem_bytes(L.k, seg_len < kTopkCapacity ? seg_len : kTopkCapacity, L.mode == kMerge);
+  const size_t smem = topk_smem_bytes(seg_len < kTopkCapacity ? seg_len : kTopkCapacity, L.mode == kMerge);
   auto kern = L.mode == kDirect ? topk_kernel<kDirect> : L.mode == kChunks ? topk_kernel<kChunks> : topk_kernel<kMerge>;
   // the 48 KB default covers static and dynamic shared memory together
   if (smem + sizeof(TopkShared) + 64 > 48 * 1024) {
