@@ -884,24 +884,56 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
 
 // Merge the partial segments of every query that more than one cluster worked on.
 __global__ void __launch_bounds__(128) mla_combine_kernel(const MlaArgs A, int G) {
-  griddep_wait();   // the partials come from the attention grid just before
   const int t = blockIdx.x;
   const int h = blockIdx.y;
   const int64_t c_first = split_owner((int64_t)t * A.C, A.n_chunks, G);
   const int64_t c_last = split_owner((int64_t)t * A.C + A.C - 1, A.n_chunks, G);
   if (c_first == c_last) return;
+  griddep_wait();   // the partials come from the attention grid just before
   const float neg_inf = -__int_as_float(0x7f800000);
-  float mx = neg_inf;
-  for (int64_t c = c_first; c <= c_last; ++c) mx = fmaxf(mx, A.ml_part[2 * ((t + c) * A.H + h)]);
-  float L = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int64_t c = c_first; c <= c_last; ++c) {
-    const int64_t r = (t + c) * A.H + h;
-    const float mj = A.ml_part[2 * r], lj = A.ml_part[2 * r + 1];
-    const float wgt = (mj == neg_inf) ? 0.f : exp2f(mj - mx);
-    L += wgt * lj;
-    const float* orow = A.o_part + r * kDimLatent;
+  const float2* ml = reinterpret_cast<const float2*>(A.ml_part);
+  // Segments in groups of four, every load of a group issued before any is used; a
+  // query of at most four segments (the usual case is two) takes one round of loads.
+  float mx = neg_inf, L = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+  float2 s4[4];
+  float o4[4][4];
+  auto load4 = [&](int64_t c0, bool rows) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) acc[j] = fmaf(wgt, orow[j * 128 + threadIdx.x], acc[j]);
+    for (int u = 0; u < 4; ++u) {
+      const int64_t r = (t + c0 + u) * A.H + h;
+      const bool in = c0 + u <= c_last;
+      s4[u] = in ? ml[r] : make_float2(neg_inf, 0.f);
+      if (rows) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o4[u][j] = in ? A.o_part[r * kDimLatent + j * 128 + threadIdx.x] : 0.f;
+      }
+    }
+  };
+  auto add4 = [&]() {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (s4[u].x == neg_inf) continue;   // no valid key in that segment (or past the last)
+      const float wgt = exp2f(s4[u].x - mx);
+      L = fmaf(wgt, s4[u].y, L);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[j] = fmaf(wgt, o4[u][j], acc[j]);
+    }
+  };
+  if (c_last - c_first < 4) {
+    load4(c_first, true);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) mx = fmaxf(mx, s4[u].x);
+    add4();
+  } else {
+    for (int64_t c0 = c_first; c0 <= c_last; c0 += 4) {
+      load4(c0, false);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) mx = fmaxf(mx, s4[u].x);
+    }
+    for (int64_t c0 = c_first; c0 <= c_last; c0 += 4) {
+      load4(c0, true);
+      add4();
+    }
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
   __nv_bfloat16* orow = A.out + ((int64_t)t * A.H + h) * kDimLatent;
