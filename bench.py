@@ -451,13 +451,14 @@ def run_one_config(name, warmup, steps, device):
 
 
 def measure_e2e(dw, graph, flush, stream, n):
-    """Same metric with per-step host inputs, all inside the timed events: the step's
-    inputs copied host->device from page-locked memory (geometry, indexer q, scales
-    and weights in one copy; the MLA query, which only the attention reads, in a second
-    copy on a side stream that overlaps the indexer and top-k), the step
-    (dsa_decode_step_wait_q: its attention waits for the MLA query's copy), and O and
-    LSE copied device->host. The copies are dsa_stage_copy; the whole is one CUDA graph
-    per step."""
+    """Same metric with per-step host inputs and outputs, all inside the timed events:
+    the step's inputs copied host->device from page-locked memory (geometry, indexer q,
+    scales and weights in one copy; the MLA query, which only the attention reads, in a
+    second copy on a side stream that overlaps the indexer and top-k), then the step
+    (dsa_decode_step_wait_q: its attention waits for the MLA query's copy) with O and
+    LSE in page-locked host memory, which the attention and combine kernels write
+    directly (device->host over the chip-to-chip link, overlapping their own work). The
+    input copies are dsa_stage_copy; the whole is one CUDA graph per step."""
     host_in = dw.inputs.detach().cpu().pin_memory()
     host_out = torch.empty(dw.outputs.shape, dtype=dw.outputs.dtype, pin_memory=True)
     h2d = host_in.numel() * host_in.element_size()
@@ -465,6 +466,14 @@ def measure_e2e(dw, graph, flush, stream, n):
     off = dw.inputs_mla_q_offset
     side = torch.cuda.Stream()
     fork, q_ready = torch.cuda.Event(), torch.cuda.Event()
+    # the step's arguments with every layer's O and LSE at the same offsets of host_out
+    base, hbase = dw.outputs.data_ptr(), host_out.data_ptr()
+    host_args = []
+    for a in dw.args:
+        ha = _lib.dsa_step_args_t.from_buffer_copy(a)
+        ha.out = hbase + (a.out - base)
+        ha.lse = hbase + (a.lse - base)
+        host_args.append(ha)
 
     def enqueue():
         cur = torch.cuda.current_stream()
@@ -474,12 +483,11 @@ def measure_e2e(dw, graph, flush, stream, n):
             _lib.dsa_stage_copy(dw.inputs[off:], host_in[off:], h2d - off)
             q_ready.record(side)
         _lib.dsa_stage_copy(dw.inputs, host_in, off)
-        for i, a in enumerate(dw.args):
+        for i, a in enumerate(host_args):
             if i == 0:
                 _lib.dsa_decode_step_wait_q(a, q_ready, dw.ws)
             else:
                 _lib.dsa_decode_step(a, dw.ws)
-        _lib.dsa_stage_copy(host_out, dw.outputs, d2h)
 
     warm = torch.cuda.Stream()
     warm.wait_stream(stream)
@@ -500,10 +508,16 @@ def measure_e2e(dw, graph, flush, stream, n):
         e1.synchronize()
         ms.append(e0.elapsed_time(e1))
     avg = sum(ms) / len(ms)
+    # the host copy of the outputs is the device step's, bit for bit
+    dw.step()
+    torch.cuda.synchronize()
+    if dw.check_error() != 0 or not torch.equal(host_out, dw.outputs.cpu()):
+        raise SystemExit("end-to-end outputs differ from the device step's")
     return {"value": dw.wl.T / (avg / 1000.0), "unit": "queries/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": avg,
-            "copies": ("dsa_stage_copy (an SM copy kernel) from and to page-locked host memory: the indexer's "
-                       "inputs and the MLA query (overlapping the indexer and top-k) in, O and LSE out")}
+            "copies": ("dsa_stage_copy (an SM copy kernel) from page-locked host memory: the indexer's inputs and "
+                       "the MLA query (overlapping the indexer and top-k) in; O and LSE written to page-locked host "
+                       "memory by the attention and combine kernels")}
 
 
 def measure_indexer_prefill(flush, stream, n, device):

@@ -115,6 +115,41 @@ dsa_status_t check_attend(const dsa_geom_t* g, dsa_dtype_t dt, int H, const void
   return DSA_OK;
 }
 
+// Device-visible address of the range [p, p + bytes): device or managed memory, or
+// page-locked host memory the device maps; both ends must resolve to one contiguous
+// mapping. Anything else (pageable host memory, unknown pointers) is refused.
+bool device_range(const void* p, size_t bytes, const void** out) {
+  cudaPointerAttributes a0, a1;
+  const void* last = reinterpret_cast<const uint8_t*>(p) + (bytes - 1);
+  if (cudaPointerGetAttributes(&a0, p) != cudaSuccess || cudaPointerGetAttributes(&a1, last) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  auto visible = [](const cudaPointerAttributes& a) {
+    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged ||
+           (a.type == cudaMemoryTypeHost && a.devicePointer != nullptr);
+  };
+  if (!visible(a0) || !visible(a1) || a0.type != a1.type || a0.device != a1.device) return false;
+  const uint8_t* d0 = reinterpret_cast<const uint8_t*>(a0.devicePointer ? a0.devicePointer : p);
+  const uint8_t* d1 = reinterpret_cast<const uint8_t*>(a1.devicePointer ? a1.devicePointer : last);
+  if (d1 != d0 + (bytes - 1)) return false;
+  *out = d0;
+  return true;
+}
+
+
+dsa_status_t resolve_outputs(const dsa_geom_t* g, int H, void* out, float* lse, void** dout, float** dlse) {
+  const void* o = nullptr;
+  const void* l = nullptr;
+  if (!device_range(out, (size_t)g->T * H * 512 * 2, &o) || (lse && !device_range(lse, (size_t)g->T * H * 4, &l))) {
+    set_last_error("sparse MLA outputs", "out and lse must be device memory or page-locked host memory the device maps");
+    return DSA_ERR_INVALID_ARG;
+  }
+  *dout = const_cast<void*>(o);
+  *dlse = reinterpret_cast<float*>(const_cast<void*>(l));
+  return DSA_OK;
+}
+
 }  // namespace dsa
 
 namespace {
@@ -207,12 +242,16 @@ size_t attend_scratch_bytes(const dsa_geom_t* g, int H, int k) {
 dsa_status_t run_attend(const dsa_geom_t* g, dsa_dtype_t dt, int H, const void* q, const void* kv, const int* idx,
                         int k, float sm_scale, void* out, float* lse, void* scratch, int* err, bool pdl,
                         cudaStream_t st) {
+  void* dout = nullptr;
+  float* dlse = nullptr;
+  const dsa_status_t rs = resolve_outputs(g, H, out, lse, &dout, &dlse);
+  if (rs != DSA_OK) return rs;
   CUtensorMap mq;
   if (!encode_mla_q_map(&mq, q, g->T, H)) return DSA_ERR_CUDA;
   MlaArgs A;
   A.g = to_dev(g); A.H = H; A.k = k; A.C = (k + 127) / 128; A.n_chunks = (int64_t)g->T * A.C;
   A.kv = reinterpret_cast<const uint8_t*>(kv); A.idx = idx; A.scale_log2 = sm_scale * 1.4426950408889634f;
-  A.out = reinterpret_cast<__nv_bfloat16*>(out); A.lse = lse;
+  A.out = reinterpret_cast<__nv_bfloat16*>(dout); A.lse = dlse;
   const int grid = mla_grid(A.n_chunks, num_sms());
   const size_t rows = (size_t)(g->T + grid) * H;
   A.o_part = reinterpret_cast<float*>(scratch);
@@ -521,28 +560,6 @@ dsa_status_t dsa_cache_append(const dsa_geom_t* geom, dsa_dtype_t kv_dtype, cons
 }  // extern "C"
 
 namespace {
-
-// Device-visible address of the range [p, p + bytes): device or managed memory, or
-// page-locked host memory the device maps; both ends must resolve to one contiguous
-// mapping. Anything else (pageable host memory, unknown pointers) is refused.
-bool device_range(const void* p, size_t bytes, const void** out) {
-  cudaPointerAttributes a0, a1;
-  const void* last = reinterpret_cast<const uint8_t*>(p) + (bytes - 1);
-  if (cudaPointerGetAttributes(&a0, p) != cudaSuccess || cudaPointerGetAttributes(&a1, last) != cudaSuccess) {
-    cudaGetLastError();
-    return false;
-  }
-  auto visible = [](const cudaPointerAttributes& a) {
-    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged ||
-           (a.type == cudaMemoryTypeHost && a.devicePointer != nullptr);
-  };
-  if (!visible(a0) || !visible(a1) || a0.type != a1.type || a0.device != a1.device) return false;
-  const uint8_t* d0 = reinterpret_cast<const uint8_t*>(a0.devicePointer ? a0.devicePointer : p);
-  const uint8_t* d1 = reinterpret_cast<const uint8_t*>(a1.devicePointer ? a1.devicePointer : last);
-  if (d1 != d0 + (bytes - 1)) return false;
-  *out = d0;
-  return true;
-}
 
 }  // namespace
 

@@ -122,6 +122,10 @@ cudaError_t indexer_prep_launch(const PrepArgs& A, cudaStream_t st);
 dsa_status_t check_geom(const dsa_geom_t* g);
 dsa_status_t check_attend(const dsa_geom_t* g, dsa_dtype_t dt, int H, const void* q, const void* kv, const int* idx,
                           int k, float sm_scale, const void* out);
+// Device addresses of the attention's outputs: out [T, H, 512] bf16 and lse [T, H]
+// fp32 (or null) may be device memory or page-locked host memory the device maps (the
+// kernels then write the results straight to the host); anything else is refused.
+dsa_status_t resolve_outputs(const dsa_geom_t* g, int H, void* out, float* lse, void** dout, float** dlse);
 bool encode_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t cols,
                           uint64_t rows, uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows);
 void set_last_error(const char* what, const char* detail);

@@ -82,13 +82,17 @@ extern "C" dsa_status_t dsa_sparse_mla_attend_static(const dsa_geom_t* geom, dsa
     set_last_error("cudaGetSymbolAddress", cudaGetErrorString(se));
     return DSA_ERR_CUDA;
   }
+  void* dout = nullptr;
+  float* dlse = nullptr;
+  const dsa_status_t rs = resolve_outputs(geom, H, out, lse, &dout, &dlse);
+  if (rs != DSA_OK) return rs;
   CUtensorMap mq;
   if (!encode_mla_q_map(&mq, q, geom->T, H)) return DSA_ERR_CUDA;
   A.g.B = geom->B; A.g.T = geom->T; A.g.max_seq_len = geom->max_seq_len; A.g.num_pages = geom->num_pages;
   A.g.bt_stride = geom->bt_stride; A.g.seq_lens = geom->seq_lens; A.g.cu_q = geom->cu_q;
   A.g.block_table = geom->block_table;
   A.kv = reinterpret_cast<const uint8_t*>(kv_cache); A.idx = idx; A.scale_log2 = sm_scale * 1.4426950408889634f;
-  A.out = reinterpret_cast<__nv_bfloat16*>(out); A.lse = lse;
+  A.out = reinterpret_cast<__nv_bfloat16*>(dout); A.lse = dlse;
   A.o_part = reinterpret_cast<float*>(scratch);
   A.ml_part = A.o_part + (size_t)(geom->T + grid) * H * 512;
   A.err = reinterpret_cast<int*>(err_word);

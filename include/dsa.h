@@ -140,9 +140,13 @@ size_t dsa_topk_workspace_size(const dsa_geom_t* geom, int32_t k);
  *   idx [T, k] int32 (device): logical positions of the request's tokens; -1 is
  *     padding and is skipped.
  *   For each (t, h): z_i = sm_scale * q[t,h,:] . kv[s_i,:] over the selected s_i,
- *     out[t,h,:] = sum_i softmax(z)_i * kv[s_i, 0:512]  (bf16, [T, H, 512], device)
- *     lse[t,h]   = ln(sum_i exp(z_i))                    (fp32, [T, H], device, or NULL)
+ *     out[t,h,:] = sum_i softmax(z)_i * kv[s_i, 0:512]  (bf16, [T, H, 512])
+ *     lse[t,h]   = ln(sum_i exp(z_i))                    (fp32, [T, H], or NULL)
  *   An all-padding row gives out = 0 and lse = -inf.
+ *   out and lse: device memory, or page-locked host memory that the device maps
+ *     (cudaHostAlloc, or cudaHostRegister with cudaHostRegisterMapped): the kernels
+ *     then write the results straight to the host, and the stream's completion means
+ *     they are there. Anything else (pageable host memory) is DSA_ERR_INVALID_ARG.
  *   H: 1..16 or a multiple of 16 up to 128. 1 <= k <= 16384.
  */
 dsa_status_t dsa_sparse_mla_attend(const dsa_geom_t* geom, dsa_dtype_t kv_dtype, int32_t H,
@@ -287,8 +291,8 @@ typedef struct {
   const void* q;
   const void* kv_cache;
   float sm_scale;
-  void* out;                   /* [T, H, 512] bf16   */
-  float* lse;                  /* [T, H] fp32 or NULL */
+  void* out;                   /* [T, H, 512] bf16; device or mapped page-locked host memory */
+  float* lse;                  /* [T, H] fp32 or NULL; the same */
 } dsa_step_args_t;
 
 /*
