@@ -197,12 +197,15 @@ dsa_status_t run_indexer(const dsa_geom_t* g, dsa_dtype_t dt, int Hi, const void
   const uint32_t box_cols = fp8 ? 128 : 64;
   const uint64_t row_bytes = fp8 ? 128 : 256;
   if (!encode_tensor_map_2d(&mk, tdt, kc, 128, (uint64_t)g->num_pages * 64, row_bytes, box_cols, 64)) return DSA_ERR_CUDA;
-  if (!encode_tensor_map_2d(&mq, tdt, q_idx, 128, (uint64_t)g->T * Hi, row_bytes, box_cols, (uint32_t)Hi)) return DSA_ERR_CUDA;
+  const bool multi = g->T > g->B;   // some request has more than one query token
+  const int q_box = indexer_q_box_rows(Hi, multi);
+  if (!encode_tensor_map_2d(&mq, tdt, q_idx, 128, (uint64_t)g->T * Hi, row_bytes, box_cols, (uint32_t)q_box))
+    return DSA_ERR_CUDA;
   IndexerArgs A;
+  A.q_group_box = q_box != Hi;
   A.Hi = Hi; A.q_scale = q_scale; A.w = w; A.k_scale = ks; A.scores = scores; A.stride = stride;
   A.key_begin = key_begin; A.key_end = key_end;
   A.err = err;
-  const bool multi = g->T > g->B;   // some request has more than one query token
   const int group = indexer_max_requests();
   for (int b0 = 0; b0 < g->B; b0 += group) {
     dsa_geom_t sub = *g;

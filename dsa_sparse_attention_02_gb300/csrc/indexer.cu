@@ -101,9 +101,12 @@ __device__ __forceinline__ UnitInfo decode_unit(const int* prefix, const int* cu
   const int q0 = cuq[lo], q1 = cuq[lo + 1];
   const int nq = q1 - q0;
   const int ngroups = (nq + kQG - 1) / kQG;
+  // group-major: a unit run keeps its query group and streams the key tiles (a
+  // group's queries are loaded once; tiles are the smaller operand)
+  const int ntiles = (prefix[lo + 1] - prefix[lo]) / ngroups;
   const int local = u - prefix[lo];
-  const int lt = local / ngroups;
-  const int grp = local - lt * ngroups;
+  const int grp = local / ntiles;
+  const int lt = local - grp * ntiles;
   ui.tile = tile0 + lt;
   ui.q_start = q0 + grp * kQG;
   ui.q_count = min(kQG, nq - grp * kQG);
@@ -282,6 +285,16 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, Ind
                 }
                 cp_async_arrive(bar);
               }
+              if (kQG > 1 && A.q_group_box) {
+                // the group's rows are consecutive in q, w and q_scale, and Hi == kHp lays
+                // them out in the slot as one box: one copy per atom and per vector (a box
+                // past the last query is zero-filled and counted in full)
+                mbar_arrive_expect_tx(bar, kQG * Hi * 128 * C::kAtoms + q_count * Hi * (kFp8 ? 8 : 4));
+                for (int a = 0; a < C::kAtoms; ++a)
+                  tma_load_2d(smem_u32(sl + a * (C::kN * 128)), &map_q, bar, a * (kFp8 ? 128 : 64), q_start * Hi);
+                bulk_load(smem_u32(sl + C::kWOff), A.w + (int64_t)q_start * Hi, q_count * Hi * 4, bar);
+                if (kFp8) bulk_load(smem_u32(sl + C::kQsOff), A.q_scale + (int64_t)q_start * Hi, q_count * Hi * 4, bar);
+              } else {
               mbar_arrive_expect_tx(bar, q_count * Hi * (128 * C::kAtoms + (vec ? 4 + (kFp8 ? 4 : 0) : 0)));
               for (int j = 0; j < q_count; ++j) {
                 const int t = q_start + j;
@@ -291,6 +304,7 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, Ind
                   bulk_load(smem_u32(sl + C::kWOff + j * kHp * 4), A.w + (int64_t)t * Hi, Hi * 4, bar);
                   if (kFp8) bulk_load(smem_u32(sl + C::kQsOff + j * kHp * 4), A.q_scale + (int64_t)t * Hi, Hi * 4, bar);
                 }
+              }
               }
               ++qcount;
             }
@@ -486,6 +500,10 @@ static cudaError_t launch_indexer_t(const CUtensorMap& mk, const CUtensorMap& mq
 }
 
 int indexer_max_requests() { return IndexerCfg<true, 64, 1>::kMaxB; }
+
+int indexer_q_box_rows(int Hi, bool multi_query) {
+  return multi_query && (Hi == 16 || Hi == 64) ? 4 * Hi : Hi;
+}
 
 cudaError_t indexer_launch(bool fp8, int Hi, bool multi_query, const CUtensorMap& mk, const CUtensorMap& mq,
                            const IndexerArgs& A, int grid, cudaStream_t st) {

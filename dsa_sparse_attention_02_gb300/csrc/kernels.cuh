@@ -20,8 +20,12 @@ struct IndexerArgs {
   int64_t stride;
   int key_begin;        // keys [key_begin, key_end) are scored; key_begin a multiple of 128
   int key_end;          // a multiple of 128, or past every request's length
+  bool q_group_box;     // map_q's box is a whole query group (indexer_q_box_rows): one copy per group
   int* err;
 };
+// Rows of the query tensor map's box: a whole group of 4 queries when several queries
+// share a unit and Hi fills the padded head count (16 or 64), else one query's Hi rows.
+int indexer_q_box_rows(int Hi, bool multi_query);
 cudaError_t indexer_launch(bool fp8, int Hi, bool multi_query, const CUtensorMap& mk, const CUtensorMap& mq,
                            const IndexerArgs& A, int grid, cudaStream_t st);
 int indexer_max_requests();   // requests per launch (a call with more loops over groups)
