@@ -19,19 +19,25 @@
 // only what changed since the previous unit: a new key tile (two pages by TMA,
 // their key scales by bulk copy) into a ring of key stages, and a new query group
 // (the QG x Hp query rows by TMA, w and q_scale by bulk copy) into a ring of query
-// slots; a small descriptor per unit names the stage and slot it uses. In decode
-// a request's query is loaded once for all its key tiles; in prefill a key tile is
-// loaded once for the run of query groups that follow it. Warp M issues the MMAs
-// into a ring of up to four TMEM accumulators; 4*EW epilogue warps drain them (one
-// 64-column TMEM load per query). The epilogue takes what it needs from a key
-// stage (the key scales) and from a query slot (w * q_scale) when it first meets
-// it and releases it at once, so a stage is held only until its MMAs complete.
-// Units are split contiguously over a persistent grid, key-tile major.
+// slots; a small descriptor per unit names the stage and slot it uses. A request's
+// units run group-major: a query group is loaded once for all its key tiles (in
+// decode the group is the request's one query; in prefill the 16 KB key tiles
+// stream past the 32 KB group), and a group's QG consecutive queries arrive in one
+// copy per operand. Warp M issues the MMAs into a ring of up to four TMEM
+// accumulators; 4*EW epilogue warps drain them (one 64-column TMEM load per query;
+// EW = 4 in the multi-query variant, one query per warp). The epilogue takes what it
+// needs from a key stage (the key scales) and from a query slot (w * q_scale) when it
+// first meets it and releases it at once, so a stage is held only until its MMAs
+// complete. Units are split contiguously over a persistent grid.
 #include <cstdint>
 #include "kernels.cuh"
 
 namespace dsa {
 
+
+// Epilogue warp groups of the multi-query variant: four, so that each of the 16
+// epilogue warps takes one query of a unit (more warps to hide the accumulator reads).
+constexpr int kMultiEpiGroups = 4;
 
 template <bool kFp8, int kHp, int kQG>
 struct IndexerCfg {
@@ -50,7 +56,8 @@ struct IndexerCfg {
   static constexpr int kKStagesFit = (kBudget - kQSlots * kQSlotBytes) / kKStageBytes;
   static constexpr int kKStages = kKStagesFit < 8 ? kKStagesFit : 8;
   static constexpr int kDescs = 16;                            // unit descriptor ring
-  static constexpr int kEW = kQG >= 2 ? 2 : 1;                 // epilogue warp groups
+  static constexpr int kEW = kQG >= 2 ? kMultiEpiGroups : 1;   // epilogue warp groups
+  static constexpr int kQPerWarp = kQG / kEW;                  // queries of a unit per epilogue warp
   static constexpr int kEpiWarps = 4 * kEW;
   static constexpr int kProdWarps = 1;
   static constexpr int kThreads = 32 * (kEpiWarps + kProdWarps + 1);
@@ -131,7 +138,7 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, Ind
   __shared__ uint64_t tfull_bar[C::kAccs], tempty_bar[C::kAccs];
   // w * q_scale of the current query group, one copy per epilogue warp
   constexpr bool kWqRegs = kQG == 1 && C::kCtasPerSm == 1;
-  __shared__ __align__(16) float wq_s[kWqRegs ? 1 : C::kEpiWarps][kWqRegs ? 4 : kQG * kHp];
+  __shared__ __align__(16) float wq_s[kWqRegs ? 1 : C::kEpiWarps][kWqRegs ? 4 : C::kQPerWarp * kHp];
   __shared__ UnitDesc descs[C::kDescs];
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
@@ -410,7 +417,12 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, Ind
           __syncwarp();   // the previous group's copy has been read by every lane
           const float* wv = reinterpret_cast<const float*>(sl + C::kWOff);
           const float* qv = reinterpret_cast<const float*>(sl + C::kQsOff);
-          for (int e = lane; e < kQG * kHp; e += 32) wq_s[warp][e] = wv[e] * (kFp8 ? qv[e] : 1.f);
+          // this warp's queries of the group: half, half + kEW, ...
+#pragma unroll
+          for (int jj = 0; jj < C::kQPerWarp; ++jj) {
+            const int o = (half + jj * C::kEW) * kHp;
+            for (int e = lane; e < kHp; e += 32) wq_s[warp][jj * kHp + e] = wv[o + e] * (kFp8 ? qv[o + e] : 1.f);
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&q_empty[cur_q]));
@@ -421,27 +433,29 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, Ind
       const int sidx = d.tile * 128 + key;
       const bool in_ctx = sidx < d.len && sidx < A.key_end;
 #pragma unroll 1
-      for (int j = half; j < kQG; j += C::kEW) {
+      for (int jj = 0; jj < C::kQPerWarp; ++jj) {
+        const int j = half + jj * C::kEW;
         if (j >= d.q_count) break;
         float v[kHp];
         if constexpr (kHp == 64) tmem_ld64(tmem + acc * C::kN + j * kHp + ((uint32_t)(quarter * 32) << 16), v);
         else tmem_ld16(tmem + acc * C::kN + j * kHp + ((uint32_t)(quarter * 32) << 16), v);
         tmem_ld_wait();
-        // four partial sums (heads e, e+1, e+2, e+3 mod 4), added at the end
-        float s4[4] = {0.f, 0.f, 0.f, 0.f};
+        // four partial sums (heads e, e+1, e+2, e+3 mod 4) as two packed pairs, added at
+        // the end in the same order as four scalar sums would be
+        float2 s2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int e = 0; e < kHp; e += 4) {
-          float c[4];
+          float2 c0, c1;
           if constexpr (kWqRegs) {
-            c[0] = wq[e]; c[1] = wq[e + 1]; c[2] = wq[e + 2]; c[3] = wq[e + 3];
+            c0 = make_float2(wq[e], wq[e + 1]); c1 = make_float2(wq[e + 2], wq[e + 3]);
           } else {
-            const float4 w4 = *reinterpret_cast<const float4*>(wqw + j * kHp + e);
-            c[0] = w4.x; c[1] = w4.y; c[2] = w4.z; c[3] = w4.w;
+            const float4 w4 = *reinterpret_cast<const float4*>(wqw + jj * kHp + e);
+            c0 = make_float2(w4.x, w4.y); c1 = make_float2(w4.z, w4.w);
           }
-#pragma unroll
-          for (int x = 0; x < 4; ++x) s4[x] = fmaf(c[x], fmaxf(v[e + x], 0.f), s4[x]);
+          s2[0] = __ffma2_rn(c0, make_float2(fmaxf(v[e], 0.f), fmaxf(v[e + 1], 0.f)), s2[0]);
+          s2[1] = __ffma2_rn(c1, make_float2(fmaxf(v[e + 2], 0.f), fmaxf(v[e + 3], 0.f)), s2[1]);
         }
-        const float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+        const float sum = (s2[0].x + s2[0].y) + (s2[1].x + s2[1].y);
         if (in_ctx) {
           const int t = d.q_start + j;
           const int pos = d.pos0 + j;
