@@ -59,11 +59,11 @@ constexpr int kPairBytes = 2 * kAtomBytes;          // 32 KB
 // chunks) that the codes are converted into, so that a chunk's conversion waits only on
 // the attention of the chunk two before it, fed by three code stages of one pair each
 // (the pair's 128 codes and one scale of each of the chunk's 128 rows), so that the
-// code bytes in flight do not wait on the bf16 slots. To fit, record caches keep one P
-// buffer and one partial-score exchange buffer (the softmax writes P(i) only after
-// PV(i-1) has completed, so a second P buffer would never be used).
+// code bytes in flight do not wait on the bf16 slots. Two P buffers (P(i) is written
+// once PV(i-2) has released its buffer, without waiting for PV(i-1)); to fit, record
+// caches keep one partial-score exchange buffer.
 template <int kKv> constexpr int kPairSlotsOf = kKv == kKvBf16 ? 5 : 4;
-template <int kKv> constexpr int kPBufsOf = kKv == kKvBf16 ? 2 : 1;
+template <int kKv> constexpr int kPBufsOf = 2;
 template <int kKv> constexpr int kXBufsOf = kKv == kKvBf16 ? 2 : 1;
 constexpr int kCodeStages = 3;
 constexpr int kCodeRowBytes = 128;                          // one pair's codes of a row
@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
 
   __shared__ uint64_t pair_full[kPairSlots], pair_empty[kPairSlots], rope_full[kRopeSlots], rope_empty[kRopeSlots];
   __shared__ uint64_t q_full, q_empty;
-  __shared__ uint64_t s_full[2], s_empty[2], p_full[2], p_empty[2], o_full, o_free, grp_bar;
+  __shared__ uint64_t s_full[2], s_empty[2], p_full[2], p_empty[2], o_full[2], o_free, grp_bar;
   __shared__ uint64_t x_full[2], x_free[2];   // partial-score exchange with the other CTA
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
@@ -308,7 +308,8 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       mbar_init(smem_u32(&x_full[j]), 1);     // local expect_tx + 8 KB of st.async from the other CTA
       mbar_init(smem_u32(&x_free[j]), 4);     // one signal per softmax warp of the other CTA
     }
-    mbar_init(smem_u32(&o_full), 1);     // one phase per chunk's PV
+    mbar_init(smem_u32(&o_full[0]), 1);  // one phase per even chunk's PV
+    mbar_init(smem_u32(&o_full[1]), 1);  // and per odd chunk's
     mbar_init(smem_u32(&o_free), 4);     // softmax warps have read O at a segment end
     mbar_init(smem_u32(&grp_bar), 4);
     for (int j = 0; j < kRowBufs; ++j) {
@@ -599,7 +600,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
                            (ks != 0 || !cp.first) ? 1u : 0u);
               mma_commit(smem_u32(&pair_empty[ps]));
             }
-            mma_commit(smem_u32(&o_full));
+            mma_commit(smem_u32(&o_full[pv_i & 1]));
             mma_commit(smem_u32(&p_empty[sb]));
             chunk_next(pv_cp, ++pv_i);
             progress = true;
@@ -775,17 +776,16 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         z[h] = (z[h] == neg_inf) ? 0.f : fast_exp2(z[h] - m[h]);   // z now holds p <= 256
         l[h] += z[h];
       }
-      // o_full completes once per chunk's PV, and a parity wait is only unambiguous
-      // while the barrier is at most one phase ahead of the phase waited for. So the
-      // softmax observes every phase in order: here PV(i-1) (it observed PV(i-2) at
-      // chunk i-1, and PV(i) cannot complete before P(i) is written), and at a segment
-      // end PV(i). Waiting only at segment ends let a wait for PV(i) return on
-      // PV(i-2)'s completion while PV(i-1) was still in flight, and the epilogue then
-      // read O without the last chunks' contributions.
-      if (i > 0 && !mbar_wait(smem_u32(&o_full), (i - 1) & 1, &abort_flag, A.err)) break;
+      // PV(j) completes phase j/2 of o_full[j % 2]. A parity wait is unambiguous while
+      // the barrier's previous phase has completed: before P(j) was written, PV(j-2)
+      // had completed (P buffer j % 2 was released by it), so a wait for PV(i-1) here
+      // or for PV(i) at a segment end never returns on an older phase, and the softmax
+      // need not observe every PV. It waits for PV(i-1) only to rescale O, so P(i) no
+      // longer waits for the previous chunk's PV.
       if (any_raise && !cp.first) {
-        // O in TMEM holds this segment's earlier chunks; PV(i-1) has completed (above):
+        // O in TMEM holds this segment's earlier chunks: once PV(i-1) has completed,
         // scale the raised heads' columns by alpha (PV(i) waits for this chunk's P).
+        if (!mbar_wait(smem_u32(&o_full[(i - 1) & 1]), ((i - 1) >> 1) & 1, &abort_flag, A.err)) break;
         tc_fence_after();
 #pragma unroll
         for (int mb = 0; mb < 2; ++mb) {
@@ -824,7 +824,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         red_i ^= 1;
         // O^T after this chunk's PV (lane = latent column within a 128-block),
         // streamed out one 16-column block of TMEM at a time
-        if (!mbar_wait(smem_u32(&o_full), i & 1, &abort_flag, A.err)) break;
+        if (!mbar_wait(smem_u32(&o_full[i & 1]), (i >> 1) & 1, &abort_flag, A.err)) break;
         tc_fence_after();
         const int64_t c_first = split_owner((int64_t)cp.t * A.C, A.n_chunks, G);
         const int64_t c_last = split_owner((int64_t)cp.t * A.C + A.C - 1, A.n_chunks, G);
