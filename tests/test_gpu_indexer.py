@@ -79,11 +79,14 @@ def test_topk_of_gpu_scores_exact_and_index_sets_match_oracle(name, kw):
         assert ok, (t, msg)
 
 
-@pytest.mark.parametrize("hi", [1, 3, 5, 63])
+@pytest.mark.parametrize("hi", [1, 3, 5, 16, 63, 64])
 @pytest.mark.parametrize("qk", ["e4m3", "bf16"])
 def test_indexer_any_head_count(hi, qk):
     """Head counts that are not a multiple of 4 (w and q_scale rows off 16-byte copies)
-    and below the MMA's 16: padded with zero weights in the kernel."""
+    and below the MMA's 16: padded with zero weights in the kernel. Hi = 16 and 64 fill
+    the padded head count, so a multi-query group arrives as one copy per operand
+    (requests of 1, 3 and 2 queries: groups shorter than 4, and a last group whose box
+    runs past the final query row)."""
     wl = inputs.make_workload(f"hi{hi}", [700, 3000, 129], [1, 3, 2], topk=256, hi=hi, qk_dtype=qk, seed=20 + hi)
     dw = runner.DeviceWorkload(wl, DEV)
     sc = _scores(wl, dw).cpu().numpy()
