@@ -221,3 +221,72 @@ def test_record_dequantization_bit_exact(kv_dtype):
             assert np.array_equal(got[t, h], exp), (t, h, r)
             assert np.all(np.abs(got[t, h] - exact) <= 2.0 ** -8 * np.abs(exact)), (t, h)
             assert np.all(np.abs(got[t, h] - ref[h]) <= 2.0 ** -8 * np.abs(ref[h]) + 1e-12), (t, h)
+
+
+def _scale_rows(lay, rows, e):
+    """Multiply the latent rows `rows` (physical) by 2**e exactly, in place: bf16 values
+    by their exponent; records by their four scales and their bf16 RoPE values."""
+    def bf16_times(bits, e):
+        f = (bits.astype(np.uint32) << 16).view(np.float32) * np.float32(2.0 ** e)
+        return (f.view(np.uint32) >> 16).astype(np.uint16)
+    P = lay.kv.shape[0]
+    if lay.kv_dtype == "bf16":
+        kv = lay.kv.reshape(P * inputs.PAGE, -1)
+        kv[rows] = bf16_times(kv[rows].view(np.uint16), e).view(kv.dtype)
+        return
+    pages = lay.kv.reshape(P, -1)
+    for r in rows:
+        p, s = divmod(int(r), inputs.PAGE)
+        sa = inputs.PAGE * inputs.D_LATENT + 16 * s
+        sc = pages[p, sa:sa + 16].view(np.float32) * np.float32(2.0 ** e)
+        pages[p, sa:sa + 16] = sc.view(np.uint8)
+        ra = inputs.PAGE * inputs.D_LATENT + inputs.PAGE * 16 + 128 * s
+        pages[p, ra:ra + 128] = bf16_times(pages[p, ra:ra + 128].view(np.uint16), e).view(np.uint8)
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
+def test_attend_reference_max_rises_over_chunks(kv_dtype):
+    """Scores that grow chunk after chunk (the rows of a query's 128-key chunk c scaled by
+    2**(c // 2)), so the online softmax's reference max moves by more than 2**8 several
+    times within a segment and O is rescaled in TMEM between PVs (both the bf16 and the
+    record producers feed it)."""
+    rng = np.random.default_rng(77)
+    k = 2048
+    wl = inputs.make_workload("rise", [3000, 5000, 2600, 8000], [1, 1, 1, 1], topk=k, hi=4,
+                              qk_dtype="bf16", kv_dtypes=(kv_dtype,), seed=41)
+    lay = wl.layers[0]
+    if kv_dtype != "bf16":
+        # every record scale a power of two, so that code x scale is exact in bf16 and the
+        # kernel's bf16 operands equal the oracle's values: at scores of a few hundred a
+        # 2**-9 rounding of the operands would move the softmax weights by itself
+        P = lay.kv.shape[0]
+        pages = lay.kv.reshape(P, -1)
+        sa = inputs.PAGE * inputs.D_LATENT
+        pages[:, sa:sa + inputs.PAGE * 16] = np.full(P * inputs.PAGE * 4, 2.0 ** -8, np.float32).view(
+            np.uint8).reshape(P, -1)
+    _, pos = oracle.query_positions(wl.seq_lens, wl.n_q)
+    idx = np.full((wl.T, k), -1, dtype=np.int32)
+    for t in range(wl.T):
+        sel = np.sort(rng.choice(int(pos[t]) + 1, size=k, replace=False)).astype(np.int32)
+        idx[t] = sel
+        bt = wl.block_table[t]
+        phys = bt[sel // inputs.PAGE].astype(np.int64) * inputs.PAGE + sel % inputs.PAGE
+        for c in range(k // 128):
+            _scale_rows(lay, phys[128 * c: 128 * (c + 1)], c // 2)
+    dw = runner.DeviceWorkload(wl, DEV)
+    out, lse = _attend(wl, dw, 0, idx, k)
+    # The values are up to 2**7 times the usual latent scale, so the absolute part of the
+    # tolerance scales with them: TOL of max|O_ref| (the same relative bound as at unit
+    # scale; bf16 output rounding alone is 2**-9 of it). A lost rescale or a PV read
+    # before it completed is off by a large fraction of max|O_ref|.
+    ref = oracle.sparse_mla(lay.q, lay.kv, lay.kv_dtype, {t: idx[t] for t in range(wl.T)}, wl.seq_lens,
+                            wl.n_q, wl.block_table, wl.sm_scale, range(wl.T))
+    tol = TOL[kv_dtype]
+    worst = 0.0
+    for t in range(wl.T):
+        o_ref, l_ref = ref[t]
+        scale = max(1.0, float(np.abs(o_ref).max()))
+        worst = max(worst, assert_close(out[t], o_ref, tol * scale, tol, f"out t={t}") / scale)
+        assert_close(lse[t], l_ref, tol, tol, f"lse t={t}")
+        assert l_ref.min() > 20.0 and scale > 100.0   # the last chunks dominate
+    print(f"{kv_dtype}: max |O err| / max|O| {worst:.3g}")

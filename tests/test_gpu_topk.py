@@ -105,3 +105,24 @@ def test_long_rows_multi_level_merges():
     _run(rows, lengths, 4096)
     _run(rows[2:5], lengths[2:5], 8192)
     _run(rows[:1], lengths[:1], 1)
+
+
+def test_third_digit_and_whole_bin_paths():
+    """Rows whose keys differ only in their lowest bits after a sign split, so the
+    selection needs all three radix digits (the third re-uses the first digit's cleared
+    histogram); rows where the threshold bin is taken whole after one or two digits; and
+    the same through the chunk and merge levels of a long row."""
+    rng = np.random.default_rng(11)
+    one = np.float32(1.0)
+    ulps = (np.arange(9000, dtype=np.int64) + np.int64(np.float32(1.0).view(np.int32))).astype(np.int32).view(np.float32)
+    third = np.concatenate([np.full(3000, -1.0, np.float32), rng.permutation(ulps)])       # 1 + j ulp, j < 9000
+    dup_low = np.concatenate([rng.permutation(ulps)[:6000], rng.permutation(ulps)[:6000]])  # every value twice
+    whole1 = np.concatenate([np.full(2048, 4.0, np.float32), rng.uniform(0, 1, 6000).astype(np.float32)])
+    whole2 = np.concatenate([np.full(1000, 8.0, np.float32), np.full(1048, 4.0 + 2 ** -10, np.float32),
+                             np.full(3000, 4.0, np.float32), rng.uniform(0, 1, 3000).astype(np.float32)])
+    rows = [third, dup_low, whole1, whole2, one + rng.permutation(ulps - one)]
+    for k in (2048, 777, 1):
+        _run(rows, [len(r) for r in rows], k)
+    long_row = np.concatenate([rng.permutation(np.tile(ulps, 4)), np.full(5000, -2.0, np.float32)])
+    _run([long_row], [len(long_row)], 2048)
+    _run([long_row], [len(long_row)], 100)
