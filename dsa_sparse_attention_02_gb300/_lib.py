@@ -130,6 +130,17 @@ def _dptr(t):
     return t.data_ptr()
 
 
+def _optr(t):
+    """Address of an attention output (None -> NULL): a CUDA tensor, or a page-locked
+    host tensor, which the C side resolves to its device mapping (and refuses if it has
+    none). Anything else is refused here."""
+    if t is None:
+        return None
+    if isinstance(t, torch.Tensor) and not t.is_cuda and t.is_pinned():
+        return t.data_ptr()
+    return _dptr(t)
+
+
 def _stream(stream=None):
     s = torch.cuda.current_stream() if stream is None else stream
     return C.c_void_p(s.cuda_stream)
@@ -199,7 +210,7 @@ def dsa_sparse_mla_attend(geom: Geometry, kv_dtype: int, q, kv_cache, idx, k: in
                           out, lse, ws, stream=None):
     H = int(q.shape[1])
     st = load().dsa_sparse_mla_attend(geom.ref, kv_dtype, H, _dptr(q), _dptr(kv_cache), _dptr(idx),
-                                      int(k), float(sm_scale), _dptr(out), _dptr(lse),
+                                      int(k), float(sm_scale), _optr(out), _optr(lse),
                                       _dptr(ws), ws.numel(), _stream(stream))
     _check(st, "dsa_sparse_mla_attend")
 
@@ -211,7 +222,7 @@ def dsa_sparse_mla_attend_static(geom: Geometry, kv_dtype: int, q, kv_cache, idx
     is a device int32 (zeroed by the caller) that receives device-side errors."""
     H = int(q.shape[1])
     st = load().dsa_sparse_mla_attend_static(geom.ref, kv_dtype, H, _dptr(q), _dptr(kv_cache), _dptr(idx),
-                                             int(k), float(sm_scale), _dptr(out), _dptr(lse),
+                                             int(k), float(sm_scale), _optr(out), _optr(lse),
                                              _dptr(err_word), _stream(stream))
     _check(st, "dsa_sparse_mla_attend_static")
 
@@ -254,7 +265,7 @@ def make_step_args(geom: Geometry, topk: int, *, qk_dtype=DSA_E4M3, q_idx=None, 
     return dsa_step_args_t(geom.c, int(topk), int(qk_dtype), Hi, _dptr(q_idx), _dptr(q_scale),
                            _dptr(w), _dptr(idx_k_cache), _dptr(idx_k_scale), _dptr(reuse_idx),
                            _dptr(idx_out), int(kv_dtype), H, _dptr(q), _dptr(kv_cache),
-                           float(sm_scale), _dptr(out), _dptr(lse))
+                           float(sm_scale), _optr(out), _optr(lse))
 
 
 def dsa_decode_step_workspace_size(args: dsa_step_args_t) -> int:

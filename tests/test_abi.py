@@ -235,8 +235,9 @@ def test_binding_structs_match_the_header(name):
 
 def test_binding_refuses_host_tensors_for_device_arguments(lib):
     """Host tensors are refused by the binding before any call reaches the library,
-    so a host address never reaches a kernel (dsa_stage_copy alone takes host memory,
-    and checks it on the C side)."""
+    so a host address never reaches a kernel (dsa_stage_copy takes host memory, and the
+    attention's outputs may be page-locked host memory; the C side checks both). A
+    pageable host tensor is refused for an output too."""
     import torch
     seq = torch.tensor([64], dtype=torch.int32)
     cu = torch.tensor([0, 1], dtype=torch.int32)
@@ -250,6 +251,9 @@ def test_binding_refuses_host_tensors_for_device_arguments(lib):
     with pytest.raises(TypeError, match="CUDA tensor"):
         _lib._dptr(bytearray(16))
     assert _lib._dptr(None) is None
+    with pytest.raises(TypeError, match="CUDA tensor"):
+        _lib._optr(torch.zeros(16))                      # pageable
+    assert _lib._optr(None) is None
 
 
 def test_wait_probe_validates_before_launch(lib):

@@ -78,3 +78,30 @@ def test_static_scratch_rejects_calls_beyond_its_size():
                                           L.out, L.lse, err)
     assert e.value.status == _lib.DSA_ERR_WORKSPACE
     assert "static scratch" in str(e.value)
+
+
+def test_attend_entry_points_write_page_locked_host_outputs():
+    """Both attention entry points with O and LSE in page-locked host memory give the
+    device-output results bit for bit."""
+    wl = inputs.make_config("decode", batch=6)
+    dw = runner.DeviceWorkload(wl, DEV)
+    L = dw.layers[0]
+    idx = _selection(wl, wl.topk, 5)
+    dev_out, dev_lse = torch.empty_like(L.out), torch.empty_like(L.lse)
+    ws = _lib.workspace(_lib.dsa_sparse_mla_attend_workspace_size(dw.geom, 16, wl.topk), DEV)
+    _lib.dsa_sparse_mla_attend(dw.geom, L.kv_dtype, L.q, L.kv, idx, wl.topk, wl.sm_scale, dev_out, dev_lse, ws)
+    torch.cuda.synchronize()
+    assert _lib.dsa_get_error(ws) == 0
+    host_out = torch.full(L.out.shape, float("nan"), dtype=L.out.dtype).pin_memory()
+    host_lse = torch.full(L.lse.shape, float("nan"), dtype=L.lse.dtype).pin_memory()
+    _lib.dsa_sparse_mla_attend(dw.geom, L.kv_dtype, L.q, L.kv, idx, wl.topk, wl.sm_scale, host_out, host_lse, ws)
+    torch.cuda.synchronize()
+    assert _lib.dsa_get_error(ws) == 0
+    assert torch.equal(host_out, dev_out.cpu()) and torch.equal(host_lse, dev_lse.cpu())
+    host_out.fill_(float("nan")); host_lse.fill_(float("nan"))
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    _lib.dsa_sparse_mla_attend_static(dw.geom, L.kv_dtype, L.q, L.kv, idx, wl.topk, wl.sm_scale, host_out,
+                                      host_lse, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(host_out, dev_out.cpu()) and torch.equal(host_lse, dev_lse.cpu())
