@@ -190,7 +190,7 @@ dsa_status_t check_indexer(const dsa_geom_t* g, dsa_dtype_t dt, int Hi, const vo
 // launch each (query rows stay absolute: each group's cu_q entries index them).
 dsa_status_t run_indexer(const dsa_geom_t* g, dsa_dtype_t dt, int Hi, const void* q_idx, const float* q_scale,
                          const float* w, const void* kc, const float* ks, float* scores, int64_t stride, int* err,
-                         cudaStream_t st, int key_begin = 0, int key_end = INT32_MAX) {
+                         cudaStream_t st, int key_begin = 0, int key_end = INT32_MAX, bool pdl = false) {
   const bool fp8 = dt == DSA_E4M3;
   CUtensorMap mk, mq;
   const CUtensorMapDataType tdt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -214,7 +214,7 @@ dsa_status_t run_indexer(const dsa_geom_t* g, dsa_dtype_t dt, int Hi, const void
     sub.cu_q = g->cu_q + b0;
     sub.block_table = g->block_table + (int64_t)b0 * g->bt_stride;
     A.g = to_dev(&sub);
-    const dsa_status_t s = from_cuda(indexer_launch(fp8, Hi, multi, mk, mq, A, num_sms(), st));
+    const dsa_status_t s = from_cuda(indexer_launch(fp8, Hi, multi, mk, mq, A, num_sms(), pdl || b0 > 0, st));
     if (s != DSA_OK) return s;
   }
   return DSA_OK;
@@ -352,6 +352,16 @@ ScorePlan whole_rows(const dsa_step_args_t* a) { return ScorePlan{a->geom.T, 0};
 // Width of the score buffer's rows.
 int64_t plan_width(const dsa_geom_t* g, const ScorePlan& p) { return p.span > 0 ? p.span : step_score_stride(g); }
 
+// Query ranges of the bounded step: the geometry of up to kRangeRing ranges is written
+// by one launch before the first of them, each range's in a slot of range_stride ints
+// (a few KB, small beside even a one-row score budget).
+constexpr int kRangeRing = 8;
+int range_stride(const dsa_geom_t* g) { return (2 * g->B + 1 + 3) / 4 * 4; }
+size_t range_ring_bytes(const dsa_geom_t* g, int64_t rows) {
+  const int64_t n = (g->T + rows - 1) / rows;
+  return align_up((size_t)(n < kRangeRing ? n : kRangeRing) * range_stride(g) * sizeof(int32_t), 256);
+}
+
 // Workspace of the step under a score plan. Layout: header | query-range geometry
 // (ranges only) | scores [rows, width] | idx [T, k] (unless idx_out) | attention /
 // top-k scratch.
@@ -360,7 +370,7 @@ size_t step_workspace_bytes(const dsa_step_args_t* a, const ScorePlan& p) {
   size_t bytes = kHeaderBytes;
   const int64_t r = p.rows < g->T ? p.rows : g->T;
   if (!a->reuse_idx) {
-    if (r < g->T) bytes += align_up((size_t)(2 * g->B + 1) * sizeof(int32_t), 256);
+    if (r < g->T) bytes += range_ring_bytes(g, r);
     bytes += align_up((size_t)r * plan_width(g, p) * sizeof(float), 256);
     if (!a->idx_out) bytes += align_up((size_t)g->T * (a->topk > 0 ? a->topk : 1) * sizeof(int32_t), 256);
   }
@@ -375,8 +385,10 @@ size_t step_workspace_bytes(const dsa_step_args_t* a, const ScorePlan& p) {
 // Scores and selects one range of queries (geometry `sub`, whose rows are the step's
 // rows t0.. onward) into idx_out: the whole rows at once, or span by span, each
 // span's chunks reduced to candidate lists before the next span is scored.
+// pdl_first: the range's first indexer launch may start before the kernel just before
+// it ends (that kernel is our own and the range's geometry is already written).
 dsa_status_t select_range(const dsa_step_args_t* a, const dsa_geom_t* sub, int64_t t0, const ScorePlan& p,
-                          float* scores, int32_t* idx_out, void* scratch, int* err, cudaStream_t st) {
+                          float* scores, int32_t* idx_out, void* scratch, int* err, bool pdl_first, cudaStream_t st) {
   const dsa_geom_t* g = &a->geom;
   const size_t qrow = (size_t)a->Hi * 128 * (a->qk_dtype == DSA_E4M3 ? 1 : 2);
   const uint8_t* q_idx = reinterpret_cast<const uint8_t*>(a->q_idx) + (size_t)t0 * qrow;
@@ -385,7 +397,8 @@ dsa_status_t select_range(const dsa_step_args_t* a, const dsa_geom_t* sub, int64
   dsa_status_t s;
   if (p.span == 0) {
     const int64_t stride = step_score_stride(g);
-    s = run_indexer(sub, a->qk_dtype, a->Hi, q_idx, q_scale, w, a->idx_k_cache, a->idx_k_scale, scores, stride, err, st);
+    s = run_indexer(sub, a->qk_dtype, a->Hi, q_idx, q_scale, w, a->idx_k_cache, a->idx_k_scale, scores, stride, err, st,
+                    0, INT32_MAX, pdl_first);
     if (s != DSA_OK) return s;
     // The top-k kernels follow this call's own kernels, so they may launch early
     // (programmatic dependent launch) and wait for their inputs inside.
@@ -397,8 +410,10 @@ dsa_status_t select_range(const dsa_step_args_t* a, const dsa_geom_t* sub, int64
   for (int c0 = 0; c0 < nch; c0 += per_span) {
     const int nl = nch - c0 < per_span ? nch - c0 : per_span;
     const int64_t k0 = (int64_t)c0 * chunk;
+    // a later span's scores overwrite the buffer only after its grid-dependency wait,
+    // which the previous span's chunk pass ends
     s = run_indexer(sub, a->qk_dtype, a->Hi, q_idx, q_scale, w, a->idx_k_cache, a->idx_k_scale, scores, p.span, err,
-                    st, (int)k0, (int)(k0 + p.span < INT32_MAX ? k0 + p.span : INT32_MAX));
+                    st, (int)k0, (int)(k0 + p.span < INT32_MAX ? k0 + p.span : INT32_MAX), pdl_first || c0 > 0);
     if (s != DSA_OK) return s;
     s = from_cuda(topk_chunks_launch(to_dev(sub), scores, p.span, a->topk, c0, nl, scratch, err, true, st));
     if (s != DSA_OK) return s;
@@ -436,7 +451,7 @@ dsa_status_t run_step(const dsa_step_args_t* a, const ScorePlan& p, void* ws, si
     int32_t* range_geom = nullptr;
     if (ranges) {
       range_geom = reinterpret_cast<int32_t*>(ptr);
-      ptr += align_up((size_t)(2 * g->B + 1) * sizeof(int32_t), 256);
+      ptr += range_ring_bytes(g, p.rows);
     }
     const int64_t r = ranges ? p.rows : g->T;
     float* scores = reinterpret_cast<float*>(ptr);
@@ -447,22 +462,32 @@ dsa_status_t run_step(const dsa_step_args_t* a, const ScorePlan& p, void* ws, si
       ptr += align_up((size_t)g->T * a->topk * sizeof(int32_t), 256);
     }
     if (!ranges) {
-      s = select_range(a, g, 0, p, scores, idx_buf, ptr, err, st);
+      s = select_range(a, g, 0, p, scores, idx_buf, ptr, err, false, st);
       if (s != DSA_OK) return s;
     } else {
       // Bounded scoring: queries [t0, t0 + rows) at a time, each range described by
       // its own geometry (same requests, block table and positions), scored into the
-      // same rows of `scores` and reduced to its selection before the next range.
-      for (int64_t t0 = 0; t0 < g->T; t0 += p.rows) {
+      // same rows of `scores` and reduced to its selection before the next range. The
+      // geometries of up to kRangeRing ranges are written by one launch ahead of them,
+      // so each later range's indexer may start (programmatic dependent launch) while
+      // the previous range's top-k finishes; its scores wait for it.
+      const int stride = range_stride(g);
+      const int64_t n_ranges = (g->T + p.rows - 1) / p.rows;
+      for (int64_t r = 0; r < n_ranges; ++r) {
+        const int64_t t0 = r * p.rows;
         const int t1 = (int)(t0 + p.rows < g->T ? t0 + p.rows : g->T);
-        s = from_cuda(query_range_launch(g->cu_q, g->seq_lens, g->B, (int)t0, t1, range_geom,
-                                         range_geom + g->B + 1, st));
-        if (s != DSA_OK) return s;
+        const int slot = (int)(r % kRangeRing);
+        if (slot == 0) {
+          const int n = (int)(n_ranges - r < kRangeRing ? n_ranges - r : kRangeRing);
+          s = from_cuda(query_ranges_launch(g->cu_q, g->seq_lens, g->B, g->T, (int)t0, (int)p.rows, n, range_geom,
+                                            stride, st));
+          if (s != DSA_OK) return s;
+        }
         dsa_geom_t sub = *g;
         sub.T = t1 - (int)t0;
-        sub.cu_q = range_geom;
-        sub.seq_lens = range_geom + g->B + 1;
-        s = select_range(a, &sub, t0, p, scores, idx_buf + (size_t)t0 * a->topk, ptr, err, st);
+        sub.cu_q = range_geom + (size_t)slot * stride;
+        sub.seq_lens = sub.cu_q + g->B + 1;
+        s = select_range(a, &sub, t0, p, scores, idx_buf + (size_t)t0 * a->topk, ptr, err, slot != 0, st);
         if (s != DSA_OK) return s;
       }
     }

@@ -482,8 +482,13 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, Ind
 // of its queries inside the range, and its length becomes the last such query's
 // position + 1, so every kept query keeps its position (L - n + j) and the keys it
 // can see; a request with no query in the range gets none and length 0.
-__global__ void query_range_kernel(const int* __restrict__ cu_q, const int* __restrict__ seq_lens, int B, int t0,
-                                   int t1, int* __restrict__ cu_out, int* __restrict__ len_out) {
+__global__ void query_ranges_kernel(const int* __restrict__ cu_q, const int* __restrict__ seq_lens, int B, int T,
+                                    int t_first, int rows, int* __restrict__ out, int stride) {
+  // block j: the range of queries [t_first + j*rows, +rows) into out + j*stride (cu_q
+  // of the range, then its lengths)
+  const int t0 = t_first + blockIdx.x * rows, t1 = min(t0 + rows, T);
+  int* cu_out = out + (int64_t)blockIdx.x * stride;
+  int* len_out = cu_out + B + 1;
   for (int b = threadIdx.x; b <= B; b += blockDim.x) {
     const int q0 = cu_q[b];
     cu_out[b] = min(max(q0, t0), t1) - t0;
@@ -495,22 +500,30 @@ __global__ void query_range_kernel(const int* __restrict__ cu_q, const int* __re
   }
 }
 
-cudaError_t query_range_launch(const int* cu_q, const int* seq_lens, int B, int t0, int t1, int* cu_out,
-                               int* len_out, cudaStream_t st) {
-  query_range_kernel<<<1, 1024, 0, st>>>(cu_q, seq_lens, B, t0, t1, cu_out, len_out);
+cudaError_t query_ranges_launch(const int* cu_q, const int* seq_lens, int B, int T, int t_first, int rows, int n,
+                                int* out, int stride, cudaStream_t st) {
+  query_ranges_kernel<<<n, 1024, 0, st>>>(cu_q, seq_lens, B, T, t_first, rows, out, stride);
   return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ host side
 template <bool kFp8, int kHp, int kQG>
 static cudaError_t launch_indexer_t(const CUtensorMap& mk, const CUtensorMap& mq, const IndexerArgs& A,
-                                    int grid, cudaStream_t st) {
+                                    int grid, bool pdl, cudaStream_t st) {
   using C = IndexerCfg<kFp8, kHp, kQG>;
   auto kern = indexer_kernel<kFp8, kHp, kQG>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  kern<<<grid * C::kCtasPerSm, C::kThreads, C::kSmemBytes, st>>>(mk, mq, A);
-  return cudaGetLastError();
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid * C::kCtasPerSm, 1, 1);
+  cfg.blockDim = dim3(C::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = st;
+  cfg.attrs = at; cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, mk, mq, A);
 }
 
 int indexer_max_requests() { return IndexerCfg<true, 64, 1>::kMaxB; }
@@ -520,14 +533,14 @@ int indexer_q_box_rows(int Hi, bool multi_query) {
 }
 
 cudaError_t indexer_launch(bool fp8, int Hi, bool multi_query, const CUtensorMap& mk, const CUtensorMap& mq,
-                           const IndexerArgs& A, int grid, cudaStream_t st) {
+                           const IndexerArgs& A, int grid, bool pdl, cudaStream_t st) {
   const bool small = Hi <= 16;
   if (fp8) {
-    if (small) return multi_query ? launch_indexer_t<true, 16, 4>(mk, mq, A, grid, st) : launch_indexer_t<true, 16, 1>(mk, mq, A, grid, st);
-    return multi_query ? launch_indexer_t<true, 64, 4>(mk, mq, A, grid, st) : launch_indexer_t<true, 64, 1>(mk, mq, A, grid, st);
+    if (small) return multi_query ? launch_indexer_t<true, 16, 4>(mk, mq, A, grid, pdl, st) : launch_indexer_t<true, 16, 1>(mk, mq, A, grid, pdl, st);
+    return multi_query ? launch_indexer_t<true, 64, 4>(mk, mq, A, grid, pdl, st) : launch_indexer_t<true, 64, 1>(mk, mq, A, grid, pdl, st);
   }
-  if (small) return multi_query ? launch_indexer_t<false, 16, 4>(mk, mq, A, grid, st) : launch_indexer_t<false, 16, 1>(mk, mq, A, grid, st);
-  return multi_query ? launch_indexer_t<false, 64, 4>(mk, mq, A, grid, st) : launch_indexer_t<false, 64, 1>(mk, mq, A, grid, st);
+  if (small) return multi_query ? launch_indexer_t<false, 16, 4>(mk, mq, A, grid, pdl, st) : launch_indexer_t<false, 16, 1>(mk, mq, A, grid, pdl, st);
+  return multi_query ? launch_indexer_t<false, 64, 4>(mk, mq, A, grid, pdl, st) : launch_indexer_t<false, 64, 1>(mk, mq, A, grid, pdl, st);
 }
 
 }  // namespace dsa

@@ -26,8 +26,10 @@ struct IndexerArgs {
 // Rows of the query tensor map's box: a whole group of 4 queries when several queries
 // share a unit and Hi fills the padded head count (16 or 64), else one query's Hi rows.
 int indexer_q_box_rows(int Hi, bool multi_query);
+// pdl: launched with programmatic stream serialization (the kernel reads only call
+// inputs before its grid-dependency wait; the scores are written after it).
 cudaError_t indexer_launch(bool fp8, int Hi, bool multi_query, const CUtensorMap& mk, const CUtensorMap& mq,
-                           const IndexerArgs& A, int grid, cudaStream_t st);
+                           const IndexerArgs& A, int grid, bool pdl, cudaStream_t st);
 int indexer_max_requests();   // requests per launch (a call with more loops over groups)
 
 // ---- radix top-k (topk.cu)
@@ -91,10 +93,11 @@ struct AppendArgs {
 };
 cudaError_t cache_append_launch(const AppendArgs& A, cudaStream_t st);
 
-// ---- query ranges (indexer.cu): cu_out [B+1] and len_out [B] describe queries
-// [t0, t1) of the geometry alone, with their positions unchanged.
-cudaError_t query_range_launch(const int* cu_q, const int* seq_lens, int B, int t0, int t1, int* cu_out,
-                               int* len_out, cudaStream_t st);
+// ---- query ranges (indexer.cu): for j < n, the range of queries [t_first + j*rows,
+// + rows) of the geometry alone, with their positions unchanged, as cu_q [B+1] then
+// seq_lens [B] at out + j*stride.
+cudaError_t query_ranges_launch(const int* cu_q, const int* seq_lens, int B, int T, int t_first, int rows, int n,
+                                int* out, int stride, cudaStream_t st);
 
 // ---- staging copy (stage_copy.cu): `bytes` from src to dst by the SMs; both are
 // device-visible addresses (device memory, or mapped page-locked host memory).
