@@ -21,7 +21,7 @@
 //
 // Rows longer than one CTA's capacity are cut into chunks of 16384 positions whose
 // exact top-k (with their keys) become candidate lists. Lists are then merged in
-// groups of floor(16384 / k), level after level, until one list remains: a group's
+// groups of min(4, floor(16384 / k)), level after level, until one list remains: a group's
 // lists are concatenated in chunk order, so its candidates stay in ascending
 // position and ties still go to the lower position. Any element of the row's top-k
 // is in the top-k of every group that contains it, so every level is exact.
@@ -368,7 +368,10 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkLaunch 
 int topk_chunk_len() { return kTopkCapacity; }
 
 // Lists merged per group: as many whole lists of k as one CTA holds.
-int topk_fan_in(int k) { return kTopkCapacity / k; }
+// Lists merged per group: at most four (a merge CTA of 4 x 2048 candidates is much
+// quicker than one of 8 x 2048, and a level more costs less than that on these rows),
+// and at most what one CTA holds.
+int topk_fan_in(int k) { return kTopkCapacity / k < 4 ? kTopkCapacity / k : 4; }
 
 // Merge levels after the chunk pass for rows of up to max_seq_len (0: no chunking).
 int topk_merge_levels(int max_seq_len, int k) {

@@ -116,7 +116,7 @@ size_t dsa_indexer_scores_workspace_size(const dsa_geom_t* geom);
  *     followed by -1 up to k. -0.0 and +0.0 compare equal. Scores must not be NaN.
  *   1 <= k <= 16384. Rows of up to 16384 positions are selected in one pass; longer
  *     rows are cut into 16384-position chunks whose top-k lists (keys and positions, in
- *     the workspace) are merged floor(16384/k) at a time, level after level, so any
+ *     the workspace) are merged min(4, floor(16384/k)) at a time, level after level, so any
  *     max_seq_len works when k <= 8192; k > 8192 with max_seq_len > 16384 returns
  *     DSA_ERR_UNSUPPORTED.
  */
