@@ -385,6 +385,7 @@ def main():
     prep = measure_indexer_prep(dw, flush, stream, max(20, min(args.steps, 100)))
     idx_prefill = measure_indexer_prefill(flush, stream, max(10, min(args.steps, 30)), dev)
     bounded = measure_bounded_step(dw, flush, stream, max(20, min(args.steps, 100)))
+    hist_steps = measure_hist_steps(flush, stream, max(10, min(args.steps, 30)), dev)
     configs = {} if args.no_configs else {
         c: measure_config(c, flush, stream, max(10, min(args.steps, 30)), dev) for c in ("tiny", "mtp", "prefill", "longctx")}
 
@@ -414,7 +415,7 @@ def main():
                      "traffic": load_traffic("sparse_mla_kernel")},
         "components_ms": comp,
         "next_rows": {"cache_append": append, "int8_latent_attend": int8_attend, "indexer_prep": prep,
-                      "bounded_scoring": bounded},
+                      "bounded_scoring": bounded, "indexer_histogram": hist_steps},
         "e4m3_latent_attend": fp8_attend,
         "configs": configs,
         "indexer_prefill": idx_prefill,
@@ -819,6 +820,45 @@ def measure_config(name, flush, stream, n, device, oracle_budget_s=3.0):
                      "sample": f"the first {nq} queries of the workload, repeated for >= {oracle_budget_s:.0f} s"}
     del dw
     torch.cuda.empty_cache()
+    return out
+
+
+def measure_hist_steps(flush, stream, n, device, names=("decode", "prefill")):
+    """The step through dsa_decode_step_hist (the top-k's first radix digit counted by
+    the indexer) on the decode and chunked-prefill workloads, captured and replayed like
+    the headline step (median of n), with the number of segments whose histogram the
+    top-k rejected (0: every selection used the indexer's counts)."""
+    out = {}
+    for name in names:
+        wl = inputs.make_config(name)
+        dw = runner.DeviceWorkload(wl, device, hist=True)
+        for _ in range(3):
+            dw.step()
+        torch.cuda.synchronize()
+        if dw.check_error() != 0:
+            raise SystemExit(f"device error in the {name} step with histograms")
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            dw.step()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            dw.step()
+        ms = []
+        for i in range(n):
+            flush.fill_(i & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            e1.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        out[name] = {"ms": statistics.median(ms), "rejected_segments": int(dw.ws[:8].view(torch.int32)[1])}
+        del dw, g
+        torch.cuda.empty_cache()
+    out["entry_point"] = "dsa_decode_step_hist (opt-in; dsa_decode_step, timed above, counts the digit in the top-k)"
     return out
 
 

@@ -24,6 +24,7 @@ EXPORTED = (
     "dsa_sparse_mla_attend", "dsa_sparse_mla_attend_workspace_size", "dsa_sparse_mla_attend_static",
     "dsa_decode_step", "dsa_decode_step_workspace_size",
     "dsa_decode_step_bounded", "dsa_decode_step_bounded_workspace_size", "dsa_decode_step_wait_q",
+    "dsa_decode_step_hist", "dsa_decode_step_hist_workspace_size",
     "dsa_cache_append", "dsa_cache_append_workspace_size",
     "dsa_indexer_prepare", "dsa_indexer_prepare_workspace_size", "dsa_stage_copy",
     "dsa_get_error", "dsa_clear_error", "dsa_wait_probe", "dsa_status_string", "dsa_last_error", "dsa_abi_version",
@@ -85,6 +86,8 @@ def load(path: str = LIB_PATH):
         "dsa_decode_step_workspace_size": (SZ, [S]),
         "dsa_decode_step_bounded": (C.c_int, [S, SZ, P, SZ, P]),
         "dsa_decode_step_wait_q": (C.c_int, [S, P, P, SZ, P]),
+        "dsa_decode_step_hist": (C.c_int, [S, P, SZ, P]),
+        "dsa_decode_step_hist_workspace_size": (SZ, [S]),
         "dsa_decode_step_bounded_workspace_size": (SZ, [S, SZ]),
         "dsa_cache_append": (C.c_int, [G, C.c_int, P, P, C.c_int, P, P, P, P, SZ, P]),
         "dsa_cache_append_workspace_size": (SZ, [G]),
@@ -275,6 +278,16 @@ def dsa_decode_step_workspace_size(args: dsa_step_args_t) -> int:
 def dsa_decode_step(args: dsa_step_args_t, ws: torch.Tensor, stream=None):
     st = load().dsa_decode_step(C.byref(args), _dptr(ws), ws.numel(), _stream(stream))
     _check(st, "dsa_decode_step")
+
+
+def dsa_decode_step_hist_workspace_size(args: dsa_step_args_t) -> int:
+    return int(load().dsa_decode_step_hist_workspace_size(C.byref(args)))
+
+
+def dsa_decode_step_hist(args: dsa_step_args_t, ws: torch.Tensor, stream=None):
+    """dsa_decode_step with the top-k's first radix digit counted by the indexer."""
+    st = load().dsa_decode_step_hist(C.byref(args), _dptr(ws), ws.numel(), _stream(stream))
+    _check(st, "dsa_decode_step_hist")
 
 
 def dsa_stage_copy(dst, src, nbytes: int, stream=None):

@@ -190,7 +190,8 @@ dsa_status_t check_indexer(const dsa_geom_t* g, dsa_dtype_t dt, int Hi, const vo
 // launch each (query rows stay absolute: each group's cu_q entries index them).
 dsa_status_t run_indexer(const dsa_geom_t* g, dsa_dtype_t dt, int Hi, const void* q_idx, const float* q_scale,
                          const float* w, const void* kc, const float* ks, float* scores, int64_t stride, int* err,
-                         cudaStream_t st, int key_begin = 0, int key_end = INT32_MAX, bool pdl = false) {
+                         cudaStream_t st, int key_begin = 0, int key_end = INT32_MAX, bool pdl = false,
+                         int* hist = nullptr) {
   const bool fp8 = dt == DSA_E4M3;
   CUtensorMap mk, mq;
   const CUtensorMapDataType tdt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -205,6 +206,7 @@ dsa_status_t run_indexer(const dsa_geom_t* g, dsa_dtype_t dt, int Hi, const void
   A.q_group_box = q_box != Hi;
   A.Hi = Hi; A.q_scale = q_scale; A.w = w; A.k_scale = ks; A.scores = scores; A.stride = stride;
   A.key_begin = key_begin; A.key_end = key_end;
+  A.hist = hist; A.hist_chunks = topk_row_chunks(g->max_seq_len);
   A.err = err;
   const int group = indexer_max_requests();
   for (int b0 = 0; b0 < g->B; b0 += group) {
@@ -362,10 +364,16 @@ size_t range_ring_bytes(const dsa_geom_t* g, int64_t rows) {
   return align_up((size_t)(n < kRangeRing ? n : kRangeRing) * range_stride(g) * sizeof(int32_t), 256);
 }
 
+// Whole rows at once, when asked for: the indexer also counts the top-k's first-digit
+// histograms.
+bool plan_hist(const dsa_geom_t* g, const ScorePlan& p, bool hist) { return hist && p.rows >= g->T && p.span == 0; }
+
 // Workspace of the step under a score plan. Layout: header | query-range geometry
 // (ranges only) | scores [rows, width] | idx [T, k] (unless idx_out) | attention /
-// top-k scratch.
-size_t step_workspace_bytes(const dsa_step_args_t* a, const ScorePlan& p) {
+// top-k scratch | first-digit histograms (whole rows only). The histograms come last:
+// the top-k leaves them zero for the next step, and a shared layer's step on the same
+// workspace (header | scratch) stays clear of them.
+size_t step_workspace_bytes(const dsa_step_args_t* a, const ScorePlan& p, bool hist = false) {
   const dsa_geom_t* g = &a->geom;
   size_t bytes = kHeaderBytes;
   const int64_t r = p.rows < g->T ? p.rows : g->T;
@@ -379,7 +387,9 @@ size_t step_workspace_bytes(const dsa_step_args_t* a, const ScorePlan& p) {
     const size_t tk = topk_workspace_bytes((int)r, g->max_seq_len, a->topk);
     if (tk > scratch) scratch = tk;
   }
-  return bytes + align_up(scratch, 256);
+  bytes += align_up(scratch, 256);
+  if (!a->reuse_idx && plan_hist(g, p, hist)) bytes += align_up(topk_hist_bytes(g->T, g->max_seq_len), 256);
+  return bytes;
 }
 
 // Scores and selects one range of queries (geometry `sub`, whose rows are the step's
@@ -387,8 +397,10 @@ size_t step_workspace_bytes(const dsa_step_args_t* a, const ScorePlan& p) {
 // span's chunks reduced to candidate lists before the next span is scored.
 // pdl_first: the range's first indexer launch may start before the kernel just before
 // it ends (that kernel is our own and the range's geometry is already written).
+// hist: first-digit histograms for whole rows (p.span == 0), or null.
 dsa_status_t select_range(const dsa_step_args_t* a, const dsa_geom_t* sub, int64_t t0, const ScorePlan& p,
-                          float* scores, int32_t* idx_out, void* scratch, int* err, bool pdl_first, cudaStream_t st) {
+                          float* scores, int32_t* idx_out, void* scratch, int* err, bool pdl_first, cudaStream_t st,
+                          int* hist = nullptr) {
   const dsa_geom_t* g = &a->geom;
   const size_t qrow = (size_t)a->Hi * 128 * (a->qk_dtype == DSA_E4M3 ? 1 : 2);
   const uint8_t* q_idx = reinterpret_cast<const uint8_t*>(a->q_idx) + (size_t)t0 * qrow;
@@ -398,11 +410,11 @@ dsa_status_t select_range(const dsa_step_args_t* a, const dsa_geom_t* sub, int64
   if (p.span == 0) {
     const int64_t stride = step_score_stride(g);
     s = run_indexer(sub, a->qk_dtype, a->Hi, q_idx, q_scale, w, a->idx_k_cache, a->idx_k_scale, scores, stride, err, st,
-                    0, INT32_MAX, pdl_first);
+                    0, INT32_MAX, pdl_first, hist);
     if (s != DSA_OK) return s;
     // The top-k kernels follow this call's own kernels, so they may launch early
     // (programmatic dependent launch) and wait for their inputs inside.
-    return from_cuda(topk_launch(to_dev(sub), scores, stride, a->topk, idx_out, scratch, err, true, st));
+    return from_cuda(topk_launch(to_dev(sub), scores, stride, a->topk, idx_out, scratch, err, true, st, hist));
   }
   const int chunk = topk_chunk_len();
   const int nch = (g->max_seq_len + chunk - 1) / chunk;
@@ -425,7 +437,7 @@ dsa_status_t select_range(const dsa_step_args_t* a, const dsa_geom_t* sub, int64
 // query does not depend on the others', and a span's chunk lists are those the whole
 // row gives, so the result is the same for every plan).
 dsa_status_t run_step(const dsa_step_args_t* a, const ScorePlan& p, void* ws, size_t ws_bytes, void* stream,
-                      cudaEvent_t q_ready = nullptr) {
+                      cudaEvent_t q_ready = nullptr, bool hist = false) {
   const dsa_geom_t* g = &a->geom;
   dsa_status_t s;
   if (!a->reuse_idx) {
@@ -438,7 +450,7 @@ dsa_status_t run_step(const dsa_step_args_t* a, const ScorePlan& p, void* ws, si
   s = check_attend(g, a->kv_dtype, a->H, a->q, a->kv_cache, a->reuse_idx ? a->reuse_idx : reinterpret_cast<const int*>(ws),
                    a->topk, a->sm_scale, a->out);
   if (s != DSA_OK) return s;
-  if (!ws || ws_bytes < step_workspace_bytes(a, p) || (reinterpret_cast<uintptr_t>(ws) & 255u))
+  if (!ws || ws_bytes < step_workspace_bytes(a, p, hist) || (reinterpret_cast<uintptr_t>(ws) & 255u))
     return DSA_ERR_WORKSPACE;
   if (g->T == 0) return DSA_OK;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -462,7 +474,11 @@ dsa_status_t run_step(const dsa_step_args_t* a, const ScorePlan& p, void* ws, si
       ptr += align_up((size_t)g->T * a->topk * sizeof(int32_t), 256);
     }
     if (!ranges) {
-      s = select_range(a, g, 0, p, scores, idx_buf, ptr, err, false, st);
+      int* hist_buf = nullptr;
+      if (plan_hist(g, p, hist) && indexer_counts_hist(a->qk_dtype == DSA_E4M3, a->Hi, g->T > g->B))
+        hist_buf = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(ws) + step_workspace_bytes(a, p, true) -
+                                          align_up(topk_hist_bytes(g->T, g->max_seq_len), 256));
+      s = select_range(a, g, 0, p, scores, idx_buf, ptr, err, false, st, hist_buf);
       if (s != DSA_OK) return s;
     } else {
       // Bounded scoring: queries [t0, t0 + rows) at a time, each range described by
@@ -521,6 +537,16 @@ dsa_status_t dsa_decode_step(const dsa_step_args_t* a, void* ws, size_t ws_bytes
 dsa_status_t dsa_decode_step_wait_q(const dsa_step_args_t* a, void* q_ready, void* ws, size_t ws_bytes, void* stream) {
   if (!a) return DSA_ERR_INVALID_ARG;
   return run_step(a, whole_rows(a), ws, ws_bytes, stream, reinterpret_cast<cudaEvent_t>(q_ready));
+}
+
+size_t dsa_decode_step_hist_workspace_size(const dsa_step_args_t* a) {
+  if (!a) return kHeaderBytes;
+  return step_workspace_bytes(a, whole_rows(a), true);
+}
+
+dsa_status_t dsa_decode_step_hist(const dsa_step_args_t* a, void* ws, size_t ws_bytes, void* stream) {
+  if (!a) return DSA_ERR_INVALID_ARG;
+  return run_step(a, whole_rows(a), ws, ws_bytes, stream, nullptr, true);
 }
 
 // The score plan a budget allows: as many whole rows as fit; below one row, one query

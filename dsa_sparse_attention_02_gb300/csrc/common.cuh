@@ -19,6 +19,23 @@ constexpr int kRecPageBytes = kPage * kFp8Record;                   // 41984
 constexpr int kRecScalesAt = kPage * kDimLatent;                    // 32768
 constexpr int kRecRopeAt = kRecScalesAt + kPage * 16;               // 33792
 
+// Radix keys of the top-k: a 32-bit key whose unsigned order is the order of the
+// fp32 scores (-0 folded onto +0). The top-k's first digit is the key's top 11 bits;
+// the fused step's indexer counts them per row and per 16384-position chunk
+// (first-digit histograms of kHistBins ints), which the top-k then reads instead of
+// counting them itself.
+__device__ __forceinline__ uint32_t orderable_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;  // -0 == +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+constexpr int kHistBins = 2048;
+constexpr int kHistShift = 21;          // bin = key >> 21
+constexpr int kTopkChunkLog2 = 14;      // top-k chunks of 16384 positions
+// Word of the workspace header (after the error word) that counts the segments whose
+// first-digit histogram the top-k rejected.
+constexpr int kHistRejectedWord = 1;
+
 struct GeomDev {
   int B, T, max_seq_len, num_pages, bt_stride;
   const int* seq_lens;

@@ -13,7 +13,10 @@
 // bf16: kind::f16, 8 MMAs of K=16). The fp32 accumulator sits in TMEM, one lane
 // per key; the epilogue thread of that lane applies ReLU, the per-head weight and
 // the head sum within its own registers, multiplies the key's scale and writes
-// one score per query, -inf past the query's causal position.
+// one score per query, -inf past the query's causal position. The histogram variant
+// (dsa_decode_step_hist) also counts the top 11 bits of each visible score's radix key
+// per query and 16384-position chunk: the first pass of the radix top-k (lmdeploy
+// "feat: support GLM-5.2", Changes) moved into the epilogue that makes the scores.
 //
 // Roles: warp P decodes 32 units at a time (one per lane) and, per unit, loads
 // only what changed since the previous unit: a new key tile (two pages by TMA,
@@ -75,6 +78,13 @@ struct IndexerCfg {
                                    : (kAccs * kN) <= 256 ? 256 : 512;
   static constexpr int kMaxB = 1024;                           // requests per call
   static constexpr int kSmemBytes = 1024 + kQSlots * kQSlotBytes + kKStages * kKStageBytes;
+  // First-digit histograms (16-bit counts, two bins per word), in dynamic shared memory
+  // after the key stages when a launch asks for them: e4m3 keys only (the bf16
+  // query-group variants have no room beside their operands; for bf16 keys the fused
+  // step lets the top-k count the digit).
+  static constexpr bool kHist = kFp8;
+  static constexpr int kHistWords = kQG * kHistBins / 2;
+  static constexpr int kHistBytes = kHist ? 4 * kHistWords + 16 : 0;   // + the two flush barriers
   static constexpr int kKSteps = kFp8 ? 4 : 8;
   static_assert(kN <= 256 && kN % 16 == 0, "MMA N");
   static_assert(kKStages >= 2, "key stages");
@@ -123,7 +133,35 @@ __device__ __forceinline__ UnitInfo decode_unit(const int* prefix, const int* cu
   return ui;
 }
 
-template <bool kFp8, int kHp, int kQG>
+// Adds the shared first-digit histograms of queries hq .. hq+hn-1 (chunk hc) into the
+// global ones and clears them; every epilogue warp calls it at the same point of the
+// unit sequence (the barriers' phase hph), each taking its share of the words.
+template <int kEpiWarps>
+__device__ __noinline__ bool hist_flush(uint32_t* hist_s, int hq, int hc, int hn, uint32_t& hph, uint32_t full,
+                                        uint32_t empty, const IndexerArgs& A, volatile int* abort_flag) {
+  const int lane = threadIdx.x & 31;
+  __syncwarp();
+  if (lane == 0) mbar_arrive(full);          // this warp's counts are in
+  if (!mbar_wait(full, hph & 1, abort_flag, A.err)) return false;
+  for (int i = threadIdx.x; i < hn * (kHistBins / 2); i += 32 * kEpiWarps) {
+    const uint32_t v = hist_s[i];
+    if (v != 0u) {
+      const int j = i / (kHistBins / 2), bin = 2 * (i % (kHistBins / 2));
+      int* dst = A.hist + ((int64_t)(hq + j) * A.hist_chunks + hc) * kHistBins + bin;
+      if (v & 0xffffu) atomicAdd(dst, (int)(v & 0xffffu));
+      if (v >> 16) atomicAdd(dst + 1, (int)(v >> 16));
+      hist_s[i] = 0u;
+    }
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(empty);         // this warp's share is cleared
+  if (!mbar_wait(empty, hph & 1, abort_flag, A.err)) return false;
+  ++hph;
+  return true;
+}
+
+// kHistT: the variant that also counts first-digit histograms (A.hist set).
+template <bool kFp8, int kHp, int kQG, bool kHistT>
 __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, IndexerCfg<kFp8, kHp, kQG>::kBoundCtas)
     indexer_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_q,
                    const IndexerArgs A) {
@@ -142,6 +180,13 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, Ind
   __shared__ UnitDesc descs[C::kDescs];
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
+  // First-digit histograms of the query group being scored (A.hist set: the launch's
+  // dynamic shared memory holds them after the key stages): 16-bit counts, two bins per
+  // word (a group's count in one bin and chunk is at most 16384), added to the global
+  // histograms when the group or the 16384-position chunk changes and at the end, the
+  // epilogue warps meeting on two barriers after them around it.
+  uint32_t* hist_s = reinterpret_cast<uint32_t*>(k_stages + C::kKStages * C::kKStageBytes);
+  uint64_t* hist_bars = reinterpret_cast<uint64_t*>(hist_s + C::kHistWords);   // full, empty
   __shared__ int prefix[C::kMaxB + 1], cuq_s[C::kMaxB + 1], lens_s[C::kMaxB];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -193,8 +238,14 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, Ind
     for (int s = 0; s < C::kQSlots; ++s) { mbar_init(smem_u32(&q_full[s]), 1); mbar_init(smem_u32(&q_empty[s]), 1 + C::kEpiWarps); }
     for (int s = 0; s < C::kDescs; ++s) { mbar_init(smem_u32(&desc_full[s]), 1); mbar_init(smem_u32(&desc_empty[s]), 1 + C::kEpiWarps); }
     for (int a = 0; a < C::kAccs; ++a) { mbar_init(smem_u32(&tfull_bar[a]), 1); mbar_init(smem_u32(&tempty_bar[a]), C::kEpiWarps); }
+    if constexpr (kHistT) {
+      mbar_init(smem_u32(&hist_bars[0]), C::kEpiWarps);
+      mbar_init(smem_u32(&hist_bars[1]), C::kEpiWarps);
+    }
     fence_mbar_init();
   }
+  if constexpr (kHistT)
+    for (int i = tid; i < C::kHistWords; i += C::kThreads) hist_s[i] = 0u;
   // Query rows beyond Hi and w / q_scale entries beyond Hi stay zero for the whole
   // kernel (TMA and the bulk copies write only the first Hi of them).
   for (int i = tid; i < C::kQSlots * C::kQSlotBytes / 16; i += C::kThreads)
@@ -385,12 +436,24 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, Ind
     float ks = 1.f;
     float wq[kWqRegs ? kHp : 1];
     const float* wqw = &wq_s[kWqRegs ? 0 : warp][0];
+    // the shared histograms count queries hq .. hq+hn-1 in chunk hc (hq < 0: none yet)
+    int hq = -1, hc = 0, hn = 0;
+    uint32_t hph = 0;
     for (int u = u_begin, i = 0; u < u_end; ++u, ++i) {
       const int r = i % C::kDescs;
       if (!mbar_wait(smem_u32(&desc_full[r]), (i / C::kDescs) & 1, &abort_flag, A.err)) break;
       const UnitDesc d = descs[r];
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&desc_empty[r]));
+      if constexpr (kHistT) {
+        const int chunk = d.tile >> (kTopkChunkLog2 - 7);   // 128-key tiles
+        if (d.q_start != hq || chunk != hc) {
+          if (hq >= 0 && !hist_flush<C::kEpiWarps>(hist_s, hq, hc, hn, hph, smem_u32(&hist_bars[0]),
+                                                   smem_u32(&hist_bars[1]), A, &abort_flag))
+            break;
+          hq = d.q_start; hc = chunk; hn = d.q_count;
+        }
+      }
       const int page = (key < 64) ? d.page0 : d.page1;
       if (d.flags & kNewKey) {
         cur_k = d.kstage;
@@ -461,12 +524,22 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, Ind
           const int pos = d.pos0 + j;
           const float out = (sidx <= pos && page >= 0) ? sum * ks : neg_inf;
           A.scores[(int64_t)t * A.stride + (sidx - A.key_begin)] = out;
+          if constexpr (kHistT) {
+            if (sidx <= pos) {
+              // first-digit histogram of the positions the top-k selects from (0..pos)
+              const uint32_t bin = orderable_key(out) >> kHistShift;
+              atomicAdd(&hist_s[j * (kHistBins / 2) + (bin >> 1)], 1u << ((bin & 1u) << 4));
+            }
+          }
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[acc]));
     }
+    if constexpr (kHistT)
+      if (hq >= 0) hist_flush<C::kEpiWarps>(hist_s, hq, hc, hn, hph, smem_u32(&hist_bars[0]), smem_u32(&hist_bars[1]),
+                                            A, &abort_flag);
   }
 
   tc_fence_before();
@@ -507,12 +580,19 @@ cudaError_t query_ranges_launch(const int* cu_q, const int* seq_lens, int B, int
 }
 
 // ------------------------------------------------------------------ host side
-template <bool kFp8, int kHp, int kQG>
+template <bool kFp8, int kHp, int kQG, bool kHistT = false>
 static cudaError_t launch_indexer_t(const CUtensorMap& mk, const CUtensorMap& mq, const IndexerArgs& A,
                                     int grid, bool pdl, cudaStream_t st) {
   using C = IndexerCfg<kFp8, kHp, kQG>;
-  auto kern = indexer_kernel<kFp8, kHp, kQG>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if constexpr (!kHistT) {
+    if (A.hist != nullptr) {
+      if constexpr (C::kHist) return launch_indexer_t<kFp8, kHp, kQG, true>(mk, mq, A, grid, pdl, st);
+      return cudaErrorInvalidValue;   // indexer_counts_hist() said no
+    }
+  }
+  auto kern = indexer_kernel<kFp8, kHp, kQG, kHistT>;
+  const int smem = C::kSmemBytes + (kHistT ? C::kHistBytes : 0);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -520,13 +600,15 @@ static cudaError_t launch_indexer_t(const CUtensorMap& mk, const CUtensorMap& mq
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid * C::kCtasPerSm, 1, 1);
   cfg.blockDim = dim3(C::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = at; cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, mk, mq, A);
 }
 
 int indexer_max_requests() { return IndexerCfg<true, 64, 1>::kMaxB; }
+
+bool indexer_counts_hist(bool fp8, int, bool) { return fp8 && IndexerCfg<true, 64, 4>::kHist; }
 
 int indexer_q_box_rows(int Hi, bool multi_query) {
   return multi_query && (Hi == 16 || Hi == 64) ? 4 * Hi : Hi;

@@ -21,6 +21,8 @@ struct IndexerArgs {
   int key_begin;        // keys [key_begin, key_end) are scored; key_begin a multiple of 128
   int key_end;          // a multiple of 128, or past every request's length
   bool q_group_box;     // map_q's box is a whole query group (indexer_q_box_rows): one copy per group
+  int* hist;            // or null: first-digit histograms [T][hist_chunks][kHistBins] of the visible
+  int hist_chunks;      //   scores, added to (the top-k reads them and leaves them zero); key_begin 0
   int* err;
 };
 // Rows of the query tensor map's box: a whole group of 4 queries when several queries
@@ -31,6 +33,9 @@ int indexer_q_box_rows(int Hi, bool multi_query);
 cudaError_t indexer_launch(bool fp8, int Hi, bool multi_query, const CUtensorMap& mk, const CUtensorMap& mq,
                            const IndexerArgs& A, int grid, bool pdl, cudaStream_t st);
 int indexer_max_requests();   // requests per launch (a call with more loops over groups)
+// Whether the indexer variant for these keys and heads counts first-digit histograms
+// (IndexerArgs::hist); where it does not, the top-k must count the digit itself.
+bool indexer_counts_hist(bool fp8, int Hi, bool multi_query);
 
 // ---- radix top-k (topk.cu)
 // Rows longer than topk_chunk_len() are cut into chunks of that length whose top-k
@@ -43,13 +48,20 @@ size_t topk_workspace_bytes(int T, int max_seq_len, int k);
 // pdl: the launch may overlap the tail of the kernel just before it on the stream
 // (programmatic dependent launch); set only when that kernel is one of this library's
 // and the geometry was complete before it started.
+// hist: null, or the first-digit histograms the indexer counted for these scores,
+// [T][chunks per row][kHistBins] ints (topk_hist_bytes); each CTA reads its row's (or
+// chunk's) and zeroes it. A histogram that does not match the scores (a workspace's
+// first use) is detected by the selection's exact final counts, and the row is then
+// selected without it.
 cudaError_t topk_launch(const GeomDev& g, const float* scores, int64_t stride, int k, int* idx,
-                        void* scratch, int* err, bool pdl, cudaStream_t st);
+                        void* scratch, int* err, bool pdl, cudaStream_t st, int* hist = nullptr);
+size_t topk_hist_bytes(int T, int max_seq_len);
+int topk_row_chunks(int max_seq_len);   // first-digit histograms per row (IndexerArgs::hist_chunks)
 // The two halves of topk_launch for rows scored a key span at a time: the chunk pass
 // over chunks c0 .. c0+nl-1 of every row (scores: row t's key c0 * chunk_len at
 // scores + t * stride), writing their lists into scratch; then the merge levels.
 cudaError_t topk_chunks_launch(const GeomDev& g, const float* scores, int64_t stride, int k, int c0, int nl,
-                               void* scratch, int* err, bool pdl, cudaStream_t st);
+                               void* scratch, int* err, bool pdl, cudaStream_t st, int* hist = nullptr);
 cudaError_t topk_merge_launch(const GeomDev& g, int k, int* idx, void* scratch, int* err, bool pdl, cudaStream_t st);
 
 // ---- sparse MLA + combine (sparse_mla.cu)

@@ -33,12 +33,8 @@ namespace dsa {
 constexpr int kTopkThreads = 1024;
 constexpr int kTopkItems = 16;
 constexpr int kTopkCapacity = kTopkThreads * kTopkItems;  // 16384
-
-__device__ __forceinline__ uint32_t orderable_key(float f) {
-  uint32_t u = __float_as_uint(f);
-  if (u == 0x80000000u) u = 0u;  // -0 == +0
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
+static_assert(kTopkCapacity == 1 << kTopkChunkLog2, "chunk length");
+static_assert(kHistBins == 2 * kTopkThreads, "two first-digit bins per thread");
 
 // Modes of one launch:
 //   kDirect: score rows (<= 16384 long) -> final idx
@@ -61,6 +57,8 @@ struct TopkLaunch {
   uint32_t* cand_key_out;        // kChunks, kMerge with n_out > 1
   int* cand_idx_out;
   int* idx_out;                  // kDirect, kMerge with n_out == 1: [T, k]
+  int* hist;                     // kDirect, kChunks: first-digit histograms [T][hist_chunks][2048], or null
+  int hist_chunks;
   int* err;
 };
 
@@ -128,10 +126,10 @@ __device__ __forceinline__ TopkBin topk_find_bin(TopkShared& S, const int* h, in
 // The selection proper over a segment of n (> k) entries spread as runs of CNT per
 // thread; entries whose valid bit is clear take no part. pos_s (merges): shared array
 // of n ints for the input candidates' positions. Writes min(k, valid entries) results
-// then -1 padding.
-template <int CNT, int MODE>
-__device__ __forceinline__ void topk_select(const TopkLaunch& L, int n, int64_t in_base, int64_t out_base,
-                                            int idx_offset, TopkShared& S, int* pos_s) {
+// then -1 padding. kSeeded: hrow holds the segment's first-digit histogram (below).
+template <int CNT, int MODE, bool kSeeded>
+__device__ __forceinline__ bool topk_select(const TopkLaunch& L, int n, int64_t in_base, int64_t out_base,
+                                            int idx_offset, TopkShared& S, int* pos_s, const int* hrow) {
   const int tid = threadIdx.x;
   const int k = L.k;
   const int e0 = tid * CNT;
@@ -185,81 +183,107 @@ __device__ __forceinline__ void topk_select(const TopkLaunch& L, int n, int64_t 
     }
   }
 
-  // ---- the leading bits every valid key shares, and the number of valid keys: the
-  // radix digits start below the shared bits (scores in a narrow range, such as the
-  // top candidates a merge level sees, would otherwise crowd a few bins of the first
-  // digit), and a segment with no more valid keys than k keeps them all. Every warp
-  // reduces the per-warp values itself after one barrier.
   const int lane = tid & 31, warp = tid >> 5;
+  int rem, count, incl, wincl, wv, packed;
+  uint32_t prefix, pmask, gt_bits, eq_bits;
+  // seeded: the first digit's histogram (the top 11 bits of every entry's key) comes
+  // from the indexer, read while the entries are still in flight, and the digits start
+  // at the top bit. The selection is then checked against its exact final counts; if
+  // they disagree (a histogram that does not belong to these scores) nothing is
+  // written and false is returned, for the caller to select again without it.
+  constexpr bool seeded = MODE != kMerge && kSeeded;
   {
-    uint32_t a = 0xFFFFFFFFu, o = 0u;
-#pragma unroll
-    for (int i = 0; i < CNT; ++i)
-      if ((valid >> i) & 1u) { a &= key[i]; o |= key[i]; }
-    a = __reduce_and_sync(0xffffffffu, a);
-    o = __reduce_or_sync(0xffffffffu, o);
-    const int c = (int)__reduce_add_sync(0xffffffffu, (uint32_t)__popc(valid));
-    if (lane == 0) { S.wand[warp] = a; S.wor[warp] = o; S.wcnt[warp] = c; }
-  }
-  for (int j = tid; j < 2 * 2048; j += kTopkThreads) (&S.hist[0][0])[j] = 0;
-  __syncthreads();
-  const uint32_t common = __reduce_and_sync(0xffffffffu, S.wand[lane]);
-  const uint32_t any = __reduce_or_sync(0xffffffffu, S.wor[lane]);
-  const int nvalid = (int)__reduce_add_sync(0xffffffffu, (uint32_t)S.wcnt[lane]);
-
-  int rem, count;
-  uint32_t prefix = 0u, pmask = 0u;
-  if (nvalid <= k) {
-    // no more valid entries than k: every one of them is taken (prefix and mask 0)
-    rem = count = nvalid;
-  } else {
-    rem = count = k;
-    int consumed = (common == any) ? 32 : __clz(common ^ any);
-    pmask = consumed == 0 ? 0u : (0xFFFFFFFFu << (32 - consumed));
-    prefix = common & pmask;
-    bool done = consumed == 32;   // every valid key equal: the first k by position
-    // at most three digits (11 + 11 + 10 bits); the third reuses the first histogram,
-    // cleared while the second digit is resolved
-    for (int d = 0; d < 3 && !done; ++d) {
-      const int w = min(11, 32 - consumed), sh = 32 - consumed - w;
-      const uint32_t dmask = (1u << w) - 1u;
-      int* h = S.hist[d & 1];
+    int nvalid, consumed = 0;
+    prefix = 0u; pmask = 0u;
+    if constexpr (seeded) {
+      const int2 h2 = reinterpret_cast<const int2*>(hrow)[tid];
+      S.hist[0][2 * tid] = h2.x; S.hist[0][2 * tid + 1] = h2.y;
+      S.hist[1][2 * tid] = 0; S.hist[1][2 * tid + 1] = 0;
+      nvalid = n;   // every entry of a score segment is valid
+      // the first find_bin barrier publishes both arrays
+    } else {
+      // ---- the leading bits every valid key shares, and the number of valid keys:
+      // the radix digits start below the shared bits (scores in a narrow range, such
+      // as the top candidates a merge level sees, would otherwise crowd a few bins of
+      // the first digit), and a segment with no more valid keys than k keeps them
+      // all. Every warp reduces the per-warp values itself after one barrier.
+      uint32_t a = 0xFFFFFFFFu, o = 0u;
 #pragma unroll
       for (int i = 0; i < CNT; ++i)
-        if (((valid >> i) & 1u) && (key[i] & pmask) == prefix) atomicAdd(&h[(key[i] >> sh) & dmask], 1);
-      const TopkBin b = topk_find_bin(S, h, 1 << w, rem, (d == 1 && consumed + w < 32) ? S.hist[0] : nullptr);
-      rem -= b.above;
-      prefix |= (uint32_t)b.bin << sh;
-      pmask |= dmask << sh;
-      consumed += w;
-      done = b.cnt == rem || consumed == 32;
+        if ((valid >> i) & 1u) { a &= key[i]; o |= key[i]; }
+      a = __reduce_and_sync(0xffffffffu, a);
+      o = __reduce_or_sync(0xffffffffu, o);
+      const int c = (int)__reduce_add_sync(0xffffffffu, (uint32_t)__popc(valid));
+      if (lane == 0) { S.wand[warp] = a; S.wor[warp] = o; S.wcnt[warp] = c; }
+      for (int j = tid; j < 2 * kHistBins; j += kTopkThreads) (&S.hist[0][0])[j] = 0;
+      __syncthreads();
+      const uint32_t common = __reduce_and_sync(0xffffffffu, S.wand[lane]);
+      const uint32_t any = __reduce_or_sync(0xffffffffu, S.wor[lane]);
+      nvalid = (int)__reduce_add_sync(0xffffffffu, (uint32_t)S.wcnt[lane]);
+      consumed = (common == any) ? 32 : __clz(common ^ any);
+      pmask = consumed == 0 ? 0u : (0xFFFFFFFFu << (32 - consumed));
+      prefix = common & pmask;
     }
-  }
+    if (nvalid <= k) {
+      // no more valid entries than k: every one of them is taken (prefix and mask 0)
+      rem = count = nvalid;
+      prefix = 0u; pmask = 0u;
+    } else {
+      rem = count = k;
+      bool done = consumed == 32;   // every valid key equal: the first k by position
+      // at most three digits (11 + 11 + 10 bits); the third reuses the first histogram,
+      // cleared while the second digit is resolved
+      for (int d = 0; d < 3 && !done; ++d) {
+        const int w = min(11, 32 - consumed), sh = 32 - consumed - w;
+        const uint32_t dmask = (1u << w) - 1u;
+        int* h = S.hist[d & 1];
+        if (!(seeded && d == 0)) {
+#pragma unroll
+          for (int i = 0; i < CNT; ++i)
+            if (((valid >> i) & 1u) && (key[i] & pmask) == prefix) atomicAdd(&h[(key[i] >> sh) & dmask], 1);
+        }
+        const TopkBin b = topk_find_bin(S, h, 1 << w, rem, (d == 1 && consumed + w < 32) ? S.hist[0] : nullptr);
+        rem -= b.above;
+        prefix |= (uint32_t)b.bin << sh;
+        pmask |= dmask << sh;
+        consumed += w;
+        done = b.cnt == rem || consumed == 32;
+      }
+    }
 
-  // ---- ordered placement: one block scan of (above << 16 | equal) counts (each
-  // total <= 16384, so no carry); an element is taken if its masked key is above the
-  // prefix, or equal and among the first `rem` equal ones by position
-  uint32_t gt_bits = 0, eq_bits = 0;
+    // ---- ordered placement: one block scan of (above << 16 | equal) counts (each
+    // total <= 16384, so no carry); an element is taken if its masked key is above the
+    // prefix, or equal and among the first `rem` equal ones by position
+    gt_bits = 0; eq_bits = 0;
 #pragma unroll
-  for (int i = 0; i < CNT; ++i) {
-    const uint32_t m = key[i] & pmask;
-    if (((valid >> i) & 1u) && m > prefix) gt_bits |= 1u << i;
-    if (((valid >> i) & 1u) && m == prefix) eq_bits |= 1u << i;
-  }
-  const int packed = (__popc(gt_bits) << 16) | __popc(eq_bits);
-  int incl = packed;
+    for (int i = 0; i < CNT; ++i) {
+      const uint32_t m = key[i] & pmask;
+      if (((valid >> i) & 1u) && m > prefix) gt_bits |= 1u << i;
+      if (((valid >> i) & 1u) && m == prefix) eq_bits |= 1u << i;
+    }
+    packed = (__popc(gt_bits) << 16) | __popc(eq_bits);
+    incl = packed;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int u = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += u;
-  }
-  if (lane == 31) S.wscan[warp] = incl;
-  __syncthreads();
-  int wv = S.wscan[lane], wincl = wv;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    if (lane == 31) S.wscan[warp] = incl;
+    __syncthreads();
+    wv = S.wscan[lane];
+    wincl = wv;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int u = __shfl_up_sync(0xffffffffu, wincl, o);
-    if (lane >= o) wincl += u;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, wincl, o);
+      if (lane >= o) wincl += u;
+    }
+    if constexpr (seeded) {
+      // the selection is right exactly when it takes k entries and, unless the prefix
+      // covers all 32 bits, every entry equal to it under the mask
+      const int total = __shfl_sync(0xffffffffu, wincl, 31);
+      const int tg = total >> 16, te = total & 0xffff;
+      if (!(rem >= 0 && tg + min(rem, te) == k && (rem >= te || pmask == 0xFFFFFFFFu))) return false;
+    }
   }
   const int excl = __shfl_sync(0xffffffffu, wincl - wv, warp) + incl - packed;
   int rg = excl >> 16, re = excl & 0xffff;
@@ -283,18 +307,31 @@ __device__ __forceinline__ void topk_select(const TopkLaunch& L, int n, int64_t 
     if (lists) { L.cand_idx_out[out_base + j] = -1; L.cand_key_out[out_base + j] = 0u; }
     else L.idx_out[out_base + j] = -1;
   }
+  return true;
 }
 
-// Runs of 4, 8 or 16 entries per thread, whichever spreads the segment over the most threads.
-template <int MODE>
+// Runs of 4, 8 or 16 entries per thread, whichever spreads the segment over the most
+// threads; a seeded selection the final counts reject is done again unseeded.
+template <int MODE, int CNT, bool kSeeded>
+__device__ __forceinline__ void topk_select_seeded(const TopkLaunch& L, int n, int64_t in_base, int64_t out_base,
+                                                   int idx_offset, TopkShared& S, int* pos_s, const int* hrow) {
+  if (topk_select<CNT, MODE, kSeeded>(L, n, in_base, out_base, idx_offset, S, pos_s, hrow)) return;
+  if constexpr (kSeeded) {
+    if (threadIdx.x == 0 && L.err) atomicAdd(L.err + kHistRejectedWord, 1);
+    __syncthreads();   // every warp is done with the shared arrays of the first pass
+    topk_select<CNT, MODE, false>(L, n, in_base, out_base, idx_offset, S, pos_s, nullptr);
+  }
+}
+template <int MODE, bool kSeeded>
 __device__ __forceinline__ void topk_select_runs(const TopkLaunch& L, int n, int64_t in_base, int64_t out_base,
-                                                 int idx_offset, TopkShared& S, int* pos_s) {
-  if (n <= 4 * kTopkThreads) topk_select<4, MODE>(L, n, in_base, out_base, idx_offset, S, pos_s);
-  else if (n <= 8 * kTopkThreads) topk_select<8, MODE>(L, n, in_base, out_base, idx_offset, S, pos_s);
-  else topk_select<16, MODE>(L, n, in_base, out_base, idx_offset, S, pos_s);
+                                                 int idx_offset, TopkShared& S, int* pos_s, const int* hrow) {
+  if (n <= 4 * kTopkThreads) topk_select_seeded<MODE, 4, kSeeded>(L, n, in_base, out_base, idx_offset, S, pos_s, hrow);
+  else if (n <= 8 * kTopkThreads) topk_select_seeded<MODE, 8, kSeeded>(L, n, in_base, out_base, idx_offset, S, pos_s, hrow);
+  else topk_select_seeded<MODE, 16, kSeeded>(L, n, in_base, out_base, idx_offset, S, pos_s, hrow);
 }
 
-template <int MODE>
+// kSeeded (kDirect, kChunks): L.hist holds the indexer's first-digit histograms.
+template <int MODE, bool kSeeded>
 __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkLaunch L) {
   __shared__ TopkShared S;
   __shared__ int row_len_s, row_pos_s;
@@ -322,6 +359,9 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkLaunch 
   }
   griddep_launch_dependents();
   griddep_wait();   // scores (or candidates) come from the preceding kernel
+  // The indexer's first-digit histogram of this row (or chunk), if it counted one; it
+  // is zeroed for the next step once read, whatever path the row takes.
+  int* hrow = kSeeded ? L.hist + ((int64_t)t * L.hist_chunks + c) * kHistBins : nullptr;
   __syncthreads();
   const int n = row_len_s;
   const int k = L.k;
@@ -335,6 +375,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkLaunch 
                                                              : (int64_t)t * k;
   const int idx_offset = (MODE == kChunks) ? c * L.chunk : 0;
 
+  if (kSeeded && n <= k) reinterpret_cast<int2*>(hrow)[tid] = make_int2(0, 0);   // not read
   if (MODE == kMerge && L.n_out == 1 && row_pos_s + 1 <= k) {
     // every valid key is kept: positions 0..pos in order (no candidate is read)
     for (int i = tid; i < k; i += kTopkThreads) L.idx_out[out_base + i] = i <= row_pos_s ? i : -1;
@@ -361,7 +402,8 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkLaunch 
   }
   // Dynamic shared memory (merges only): the input candidates' positions (n).
   extern __shared__ int4 dyn_s[];
-  topk_select_runs<MODE>(L, n, in_base, out_base, idx_offset, S, reinterpret_cast<int*>(dyn_s));
+  topk_select_runs<MODE, kSeeded>(L, n, in_base, out_base, idx_offset, S, reinterpret_cast<int*>(dyn_s), hrow);
+  if (kSeeded) reinterpret_cast<int2*>(hrow)[tid] = make_int2(0, 0);   // each thread read its own two
 }
 
 // ------------------------------------------------------------------ host side
@@ -406,7 +448,10 @@ static size_t topk_smem_bytes(int seg_len, bool merge) {
 
 static cudaError_t launch_topk_kernel(const TopkLaunch& L, int grid, int seg_len, bool pdl, cudaStream_t st) {
   const size_t smem = topk_smem_bytes(seg_len < kTopkCapacity ? seg_len : kTopkCapacity, L.mode == kMerge);
-  auto kern = L.mode == kDirect ? topk_kernel<kDirect> : L.mode == kChunks ? topk_kernel<kChunks> : topk_kernel<kMerge>;
+  const bool seeded = L.hist != nullptr && L.mode != kMerge;
+  auto kern = L.mode == kDirect ? (seeded ? topk_kernel<kDirect, true> : topk_kernel<kDirect, false>)
+            : L.mode == kChunks ? (seeded ? topk_kernel<kChunks, true> : topk_kernel<kChunks, false>)
+                                : topk_kernel<kMerge, false>;
   // the 48 KB default covers static and dynamic shared memory together
   if (smem + sizeof(TopkShared) + 64 > 48 * 1024) {
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -429,11 +474,18 @@ static cudaError_t launch_topk_kernel(const TopkLaunch& L, int grid, int seg_len
   return cudaLaunchKernelEx(&cfg, kern, L);
 }
 
+int topk_row_chunks(int max_seq_len) { return max_seq_len <= kTopkCapacity ? 1 : (max_seq_len + kTopkCapacity - 1) / kTopkCapacity; }
+
+size_t topk_hist_bytes(int T, int max_seq_len) {
+  return (size_t)T * topk_row_chunks(max_seq_len) * kHistBins * sizeof(int);
+}
+
 cudaError_t topk_chunks_launch(const GeomDev& g, const float* scores, int64_t stride, int k, int c0, int nl,
-                               void* scratch, int* err, bool pdl, cudaStream_t st) {
+                               void* scratch, int* err, bool pdl, cudaStream_t st, int* hist) {
   const int nch = (g.max_seq_len + kTopkCapacity - 1) / kTopkCapacity;
   TopkLaunch L{};
   L.g = g; L.k = k; L.mode = kChunks; L.scores = scores; L.score_stride = stride; L.err = err;
+  L.hist = hist; L.hist_chunks = nch;
   L.chunk = kTopkCapacity; L.c0 = c0; L.nl = nl; L.nchunks = nch;
   L.cand_key_out = reinterpret_cast<uint32_t*>(scratch);
   L.cand_idx_out = reinterpret_cast<int*>(L.cand_key_out + (size_t)g.T * nch * k);
@@ -468,14 +520,15 @@ cudaError_t topk_merge_launch(const GeomDev& g, int k, int* idx, void* scratch, 
 }
 
 cudaError_t topk_launch(const GeomDev& g, const float* scores, int64_t stride, int k, int* idx,
-                        void* scratch, int* err, bool pdl, cudaStream_t st) {
+                        void* scratch, int* err, bool pdl, cudaStream_t st, int* hist) {
   if (g.max_seq_len <= kTopkCapacity) {
     TopkLaunch L{};
     L.g = g; L.k = k; L.mode = kDirect; L.scores = scores; L.score_stride = stride; L.idx_out = idx; L.err = err;
+    L.hist = hist; L.hist_chunks = 1;
     return launch_topk_kernel(L, g.T, g.max_seq_len, pdl, st);
   }
   const int nch = (g.max_seq_len + kTopkCapacity - 1) / kTopkCapacity;
-  cudaError_t e = topk_chunks_launch(g, scores, stride, k, 0, nch, scratch, err, pdl, st);
+  cudaError_t e = topk_chunks_launch(g, scores, stride, k, 0, nch, scratch, err, pdl, st, hist);
   if (e != cudaSuccess) return e;
   return topk_merge_launch(g, k, idx, scratch, err, true, st);   // follows the chunk pass just launched
 }

@@ -57,9 +57,10 @@ class DeviceWorkload:
     weights, each layer's MLA q) are views into one buffer, `inputs`, and the layers'
     outputs into another, `outputs`; the caches are resident tensors of their own."""
 
-    def __init__(self, wl: Workload, device="cuda"):
+    def __init__(self, wl: Workload, device="cuda", hist: bool = False):
         self.wl = wl
         self.device = torch.device(device)
+        self.hist = hist   # the full layer through dsa_decode_step_hist
         d = self.device
         fp8 = wl.qk_dtype == "e4m3"
         self.qk_dtype = _lib.DSA_E4M3 if fp8 else _lib.DSA_BF16
@@ -114,7 +115,7 @@ class DeviceWorkload:
             self.layers.append(DeviceLayer(q, kv, kd, oviews[o_idx[li][0]], oviews[o_idx[li][1]]))
         self.idx = torch.empty(wl.T, wl.topk, dtype=torch.int32, device=d)
         self.args = [self._args(i) for i in range(len(self.layers))]
-        need = max(_lib.dsa_decode_step_workspace_size(a) for a in self.args)
+        need = max(self.workspace_size(i) for i in range(len(self.args)))
         self.ws = _lib.workspace(need, d)
 
     def _args(self, i: int):
@@ -128,10 +129,18 @@ class DeviceWorkload:
                                        idx_out=self.idx, **common)
         return _lib.make_step_args(self.geom, self.wl.topk, reuse_idx=self.idx, **common)
 
+    def workspace_size(self, i: int) -> int:
+        if self.hist and i == 0:
+            return _lib.dsa_decode_step_hist_workspace_size(self.args[0])
+        return _lib.dsa_decode_step_workspace_size(self.args[i])
+
     def step(self, stream=None):
         """One DSA step over every layer, enqueued on `stream` (default: current)."""
-        for a in self.args:
-            _lib.dsa_decode_step(a, self.ws, stream)
+        for i, a in enumerate(self.args):
+            if self.hist and i == 0:
+                _lib.dsa_decode_step_hist(a, self.ws, stream)
+            else:
+                _lib.dsa_decode_step(a, self.ws, stream)
 
     def check_error(self) -> int:
         return _lib.dsa_get_error(self.ws)

@@ -36,7 +36,10 @@
  *     dsa_wait_probe; dsa_stage_copy takes none), 256-byte aligned.
  *     Its first 256 bytes hold the device error word; zero them once before
  *     first use (dsa_clear_error). Calls on the same workspace must be ordered
- *     on one stream.
+ *     on one stream. The header's second int32 counts the score segments (rows,
+ *     or 16384-position chunks of longer rows) whose first-digit histogram the
+ *     step's top-k found not to match the scores (dsa_decode_step_hist, below); it
+ *     is diagnostic only and dsa_clear_error zeroes it.
  *   - Host-side argument errors return DSA_ERR_INVALID_ARG / DSA_ERR_UNSUPPORTED
  *     / DSA_ERR_WORKSPACE before anything is enqueued. Zero work (T == 0) is a
  *     no-op returning DSA_OK. Launch failures return DSA_ERR_CUDA.
@@ -305,6 +308,27 @@ typedef struct {
 dsa_status_t dsa_decode_step(const dsa_step_args_t* args, void* ws, size_t ws_bytes,
                              void* stream);
 size_t dsa_decode_step_workspace_size(const dsa_step_args_t* args);
+
+/*
+ * dsa_decode_step_hist -- dsa_decode_step with the top-k's first radix digit
+ *   counted by the indexer (the first pass of the radix top-k, lmdeploy "feat:
+ *   support GLM-5.2", Changes, moved into the epilogue that makes the scores): per
+ *   query and per 16384-position chunk of its row, the indexer counts the top 11 bits
+ *   of every visible score's radix key in shared memory and adds them into histograms
+ *   held in the last T * ceil(max(max_seq_len, 1) / 16384) * 8 KB of the
+ *   workspace size this call asks for; the top-k reads them instead
+ *   of counting the digit itself and leaves them zero for the next call. Each
+ *   selection so made is checked against its exact final counts, so histograms that
+ *   do not belong to the scores (a workspace's first use, or one that other calls
+ *   wrote over) cost time, not exactness: the segment is selected again without them,
+ *   and the header's second word counts it. Results are bitwise those of
+ *   dsa_decode_step. With bf16 index keys (whose query-group variants leave the
+ *   indexer no shared memory for the counts) the call runs as dsa_decode_step. On
+ *   GB300 it is slower than dsa_decode_step (the counts cost the indexer more than
+ *   they save the top-k), which stays the default.
+ */
+dsa_status_t dsa_decode_step_hist(const dsa_step_args_t* args, void* ws, size_t ws_bytes, void* stream);
+size_t dsa_decode_step_hist_workspace_size(const dsa_step_args_t* args);
 
 /*
  * dsa_decode_step_wait_q -- dsa_decode_step for a caller whose MLA query (args->q)

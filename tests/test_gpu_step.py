@@ -162,3 +162,127 @@ def test_causality_on_gpu():
     dw2.step()
     torch.cuda.synchronize()
     assert torch.equal(idx0, dw2.idx[0]) and torch.equal(out0, dw2.layers[0].out[0])
+
+
+# ---- dsa_decode_step_hist: the indexer's first-digit histograms (the top 11 bits of
+# each visible score's radix key, per query and 16384-position chunk), which the top-k
+# reads instead of counting them. They sit at the end of the full layer's workspace and
+# the top-k leaves them zero; whatever else they hold, the selection stays exact.
+
+def _orderable(scores: np.ndarray) -> np.ndarray:
+    u = scores.astype(np.float32).view(np.uint32).copy()
+    u[u == 0x80000000] = 0
+    return np.where(u & 0x80000000, ~u, u | 0x80000000).astype(np.uint32)
+
+
+def _hist_view(dw, wl):
+    """The histogram region of layer 0's step workspace as [T, chunks, 2048] int32."""
+    nch = max(1, -(-wl.max_seq_len // 16384))
+    nbytes = wl.T * nch * 2048 * 4
+    end = _lib.dsa_decode_step_hist_workspace_size(dw.args[0])
+    off = end - (-(-nbytes // 256) * 256)
+    return dw.ws[off:off + nbytes].view(torch.int32).view(wl.T, nch, 2048), nch
+
+
+def _gpu_scores(dw, wl):
+    stride = int(-(-wl.max_seq_len // 64) * 64)
+    scores = torch.empty((wl.T, stride), dtype=torch.float32, device=DEV)
+    ws = _lib.workspace(_lib.dsa_indexer_scores_workspace_size(dw.geom), DEV)
+    _lib.dsa_indexer_scores(dw.geom, dw.qk_dtype, dw.q_idx, dw.q_scale, dw.w, dw.idx_k, dw.idx_k_scale,
+                            scores, ws)
+    assert _lib.dsa_get_error(ws) == 0
+    return scores.cpu().numpy()
+
+
+HIST = [
+    ("decode", dict(batch=8)),
+    ("mtp", dict(batch=3, ctx_scale=0.25)),         # query groups of 4, two layers on one workspace
+    ("longctx", dict(batch=2, ctx_scale=0.25)),    # rows of 32768: two chunks each
+]
+
+
+def _rejected(dw) -> int:
+    return int(dw.ws[:8].view(torch.int32)[1])
+
+
+@pytest.mark.parametrize("name,kw", HIST, ids=[c[0] for c in HIST])
+def test_step_histograms_accepted_on_clean_workspace(name, kw):
+    """On a zeroed workspace every segment's selection made from the indexer's
+    histogram passes the exact final-count check (none is redone), step after step
+    (the top-k leaves the region zero), equals the oracle's top-k of the GPU's scores,
+    and every output is bitwise that of dsa_decode_step."""
+    wl = inputs.make_config(name, **kw)
+    dw = runner.DeviceWorkload(wl, DEV, hist=True)
+    hv, _ = _hist_view(dw, wl)
+    for _ in range(3):
+        dw.step()
+        torch.cuda.synchronize()
+        assert dw.check_error() == 0
+        assert _rejected(dw) == 0
+        assert int(hv.abs().sum()) == 0
+    sc = _gpu_scores(dw, wl)
+    _, pos = oracle.query_positions(wl.seq_lens, wl.n_q)
+    idx = dw.idx.cpu().numpy()
+    for t in range(wl.T):
+        p = int(pos[t])
+        assert np.array_equal(idx[t], oracle.topk_row(sc[t, : p + 1].astype(np.float64), wl.topk)), t
+    ref = runner.DeviceWorkload(wl, DEV)
+    ref.step()
+    torch.cuda.synchronize()
+    assert torch.equal(ref.idx, dw.idx)
+    for L0, L1 in zip(ref.layers, dw.layers):
+        assert torch.equal(L0.out, L1.out) and torch.equal(L0.lse, L1.lse)
+
+
+@pytest.mark.parametrize("name,kw", HIST, ids=[c[0] for c in HIST])
+@pytest.mark.parametrize("plant", ["exact", "random", "top-bin", "cancel"])
+def test_step_first_digit_histograms(name, kw, plant):
+    """A histogram region holding something else when the step starts (the true
+    histogram, which the indexer then doubles; random words; the right totals in the
+    top bin, above every score; the true histogram's negative, which the indexer's counts bring
+    to zero) still gives the oracle's top-k of the GPU's scores bit for bit, the
+    segments whose check fails are counted, and the region is left zero."""
+    wl = inputs.make_config(name, **kw)
+    dw = runner.DeviceWorkload(wl, DEV, hist=True)
+    sc = _gpu_scores(dw, wl)
+    _, pos = oracle.query_positions(wl.seq_lens, wl.n_q)
+    hv, nch = _hist_view(dw, wl)
+    true = np.zeros((wl.T, nch, 2048), dtype=np.int64)
+    for t in range(wl.T):
+        p = int(pos[t])
+        keys = _orderable(sc[t, : p + 1])
+        chunk = np.arange(p + 1) >> 14
+        np.add.at(true[t], (chunk, keys >> 21), 1)
+    rng = np.random.default_rng(7)
+    if plant == "exact":
+        planted = true
+    elif plant == "random":
+        planted = rng.integers(-2**31, 2**31, size=true.shape)
+    elif plant == "top-bin":
+        # above every real score's bin, so the first digit lands there and is wrong
+        assert true[..., 2047].sum() == 0
+        planted = np.zeros_like(true)
+        planted[..., 2047] = true.sum(axis=2)
+    else:  # cancel: the indexer's counts bring the region back to zero
+        planted = -true
+    hv.copy_(torch.from_numpy(planted.astype(np.int32)))
+    dw.step()
+    torch.cuda.synchronize()
+    assert dw.check_error() == 0
+    assert int(hv.abs().sum()) == 0
+    # segments with more visible keys than index_topk are selected from a histogram
+    selected = sum(int(min(16384, int(pos[t]) + 1 - 16384 * c) > wl.topk)
+                   for t in range(wl.T) for c in range(nch) if int(pos[t]) + 1 > 16384 * c)
+    if plant in ("top-bin", "cancel"):
+        assert _rejected(dw) == selected
+    else:
+        assert 0 <= _rejected(dw) <= selected
+    idx = dw.idx.cpu().numpy()
+    for t in range(wl.T):
+        p = int(pos[t])
+        assert np.array_equal(idx[t], oracle.topk_row(sc[t, : p + 1].astype(np.float64), wl.topk)), t
+    # with the region left zero, the next step's histograms are its own and accepted
+    before, n_rej = dw.idx.clone(), _rejected(dw)
+    dw.step()
+    torch.cuda.synchronize()
+    assert torch.equal(before, dw.idx) and _rejected(dw) == n_rej
