@@ -19,8 +19,8 @@
 // "feat: support GLM-5.2", Changes) moved into the epilogue that makes the scores.
 //
 // Roles: warp P decodes 32 units at a time (one per lane) and, per unit, loads
-// only what changed since the previous unit: a new key tile (two pages by TMA,
-// their key scales by bulk copy) into a ring of key stages, and a new query group
+// only what changed since the previous unit: a new key tile (two pages by TMA) into
+// a ring of key stages, and a new query group
 // (the QG x Hp query rows by TMA, w and q_scale by bulk copy) into a ring of query
 // slots; a small descriptor per unit names the stage and slot it uses. A request's
 // units run group-major: a query group is loaded once for all its key tiles (in
@@ -42,12 +42,18 @@ namespace dsa {
 // epilogue warps takes one query of a unit (more warps to hide the accumulator reads).
 constexpr int kMultiEpiGroups = 4;
 
-template <bool kFp8, int kHp, int kQG>
+// kHistT: the first-digit histogram variant (its counters take dynamic shared memory).
+template <bool kFp8, int kHp, int kQG, bool kHistT = false>
 struct IndexerCfg {
   static constexpr int kAtoms = kFp8 ? 1 : 2;                  // 128-byte column blocks per row
   static constexpr int kN = kQG * kHp;                         // MMA N
   static constexpr int kKeyBytes = 128 * 128 * kAtoms;         // one 128-key tile
-  static constexpr int kKStageBytes = kKeyBytes + 1024;        // + key scales of its two pages (512 B)
+  // One-query units keep their tile's key scales in the key stage (copied with the
+  // codes; the epilogue reads them there and releases the stage); query-group units
+  // load them from global memory in the epilogue, so a stage holds codes alone and is
+  // released by the MMA's commit (a fourth stage fits, and a handshake per unit goes).
+  static constexpr bool kScaleInStage = kQG == 1;
+  static constexpr int kKStageBytes = kKeyBytes + (kScaleInStage ? 1024 : 0);   // + key scales of its two pages (512 B)
   static constexpr int kQBytes = kN * 128 * kAtoms;            // the group's query rows
   static constexpr int kWOff = kQBytes, kQsOff = kQBytes + kN * 4;
   static constexpr int kQSlotBytes = (kQBytes + 2 * kN * 4 + 1023) / 1024 * 1024;
@@ -55,7 +61,17 @@ struct IndexerCfg {
   // One-query e4m3 units run two CTAs per SM (two producers per SM), each with
   // half the shared memory; the other variants one CTA with the whole budget.
   static constexpr int kCtasPerSm = (kQG == 1 && kFp8) ? 2 : 1;
-  static constexpr int kBudget = kCtasPerSm == 2 ? 90112 : 204800;
+  // First-digit histograms (16-bit counts, two bins per word), in dynamic shared memory
+  // after the key stages in the histogram variant: e4m3 keys only (the bf16
+  // query-group variants have no room beside their operands; for bf16 keys the fused
+  // step lets the top-k count the digit).
+  static constexpr bool kHist = kFp8;
+  static constexpr int kHistWords = kQG * kHistBins / 2;
+  static constexpr int kHistBytes = kHist ? 4 * kHistWords + 16 : 0;   // + the two flush barriers
+  // Dynamic shared memory for the operands: one CTA per SM keeps what it takes within
+  // the 227 KB a CTA may hold beside at most 18 KB of static arrays and the histograms.
+  static constexpr int kBudget1 = 232448 - 18432 - 1024 - (kHistT ? kHistBytes : 0);
+  static constexpr int kBudget = kCtasPerSm == 2 ? 90112 : (kBudget1 < 204800 ? kBudget1 : 204800);
   static constexpr int kKStagesFit = (kBudget - kQSlots * kQSlotBytes) / kKStageBytes;
   static constexpr int kKStages = kKStagesFit < 8 ? kKStagesFit : 8;
   static constexpr int kDescs = 16;                            // unit descriptor ring
@@ -78,13 +94,6 @@ struct IndexerCfg {
                                    : (kAccs * kN) <= 256 ? 256 : 512;
   static constexpr int kMaxB = 1024;                           // requests per call
   static constexpr int kSmemBytes = 1024 + kQSlots * kQSlotBytes + kKStages * kKStageBytes;
-  // First-digit histograms (16-bit counts, two bins per word), in dynamic shared memory
-  // after the key stages when a launch asks for them: e4m3 keys only (the bf16
-  // query-group variants have no room beside their operands; for bf16 keys the fused
-  // step lets the top-k count the digit).
-  static constexpr bool kHist = kFp8;
-  static constexpr int kHistWords = kQG * kHistBins / 2;
-  static constexpr int kHistBytes = kHist ? 4 * kHistWords + 16 : 0;   // + the two flush barriers
   static constexpr int kKSteps = kFp8 ? 4 : 8;
   static_assert(kN <= 256 && kN % 16 == 0, "MMA N");
   static_assert(kKStages >= 2, "key stages");
@@ -165,7 +174,7 @@ template <bool kFp8, int kHp, int kQG, bool kHistT>
 __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, IndexerCfg<kFp8, kHp, kQG>::kBoundCtas)
     indexer_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_q,
                    const IndexerArgs A) {
-  using C = IndexerCfg<kFp8, kHp, kQG>;
+  using C = IndexerCfg<kFp8, kHp, kQG, kHistT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* q_slots = smem;                                       // kQSlots x kQSlotBytes
@@ -234,7 +243,10 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, Ind
     abort_flag = 0;
     // a stage / slot is released by the MMA thread's commit and every epilogue
     // warp once they have moved on to the next one
-    for (int s = 0; s < C::kKStages; ++s) { mbar_init(smem_u32(&key_full[s]), 1); mbar_init(smem_u32(&key_empty[s]), 1 + C::kEpiWarps); }
+    for (int s = 0; s < C::kKStages; ++s) {
+      mbar_init(smem_u32(&key_full[s]), 1);
+      mbar_init(smem_u32(&key_empty[s]), 1 + (C::kScaleInStage ? C::kEpiWarps : 0));
+    }
     for (int s = 0; s < C::kQSlots; ++s) { mbar_init(smem_u32(&q_full[s]), 1); mbar_init(smem_u32(&q_empty[s]), 1 + C::kEpiWarps); }
     for (int s = 0; s < C::kDescs; ++s) { mbar_init(smem_u32(&desc_full[s]), 1); mbar_init(smem_u32(&desc_empty[s]), 1 + C::kEpiWarps); }
     for (int a = 0; a < C::kAccs; ++a) { mbar_init(smem_u32(&tfull_bar[a]), 1); mbar_init(smem_u32(&tempty_bar[a]), C::kEpiWarps); }
@@ -311,13 +323,14 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, Ind
               uint8_t* st = k_stages + ks * C::kKStageBytes;
               const uint32_t bar = smem_u32(&key_full[ks]);
               const int np = (p0 >= 0) + (p1 >= 0);
-              mbar_arrive_expect_tx(bar, np * 64 * 128 * C::kAtoms + (kFp8 ? np * 256 : 0));
+              mbar_arrive_expect_tx(bar, np * 64 * 128 * C::kAtoms + (kFp8 && C::kScaleInStage ? np * 256 : 0));
               const int pages[2] = {p0, p1};
               for (int hp = 0; hp < 2; ++hp) {
                 if (pages[hp] < 0) continue;
                 for (int a = 0; a < C::kAtoms; ++a)
                   tma_load_2d(smem_u32(st + a * 16384 + hp * 8192), &map_k, bar, a * (kFp8 ? 128 : 64), pages[hp] * 64);
-                if (kFp8) bulk_load(smem_u32(st + C::kKeyBytes + hp * 256), A.k_scale + (int64_t)pages[hp] * 64, 256, bar);
+                if (kFp8 && C::kScaleInStage)
+                  bulk_load(smem_u32(st + C::kKeyBytes + hp * 256), A.k_scale + (int64_t)pages[hp] * 64, 256, bar);
               }
               ++kcount;
             }
@@ -424,11 +437,12 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, Ind
     }
   } else {
     // ================================================================ epilogue warps
-    // Lane = key of the tile. A new key stage: the key's scale is read into a
-    // register and the stage released at once (the MMA's commit covers its own
-    // reads). A new query group: w * q_scale is formed once (registers for one query
-    // and one CTA per SM, else this warp's shared copy) and the slot released. Then
-    // per unit only the accumulator (TMEM) is read.
+    // Lane = key of the tile. The key's scale: read from a new key stage, which is then
+    // released at once (one-query units; the MMA's commit covers its own reads), or
+    // loaded from global memory when the unit starts (query groups). A new query
+    // group: w * q_scale is formed once (registers for one query and one CTA per SM,
+    // else this warp's shared copy) and the slot released. Then per unit only the
+    // accumulator (TMEM) is read.
     const int quarter = warp & 3, half = warp >> 2;
     const int key = quarter * 32 + lane;
     const float neg_inf = -__int_as_float(0x7f800000);
@@ -454,14 +468,18 @@ __global__ void __launch_bounds__(IndexerCfg<kFp8, kHp, kQG>::kBoundThreads, Ind
           hq = d.q_start; hc = chunk; hn = d.q_count;
         }
       }
-      const int page = (key < 64) ? d.page0 : d.page1;
-      if (d.flags & kNewKey) {
-        cur_k = d.kstage;
-        if (!mbar_wait(smem_u32(&key_full[cur_k]), (kc / C::kKStages) & 1, &abort_flag, A.err)) break;   // key scales visible
-        ++kc;
-        if (kFp8) ks = reinterpret_cast<const float*>(k_stages + cur_k * C::kKStageBytes + C::kKeyBytes)[key];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&key_empty[cur_k]));
+      const int page = (key < 64) ? d.page0 : d.page1;   // -1 if unmapped or out of range
+      if constexpr (C::kScaleInStage) {
+        if (d.flags & kNewKey) {
+          cur_k = d.kstage;
+          if (!mbar_wait(smem_u32(&key_full[cur_k]), (kc / C::kKStages) & 1, &abort_flag, A.err)) break;   // key scales visible
+          ++kc;
+          if (kFp8) ks = reinterpret_cast<const float*>(k_stages + cur_k * C::kKStageBytes + C::kKeyBytes)[key];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&key_empty[cur_k]));
+        }
+      } else if (kFp8) {
+        ks = page >= 0 ? __ldg(A.k_scale + (int64_t)page * 64 + (key & 63)) : 1.f;
       }
       if (d.flags & kNewQuery) {
         cur_q = d.qslot;
@@ -583,7 +601,7 @@ cudaError_t query_ranges_launch(const int* cu_q, const int* seq_lens, int B, int
 template <bool kFp8, int kHp, int kQG, bool kHistT = false>
 static cudaError_t launch_indexer_t(const CUtensorMap& mk, const CUtensorMap& mq, const IndexerArgs& A,
                                     int grid, bool pdl, cudaStream_t st) {
-  using C = IndexerCfg<kFp8, kHp, kQG>;
+  using C = IndexerCfg<kFp8, kHp, kQG, kHistT>;
   if constexpr (!kHistT) {
     if (A.hist != nullptr) {
       if constexpr (C::kHist) return launch_indexer_t<kFp8, kHp, kQG, true>(mk, mq, A, grid, pdl, st);
