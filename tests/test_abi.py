@@ -138,6 +138,27 @@ def test_workspace_sizes_are_consistent(lib):
     assert lib.dsa_decode_step_workspace_size(C.byref(a)) < base
 
 
+def test_histogram_step_workspace_adds_the_histograms(lib):
+    """dsa_decode_step_hist asks for the default step's workspace plus 8 KB of first-digit
+    histogram per query and 16384-position chunk of max_seq_len (the region at its end);
+    a shared layer's call (reuse_idx) counts nothing and asks for the default size."""
+    a = _lib.dsa_step_args_t()
+    a.topk = 2048
+    a.H = 16
+    a.Hi = 64
+    for T, L, chunks in ((64, 8192, 1), (8, 131072, 8), (2, 16384, 1), (2, 16385, 2)):
+        a.geom = _geom(T=T, B=T, max_seq_len=L, bt_stride=-(-L // 64))
+        a.reuse_idx = None
+        base = lib.dsa_decode_step_workspace_size(C.byref(a))
+        assert lib.dsa_decode_step_hist_workspace_size(C.byref(a)) == base + T * chunks * 8192
+        a.reuse_idx = 16
+        assert lib.dsa_decode_step_hist_workspace_size(C.byref(a)) == lib.dsa_decode_step_workspace_size(C.byref(a))
+    # the same argument checks as the default step, before anything is enqueued
+    a.reuse_idx = None
+    a.topk = 0
+    assert lib.dsa_decode_step_hist(C.byref(a), 256, 1 << 30, None) == _lib.DSA_ERR_INVALID_ARG
+
+
 def test_bounded_step_budget_floor_and_workspace_sizes(lib):
     a = _lib.dsa_step_args_t()
     a.geom = _geom(T=64, B=64, max_seq_len=8192, bt_stride=128)
