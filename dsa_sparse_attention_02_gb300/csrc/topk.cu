@@ -25,6 +25,12 @@
 // lists are concatenated in chunk order, so its candidates stay in ascending
 // position and ties still go to the lower position. Any element of the row's top-k
 // is in the top-k of every group that contains it, so every level is exact.
+//
+// Seeded instantiations (dsa_decode_step_hist) take the first digit's histogram (the
+// keys' top 11 bits) from the indexer instead of counting it: the digits then start
+// at the top bit, the selection is checked against the exact totals of its placement
+// scan, and a segment whose histogram does not match its scores is selected again
+// unseeded.
 #include <cstdint>
 #include "kernels.cuh"
 
