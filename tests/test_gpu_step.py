@@ -205,7 +205,10 @@ def _rejected(dw) -> int:
     return int(dw.ws[:8].view(torch.int32)[1])
 
 
-@pytest.mark.parametrize("name,kw", HIST, ids=[c[0] for c in HIST])
+CLEAN = HIST + [("tiny", dict())]   # bf16 index keys: no histograms, the default step's path
+
+
+@pytest.mark.parametrize("name,kw", CLEAN, ids=[c[0] for c in CLEAN])
 def test_step_histograms_accepted_on_clean_workspace(name, kw):
     """On a zeroed workspace every segment's selection made from the indexer's
     histogram passes the exact final-count check (none is redone), step after step
