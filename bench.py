@@ -67,6 +67,8 @@ def parse():
     ap.add_argument("--only-config", choices=list(inputs.CONFIG_NAMES), default=None,
                     help="run just --warmup + --steps steps of one configuration (no graph, no flush; for "
                          "profiler launch lists) and print its step time")
+    ap.add_argument("--hist", action="store_true",
+                    help="with --only-config: the full layer through dsa_decode_step_hist")
     return ap.parse_args()
 
 
@@ -323,7 +325,7 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     if args.only_config:
-        run_one_config(args.only_config, args.warmup, args.steps, dev)
+        run_one_config(args.only_config, args.warmup, args.steps, dev, hist=args.hist)
         return
     dist = None
     if world > 1:
@@ -450,11 +452,12 @@ def main():
         dist.destroy_process_group()
 
 
-def run_one_config(name, warmup, steps, device):
+def run_one_config(name, warmup, steps, device, hist=False):
     """Eager steps of one configuration, for profilers: warmup + steps calls of the whole
-    step (every layer), then a device-error check and one JSON line with the mean time."""
+    step (every layer; the full layer through dsa_decode_step_hist with hist), then a
+    device-error check and one JSON line with the mean time."""
     wl = inputs.make_config(name)
-    dw = runner.DeviceWorkload(wl, device)
+    dw = runner.DeviceWorkload(wl, device, hist=hist)
     for _ in range(warmup):
         dw.step()
     torch.cuda.synchronize()
